@@ -13,7 +13,8 @@ of the output token and advances once per emitted token.  That state is the
 Stream layout (shared contract with the CUDA sampler, stated, not shared
 code): for vocabulary index i, key = (seed & 0xffffffff, seed >> 32),
 counter = (i // 4, step & 0xffffffff, step >> 32, 0x5644), and the uniform
-is word i % 4 of the block, mapped to u = (word + 0.5) / 2**32.
+is word i % 4 of the block, mapped to u = ((word >> 8) + 0.5) / 2**24, a
+24-bit uniform that float32 holds exactly and that is never 0 or 1.
 
 Pinned by tests/test_oracle_sampler.py: Philox known-answer vectors from
 the Random123 distribution, a chi-square uniformity check, argmax against
@@ -59,7 +60,7 @@ def philox_words(seed: int, step: int, n: int) -> np.ndarray:
 
 
 def uniforms(seed: int, step: int, n: int) -> np.ndarray:
-    return (philox_words(seed, step, n).astype(np.float64) + 0.5) / 2.0 ** 32
+    return ((philox_words(seed, step, n) >> np.uint64(8)).astype(np.float64) + 0.5) / 2.0 ** 24
 
 
 def argmax_lowest(logits) -> int:
