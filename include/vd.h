@@ -1,0 +1,204 @@
+/*
+ * vd.h -- C ABI of the batch-invariant decoder step (libvd.so).
+ *
+ * One engine step runs a Llama/Gemma-style decoder over a batch of
+ * requests whose K/V lives in a paged, prefix-sharing cache, and returns
+ * float32 logits for selected rows.  Every kernel choice (GEMM tile, KV
+ * split size, key tile) is fixed when the model is created, from the model
+ * shape alone, so that for every request u the logits equal
+ * Forward(W, history_u) bit for bit whatever the batch composition, chunked
+ * prefill budget, prefill/decode split, prefix reuse, recomputation or
+ * physical page placement.
+ *
+ * Sources (cited by page title and section):
+ *   [V]  "Vosti: Specifying, Implementing, and Verifying Deterministic LLM
+ *        Inference" (arXiv 2609.38981), abstract.
+ *   [B]  深入解析 Vosti (blog deep-dive on the same paper): §二 Definition 2.1
+ *        and Theorem 4.1; §三 3.2 engine invariants and the three engineering
+ *        rules (fixed kernel choices, exact prefix matching, reuse before
+ *        registration); §五 5.1 KV-value invariant; §六 6.1 matmul contract,
+ *        6.2 attention causal contract, masking rules and tile traversal.
+ *   [T]  "Deterministic and bit-exact inference" (catalogue record M-0002),
+ *        technical section: fixed KV split *size*, batch-invariant RMSNorm,
+ *        matmul and attention.
+ *
+ * Conventions for every entry point:
+ *   - Return value: VD_OK (0) or a VD_ERR_* code; vd_last_error() then gives
+ *     a message (thread-local, valid until the next call on this thread).
+ *   - Arguments are validated on the host before anything is launched; a
+ *     call that fails validation has launched nothing and changed nothing.
+ *   - "dev" pointers are CUDA device pointers of the current device; "host"
+ *     pointers are ordinary host memory (pageable or pinned) read during the
+ *     call and not retained.
+ *   - bf16 tensors are row-major; matrices are stored [out][in].
+ *   - Work is enqueued on the given stream (0 = legacy default stream); the
+ *     call returns before the GPU finishes unless stated otherwise.
+ */
+#ifndef VD_H_
+#define VD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  VD_OK = 0,
+  VD_ERR_INVALID_ARG = 1,  /* malformed descriptor, null pointer, bad size      */
+  VD_ERR_UNSUPPORTED = 2,  /* no fixed kernel configuration for this shape      */
+  VD_ERR_OUT_OF_RANGE = 3, /* page id, position, token id or row out of range   */
+  VD_ERR_CAPACITY = 4,     /* step exceeds the sizes fixed at model creation    */
+  VD_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed                 */
+  VD_ERR_TIMEOUT = 6       /* a bounded on-device wait gave up (device status)  */
+};
+
+enum { VD_ACT_SWIGLU = 0, VD_ACT_GEGLU = 1 };
+
+typedef struct vd_model vd_model;
+typedef struct vd_kv_pool vd_kv_pool;
+
+/* Model shape and numerics.  Layer i is a global attention layer iff
+ * local_global_period == 0 or (i + 1) % local_global_period == 0; other
+ * layers are local with a window of sliding_window keys (the row's own key
+ * included) [B §六 6.2, sliding-window traversal]. */
+typedef struct vd_model_config {
+  int32_t n_layers;
+  int32_t d_model;
+  int32_t n_heads;           /* query heads Hq                                */
+  int32_t n_kv_heads;        /* KV heads Hkv; Hq % Hkv == 0                   */
+  int32_t head_dim;          /* 64, 128 or 256                                */
+  int32_t ffn_dim;           /* F                                             */
+  int32_t vocab;             /* V                                             */
+  float rms_eps;
+  int32_t act;               /* VD_ACT_SWIGLU or VD_ACT_GEGLU (tanh GELU)     */
+  int32_t qk_norm;           /* 1: per-head RMSNorm of q and k before RoPE    */
+  float rope_theta;          /* global layers                                 */
+  float rope_theta_local;    /* local layers                                  */
+  int32_t sliding_window;    /* 0: no local layers                            */
+  int32_t local_global_period;
+  int32_t page_size;         /* must be 16                                    */
+  /* capacities: fix workspace sizes at creation, never numerics */
+  int32_t max_tokens;        /* max tokens (rows) per step                    */
+  int32_t max_seqs;          /* max requests per step                         */
+  int32_t max_logit_rows;    /* max rows returning logits per step            */
+  int32_t max_context;       /* max cached + new tokens of one request        */
+} vd_model_config;
+
+/* Per-layer weights: bf16 device pointers, borrowed (caller keeps them
+ * alive and unchanged until vd_destroy_model). */
+typedef struct vd_layer_weights {
+  const void* attn_norm;   /* [d]                                             */
+  const void* wqkv;        /* [(Hq + 2 Hkv) hd][d]; rows q heads, k, v        */
+  const void* q_norm;      /* [hd] (only if qk_norm)                          */
+  const void* k_norm;      /* [hd] (only if qk_norm)                          */
+  const void* wo;          /* [d][Hq hd]                                      */
+  const void* ffn_norm;    /* [d]                                             */
+  const void* w_gate_up;   /* [2F][d]; rows 0..F-1 gate, F..2F-1 up           */
+  const void* w_down;      /* [d][F]                                          */
+} vd_layer_weights;
+
+typedef struct vd_weight_ptrs {
+  const void* embed;                /* dev bf16 [V][d]                          */
+  const vd_layer_weights* layers;   /* host array [n_layers], copied            */
+  const void* final_norm;           /* dev bf16 [d]                             */
+  const void* lm_head;              /* dev bf16 [V][d]                          */
+} vd_weight_ptrs;
+
+/* One engine step.  Request b owns tokens cu_q[b] .. cu_q[b+1]-1 (q_len >= 1),
+ * at positions cached_len[b] .. cached_len[b] + q_len - 1; its logical page i
+ * (tokens 16i .. 16i+15) is physical page page_table[b * page_table_stride + i].
+ * The step writes the K/V of its new tokens into their slots and reads the
+ * cached prefix [0, cached_len[b]) from the pool [B §三 3.2 Invariant 1;
+ * §五 5.1].  All arrays are host memory. */
+typedef struct vd_batch {
+  int32_t num_tokens;          /* T = cu_q[B]                                 */
+  int32_t num_seqs;            /* B                                           */
+  int32_t num_logit_rows;      /* R                                           */
+  int32_t page_table_stride;   /* columns of page_table                       */
+  const int32_t* token_ids;    /* [T]                                         */
+  const int32_t* positions;    /* [T]; must equal cached_len[b] + i           */
+  const int32_t* cu_q;         /* [B + 1], cu_q[0] = 0, strictly increasing   */
+  const int32_t* cached_len;   /* [B]                                         */
+  const int32_t* page_table;   /* [B * page_table_stride]                     */
+  const int32_t* logit_rows;   /* [R] token indices in [0, T)                 */
+} vd_batch;
+
+/* Per-row sampler state [B §二 Definition 2.1, sampler_0]: Philox4x32-10 key
+ * = seed, counter from (vocabulary index, step).  temperature <= 0: greedy. */
+typedef struct vd_sampler {
+  uint64_t seed;
+  uint64_t step;
+  float temperature;
+  float pad_;
+} vd_sampler;
+
+typedef struct vd_kernel_stat {
+  char name[32];
+  int32_t launches;
+  double total_ms;
+} vd_kernel_stat;
+
+/* Creates a model over borrowed weights and fixes every kernel choice from
+ * the shape alone [B §三 3.2, fixed kernel choices: bound at initialisation
+ * from weight dims, dtype, head geometry and page size; no runtime tuning;
+ * a shape without a fixed configuration is rejected].  Allocates the
+ * library-owned workspace (activations, split partials, RoPE tables) on the
+ * current device.  Errors: VD_ERR_INVALID_ARG (null/inconsistent),
+ * VD_ERR_UNSUPPORTED (head_dim not 64/128/256, page_size != 16, d or 2F
+ * or V not a multiple of 128, ...), VD_ERR_CUDA. */
+int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_model** out);
+void vd_destroy_model(vd_model* m);
+
+/* Paged KV pool of num_pages pages [B §三 3.2: paged KV with page tables;
+ * §五 5.1: each slot holds fKV of its logical prefix].  Layout, per layer:
+ * [page][K=0,V=1][kv_head][16 slots][head_dim] bf16, layers contiguous, so
+ * one page of one layer is 2*Hkv*16*hd*2 bytes.  dev_mem (nullable): caller
+ * memory of at least vd_kv_pool_bytes() bytes, 256-byte aligned, borrowed;
+ * null makes the library allocate.  The pool is zero-filled on creation.
+ * Errors: VD_ERR_INVALID_ARG, VD_ERR_CAPACITY (bytes too small), VD_ERR_CUDA. */
+size_t vd_kv_pool_bytes(const vd_model* m, int32_t num_pages);
+int vd_kv_pool_alloc(vd_model* m, int32_t num_pages, void* dev_mem, size_t bytes, vd_kv_pool** out);
+void vd_destroy_kv_pool(vd_kv_pool* p);
+/* Device address of the pool (for tests that fill it directly). */
+void* vd_kv_pool_data(vd_kv_pool* p);
+
+/* One engine step [B §二 Theorem 4.1: o_u.logits = Forward(W, history_u)].
+ * logits_out: dev float32 [R][V], row j = logits of token logit_rows[j].
+ * Validates the descriptor (S5 layout consistency: positions, page ids in
+ * range, capacity; S7 write isolation: no two new tokens share a slot),
+ * uploads it, then enqueues the whole decoder forward.  Errors:
+ * VD_ERR_INVALID_ARG, VD_ERR_OUT_OF_RANGE, VD_ERR_CAPACITY, VD_ERR_CUDA.
+ * T == 0 is a no-op. */
+int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out, void* stream);
+
+/* Token choice for R rows of dev float32 logits [R][V] -> dev int32 [R]:
+ * greedy argmax (lowest index on ties) or Gumbel-max with Philox4x32-10
+ * (per-row state in host array per_row[R]). */
+int vd_sample(vd_model* m, const float* logits, int32_t R, const vd_sampler* per_row,
+              int32_t* tokens_out, void* stream);
+
+/* Debug: copies the K and V of `layer` for logical positions [0, n_tokens)
+ * of one request (host page table) into dev bf16 out_k / out_v
+ * [n_tokens][Hkv][hd], for bitwise checks of the KV-value invariant
+ * [B §五 5.1]. */
+int vd_copy_kv(vd_model* m, vd_kv_pool* pool, int32_t layer, const int32_t* page_table,
+               int32_t n_tokens, void* out_k, void* out_v, void* stream);
+
+/* Reads (synchronising the device) the on-device status word: VD_OK, or
+ * VD_ERR_TIMEOUT if a bounded wait in a kernel gave up; clears it. */
+int vd_device_status(vd_model* m);
+
+/* Per-kernel timing with CUDA events on the launching stream. */
+int vd_profile_enable(vd_model* m, int32_t on);
+/* Synchronises, returns the number of kernel classes written to out. */
+int vd_profile_collect(vd_model* m, vd_kernel_stat* out, int32_t max_out);
+
+const char* vd_last_error(void);
+const char* vd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VD_H_ */

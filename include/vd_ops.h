@@ -1,0 +1,72 @@
+/*
+ * vd_ops.h -- single-kernel entry points of libvd.so.
+ *
+ * Each call runs exactly one of the kernels vd_step uses, with the same
+ * fixed configuration, on caller-provided device buffers.  They exist so
+ * that each kernel can be checked on its own: against the CPU oracle on
+ * seeded inputs, and against itself across batch shapes (the relational
+ * contracts of 深入解析 Vosti §六 6.1 / 6.2).  Conventions (return codes,
+ * validation before launch, dev/host pointers, streams) are those of vd.h.
+ */
+#ifndef VD_OPS_H_
+#define VD_OPS_H_
+
+#include <stdint.h>
+
+#include "vd.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  VD_EPI_BF16 = 0,      /* C = bf16(acc)                                       */
+  VD_EPI_RESIDUAL = 1,  /* C = bf16(bf16(acc) + R); R may alias C              */
+  VD_EPI_F32 = 2,       /* C = acc (float32)                                   */
+  VD_EPI_SWIGLU = 3,    /* C[t][f] = bf16(silu(bf16(g)) * bf16(u))             */
+  VD_EPI_GEGLU = 4      /* C[t][f] = bf16(gelu_tanh(bf16(g)) * bf16(u))        */
+};
+
+/* Batch-invariant bf16 GEMM [B §六 6.1 matmul contract: row x of a batched
+ * run equals the singleton run bit for bit].  acc[t][n] = sum_k A[t][k] W[n][k]
+ * in fp32 on tcgen05 tensor cores, tile 128 (weight rows) x 128 (tokens) x 64,
+ * one tile shape for every T, K traversed in one fixed order, no split-K.
+ * A: dev bf16 [T][K]; W: dev bf16 [N][K] (GLU: [2F][K], rows F.. are "up",
+ * N = F); C: dev [T][N] bf16 (float32 for VD_EPI_F32); residual: dev bf16
+ * [T][N] or null.  Requires N % 128 == 0 (GLU: F % 64 == 0), K % 64 == 0,
+ * 16-byte aligned pointers, T >= 1.  Errors: VD_ERR_INVALID_ARG,
+ * VD_ERR_UNSUPPORTED, VD_ERR_CUDA. */
+int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int32_t K, int32_t epilogue,
+               const void* residual, void* stream);
+
+/* Batch-invariant RMSNorm [T technical: batch-invariant RMSNorm]:
+ * y[r] = bf16(x[r] / sqrt(mean(x[r]^2) + eps) * w), one warp per row, fixed
+ * lane-strided sum of squares and fixed butterfly.  x, y: dev bf16 [rows][d],
+ * w: dev bf16 [d]; d % 8 == 0. */
+int vd_op_rmsnorm(const void* x, const void* w, void* y, int32_t rows, int32_t d, float eps, void* stream);
+
+/* Unified paged attention + fixed-order split merge for `layer` of model m
+ * over pool p [B §六 6.2: causal contract, masking rules, tile traversal;
+ * T technical: fixed KV split size].  q: dev bf16 [T][Hq][hd] (rotated),
+ * out: dev bf16 [T][Hq][hd].  Reads K/V of positions [0, cached_len+q_len)
+ * through the batch's page tables (host descriptor as for vd_step; token ids
+ * and logit rows are ignored).  The K/V of the new tokens must already be in
+ * the pool. */
+int vd_op_attention(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, const void* q, void* out,
+                    void* stream);
+
+/* RoPE + K/V write for `layer` (and per-head QK RMSNorm if the model has
+ * it): qkv dev bf16 [T][(Hq+2Hkv) hd] -> q_out dev bf16 [T][Hq][hd]; k and v
+ * of token t go to the pool slot of (request, position) via the batch's
+ * page tables [B §五 5.1: KV keyed to its logical prefix]. */
+int vd_op_rope_kv(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, const void* qkv, void* q_out,
+                  void* stream);
+
+/* The sampler's Philox4x32-10 stream: out[i] = word used for vocabulary index
+ * i at (seed, step); dev uint32 [n]. */
+int vd_op_philox(uint64_t seed, uint64_t step, int32_t n, uint32_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VD_OPS_H_ */

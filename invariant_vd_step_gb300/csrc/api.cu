@@ -1,0 +1,859 @@
+// C ABI of libvd.so: model creation with kernel choices fixed from the
+// model shape, the paged KV pool, descriptor validation and upload, and the
+// kernel sequence of one engine step.
+//
+// Fixed kernel choices (深入解析 Vosti §三 3.2): every constant that shapes a
+// reduction -- GEMM tile 128x128x64, attention key tile B_N (64 keys, 32 for
+// hd 256), KV split size S_kv (512 keys), RMSNorm lane layout -- is chosen
+// here from (dims, dtype, head geometry, page size) and never from a batch.
+// What varies per step (grid sizes, which TMA map bucket covers the T
+// activation rows, NW of the attention CTA) changes no row's arithmetic.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <string>
+#include <unordered_set>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "vd_device.cuh"
+#include "vd_internal.h"
+
+namespace vd {
+
+static thread_local std::string g_err;
+void set_error(const std::string& msg) { g_err = msg; }
+int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+// ---------------------------------------------------------------- TMA maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(VD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16) return fail(VD_ERR_INVALID_ARG, "TMA base/stride not 16-byte aligned");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(VD_ERR_CUDA, "cuTensorMapEncodeTiled(2d) failed: " + std::to_string(r));
+  return VD_OK;
+}
+
+int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd) {
+  auto fn = encode_fn();
+  if (!fn) return fail(VD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(hd / 64), rows};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(hd) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(hd / 64), 16};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(VD_ERR_CUDA, "cuTensorMapEncodeTiled(kv) failed: " + std::to_string(r));
+  return VD_OK;
+}
+
+}  // namespace vd
+
+using namespace vd;
+
+namespace {
+
+constexpr int kSplitKeys = 512;  // S_kv, fixed for every model
+
+struct ProfRec {
+  int cls;
+  cudaEvent_t a, b;
+};
+const char* const kKernelNames[] = {"embed",     "rmsnorm",  "gemm_qkv",     "rope_kv",   "attention",
+                                    "attn_merge", "gemm_o",  "gemm_gate_up", "gemm_down", "final_norm",
+                                    "gemm_lm_head", "sample"};
+enum KernelClass {
+  K_EMBED, K_RMSNORM, K_GEMM_QKV, K_ROPE, K_ATTN, K_MERGE, K_GEMM_O, K_GEMM_GU, K_GEMM_DOWN, K_FINAL_NORM,
+  K_GEMM_LM, K_SAMPLE, K_COUNT
+};
+
+// Activation buffer with TMA maps for row counts 1, 2, 4, ... (capped at
+// the capacity): a GEMM over T rows uses the smallest map covering T, so
+// rows past T are either never fetched or (within the bucket) computed and
+// discarded -- a GEMM column depends on its own row only.
+struct ActBuf {
+  __nv_bfloat16* ptr = nullptr;
+  int cols = 0;
+  std::vector<int> rows;
+  std::vector<CUtensorMap> maps;
+  const CUtensorMap& map_for(int T) const {
+    for (size_t i = 0; i < rows.size(); ++i)
+      if (rows[i] >= T) return maps[i];
+    return maps.back();
+  }
+};
+
+// Host-side layout of the uploaded step descriptor (int32 offsets).
+struct Desc {
+  int T = 0, B = 0, R = 0, stride = 0;
+  int tokens, positions, slot_page, cu_q, cached, page_table, logit_rows, dec_seq, dec_start, pre_seq, pre_start;
+  int n_dec = 0, n_pre = 0, items_dec = 0, items_pre = 0;
+  int total = 0;
+};
+
+}  // namespace
+
+struct vd_model {
+  vd_model_config cfg{};
+  int device = 0;
+  const __nv_bfloat16* embed = nullptr;
+  const __nv_bfloat16* final_norm = nullptr;
+  const __nv_bfloat16* lm_head = nullptr;
+  std::vector<vd_layer_weights> layers;
+  // fixed kernel choices
+  int split = kSplitKeys;
+  int key_tile = 64;
+  int max_splits = 0;
+  int G = 1;
+  // TMA maps
+  std::vector<CUtensorMap> m_qkv, m_o, m_gu, m_down;
+  CUtensorMap m_lm{};
+  ActBuf a, o, z, ar;
+  // workspace
+  __nv_bfloat16 *x = nullptr, *qkv = nullptr, *q = nullptr;
+  float *part_o = nullptr, *part_ml = nullptr;
+  float *cos_g = nullptr, *sin_g = nullptr, *cos_l = nullptr, *sin_l = nullptr;
+  int* status = nullptr;
+  int* d_desc = nullptr;
+  int* h_desc[2] = {nullptr, nullptr};
+  cudaEvent_t desc_ev[2] = {nullptr, nullptr};
+  int desc_slot = 0;
+  size_t desc_cap = 0;
+  vd_sampler* d_samp = nullptr;
+  vd_sampler* h_samp = nullptr;
+  cudaEvent_t samp_ev = nullptr;
+  std::vector<void*> dev_allocs;
+  // profiling
+  bool profiling = false;
+  std::vector<ProfRec> recs;
+  std::vector<cudaEvent_t> ev_pool;
+  double prof_ms[K_COUNT] = {};
+  int prof_n[K_COUNT] = {};
+};
+
+struct vd_kv_pool {
+  vd_model* m = nullptr;
+  int num_pages = 0;
+  void* data = nullptr;
+  bool owned = false;
+  long long rows = 0;  // 16-slot rows of hd elements
+  CUtensorMap map{};
+};
+
+namespace {
+
+// ---------------------------------------------------------------- profiling
+cudaEvent_t take_event(vd_model* m) {
+  if (!m->ev_pool.empty()) {
+    cudaEvent_t e = m->ev_pool.back();
+    m->ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+struct Prof {
+  vd_model* m;
+  int cls;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  Prof(vd_model* m_, int cls_, cudaStream_t s_) : m(m_), cls(cls_), s(s_) {
+    if (m->profiling) {
+      a = take_event(m);
+      cudaEventRecord(a, s);
+    }
+  }
+  ~Prof() {
+    if (m->profiling) {
+      cudaEvent_t b = take_event(m);
+      cudaEventRecord(b, s);
+      m->recs.push_back({cls, a, b});
+    }
+  }
+};
+
+int dev_alloc(vd_model* m, void** p, size_t bytes) {
+  if (bytes == 0) bytes = 256;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) return fail(VD_ERR_CUDA, std::string("cudaMalloc: ") + cudaGetErrorString(e));
+  m->dev_allocs.push_back(*p);
+  cudaMemset(*p, 0, bytes);
+  return VD_OK;
+}
+
+int make_act(vd_model* m, ActBuf& buf, int cap_rows, int cols) {
+  int rc = dev_alloc(m, reinterpret_cast<void**>(&buf.ptr), static_cast<size_t>(cap_rows) * cols * 2);
+  if (rc) return rc;
+  buf.cols = cols;
+  for (int r = 1;; r *= 2) {
+    const int rows = std::min(r, cap_rows);
+    CUtensorMap mp;
+    if ((rc = make_map_2d(&mp, buf.ptr, rows, cols, kGemmBN))) return rc;
+    buf.rows.push_back(rows);
+    buf.maps.push_back(mp);
+    if (rows >= cap_rows) break;
+  }
+  return VD_OK;
+}
+
+int rope_table(vd_model* m, float theta, int hd, float** cs, float** sn) {
+  const int half = hd / 2;
+  const size_t n = static_cast<size_t>(m->cfg.max_context) * half;
+  std::vector<float> c(n), s(n);
+  for (int p = 0; p < m->cfg.max_context; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double inv = pow(static_cast<double>(theta), -2.0 * i / hd);
+      const double ang = static_cast<double>(p) * inv;
+      c[static_cast<size_t>(p) * half + i] = static_cast<float>(cos(ang));
+      s[static_cast<size_t>(p) * half + i] = static_cast<float>(sin(ang));
+    }
+  int rc;
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(cs), n * 4))) return rc;
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(sn), n * 4))) return rc;
+  VD_CUDA_TRY(cudaMemcpy(*cs, c.data(), n * 4, cudaMemcpyHostToDevice));
+  VD_CUDA_TRY(cudaMemcpy(*sn, s.data(), n * 4, cudaMemcpyHostToDevice));
+  return VD_OK;
+}
+
+bool layer_is_local(const vd_model_config& c, int i) {
+  return c.sliding_window > 0 && c.local_global_period > 0 && ((i + 1) % c.local_global_period) != 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Items of one attention work class for request with q_len, kv_len.
+int attn_items(int qlen, int kv_len, int G, int Hkv, int rows_per_cta) {
+  const int rows = qlen * G;
+  const int nrb = (rows + rows_per_cta - 1) / rows_per_cta;
+  const int nsplit = (kv_len - 1) / kSplitKeys + 1;
+  return nrb * Hkv * nsplit;
+}
+
+// Validates a step descriptor and builds the upload image in h.
+int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_tokens, Desc& d, int* h) {
+  const vd_model_config& c = m->cfg;
+  if (!b) return fail(VD_ERR_INVALID_ARG, "null batch");
+  const int T = b->num_tokens, B = b->num_seqs, R = b->num_logit_rows;
+  if (T < 0 || B < 0 || R < 0) return fail(VD_ERR_INVALID_ARG, "negative size");
+  if (T > c.max_tokens || B > c.max_seqs || R > c.max_logit_rows)
+    return fail(VD_ERR_CAPACITY, "step exceeds max_tokens / max_seqs / max_logit_rows");
+  if (T == 0) {
+    d.T = 0;
+    return VD_OK;
+  }
+  if (B == 0 || !b->cu_q || !b->cached_len || !b->page_table || !b->positions)
+    return fail(VD_ERR_INVALID_ARG, "missing descriptor array");
+  if (need_tokens && !b->token_ids) return fail(VD_ERR_INVALID_ARG, "missing token_ids");
+  if (R > 0 && !b->logit_rows) return fail(VD_ERR_INVALID_ARG, "missing logit_rows");
+  if (b->cu_q[0] != 0 || b->cu_q[B] != T) return fail(VD_ERR_INVALID_ARG, "cu_q must run from 0 to num_tokens");
+  int stride = 0;
+  for (int s = 0; s < B; ++s) {
+    const int ql = b->cu_q[s + 1] - b->cu_q[s];
+    if (ql < 1) return fail(VD_ERR_INVALID_ARG, "every request needs q_len >= 1");
+    if (b->cached_len[s] < 0) return fail(VD_ERR_INVALID_ARG, "negative cached_len");
+    const long long kv = static_cast<long long>(b->cached_len[s]) + ql;
+    if (kv > c.max_context) return fail(VD_ERR_CAPACITY, "request exceeds max_context");
+    const int np = static_cast<int>((kv + 15) / 16);
+    if (np > b->page_table_stride) return fail(VD_ERR_OUT_OF_RANGE, "page table narrower than the request");
+    stride = std::max(stride, np);
+  }
+  d.T = T;
+  d.B = B;
+  d.R = R;
+  d.stride = stride;
+  int off = 0;
+  auto take = [&](int n) {
+    const int o = off;
+    off += n;
+    return o;
+  };
+  d.tokens = take(T);
+  d.positions = take(T);
+  d.slot_page = take(T);
+  d.cu_q = take(B + 1);
+  d.cached = take(B);
+  d.page_table = take(B * stride);
+  d.logit_rows = take(R);
+  d.dec_seq = take(B);
+  d.dec_start = take(B + 1);
+  d.pre_seq = take(B);
+  d.pre_start = take(B + 1);
+  d.total = off;
+  if (static_cast<size_t>(off) > m->desc_cap) return fail(VD_ERR_CAPACITY, "descriptor exceeds capacity");
+  std::unordered_set<long long> slots;
+  slots.reserve(static_cast<size_t>(T) * 2);
+  const int V = c.vocab;
+  for (int s = 0; s < B; ++s) {
+    const int q0 = b->cu_q[s], ql = b->cu_q[s + 1] - q0, cached = b->cached_len[s];
+    const int np = (cached + ql + 15) / 16;
+    for (int i = 0; i < np; ++i) {
+      const int pg = b->page_table[static_cast<size_t>(s) * b->page_table_stride + i];
+      if (pg < 0 || pg >= pool->num_pages) return fail(VD_ERR_OUT_OF_RANGE, "page id out of range");
+      h[d.page_table + s * stride + i] = pg;
+    }
+    for (int i = np; i < stride; ++i) h[d.page_table + s * stride + i] = 0;
+    for (int i = 0; i < ql; ++i) {
+      const int t = q0 + i, p = cached + i;
+      if (b->positions[t] != p) return fail(VD_ERR_INVALID_ARG, "positions[t] must equal cached_len + offset");
+      if (need_tokens && (b->token_ids[t] < 0 || b->token_ids[t] >= V))
+        return fail(VD_ERR_OUT_OF_RANGE, "token id out of range");
+      const int pg = h[d.page_table + s * stride + p / 16];
+      if (!slots.insert(static_cast<long long>(pg) * 16 + (p & 15)).second)
+        return fail(VD_ERR_INVALID_ARG, "two new tokens of the step write the same KV slot");
+      h[d.tokens + t] = need_tokens ? b->token_ids[t] : 0;
+      h[d.positions + t] = p;
+      h[d.slot_page + t] = pg;
+    }
+    h[d.cu_q + s] = q0;
+    h[d.cached + s] = cached;
+  }
+  h[d.cu_q + B] = T;
+  for (int j = 0; j < R; ++j) {
+    if (b->logit_rows[j] < 0 || b->logit_rows[j] >= T) return fail(VD_ERR_OUT_OF_RANGE, "logit row out of range");
+    h[d.logit_rows + j] = b->logit_rows[j];
+  }
+  // attention work classes: decode-shaped requests (one warp of rows) and the rest
+  int nd = 0, npre = 0, idec = 0, ipre = 0;
+  for (int s = 0; s < B; ++s) {
+    const int ql = b->cu_q[s + 1] - b->cu_q[s], kv = b->cached_len[s] + ql;
+    if (ql * m->G <= 16) {
+      h[d.dec_seq + nd] = s;
+      h[d.dec_start + nd] = idec;
+      idec += attn_items(ql, kv, m->G, c.n_kv_heads, 16);
+      ++nd;
+    } else {
+      h[d.pre_seq + npre] = s;
+      h[d.pre_start + npre] = ipre;
+      ipre += attn_items(ql, kv, m->G, c.n_kv_heads, 64);
+      ++npre;
+    }
+  }
+  h[d.dec_start + nd] = idec;
+  h[d.pre_start + npre] = ipre;
+  d.n_dec = nd;
+  d.n_pre = npre;
+  d.items_dec = idec;
+  d.items_pre = ipre;
+  return VD_OK;
+}
+
+int upload_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_tokens, Desc& d, cudaStream_t s) {
+  const int slot = m->desc_slot;
+  m->desc_slot ^= 1;
+  VD_CUDA_TRY(cudaEventSynchronize(m->desc_ev[slot]));  // previous upload from this staging slot is done
+  int* h = m->h_desc[slot];
+  int rc = build_desc(m, pool, b, need_tokens, d, h);
+  if (rc || d.T == 0) return rc;
+  VD_CUDA_TRY(cudaMemcpyAsync(m->d_desc, h, static_cast<size_t>(d.total) * 4, cudaMemcpyHostToDevice, s));
+  VD_CUDA_TRY(cudaEventRecord(m->desc_ev[slot], s));
+  return VD_OK;
+}
+
+int run_attention(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d, const __nv_bfloat16* q,
+                  __nv_bfloat16* out, cudaStream_t s) {
+  const vd_model_config& c = m->cfg;
+  const int hd = c.head_dim;
+  const int window = layer_is_local(c, layer) ? c.sliding_window : 0;
+  AttnArgs a{};
+  a.q = q;
+  a.part_o = m->part_o;
+  a.part_ml = m->part_ml;
+  a.cu_q = m->d_desc + d.cu_q;
+  a.cached_len = m->d_desc + d.cached;
+  a.page_table = m->d_desc + d.page_table;
+  a.pt_stride = d.stride;
+  a.Hq = c.n_heads;
+  a.Hkv = c.n_kv_heads;
+  a.layer_row0 = static_cast<int>(static_cast<long long>(layer) * pool->num_pages * 2 * c.n_kv_heads * 16);
+  a.pool_rows = static_cast<int>(pool->rows);
+  a.window = window;
+  a.split = m->split;
+  a.max_splits = m->max_splits;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(hd)));
+  a.status = m->status;
+  int rc;
+  {
+    Prof p(m, K_ATTN, s);
+    if (d.n_dec) {
+      a.cls_seq = m->d_desc + d.dec_seq;
+      a.cls_start = m->d_desc + d.dec_start;
+      a.n_cls = d.n_dec;
+      if ((rc = launch_attention(pool->map, a, hd, false, d.items_dec, s))) return rc;
+    }
+    if (d.n_pre) {
+      a.cls_seq = m->d_desc + d.pre_seq;
+      a.cls_start = m->d_desc + d.pre_start;
+      a.n_cls = d.n_pre;
+      if ((rc = launch_attention(pool->map, a, hd, true, d.items_pre, s))) return rc;
+    }
+  }
+  MergeArgs g{};
+  g.part_o = m->part_o;
+  g.part_ml = m->part_ml;
+  g.out = out;
+  g.positions = m->d_desc + d.positions;
+  g.T = d.T;
+  g.Hq = c.n_heads;
+  g.window = window;
+  g.split = m->split;
+  g.max_splits = m->max_splits;
+  Prof p(m, K_MERGE, s);
+  return launch_merge(g, hd, s);
+}
+
+int run_rope(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d, const __nv_bfloat16* qkv,
+             __nv_bfloat16* q_out, cudaStream_t s) {
+  const vd_model_config& c = m->cfg;
+  const bool local = layer_is_local(c, layer);
+  RopeArgs r{};
+  r.qkv = qkv;
+  r.q_out = q_out;
+  r.pool = static_cast<__nv_bfloat16*>(pool->data);
+  r.positions = m->d_desc + d.positions;
+  r.slot_page = m->d_desc + d.slot_page;
+  r.cos_t = local ? m->cos_l : m->cos_g;
+  r.sin_t = local ? m->sin_l : m->sin_g;
+  r.q_norm = c.qk_norm ? static_cast<const __nv_bfloat16*>(m->layers[layer].q_norm) : nullptr;
+  r.k_norm = c.qk_norm ? static_cast<const __nv_bfloat16*>(m->layers[layer].k_norm) : nullptr;
+  r.eps = c.rms_eps;
+  r.T = d.T;
+  r.Hq = c.n_heads;
+  r.Hkv = c.n_kv_heads;
+  r.hd = c.head_dim;
+  r.layer_elem0 = static_cast<long long>(layer) * pool->num_pages * 2 * c.n_kv_heads * 16 * c.head_dim;
+  Prof p(m, K_ROPE, s);
+  return launch_rope_kv(r, s);
+}
+
+int check_model(const vd_model* m) { return m ? VD_OK : fail(VD_ERR_INVALID_ARG, "null model"); }
+
+}  // namespace
+
+// ====================================================================== API
+extern "C" {
+
+const char* vd_last_error(void) { return g_err.c_str(); }
+const char* vd_version(void) { return "vd 0.1 (sm_103a)"; }
+
+int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_model** out) {
+  if (!cfg || !w || !out) return fail(VD_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  const vd_model_config& c = *cfg;
+  if (c.n_layers < 1 || c.d_model < 1 || c.n_heads < 1 || c.n_kv_heads < 1 || c.ffn_dim < 1 || c.vocab < 1 ||
+      c.max_tokens < 1 || c.max_seqs < 1 || c.max_logit_rows < 1 || c.max_context < 1)
+    return fail(VD_ERR_INVALID_ARG, "non-positive dimension or capacity");
+  if (c.n_heads % c.n_kv_heads) return fail(VD_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
+  if (c.page_size != 16) return fail(VD_ERR_UNSUPPORTED, "page_size must be 16");
+  if (c.head_dim != 64 && c.head_dim != 128 && c.head_dim != 256)
+    return fail(VD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+  if (c.d_model % kGemmBM || c.vocab % kGemmBM || c.ffn_dim % 64 || c.ffn_dim % kGemmBK ||
+      ((c.n_heads + 2 * c.n_kv_heads) * c.head_dim) % kGemmBM || (c.n_heads * c.head_dim) % kGemmBK ||
+      c.d_model % kGemmBK)
+    return fail(VD_ERR_UNSUPPORTED, "no fixed GEMM tiling: d, V, (Hq+2Hkv)hd must be multiples of 128; F, Hq*hd multiples of 64");
+  if (c.n_heads / c.n_kv_heads > 16) return fail(VD_ERR_UNSUPPORTED, "GQA group larger than 16");
+  if (c.act != VD_ACT_SWIGLU && c.act != VD_ACT_GEGLU) return fail(VD_ERR_INVALID_ARG, "unknown activation");
+  if (c.sliding_window < 0 || c.local_global_period < 0) return fail(VD_ERR_INVALID_ARG, "negative window");
+  if (!w->embed || !w->final_norm || !w->lm_head || !w->layers) return fail(VD_ERR_INVALID_ARG, "null weight");
+  for (int i = 0; i < c.n_layers; ++i) {
+    const vd_layer_weights& L = w->layers[i];
+    if (!L.attn_norm || !L.wqkv || !L.wo || !L.ffn_norm || !L.w_gate_up || !L.w_down ||
+        (c.qk_norm && (!L.q_norm || !L.k_norm)))
+      return fail(VD_ERR_INVALID_ARG, "null layer weight");
+    if (!aligned16(L.wqkv) || !aligned16(L.wo) || !aligned16(L.w_gate_up) || !aligned16(L.w_down) ||
+        !aligned16(L.attn_norm) || !aligned16(L.ffn_norm))
+      return fail(VD_ERR_INVALID_ARG, "weights must be 16-byte aligned");
+  }
+  if (!aligned16(w->embed) || !aligned16(w->lm_head) || !aligned16(w->final_norm))
+    return fail(VD_ERR_INVALID_ARG, "weights must be 16-byte aligned");
+
+  vd_model* m = new vd_model();
+  m->cfg = c;
+  cudaGetDevice(&m->device);
+  m->embed = static_cast<const __nv_bfloat16*>(w->embed);
+  m->final_norm = static_cast<const __nv_bfloat16*>(w->final_norm);
+  m->lm_head = static_cast<const __nv_bfloat16*>(w->lm_head);
+  m->layers.assign(w->layers, w->layers + c.n_layers);
+  m->G = c.n_heads / c.n_kv_heads;
+  m->key_tile = attn_key_tile(c.head_dim);
+  m->split = kSplitKeys;
+  m->max_splits = (c.max_context - 1) / m->split + 1;
+  const int d = c.d_model, hd = c.head_dim, F = c.ffn_dim, V = c.vocab;
+  const int qkv_dim = (c.n_heads + 2 * c.n_kv_heads) * hd, attn_dim = c.n_heads * hd;
+  int rc = VD_OK;
+  auto bail = [&](int r) {
+    vd_destroy_model(m);
+    return r;
+  };
+  for (int i = 0; i < c.n_layers; ++i) {
+    CUtensorMap mp;
+    const vd_layer_weights& L = m->layers[i];
+    if ((rc = make_map_2d(&mp, L.wqkv, qkv_dim, d, kGemmBM))) return bail(rc);
+    m->m_qkv.push_back(mp);
+    if ((rc = make_map_2d(&mp, L.wo, d, attn_dim, kGemmBM))) return bail(rc);
+    m->m_o.push_back(mp);
+    if ((rc = make_map_2d(&mp, L.w_gate_up, 2 * F, d, 64))) return bail(rc);
+    m->m_gu.push_back(mp);
+    if ((rc = make_map_2d(&mp, L.w_down, d, F, kGemmBM))) return bail(rc);
+    m->m_down.push_back(mp);
+  }
+  if ((rc = make_map_2d(&m->m_lm, w->lm_head, V, d, kGemmBM))) return bail(rc);
+  const int TM = c.max_tokens;
+  if ((rc = make_act(m, m->a, TM, d))) return bail(rc);
+  if ((rc = make_act(m, m->o, TM, attn_dim))) return bail(rc);
+  if ((rc = make_act(m, m->z, TM, F))) return bail(rc);
+  if ((rc = make_act(m, m->ar, c.max_logit_rows, d))) return bail(rc);
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->x), static_cast<size_t>(TM) * d * 2))) return bail(rc);
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->qkv), static_cast<size_t>(TM) * qkv_dim * 2))) return bail(rc);
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->q), static_cast<size_t>(TM) * attn_dim * 2))) return bail(rc);
+  const size_t np = static_cast<size_t>(TM) * c.n_heads * m->max_splits;
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->part_o), np * hd * 4))) return bail(rc);
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->part_ml), np * 2 * 4))) return bail(rc);
+  if ((rc = rope_table(m, c.rope_theta, hd, &m->cos_g, &m->sin_g))) return bail(rc);
+  if ((rc = rope_table(m, c.rope_theta_local, hd, &m->cos_l, &m->sin_l))) return bail(rc);
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->status), 256))) return bail(rc);
+  const int max_pages = (c.max_context + 15) / 16;
+  m->desc_cap = 3 * static_cast<size_t>(TM) + 6 * static_cast<size_t>(c.max_seqs) + 8 +
+                static_cast<size_t>(c.max_seqs) * max_pages + c.max_logit_rows;
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->d_desc), m->desc_cap * 4))) return bail(rc);
+  for (int k = 0; k < 2; ++k) {
+    if (cudaMallocHost(reinterpret_cast<void**>(&m->h_desc[k]), m->desc_cap * 4) != cudaSuccess ||
+        cudaEventCreateWithFlags(&m->desc_ev[k], cudaEventDisableTiming) != cudaSuccess)
+      return bail(fail(VD_ERR_CUDA, "pinned descriptor buffer"));
+  }
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->d_samp), sizeof(vd_sampler) * c.max_logit_rows))) return bail(rc);
+  if (cudaMallocHost(reinterpret_cast<void**>(&m->h_samp), sizeof(vd_sampler) * c.max_logit_rows) != cudaSuccess ||
+      cudaEventCreateWithFlags(&m->samp_ev, cudaEventDisableTiming) != cudaSuccess)
+    return bail(fail(VD_ERR_CUDA, "pinned sampler buffer"));
+  VD_CUDA_TRY(cudaDeviceSynchronize());
+  *out = m;
+  return VD_OK;
+}
+
+void vd_destroy_model(vd_model* m) {
+  if (!m) return;
+  cudaDeviceSynchronize();
+  for (void* p : m->dev_allocs) cudaFree(p);
+  for (int k = 0; k < 2; ++k) {
+    if (m->h_desc[k]) cudaFreeHost(m->h_desc[k]);
+    if (m->desc_ev[k]) cudaEventDestroy(m->desc_ev[k]);
+  }
+  if (m->h_samp) cudaFreeHost(m->h_samp);
+  if (m->samp_ev) cudaEventDestroy(m->samp_ev);
+  for (auto& r : m->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : m->ev_pool) cudaEventDestroy(e);
+  delete m;
+}
+
+size_t vd_kv_pool_bytes(const vd_model* m, int32_t num_pages) {
+  if (!m || num_pages < 0) return 0;
+  const vd_model_config& c = m->cfg;
+  return static_cast<size_t>(c.n_layers) * num_pages * 2 * c.n_kv_heads * 16 * c.head_dim * 2;
+}
+
+int vd_kv_pool_alloc(vd_model* m, int32_t num_pages, void* dev_mem, size_t bytes, vd_kv_pool** out) {
+  if (check_model(m) || !out) return fail(VD_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  if (num_pages < 1) return fail(VD_ERR_INVALID_ARG, "num_pages must be >= 1");
+  const size_t need = vd_kv_pool_bytes(m, num_pages);
+  const vd_model_config& c = m->cfg;
+  const long long rows = static_cast<long long>(c.n_layers) * num_pages * 2 * c.n_kv_heads * 16;
+  if (rows + 16 > 0x7fffffffLL) return fail(VD_ERR_CAPACITY, "pool too large for 32-bit TMA row coordinates");
+  vd_kv_pool* p = new vd_kv_pool();
+  p->m = m;
+  p->num_pages = num_pages;
+  p->rows = rows;
+  if (dev_mem) {
+    if (bytes < need) {
+      delete p;
+      return fail(VD_ERR_CAPACITY, "dev_mem smaller than vd_kv_pool_bytes()");
+    }
+    if (reinterpret_cast<uintptr_t>(dev_mem) & 255) {
+      delete p;
+      return fail(VD_ERR_INVALID_ARG, "dev_mem must be 256-byte aligned");
+    }
+    p->data = dev_mem;
+  } else {
+    if (cudaMalloc(&p->data, need) != cudaSuccess) {
+      delete p;
+      return fail(VD_ERR_CUDA, "cudaMalloc(pool) failed");
+    }
+    p->owned = true;
+  }
+  if (cudaMemset(p->data, 0, need) != cudaSuccess) {
+    vd_destroy_kv_pool(p);
+    return fail(VD_ERR_CUDA, "cudaMemset(pool) failed");
+  }
+  int rc = make_map_kv(&p->map, p->data, static_cast<uint64_t>(rows), c.head_dim);
+  if (rc) {
+    vd_destroy_kv_pool(p);
+    return rc;
+  }
+  cudaDeviceSynchronize();
+  *out = p;
+  return VD_OK;
+}
+
+void vd_destroy_kv_pool(vd_kv_pool* p) {
+  if (!p) return;
+  if (p->owned && p->data) {
+    cudaDeviceSynchronize();
+    cudaFree(p->data);
+  }
+  delete p;
+}
+
+void* vd_kv_pool_data(vd_kv_pool* p) { return p ? p->data : nullptr; }
+
+int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out, void* stream) {
+  if (check_model(m) || !pool || pool->m != m) return fail(VD_ERR_INVALID_ARG, "null or foreign model/pool");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (b && b->num_logit_rows > 0 && !logits_out) return fail(VD_ERR_INVALID_ARG, "null logits_out");
+  Desc d;
+  int rc = upload_desc(m, pool, b, true, d, s);
+  if (rc || d.T == 0) return rc;
+  const vd_model_config& c = m->cfg;
+  const int T = d.T, dm = c.d_model, hd = c.head_dim, F = c.ffn_dim;
+  const int qkv_dim = (c.n_heads + 2 * c.n_kv_heads) * hd;
+  {
+    Prof p(m, K_EMBED, s);
+    if ((rc = launch_embed(m->embed, m->d_desc + d.tokens, m->x, T, dm, s))) return rc;
+  }
+  GemmArgs g{};
+  g.status = m->status;
+  g.T = T;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const vd_layer_weights& L = m->layers[l];
+    {
+      Prof p(m, K_RMSNORM, s);
+      if ((rc = launch_rmsnorm(m->x, nullptr, L.attn_norm, m->a.ptr, T, dm, c.rms_eps, s))) return rc;
+    }
+    {
+      Prof p(m, K_GEMM_QKV, s);
+      g.out = m->qkv; g.residual = nullptr; g.K = dm; g.ldo = qkv_dim;
+      if ((rc = launch_gemm(m->m_qkv[l], m->a.map_for(T), qkv_dim / kGemmBM, g, EPI_BF16, s))) return rc;
+    }
+    if ((rc = run_rope(m, pool, l, d, m->qkv, m->q, s))) return rc;
+    if ((rc = run_attention(m, pool, l, d, m->q, m->o.ptr, s))) return rc;
+    {
+      Prof p(m, K_GEMM_O, s);
+      g.out = m->x; g.residual = m->x; g.K = c.n_heads * hd; g.ldo = dm;
+      if ((rc = launch_gemm(m->m_o[l], m->o.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
+    }
+    {
+      Prof p(m, K_RMSNORM, s);
+      if ((rc = launch_rmsnorm(m->x, nullptr, L.ffn_norm, m->a.ptr, T, dm, c.rms_eps, s))) return rc;
+    }
+    {
+      Prof p(m, K_GEMM_GU, s);
+      g.out = m->z.ptr; g.residual = nullptr; g.K = dm; g.ldo = F; g.glu_up_row = F;
+      if ((rc = launch_gemm(m->m_gu[l], m->a.map_for(T), F / 64, g,
+                            c.act == VD_ACT_GEGLU ? EPI_GEGLU : EPI_SWIGLU, s)))
+        return rc;
+    }
+    {
+      Prof p(m, K_GEMM_DOWN, s);
+      g.out = m->x; g.residual = m->x; g.K = F; g.ldo = dm;
+      if ((rc = launch_gemm(m->m_down[l], m->z.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
+    }
+  }
+  if (d.R > 0) {
+    {
+      Prof p(m, K_FINAL_NORM, s);
+      if ((rc = launch_rmsnorm(m->x, m->d_desc + d.logit_rows, m->final_norm, m->ar.ptr, d.R, dm, c.rms_eps, s)))
+        return rc;
+    }
+    Prof p(m, K_GEMM_LM, s);
+    GemmArgs h{};
+    h.status = m->status;
+    h.T = d.R;
+    h.out = logits_out;
+    h.K = dm;
+    h.ldo = c.vocab;
+    if ((rc = launch_gemm(m->m_lm, m->ar.map_for(d.R), c.vocab / kGemmBM, h, EPI_F32, s))) return rc;
+  }
+  return VD_OK;
+}
+
+int vd_sample(vd_model* m, const float* logits, int32_t R, const vd_sampler* per_row, int32_t* tokens_out,
+              void* stream) {
+  if (check_model(m)) return VD_ERR_INVALID_ARG;
+  if (R < 0 || R > m->cfg.max_logit_rows) return fail(VD_ERR_CAPACITY, "R exceeds max_logit_rows");
+  if (R == 0) return VD_OK;
+  if (!logits || !per_row || !tokens_out) return fail(VD_ERR_INVALID_ARG, "null argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  VD_CUDA_TRY(cudaEventSynchronize(m->samp_ev));
+  memcpy(m->h_samp, per_row, sizeof(vd_sampler) * R);
+  VD_CUDA_TRY(cudaMemcpyAsync(m->d_samp, m->h_samp, sizeof(vd_sampler) * R, cudaMemcpyHostToDevice, s));
+  VD_CUDA_TRY(cudaEventRecord(m->samp_ev, s));
+  Prof p(m, K_SAMPLE, s);
+  return launch_sample(logits, R, m->cfg.vocab, m->d_samp, tokens_out, s);
+}
+
+int vd_copy_kv(vd_model* m, vd_kv_pool* pool, int32_t layer, const int32_t* page_table, int32_t n_tokens,
+               void* out_k, void* out_v, void* stream) {
+  if (check_model(m) || !pool || pool->m != m) return fail(VD_ERR_INVALID_ARG, "null or foreign model/pool");
+  const vd_model_config& c = m->cfg;
+  if (layer < 0 || layer >= c.n_layers) return fail(VD_ERR_OUT_OF_RANGE, "layer out of range");
+  if (n_tokens < 0) return fail(VD_ERR_INVALID_ARG, "negative n_tokens");
+  if (n_tokens == 0) return VD_OK;
+  if (!page_table || !out_k || !out_v) return fail(VD_ERR_INVALID_ARG, "null argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int np = (n_tokens + 15) / 16;
+  for (int i = 0; i < np; ++i)
+    if (page_table[i] < 0 || page_table[i] >= pool->num_pages) return fail(VD_ERR_OUT_OF_RANGE, "page id out of range");
+  const size_t row = static_cast<size_t>(c.head_dim) * 2;
+  const __nv_bfloat16* base = static_cast<const __nv_bfloat16*>(pool->data) +
+                              static_cast<size_t>(layer) * pool->num_pages * 2 * c.n_kv_heads * 16 * c.head_dim;
+  // one strided copy per (page, K/V): 16 slots x Hkv heads -> [pos][head][hd]
+  for (int i = 0; i < np; ++i) {
+    const int nt = std::min(16, n_tokens - i * 16);
+    for (int kv = 0; kv < 2; ++kv) {
+      const __nv_bfloat16* src = base + (static_cast<size_t>(page_table[i]) * 2 + kv) * c.n_kv_heads * 16 * c.head_dim;
+      char* dst = static_cast<char*>(kv ? out_v : out_k) + static_cast<size_t>(i) * 16 * c.n_kv_heads * row;
+      for (int h = 0; h < c.n_kv_heads; ++h)
+        VD_CUDA_TRY(cudaMemcpy2DAsync(dst + h * row, c.n_kv_heads * row, src + static_cast<size_t>(h) * 16 * c.head_dim,
+                                      row, row, nt, cudaMemcpyDeviceToDevice, s));
+    }
+  }
+  return VD_OK;
+}
+
+int vd_device_status(vd_model* m) {
+  if (check_model(m)) return VD_ERR_INVALID_ARG;
+  int v = 0;
+  VD_CUDA_TRY(cudaDeviceSynchronize());
+  VD_CUDA_TRY(cudaMemcpy(&v, m->status, 4, cudaMemcpyDeviceToHost));
+  VD_CUDA_TRY(cudaMemset(m->status, 0, 4));
+  if (v) return fail(VD_ERR_TIMEOUT, "a bounded on-device wait gave up");
+  return VD_OK;
+}
+
+int vd_profile_enable(vd_model* m, int32_t on) {
+  if (check_model(m)) return VD_ERR_INVALID_ARG;
+  m->profiling = on != 0;
+  return VD_OK;
+}
+
+int vd_profile_collect(vd_model* m, vd_kernel_stat* out, int32_t max_out) {
+  if (check_model(m)) return VD_ERR_INVALID_ARG;
+  for (auto& r : m->recs) {
+    VD_CUDA_TRY(cudaEventSynchronize(r.b));
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, r.a, r.b);
+    m->prof_ms[r.cls] += ms;
+    m->prof_n[r.cls] += 1;
+    m->ev_pool.push_back(r.a);
+    m->ev_pool.push_back(r.b);
+  }
+  m->recs.clear();
+  int n = 0;
+  for (int k = 0; k < K_COUNT && n < max_out; ++k) {
+    if (!m->prof_n[k]) continue;
+    if (out) {
+      memset(&out[n], 0, sizeof(vd_kernel_stat));
+      strncpy(out[n].name, kKernelNames[k], sizeof(out[n].name) - 1);
+      out[n].launches = m->prof_n[k];
+      out[n].total_ms = m->prof_ms[k];
+    }
+    ++n;
+  }
+  for (int k = 0; k < K_COUNT; ++k) {
+    m->prof_ms[k] = 0;
+    m->prof_n[k] = 0;
+  }
+  return n;
+}
+
+// ---------------------------------------------------------------- single ops
+int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int32_t K, int32_t epilogue,
+               const void* residual, void* stream) {
+  if (!A || !W || !C) return fail(VD_ERR_INVALID_ARG, "null pointer");
+  if (T < 1 || N < 1 || K < 1) return fail(VD_ERR_INVALID_ARG, "non-positive size");
+  const bool glu = epilogue == VD_EPI_SWIGLU || epilogue == VD_EPI_GEGLU;
+  if (epilogue < 0 || epilogue > VD_EPI_GEGLU) return fail(VD_ERR_INVALID_ARG, "unknown epilogue");
+  if (K % kGemmBK || (glu ? N % 64 : N % kGemmBM)) return fail(VD_ERR_UNSUPPORTED, "N or K not a multiple of the tile");
+  if (epilogue == VD_EPI_RESIDUAL && !residual) return fail(VD_ERR_INVALID_ARG, "residual required");
+  if (!aligned16(A) || !aligned16(W) || !aligned16(C)) return fail(VD_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  CUtensorMap wm, xm;
+  int rc;
+  if ((rc = make_map_2d(&wm, W, glu ? 2 * N : N, K, glu ? 64 : kGemmBM))) return rc;
+  if ((rc = make_map_2d(&xm, A, T, K, kGemmBN))) return rc;
+  GemmArgs g{};
+  g.out = C;
+  g.residual = residual;
+  g.T = T;
+  g.K = K;
+  g.ldo = N;
+  g.glu_up_row = N;
+  g.status = nullptr;
+  return launch_gemm(wm, xm, glu ? N / 64 : N / kGemmBM, g, epilogue, static_cast<cudaStream_t>(stream));
+}
+
+int vd_op_rmsnorm(const void* x, const void* w, void* y, int32_t rows, int32_t d, float eps, void* stream) {
+  if (!x || !w || !y) return fail(VD_ERR_INVALID_ARG, "null pointer");
+  if (rows < 0 || d < 8 || d % 8) return fail(VD_ERR_INVALID_ARG, "d must be a positive multiple of 8");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return fail(VD_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  return launch_rmsnorm(x, nullptr, w, y, rows, d, eps, static_cast<cudaStream_t>(stream));
+}
+
+int vd_op_attention(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, const void* q, void* out,
+                    void* stream) {
+  if (check_model(m) || !p || p->m != m || !q || !out) return fail(VD_ERR_INVALID_ARG, "null argument");
+  if (layer < 0 || layer >= m->cfg.n_layers) return fail(VD_ERR_OUT_OF_RANGE, "layer out of range");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Desc d;
+  int rc = upload_desc(m, p, b, false, d, s);
+  if (rc || d.T == 0) return rc;
+  return run_attention(m, p, layer, d, static_cast<const __nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(out), s);
+}
+
+int vd_op_rope_kv(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, const void* qkv, void* q_out,
+                  void* stream) {
+  if (check_model(m) || !p || p->m != m || !qkv || !q_out) return fail(VD_ERR_INVALID_ARG, "null argument");
+  if (layer < 0 || layer >= m->cfg.n_layers) return fail(VD_ERR_OUT_OF_RANGE, "layer out of range");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Desc d;
+  int rc = upload_desc(m, p, b, false, d, s);
+  if (rc || d.T == 0) return rc;
+  return run_rope(m, p, layer, d, static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(q_out), s);
+}
+
+int vd_op_philox(uint64_t seed, uint64_t step, int32_t n, uint32_t* out, void* stream) {
+  if (n < 0) return fail(VD_ERR_INVALID_ARG, "negative n");
+  if (n > 0 && !out) return fail(VD_ERR_INVALID_ARG, "null out");
+  return launch_philox(seed, step, n, out, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

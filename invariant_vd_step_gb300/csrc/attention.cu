@@ -1,0 +1,369 @@
+// Unified prefill/decode paged attention with a fixed KV split size.
+//
+// Rows.  For request b and KV head g the rows are (token i, query head of
+// the group) pairs, token-major.  A warp owns 16 rows; a CTA owns 16*NW rows
+// of one (request, KV head) and one KV split.  Decode-shaped requests
+// (q_len * Hq/Hkv <= 16) run with NW = 1, longer chunks with NW = 4 so that
+// four warps share each K/V tile.  The per-row instruction sequence is the
+// same in both instantiations (the same `attn_tile` body), so a row's result
+// does not depend on which of them ran it.
+//
+// Traversal (深入解析 Vosti §六 6.2, causal prefix equivalence and the
+// sliding-window traversal; "Deterministic and bit-exact inference",
+// technical section: fixed split *size*).  Keys are cut into splits of
+// S_kv keys and tiles of B_N keys, both aligned to absolute key positions.
+// A row at position p with window lower bound lo = max(0, p-w+1) (lo = 0 for
+// global layers) sees keys [lo, p].  Inside one split it folds the tiles
+// that intersect [lo, p] in ascending order into an online-softmax state
+// (m, l, o); tiles of the CTA's range that hold no visible key for the row
+// leave its state bit-for-bit unchanged (the masking rules of §六 6.2: a
+// masked score is -inf, its weight exactly 0, and a fully masked row keeps
+// its incoming state).  Split partials go to the workspace; the merge
+// kernel folds the splits of each row left to right, always in the same
+// order, with one merge routine, then normalises.  The tile size, split
+// size and fold order depend only on the head dimension (fixed at model
+// creation), never on the batch, q_len, page table or split placement.
+//
+// Numerics: S = Q K^T and O += P V on mma.sync m16n8k16 (bf16 in, fp32
+// accumulate), scores scaled by log2(e)/sqrt(hd), exp2 by ex2.approx,
+// P rounded to bf16 for the P V product and for the row sum, every other
+// float operation an explicitly rounded intrinsic.
+#include <math.h>
+
+#include "vd_device.cuh"
+#include "vd_internal.h"
+
+namespace vd {
+namespace {
+
+template <int HD>
+struct AttnCfg {
+  static constexpr int BNK = (HD >= 256) ? 32 : 64;  // keys per tile
+  static constexpr int PAGES = BNK / 16;             // 16-token pages per tile
+  static constexpr int PAGE_BYTES = 16 * HD * 2;     // one page of one KV head
+  static constexpr int TILE_BYTES = BNK * HD * 2;
+  static constexpr int SMEM = 1024 + 2 * 2 * TILE_BYTES + 64;
+};
+
+// Byte offset of (key, 16-byte chunk along hd) inside a K or V tile staged
+// by the 3-D TMA box (64, hd/64, 16) with the 128-byte swizzle.
+template <int HD>
+__device__ __forceinline__ uint32_t kv_off(int key, int chunk) {
+  const int pg = key >> 4, slot = key & 15;
+  const int lr = slot * (HD / 64) + (chunk >> 3);
+  return pg * AttnCfg<HD>::PAGE_BYTES + lr * 128 + (((chunk & 7) ^ (lr & 7)) << 4);
+}
+
+template <int HD>
+struct RowState {
+  float m[2], l[2];     // rows g and g+8 of the warp
+  float o[HD / 8][4];   // mma C fragments
+};
+
+// One key tile for the 16 rows of a warp.
+template <int HD, int BNK>
+__device__ __forceinline__ void attn_tile(RowState<HD>& st, const uint32_t (&qf)[HD / 16][4], uint32_t kbase,
+                                          uint32_t vbase, int key0, const int (&pos)[2], const int (&lo)[2],
+                                          float scale_log2, int lane) {
+  const int t4 = lane & 3, mi = lane >> 3, r8 = lane & 7;
+  float s[BNK / 8][4];
+#pragma unroll
+  for (int j = 0; j < BNK / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+    for (int jp = 0; jp < BNK / 16; ++jp) {
+      uint32_t b[4];
+      ldmatrix_x4(b, kbase + kv_off<HD>(jp * 16 + (mi >> 1) * 8 + r8, kk * 2 + (mi & 1)));
+      mma_bf16_16816(s[2 * jp], qf[kk], b);
+      mma_bf16_16816(s[2 * jp + 1], qf[kk], b + 2);
+    }
+  }
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int j = 0; j < BNK / 8; ++j) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = e >> 1;
+      const int key = key0 + j * 8 + t4 * 2 + (e & 1);
+      const bool vis = key >= lo[r] && key <= pos[r];
+      const float v = vis ? __fmul_rn(s[j][e], scale_log2) : -INFINITY;
+      s[j][e] = v;
+      mx[r] = fmaxf(mx[r], v);
+    }
+  }
+  float mnew[2], alpha[2];
+  bool rv[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+    rv[r] = mx[r] != -INFINITY;
+    mnew[r] = rv[r] ? fmaxf(st.m[r], mx[r]) : st.m[r];
+    alpha[r] = rv[r] ? ex2(__fsub_rn(st.m[r], mnew[r])) : 1.0f;
+  }
+  uint32_t pa[BNK / 16][4];
+  float rs[2] = {0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < BNK / 8; ++j) {
+    float p[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = e >> 1;
+      p[e] = (s[j][e] == -INFINITY) ? 0.f : bf16_round(ex2(__fsub_rn(s[j][e], mnew[r])));
+    }
+    rs[0] = __fadd_rn(__fadd_rn(rs[0], p[0]), p[1]);
+    rs[1] = __fadd_rn(__fadd_rn(rs[1], p[2]), p[3]);
+    pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p[0], p[1]);
+    pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p[2], p[3]);
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    rs[r] = __fadd_rn(rs[r], __shfl_xor_sync(0xffffffffu, rs[r], 1));
+    rs[r] = __fadd_rn(rs[r], __shfl_xor_sync(0xffffffffu, rs[r], 2));
+    st.l[r] = rv[r] ? __fadd_rn(__fmul_rn(st.l[r], alpha[r]), rs[r]) : st.l[r];
+    st.m[r] = mnew[r];
+  }
+#pragma unroll
+  for (int n = 0; n < HD / 8; ++n) {
+    st.o[n][0] = __fmul_rn(st.o[n][0], alpha[0]);
+    st.o[n][1] = __fmul_rn(st.o[n][1], alpha[0]);
+    st.o[n][2] = __fmul_rn(st.o[n][2], alpha[1]);
+    st.o[n][3] = __fmul_rn(st.o[n][3], alpha[1]);
+  }
+#pragma unroll
+  for (int ks = 0; ks < BNK / 16; ++ks) {
+#pragma unroll
+    for (int np = 0; np < HD / 16; ++np) {
+      uint32_t b[4];
+      ldmatrix_x4_trans(b, vbase + kv_off<HD>(ks * 16 + (mi & 1) * 8 + r8, np * 2 + (mi >> 1)));
+      mma_bf16_16816(st.o[2 * np], pa[ks], b);
+      mma_bf16_16816(st.o[2 * np + 1], pa[ks], b + 2);
+    }
+  }
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+}
+
+template <int HD, int NW>
+__global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ CUtensorMap kvmap, AttnArgs a) {
+  using C = AttnCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 4 * C::TILE_BYTES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+
+  // ---- work item -> (request, row block, KV head, split)
+  const int item = blockIdx.x;
+  int lo_i = 0, hi_i = a.n_cls - 1;
+  while (lo_i < hi_i) {  // last j with cls_start[j] <= item
+    const int mid = (lo_i + hi_i + 1) >> 1;
+    if (a.cls_start[mid] <= item) lo_i = mid; else hi_i = mid - 1;
+  }
+  const int b = a.cls_seq[lo_i];
+  int local = item - a.cls_start[lo_i];
+  const int q0 = a.cu_q[b], qlen = a.cu_q[b + 1] - q0, cached = a.cached_len[b];
+  const int kv_len = cached + qlen;
+  const int G = a.Hq / a.Hkv;
+  const int nsplit = (kv_len - 1) / a.split + 1;
+  const int sidx = local % nsplit;
+  local /= nsplit;
+  const int kvh = local % a.Hkv;
+  const int rb = local / a.Hkv;
+  const int rows = qlen * G;
+  const int r0 = rb * 16 * NW;
+  const int r_end = min(rows, r0 + 16 * NW);
+  const int p_min = cached + r0 / G, p_max = cached + (r_end - 1) / G;
+  const int lo_min = a.window > 0 ? max(0, p_min - a.window + 1) : 0;
+  const int key_lo = max(sidx * a.split, lo_min);
+  const int key_hi = min((sidx + 1) * a.split - 1, p_max);
+  if (key_lo > key_hi) return;  // no visible key of these rows in this split
+  const int tile_lo = key_lo / C::BNK;
+  const int ntiles = key_hi / C::BNK - tile_lo + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int it) {
+    const int stg = it & 1;
+    uint8_t* sk = smem + stg * 2 * C::TILE_BYTES;
+    uint8_t* sv = sk + C::TILE_BYTES;
+    mbar_arrive_expect_tx(&full[stg], 2 * C::TILE_BYTES);
+    const int lp0 = ((tile_lo + it) * C::BNK) >> 4;
+#pragma unroll
+    for (int pg = 0; pg < C::PAGES; ++pg) {
+      const int lp = lp0 + pg;
+      int rk = a.pool_rows, rvw = a.pool_rows;  // outside the pool: zero fill
+      if (lp * 16 < kv_len) {
+        const int phys = a.page_table[static_cast<size_t>(b) * a.pt_stride + lp];
+        rk = a.layer_row0 + ((phys * 2) * a.Hkv + kvh) * 16;
+        rvw = rk + a.Hkv * 16;
+      }
+      tma_load_3d(sk + pg * C::PAGE_BYTES, &kvmap, &full[stg], 0, 0, rk);
+      tma_load_3d(sv + pg * C::PAGE_BYTES, &kvmap, &full[stg], 0, 0, rvw);
+    }
+  };
+  int issued = 0;
+  if (threadIdx.x == 0) {
+    issue(0);
+    issued = 1;
+    if (ntiles > 1) {
+      issue(1);
+      issued = 2;
+    }
+  }
+
+  // ---- this warp's rows
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, t4 = lane & 3;
+  int pos[2], lo[2], tok[2], hq[2];
+  bool valid[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int row = r0 + warp * 16 + gq + 8 * r;
+    valid[r] = row < rows;
+    tok[r] = row / G;
+    hq[r] = kvh * G + row % G;
+    pos[r] = valid[r] ? cached + tok[r] : -1;
+    lo[r] = valid[r] ? (a.window > 0 ? max(0, pos[r] - a.window + 1) : 0) : 1;
+  }
+  uint32_t qf[HD / 16][4];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const __nv_bfloat16* qr = a.q + (static_cast<size_t>(q0 + tok[r]) * a.Hq + hq[r]) * HD;
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      qf[kk][r] = valid[r] ? *reinterpret_cast<const uint32_t*>(qr + kk * 16 + t4 * 2) : 0u;
+      qf[kk][2 + r] = valid[r] ? *reinterpret_cast<const uint32_t*>(qr + kk * 16 + 8 + t4 * 2) : 0u;
+    }
+  }
+  RowState<HD> st;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    st.m[r] = -INFINITY;
+    st.l[r] = 0.f;
+  }
+#pragma unroll
+  for (int n = 0; n < HD / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
+
+  bool ok = true;
+  int it = 0;
+  for (; it < ntiles; ++it) {
+    const int stg = it & 1;
+    if (!mbar_wait(&full[stg], (it >> 1) & 1, abort_flag, a.status)) ok = false;
+    const int key0 = (tile_lo + it) * C::BNK;
+    bool mine = false;  // any row of this warp sees a key of this tile
+#pragma unroll
+    for (int r = 0; r < 2; ++r) mine |= max(lo[r], key0) <= min(pos[r], key0 + C::BNK - 1);
+    mine = __any_sync(0xffffffffu, mine);
+    if (ok && mine) {
+      const uint32_t kb = smem_u32(smem + stg * 2 * C::TILE_BYTES);
+      attn_tile<HD, C::BNK>(st, qf, kb, kb + C::TILE_BYTES, key0, pos, lo, a.scale_log2, lane);
+    }
+    if (__syncthreads_or(!ok)) break;
+    if (threadIdx.x == 0 && it + 2 < ntiles) {
+      issue(it + 2);
+      issued = it + 3;
+    }
+  }
+  if (it < ntiles) {  // gave up: let copies in flight land before leaving
+    if (threadIdx.x == 0)
+      for (int k = it; k < issued; ++k) drain_wait(&full[k & 1], (k >> 1) & 1);
+    return;
+  }
+
+  // ---- split partial of every row that saw a key here
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (!valid[r] || st.m[r] == -INFINITY) continue;
+    const size_t base = (static_cast<size_t>(q0 + tok[r]) * a.Hq + hq[r]) * a.max_splits + sidx;
+    if (t4 == 0) {
+      a.part_ml[base * 2] = st.m[r];
+      a.part_ml[base * 2 + 1] = st.l[r];
+    }
+    float* po = a.part_o + base * HD;
+#pragma unroll
+    for (int n = 0; n < HD / 8; ++n)
+      *reinterpret_cast<float2*>(po + n * 8 + t4 * 2) = make_float2(st.o[n][2 * r], st.o[n][2 * r + 1]);
+  }
+}
+
+// Left-to-right fold of a row's split partials, then o / l -> bf16.
+template <int HD>
+__global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
+  constexpr int PER = HD / 32;
+  const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (w >= a.T * a.Hq) return;
+  const int tok = w / a.Hq, h = w % a.Hq;
+  const int p = a.positions[tok];
+  const int lo = a.window > 0 ? max(0, p - a.window + 1) : 0;
+  const int s0 = lo / a.split, s1 = p / a.split;
+  const size_t base = (static_cast<size_t>(tok) * a.Hq + h) * a.max_splits;
+  float M = a.part_ml[(base + s0) * 2], L = a.part_ml[(base + s0) * 2 + 1];
+  float O[PER];
+  const float* po = a.part_o + (base + s0) * HD + lane * PER;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) O[i] = po[i];
+  for (int s = s0 + 1; s <= s1; ++s) {
+    const float m = a.part_ml[(base + s) * 2], l = a.part_ml[(base + s) * 2 + 1];
+    const float mn = fmaxf(M, m);
+    const float ca = ex2(__fsub_rn(M, mn)), cb = ex2(__fsub_rn(m, mn));
+    L = __fadd_rn(__fmul_rn(L, ca), __fmul_rn(l, cb));
+    const float* ps = a.part_o + (base + s) * HD + lane * PER;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) O[i] = __fadd_rn(__fmul_rn(O[i], ca), __fmul_rn(ps[i], cb));
+    M = mn;
+  }
+  __nv_bfloat16* out = a.out + (static_cast<size_t>(tok) * a.Hq + h) * HD + lane * PER;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) out[i] = __float2bfloat16_rn(__fdiv_rn(O[i], L));
+}
+
+template <int HD, int NW>
+int launch_attn_t(const CUtensorMap& kvmap, const AttnArgs& a, int n_items, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    VD_CUDA_TRY(cudaFuncSetAttribute(attn_kernel<HD, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     AttnCfg<HD>::SMEM));
+    configured = true;
+  }
+  attn_kernel<HD, NW><<<n_items, NW * 32, AttnCfg<HD>::SMEM, s>>>(kvmap, a);
+  VD_CUDA_TRY(cudaGetLastError());
+  return VD_OK;
+}
+
+}  // namespace
+
+int attn_key_tile(int hd) { return hd >= 256 ? AttnCfg<256>::BNK : AttnCfg<128>::BNK; }
+
+int launch_attention(const CUtensorMap& kvmap, const AttnArgs& a, int hd, bool prefill_class, int n_items,
+                     cudaStream_t s) {
+  if (n_items <= 0) return VD_OK;
+  if (hd == 64) return prefill_class ? launch_attn_t<64, 4>(kvmap, a, n_items, s) : launch_attn_t<64, 1>(kvmap, a, n_items, s);
+  if (hd == 128) return prefill_class ? launch_attn_t<128, 4>(kvmap, a, n_items, s) : launch_attn_t<128, 1>(kvmap, a, n_items, s);
+  if (hd == 256) return prefill_class ? launch_attn_t<256, 4>(kvmap, a, n_items, s) : launch_attn_t<256, 1>(kvmap, a, n_items, s);
+  return fail(VD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+}
+
+int launch_merge(const MergeArgs& a, int hd, cudaStream_t s) {
+  const int warps = a.T * a.Hq;
+  if (warps <= 0) return VD_OK;
+  const int blocks = (warps + 3) / 4;
+  if (hd == 64) merge_kernel<64><<<blocks, 128, 0, s>>>(a);
+  else if (hd == 128) merge_kernel<128><<<blocks, 128, 0, s>>>(a);
+  else if (hd == 256) merge_kernel<256><<<blocks, 128, 0, s>>>(a);
+  else return fail(VD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+  VD_CUDA_TRY(cudaGetLastError());
+  return VD_OK;
+}
+
+}  // namespace vd

@@ -1,0 +1,166 @@
+// Bandwidth-bound row kernels of the step: embedding gather, RMSNorm,
+// RoPE + K/V scatter into the paged pool, and the debug K/V gather.
+//
+// Batch invariance ("Deterministic and bit-exact inference", technical
+// section: batch-invariant RMSNorm): every reduction here runs inside one
+// warp over one row, lane l summing elements l, l+32, ... (in 8-element
+// chunks) in ascending order, followed by a fixed xor butterfly, so the
+// result of a row depends on that row and the model dimension only.
+#include "vd_device.cuh"
+#include "vd_internal.h"
+
+namespace vd {
+namespace {
+
+__global__ void embed_kernel(const uint4* __restrict__ E, const int* __restrict__ tok, uint4* __restrict__ x,
+                             int d8) {
+  const int t = blockIdx.x;
+  const size_t src = static_cast<size_t>(tok[t]) * d8;
+  for (int c = threadIdx.x; c < d8; c += blockDim.x) x[static_cast<size_t>(t) * d8 + c] = E[src + c];
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_lo(w[i]);
+    f[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+
+__device__ __forceinline__ float warp_sum_fixed(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// y[r] = bf16(x[row_idx[r]] * (1 / sqrt(mean(x^2) + eps)) * w)
+__global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ row_idx,
+                               const __nv_bfloat16* __restrict__ w, __nv_bfloat16* __restrict__ y, int rows, int d,
+                               float eps) {
+  const int r = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const int src = row_idx ? row_idx[r] : r;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(src) * d);
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  uint4* yr = reinterpret_cast<uint4*>(y + static_cast<size_t>(r) * d);
+  const int d8 = d >> 3;
+  float ss = 0.f;
+  for (int c = lane; c < d8; c += 32) {
+    float f[8];
+    unpack8(xr[c], f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(f[i], f[i]));
+  }
+  ss = warp_sum_fixed(ss);
+  const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(d)), eps)));
+  for (int c = lane; c < d8; c += 32) {
+    float f[8], g[8];
+    unpack8(xr[c], f);
+    unpack8(wr[c], g);
+    uint4 o;
+    o.x = pack_bf16x2(__fmul_rn(__fmul_rn(f[0], inv), g[0]), __fmul_rn(__fmul_rn(f[1], inv), g[1]));
+    o.y = pack_bf16x2(__fmul_rn(__fmul_rn(f[2], inv), g[2]), __fmul_rn(__fmul_rn(f[3], inv), g[3]));
+    o.z = pack_bf16x2(__fmul_rn(__fmul_rn(f[4], inv), g[4]), __fmul_rn(__fmul_rn(f[5], inv), g[5]));
+    o.w = pack_bf16x2(__fmul_rn(__fmul_rn(f[6], inv), g[6]), __fmul_rn(__fmul_rn(f[7], inv), g[7]));
+    yr[c] = o;
+  }
+}
+
+// One warp per (token, head).  Lane l owns the rotate-half pairs
+// (i, i + hd/2) for i = l, l+32, ...  q heads -> q_out, k heads -> pool K
+// slot, v heads -> pool V slot of the token's (page, position % 16).
+constexpr int kRopeWarps = 8;
+__global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_kernel(RopeArgs a) {
+  const int t = blockIdx.x;
+  const int head = blockIdx.y * kRopeWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int nh = a.Hq + 2 * a.Hkv;
+  if (head >= nh) return;
+  const int hd = a.hd, half = hd >> 1;
+  const __nv_bfloat16* src = a.qkv + (static_cast<size_t>(t) * nh + head) * hd;
+  const int p = a.positions[t];
+  const size_t page = static_cast<size_t>(a.slot_page[t]);
+  const int slot = p & 15;
+  if (head >= a.Hq + a.Hkv) {  // v: plain copy
+    const int g = head - a.Hq - a.Hkv;
+    __nv_bfloat16* dst = a.pool + a.layer_elem0 + ((page * 2 + 1) * a.Hkv + g) * 16 * hd + slot * hd;
+    for (int i = lane; i < hd; i += 32) dst[i] = src[i];
+    return;
+  }
+  const bool is_q = head < a.Hq;
+  float x1[4], x2[4];
+  const int np = (half + 31) / 32;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = lane + 32 * k;
+    x1[k] = (k < np && i < half) ? __bfloat162float(src[i]) : 0.f;
+    x2[k] = (k < np && i < half) ? __bfloat162float(src[i + half]) : 0.f;
+  }
+  const __nv_bfloat16* nw = is_q ? a.q_norm : a.k_norm;
+  if (nw) {  // per-head RMSNorm (QK-norm), rounded to bf16 before RoPE
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      ss = __fadd_rn(ss, __fmul_rn(x1[k], x1[k]));
+      ss = __fadd_rn(ss, __fmul_rn(x2[k], x2[k]));
+    }
+    ss = warp_sum_fixed(ss);
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(hd)), a.eps)));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = lane + 32 * k;
+      if (k < np && i < half) {
+        x1[k] = bf16_round(__fmul_rn(__fmul_rn(x1[k], inv), __bfloat162float(nw[i])));
+        x2[k] = bf16_round(__fmul_rn(__fmul_rn(x2[k], inv), __bfloat162float(nw[i + half])));
+      }
+    }
+  }
+  __nv_bfloat16* dst;
+  if (is_q) {
+    dst = a.q_out + (static_cast<size_t>(t) * a.Hq + head) * hd;
+  } else {
+    const int g = head - a.Hq;
+    dst = a.pool + a.layer_elem0 + ((page * 2 + 0) * a.Hkv + g) * 16 * hd + slot * hd;
+  }
+  const float* ct = a.cos_t + static_cast<size_t>(p) * half;
+  const float* st = a.sin_t + static_cast<size_t>(p) * half;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = lane + 32 * k;
+    if (k < np && i < half) {
+      const float c = ct[i], s = st[i];
+      dst[i] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(x1[k], c), __fmul_rn(x2[k], s)));
+      dst[i + half] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(x2[k], c), __fmul_rn(x1[k], s)));
+    }
+  }
+}
+
+}  // namespace
+
+int launch_embed(const void* embed, const int* tokens, void* x, int T, int d, cudaStream_t s) {
+  if (T <= 0) return VD_OK;
+  embed_kernel<<<T, 128, 0, s>>>(static_cast<const uint4*>(embed), tokens, static_cast<uint4*>(x), d / 8);
+  VD_CUDA_TRY(cudaGetLastError());
+  return VD_OK;
+}
+
+int launch_rmsnorm(const void* x, const int* row_idx, const void* w, void* y, int rows, int d, float eps,
+                   cudaStream_t s) {
+  if (rows <= 0) return VD_OK;
+  rmsnorm_kernel<<<(rows + 3) / 4, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(x), row_idx,
+                                                static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(y),
+                                                rows, d, eps);
+  VD_CUDA_TRY(cudaGetLastError());
+  return VD_OK;
+}
+
+int launch_rope_kv(const RopeArgs& a, cudaStream_t s) {
+  if (a.T <= 0) return VD_OK;
+  const int nh = a.Hq + 2 * a.Hkv;
+  dim3 grid(a.T, (nh + kRopeWarps - 1) / kRopeWarps);
+  rope_kv_kernel<<<grid, kRopeWarps * 32, 0, s>>>(a);
+  VD_CUDA_TRY(cudaGetLastError());
+  return VD_OK;
+}
+
+}  // namespace vd

@@ -1,0 +1,213 @@
+// Batch-invariant bf16 GEMM on 5th-generation tensor cores (tcgen05).
+//
+// acc[t][n] = sum_k X[t][k] * W[n][k], fp32 accumulation in TMEM.  The
+// weight matrix is the MMA's A operand (M = 128 weight rows per tile) and
+// the tokens are its N dimension (N = 128 per tile), so decode batches of
+// any size stream each weight tile exactly once per 128 tokens.  Every
+// launch, whatever the number of tokens T, uses the same instruction shape
+// (M=128, N=128, K=16), the same K order (stage by stage, 4 MMAs of K=16 per
+// 64-wide stage) and no split-K: column t of D depends only on row t of X and
+// on W, which is the matmul contract of 深入解析 Vosti §六 6.1 (row x of a
+// batched run equals the singleton run bit for bit; zero-initialised
+// accumulator, same iteration order).
+//
+// Warp roles (192 threads): warp 0 issues TMA loads (one elected lane) and
+// owns the TMEM allocation; warp 1 issues tcgen05.mma (one lane); warps 2..5
+// read the accumulator from TMEM (warp w reaches lanes 32*(w%4)..+31) and run
+// the fused epilogue.  Every wait is bounded (see vd_device.cuh).
+#include "vd_device.cuh"
+#include "vd_internal.h"
+
+namespace vd {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kAStageBytes = kGemmBM * kGemmBK * 2;
+constexpr int kBStageBytes = kGemmBN * kGemmBK * 2;
+constexpr int kXchgFloats = 64 * 33;  // GLU: up-half values handed to the gate-half warps
+constexpr int kSmemBytes = 1024 + kStages * (kAStageBytes + kBStageBytes) + kXchgFloats * 4 + 256;
+
+__device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+__device__ __forceinline__ float gelu_tanh_f(float g) {
+  const float g3 = __fmul_rn(__fmul_rn(g, g), g);
+  const float inner = __fmul_rn(0.7978845608028654f, __fadd_rn(g, __fmul_rn(0.044715f, g3)));
+  return __fmul_rn(__fmul_rn(0.5f, g), __fadd_rn(1.0f, tanhf(inner)));
+}
+
+__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Waits without looking at the abort flag (used only on the teardown path to
+// let copies and MMAs already in flight finish before the CTA exits).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kAStageBytes;
+  float* xchg = reinterpret_cast<float*>(sB + kStages * kBStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(xchg + kXchgFloats);
+  uint64_t* empty = full + kStages;
+  uint64_t* accum = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  constexpr bool kGlu = (EPI == EPI_SWIGLU || EPI == EPI_GEGLU);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_t = blockIdx.x, tile_n = blockIdx.y;
+  const int KB = args.K / kGemmBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&wmap);
+    tma_prefetch_desc(&xmap);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kGemmBN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  int issued = 0;  // producer: stages loaded so far
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % kStages;
+        if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, abort_flag, args.status)) break;
+        mbar_arrive_expect_tx(&full[s], kAStageBytes + kBStageBytes);
+        uint8_t* a = sA + s * kAStageBytes;
+        if (kGlu) {
+          tma_load_2d(a, &wmap, &full[s], kb * kGemmBK, tile_n * 64);
+          tma_load_2d(a + 64 * 128, &wmap, &full[s], kb * kGemmBK, args.glu_up_row + tile_n * 64);
+        } else {
+          tma_load_2d(a, &wmap, &full[s], kb * kGemmBK, tile_n * kGemmBM);
+        }
+        tma_load_2d(sB + s * kBStageBytes, &xmap, &full[s], kb * kGemmBK, tile_t * kGemmBN);
+        issued = kb + 1;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(kGemmBM, kGemmBN);
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % kStages;
+        if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag, args.status)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + s * kAStageBytes);
+        const uint32_t b0 = smem_u32(sB + s * kBStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < kGemmBK / 16; ++kk)
+          umma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (kb | kk) != 0);
+        umma_commit(&empty[s]);
+      }
+      umma_commit(accum);  // fires once every issued MMA has completed
+    }
+  } else {
+    const int lg = warp & 3;  // TMEM lane group reachable by this warp
+    const bool ok = mbar_wait(accum, 0, abort_flag, args.status);
+    tc_fence_after();
+    if (ok) {
+      const int row = lg * 32 + lane;  // tile row == TMEM lane
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(lg * 32) << 16);
+      for (int c = 0; c < kGemmBN / 32; ++c) {
+        const int t0 = tile_t * kGemmBN + c * 32;
+        if (t0 >= args.T) break;  // uniform over the four epilogue warps
+        float v[32];
+        tmem_ld32(taddr + c * 32, v);
+        const int nt = min(32, args.T - t0);
+        if (EPI == EPI_F32) {
+          float* out = static_cast<float*>(args.out) + tile_n * kGemmBM + row;
+          for (int j = 0; j < nt; ++j) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
+        } else if (EPI == EPI_BF16) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * kGemmBM + row;
+          for (int j = 0; j < nt; ++j) out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(v[j]);
+        } else if (EPI == EPI_RESIDUAL) {
+          const size_t col = static_cast<size_t>(tile_n) * kGemmBM + row;
+          const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(args.residual) + col;
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + col;
+          for (int j = 0; j < nt; ++j) {
+            const size_t o = static_cast<size_t>(t0 + j) * args.ldo;
+            const float r = __bfloat162float(res[o]);
+            out[o] = __float2bfloat16_rn(__fadd_rn(bf16_round(v[j]), r));
+          }
+        } else {  // GLU: rows 0..63 gate, 64..127 up of the same 64 features
+          if (lg >= 2) {
+            float* xr = xchg + ((lg - 2) * 32 + lane) * 33;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) xr[j] = bf16_round(v[j]);
+          }
+          epi_barrier();
+          if (lg < 2) {
+            const float* xr = xchg + (lg * 32 + lane) * 33;
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * 64 + lg * 32 + lane;
+            for (int j = 0; j < nt; ++j) {
+              const float g = bf16_round(v[j]);
+              const float a = (EPI == EPI_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
+              out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fmul_rn(a, xr[j]));
+            }
+          }
+          epi_barrier();
+        }
+      }
+    }
+  }
+
+  // Teardown: let in-flight TMA copies land and issued MMAs finish, then
+  // release TMEM.  On the normal path these waits return at once.
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    for (int kb = max(0, issued - kStages); kb < issued; ++kb) drain_wait(&full[kb % kStages], (kb / kStages) & 1);
+  }
+  if (warp == 1 && lane == 0 && *abort_flag) drain_wait(accum, 0);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kGemmBN);
+  }
+}
+
+template <int EPI>
+int launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, const GemmArgs& a, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    VD_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+    configured = true;
+  }
+  dim3 grid((a.T + kGemmBN - 1) / kGemmBN, n_tiles);
+  gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(wmap, xmap, a);
+  VD_CUDA_TRY(cudaGetLastError());
+  return VD_OK;
+}
+
+}  // namespace
+
+int launch_gemm(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, const GemmArgs& a, int epi,
+                cudaStream_t s) {
+  if (a.T <= 0) return VD_OK;
+  switch (epi) {
+    case EPI_BF16: return launch_one<EPI_BF16>(wmap, xmap, n_tiles, a, s);
+    case EPI_RESIDUAL: return launch_one<EPI_RESIDUAL>(wmap, xmap, n_tiles, a, s);
+    case EPI_F32: return launch_one<EPI_F32>(wmap, xmap, n_tiles, a, s);
+    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(wmap, xmap, n_tiles, a, s);
+    case EPI_GEGLU: return launch_one<EPI_GEGLU>(wmap, xmap, n_tiles, a, s);
+    default: return fail(VD_ERR_INVALID_ARG, "unknown GEMM epilogue");
+  }
+}
+
+}  // namespace vd

@@ -1,0 +1,110 @@
+// Host-side declarations shared by the translation units of libvd.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "vd.h"
+#include "vd_ops.h"
+
+namespace vd {
+
+// ---------------------------------------------------------------- errors
+void set_error(const std::string& msg);
+int fail(int code, const std::string& msg);
+#define VD_CUDA_TRY(expr)                                                          \
+  do {                                                                             \
+    cudaError_t e_ = (expr);                                                       \
+    if (e_ != cudaSuccess)                                                         \
+      return ::vd::fail(VD_ERR_CUDA, std::string(#expr) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+// ---------------------------------------------------------------- TMA maps
+// 2-D bf16 map over a row-major [rows][cols] matrix; box = box_rows x 64
+// columns (128 bytes), 128-byte swizzle, zero fill outside the matrix.
+int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// 3-D bf16 map for the KV pool: dims (64, hd/64, rows), box (64, hd/64, 16).
+int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd);
+
+// ---------------------------------------------------------------- GEMM
+enum Epilogue { EPI_BF16 = 0, EPI_RESIDUAL = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_GEGLU = 4 };
+constexpr int kGemmBM = 128;  // weight rows per tile (MMA M)
+constexpr int kGemmBN = 128;  // tokens per tile (MMA N), one shape for every T
+constexpr int kGemmBK = 64;   // K per pipeline stage (one 128-byte swizzle row)
+
+struct GemmArgs {
+  void* out;             // [T][ldo] bf16 (or fp32 for EPI_F32)
+  const void* residual;  // [T][ldo] bf16 (EPI_RESIDUAL; may alias out)
+  int T;                 // valid tokens
+  int K;                 // reduction length
+  int ldo;               // output row stride (elements)
+  int glu_up_row;        // GLU: first row of the up half in the weight matrix (= F)
+  int* status;           // device status word
+};
+// A = weight map (box 128 rows, or 64 for GLU), B = activation map (box 128 rows).
+int launch_gemm(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, const GemmArgs& a, int epi,
+                cudaStream_t s);
+
+// ---------------------------------------------------------------- attention
+struct AttnArgs {
+  const __nv_bfloat16* q;  // [T][Hq][hd]
+  float* part_o;           // [T][Hq][max_splits][hd]
+  float* part_ml;          // [T][Hq][max_splits][2]
+  const int* cu_q;         // [B+1]
+  const int* cached_len;   // [B]
+  const int* page_table;   // [B][pt_stride]
+  const int* cls_seq;      // seqs of this launch class
+  const int* cls_start;    // [n + 1] item prefix sums
+  int n_cls;
+  int pt_stride;
+  int Hq, Hkv;
+  int layer_row0;          // first pool row of this layer
+  int pool_rows;           // total pool rows (zero-fill coordinate)
+  int window;              // 0: global
+  int split;               // S_kv keys
+  int max_splits;
+  float scale_log2;        // log2(e) / sqrt(hd)
+  int* status;
+};
+struct MergeArgs {
+  const float* part_o;
+  const float* part_ml;
+  __nv_bfloat16* out;      // [T][Hq][hd]
+  const int* positions;    // [T]
+  int T, Hq, window, split, max_splits;
+};
+int attn_key_tile(int hd);
+// Items of one sequence (both host and device use the same formula).
+int launch_attention(const CUtensorMap& kvmap, const AttnArgs& a, int hd, bool prefill_class, int n_items,
+                     cudaStream_t s);
+int launch_merge(const MergeArgs& a, int hd, cudaStream_t s);
+
+// ---------------------------------------------------------------- elementwise
+int launch_embed(const void* embed, const int* tokens, void* x, int T, int d, cudaStream_t s);
+int launch_rmsnorm(const void* x, const int* row_idx, const void* w, void* y, int rows, int d, float eps,
+                   cudaStream_t s);
+struct RopeArgs {
+  const __nv_bfloat16* qkv;   // [T][(Hq+2Hkv) hd]
+  __nv_bfloat16* q_out;       // [T][Hq][hd]
+  __nv_bfloat16* pool;        // pool base
+  const int* positions;       // [T]
+  const int* slot_page;       // [T] physical page of the token's slot
+  const float* cos_t;         // [max_ctx][hd/2]
+  const float* sin_t;
+  const __nv_bfloat16* q_norm;  // nullable
+  const __nv_bfloat16* k_norm;
+  float eps;
+  int T, Hq, Hkv, hd;
+  long long layer_elem0;      // first element of this layer in the pool
+};
+int launch_rope_kv(const RopeArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- sampling
+int launch_sample(const float* logits, int R, int V, const vd_sampler* dev_params, int* out, cudaStream_t s);
+int launch_philox(uint64_t seed, uint64_t step, int n, uint32_t* out, cudaStream_t s);
+
+}  // namespace vd

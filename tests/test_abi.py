@@ -1,0 +1,54 @@
+"""The C-ABI library builds, loads and exports every declared symbol (CPU)."""
+
+import ctypes
+
+import pytest
+
+from invariant_vd_step_gb300 import build, vd
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return vd.lib()
+
+
+def test_exports_every_header_symbol(L):
+    names = vd.header_symbols()
+    assert {"vd_create_model", "vd_kv_pool_alloc", "vd_step", "vd_sample"} <= names
+    raw = ctypes.CDLL(build.LIB)
+    missing = [n for n in sorted(names) if not hasattr(raw, n)]
+    assert not missing, missing
+    assert names == set(vd._SIGS), names ^ set(vd._SIGS)
+    assert L.vd_version().decode().startswith("vd ")
+
+
+def test_create_model_rejects_unsupported_shapes_before_any_cuda_call(L):
+    from invariant_vd_step_gb300 import synth
+    lw = (vd.LayerWeights * 2)()
+    for i in range(2):
+        lw[i] = vd.LayerWeights(*([16] * 8))
+    w = vd.WeightPtrs(16, lw, 16, 16)
+    h = ctypes.c_void_p()
+    bad = [
+        (synth.TINY.with_(head_dim=96), vd.ERRORS and 2),       # head_dim
+        (synth.TINY.with_(page_size=32), 2),                     # page size
+        (synth.TINY.with_(d_model=200), 2),                      # no GEMM tiling
+        (synth.TINY.with_(n_kv_heads=3), 1),                     # Hq % Hkv
+    ]
+    for spec, code in bad:
+        cfg = vd.config_of(spec, 64, 4, 8, 256)
+        assert L.vd_create_model(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == code
+        assert L.vd_last_error()
+    assert L.vd_create_model(None, None, None) == 1
+
+
+def test_ops_validate_arguments(L):
+    assert L.vd_op_gemm(None, None, None, 1, 128, 64, 0, None, None) == 1
+    assert L.vd_op_gemm(16, 16, 16, 1, 100, 64, 0, None, None) == 2      # N not a tile multiple
+    assert L.vd_op_gemm(16, 16, 16, 1, 128, 64, 1, None, None) == 1      # residual missing
+    assert L.vd_op_gemm(16, 16, 16, 1, 128, 64, 9, None, None) == 1      # unknown epilogue
+    assert L.vd_op_rmsnorm(16, 16, 16, 4, 12, 1e-5, None) == 1           # d % 8
+    assert L.vd_op_philox(1, 2, -1, None, None) == 1
+    assert L.vd_sample(None, None, 1, None, None, None) == 1
+    assert L.vd_step(None, None, None, None, None) == 1

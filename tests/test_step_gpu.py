@@ -1,0 +1,155 @@
+"""End-to-end engine step through the C ABI: oracle parity and invariance."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_logits_close, bits, f64, ready
+from invariant_vd_step_gb300 import synth, vd
+from oracle.decoder import OracleDecoder
+
+pytestmark = pytest.mark.gpu
+
+GEMMA_TINY = synth.ModelSpec("gemma-tiny", 3, 256, 2, 1, 256, 512, 512, act="geglu", qk_norm=True,
+                             rope_theta=1e6, rope_theta_local=1e4, sliding_window=24, local_global_period=2)
+LLAMA_TINY128 = synth.ModelSpec("llama-tiny-128", 2, 512, 8, 2, 128, 1024, 1024, rope_theta=5e5,
+                                rope_theta_local=5e5)
+
+
+class Runner:
+    """Runs teacher-forced schedules of chunks; pages handed out from a permutation."""
+
+    def __init__(self, spec, seed=0, gain_std=0.1, num_pages=256, zero=False, max_tokens=512):
+        self.spec = spec
+        self.Wc = synth.make_weights(spec, seed=seed, gain_std=gain_std, zero=zero)
+        self.W = {k: v.cuda() for k, v in self.Wc.items()}
+        self.model = vd.Model(spec, self.W, max_tokens=max_tokens, max_seqs=32, max_logit_rows=max_tokens,
+                              max_context=1024)
+        self.pool = vd.KVPool(self.model, num_pages)
+        self.num_pages = num_pages
+
+    def execute(self, histories, steps, perm_seed=None):
+        """steps: list of lists of (request, n_new_tokens).  Returns {(r, pos): logits bits row}."""
+        perm = synth.page_permutation(self.num_pages, seed=perm_seed) if perm_seed is not None \
+            else np.arange(self.num_pages, dtype=np.int32)
+        nxt = 0
+        tables = {r: [] for r in range(len(histories))}
+        done = {r: 0 for r in range(len(histories))}
+        out = {}
+        for step in steps:
+            seqs, keys = [], []
+            for r, n in step:
+                c = done[r]
+                need = (c + n + 15) // 16
+                while len(tables[r]) < need:
+                    tables[r].append(int(perm[nxt]))
+                    nxt += 1
+                seqs.append((histories[r][c:c + n], c, np.array(tables[r], np.int32)))
+                keys += [(r, c + i) for i in range(n)]
+                done[r] = c + n
+            T = len(keys)
+            logits = torch.full((T, self.spec.vocab), float("nan"), device="cuda")
+            self.model.step(self.pool, vd.StepBatch(seqs, logit_rows=range(T)), logits)
+            torch.cuda.synchronize()
+            for i, k in enumerate(keys):
+                out[k] = logits[i].clone()
+        self.tables = tables
+        return out
+
+    def oracle_all(self, history):
+        return OracleDecoder(self.spec, synth.weights_to_numpy(self.Wc)).forward_all(history)
+
+
+@pytest.mark.parametrize("spec", [synth.TINY, GEMMA_TINY, LLAMA_TINY128], ids=lambda s: s.name)
+def test_step_logits_vs_oracle(spec):
+    ready()
+    run = Runner(spec, seed=1)
+    hist = synth.make_prompts(3, 20, 70, spec.vocab, seed=2)
+    hist = [np.concatenate([h, synth.make_tokens(5, spec.vocab, seed=10 + i)]) for i, h in enumerate(hist)]
+    L = [len(h) for h in hist]
+    steps = [[(0, L[0] - 5), (1, 16)], [(1, L[1] - 21), (2, L[2] - 5)]]
+    steps += [[(0, 1), (1, 1), (2, 1)] for _ in range(5)]
+    res = run.execute(hist, steps, perm_seed=3)
+    for r, h in enumerate(hist):
+        ref = run.oracle_all(h)
+        got = np.stack([f64(res[(r, p)]) for p in range(len(h))])
+        assert_logits_close(got, ref)
+
+
+def test_zero_model_gives_zero_logits_bitwise():
+    ready()
+    run = Runner(synth.TINY, zero=True)
+    hist = synth.make_prompts(2, 10, 40, synth.TINY.vocab, seed=4)
+    res = run.execute(hist, [[(0, len(hist[0])), (1, len(hist[1]))]])
+    for row in res.values():
+        assert torch.all(row == 0)
+
+
+def test_invariance_across_batching_chunking_and_pages():
+    # Definition 2.1: per-request logit views are equal bit for bit whatever
+    # the batch composition, chunk budget, prefill/decode split and pages.
+    ready()
+    spec = synth.TINY
+    hist = synth.make_prompts(4, 30, 60, spec.vocab, seed=5, shared_prefix=32, n_sharing=2)
+    L = [len(h) for h in hist]
+    schedules = [
+        ([[(r, L[r])] for r in range(4)], None),                                  # one request at a time
+        ([[(r, L[r]) for r in range(4)]], 1),                                     # all in one step
+        ([[(r, 16) for r in range(4)]] + [[(r, L[r] - 16) for r in range(4)]], 2),  # chunk 16 then rest
+        ([[(0, 5), (1, 30)], [(0, L[0] - 5), (2, L[2])], [(1, L[1] - 30), (3, L[3] - 1)], [(3, 1)]], 3),
+        ([[(r, 1)] for r in range(4) for _ in range(1)] + [[(r, L[r] - 1) for r in (2, 0, 3, 1)]], 4),
+    ]
+    ref = None
+    for steps, seed in schedules:
+        run = Runner(spec, seed=7, num_pages=64)
+        res = run.execute(hist, steps, perm_seed=seed)
+        b = {k: bits(v) for k, v in res.items()}
+        if ref is None:
+            ref = b
+            continue
+        for k in ref:
+            np.testing.assert_array_equal(b[k], ref[k], err_msg=f"row {k}")
+
+
+def test_kv_written_by_chunked_and_whole_prefill_is_bitwise_equal():
+    # KV-value invariant: the slot of position p holds fKV(W, h, p) however
+    # the prefix was scheduled.
+    ready()
+    spec = synth.TINY
+    h = synth.make_tokens(90, spec.vocab, seed=8)
+    kv = []
+    for steps in ([[(0, 90)]], [[(0, 7)], [(0, 40)], [(0, 43)]]):
+        run = Runner(spec, seed=9, num_pages=32)
+        run.execute([h], steps, perm_seed=len(steps))
+        per_layer = []
+        for layer in range(spec.n_layers):
+            k = torch.empty((90, spec.n_kv_heads, spec.head_dim), dtype=torch.bfloat16, device="cuda")
+            v = torch.empty_like(k)
+            run.model.copy_kv(run.pool, layer, run.tables[0], 90, k, v)
+            torch.cuda.synchronize()
+            per_layer.append((bits(k), bits(v)))
+        kv.append(per_layer)
+    for (ka, va), (kb, vb) in zip(*kv):
+        np.testing.assert_array_equal(ka, kb)
+        np.testing.assert_array_equal(va, vb)
+
+
+def test_descriptor_validation_rejects_bad_steps():
+    ready()
+    run = Runner(synth.TINY, num_pages=8)
+    lg = torch.empty((4, synth.TINY.vocab), device="cuda")
+    m, p = run.model, run.pool
+    cases = [
+        (vd.StepBatch([(np.array([1, 2]), 0, np.array([99]))], [0]), 3),        # page id out of range
+        (vd.StepBatch([(np.array([1, 5000]), 0, np.array([1]))], [0]), 3),      # token id out of range
+        (vd.StepBatch([(np.array([1] * 20), 0, np.array([1]))], [0]), 3),       # page table too narrow
+        (vd.StepBatch([(np.array([1]), 0, np.array([1])), (np.array([2]), 0, np.array([1]))], [0]), 1),  # slot clash
+        (vd.StepBatch([(np.array([1]), 0, np.array([1]))], [5]), 3),            # logit row out of range
+    ]
+    for b, code in cases:
+        with pytest.raises(vd.VDError) as e:
+            m.step(p, b, lg)
+        assert e.value.code == code
+    m.step(p, vd.StepBatch([]), lg)  # empty step is a no-op
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
