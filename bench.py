@@ -1,0 +1,376 @@
+"""Decode benchmark of the batch-invariant step on the Llama-3.1-8B shape.
+
+Workload (one step = one pass of the whole hot path): one decoder layer of
+the Llama-3.1-8B shape plus the LM head (d 4096, 32 q / 8 kv heads, hd 128,
+SwiGLU 14336, vocab 128256), random-init bf16 weights N(0, 0.02), a pure
+decode batch of B requests (default 256) whose cached contexts are
+U[512, 8192] tokens, KV page size 16 with physical pages randomly permuted.
+Each step: descriptor upload + validation, embedding, RMSNorm, QKV GEMM,
+RoPE + KV write, paged attention + split merge, O GEMM + residual,
+RMSNorm, gate/up GEMM + SwiGLU, down GEMM + residual, final norm, LM head
+(fp32 logits), greedy token choice.  The cached K/V is seeded random
+N(0, 1) bf16 (timing is independent of the values); each step appends one
+token per request.
+
+  value  -- decode tokens/s with inputs resident in HBM (device time, CUDA
+            events on the launching stream, max over ranks).
+  e2e    -- the same through the public API with host buffers: every step
+            feeds the previous step's sampled tokens back, uploads the host
+            descriptor and reads the sampled tokens back to the host.
+
+Usage: python bench.py [--gpus N --steps K --warmup W --batch B]
+       python bench.py --impl reference ...   (the CPU oracle, bounded sample)
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s (Llama-8B shape, 1 GB300)"
+UNIT = "tok/s"
+CTX_LO, CTX_HI = 512, 8192
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), float(f[3]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        power_med = statistics.median(r[2] for r in rows)
+        loaded = [r for r in rows if r[2] >= 0.5 * max(r[2] for r in rows)] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "power_w_median": power_med}
+
+
+def make_workload(B: int, steps: int, seed_ctx: int = 3):
+    from invariant_vd_step_gb300 import synth
+    spec = synth.LLAMA8B_1L
+    ctx = synth.make_context_lengths(B, CTX_LO, CTX_HI, seed=seed_ctx)
+    need = [(int(c) + steps + 15) // 16 for c in ctx]
+    num_pages = int(sum(need))
+    perm = synth.page_permutation(num_pages, seed=2)
+    tables, k = [], 0
+    for n in need:
+        tables.append(perm[k:k + n].copy())
+        k += n
+    return spec, ctx, tables, num_pages
+
+
+def algorithmic_bytes(spec, ctx_lens, B):
+    """Per decode step: weights + KV read/write + activations, and per kernel."""
+    d, hd, Hq, Hkv, F, V = spec.d_model, spec.head_dim, spec.n_heads, spec.n_kv_heads, spec.ffn_dim, spec.vocab
+    L = spec.n_layers
+    kv_tok = 2 * Hkv * hd * 2  # K+V bytes per token per layer
+    attn = L * (int(np.sum(ctx_lens + 1)) * kv_tok + B * Hq * hd * 2)  # K/V read incl. the new token + q read
+    w_layer = (spec.qkv_dim * d + d * spec.attn_dim + 2 * F * d + d * F) * 2 + 2 * d * 2
+    lm = V * d * 2
+    kernels = {
+        "attention": attn,
+        "gemm_qkv": L * (spec.qkv_dim * d * 2 + B * (d + spec.qkv_dim) * 2),
+        "gemm_o": L * (d * spec.attn_dim * 2 + B * (spec.attn_dim + 2 * d) * 2),
+        "gemm_gate_up": L * (2 * F * d * 2 + B * (d + F) * 2),
+        "gemm_down": L * (d * F * 2 + B * (F + 2 * d) * 2),
+        "gemm_lm_head": lm + B * (d * 2 + V * 4),
+    }
+    total = L * w_layer + lm + attn + L * B * kv_tok + B * V * 4
+    return total, kernels
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    import __graft_entry__
+    __graft_entry__.build()
+    from invariant_vd_step_gb300 import synth, vd
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B, K, Wm = args.batch, args.steps, args.warmup
+    total_steps = Wm + K + args.e2e_steps + 2
+    spec, ctx, tables, num_pages = make_workload(B, total_steps)
+    weights = synth.make_weights(spec, seed=0, device=dev)
+    model = vd.Model(spec, weights, max_tokens=max(B, 16), max_seqs=B, max_logit_rows=B,
+                     max_context=CTX_HI + total_steps + 16)
+    mem = torch.empty(model.pool_bytes(num_pages), dtype=torch.uint8, device=dev)
+    pool = vd.KVPool(model, num_pages, memory=mem)
+    g = torch.Generator(device=dev)
+    g.manual_seed(4)
+    pv = mem.view(torch.bfloat16)
+    for i in range(0, pv.numel(), 1 << 28):  # random N(0,1) cached K/V
+        n = min(1 << 28, pv.numel() - i)
+        pv[i:i + n] = torch.randn(n, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    stream = torch.cuda.current_stream(dev)
+    toks = synth.make_tokens(B * total_steps, spec.vocab, seed=1).reshape(total_steps, B)
+
+    def batch_at(step, tok_row):
+        return vd.StepBatch([(tok_row[i:i + 1], int(ctx[i]) + step, tables[i]) for i in range(B)],
+                            logit_rows=range(B))
+
+    batches = [batch_at(s, toks[s]) for s in range(Wm + K)]
+    logits = torch.empty((B, spec.vocab), dtype=torch.float32, device=dev)
+    out_tok = torch.empty(B, dtype=torch.int32, device=dev)
+    samplers = [(1000 + i, 0, 0.0) for i in range(B)]
+
+    def one(s):
+        model.step(pool, batches[s], logits, stream)
+        model.sample(logits, samplers, out_tok, stream)
+
+    for s in range(Wm):
+        one(s)
+    torch.cuda.synchronize()
+    model.profile_collect()
+    model.profile(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        ev0.record(stream)
+        for s in range(Wm, Wm + K):
+            one(s)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    model.profile(False)
+    prof = model.profile_collect()
+    ms = ev0.elapsed_time(ev1)
+    assert model.device_status() == 0, "a bounded on-device wait timed out"
+
+    # ---- end to end: host descriptor + tokens fed back, D2H of sampled tokens each step
+    host_tok = torch.empty(B, dtype=torch.int32, pin_memory=True)
+    last = toks[Wm + K - 1].astype(np.int32)
+    base = Wm + K
+    h2d = 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(args.e2e_steps):
+        b = batch_at(base + s, last)
+        h2d = 4 * (3 * B + 2 * (B + 1) + 2 * B + B * int(b.page_table.shape[1]) + B)
+        model.step(pool, b, logits, stream)
+        model.sample(logits, samplers, out_tok, stream)
+        host_tok.copy_(out_tok, non_blocking=True)
+        stream.synchronize()
+        last = host_tok.numpy().copy()
+    e2e_s = time.perf_counter() - t0
+
+    t = torch.tensor([ms, e2e_s], dtype=torch.float64, device=dev if ws > 1 else "cpu")
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max, e2e_max = float(t[0]), float(t[1])
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    hbm, tf, peak_kind = load_peaks()
+    total_bytes, kbytes = algorithmic_bytes(spec, ctx, B)
+    step_ms = ms_max / K
+    kernels = {}
+    for name, (n, tot) in prof.items():
+        per_step = tot / K
+        e = {"launches_per_step": n / K, "ms_per_step": round(per_step, 5), "share": round(tot / ms_max, 4)}
+        if name in kbytes:
+            gbs = kbytes[name] / (per_step * 1e-3) / 1e9
+            e.update({"algorithmic_bytes": kbytes[name], "GB_s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)})
+        kernels[name] = e
+    dom = max((k for k in kernels if k in kbytes), key=lambda k: kernels[k]["ms_per_step"])
+    dk = kernels[dom]
+    launches = sum(int(round(v["launches_per_step"])) for v in kernels.values())
+    step_gbs = total_bytes / (step_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(ws * B * K / (ms_max * 1e-3), 1), "unit": UNIT, "n_gpus": ws,
+        "steps": K, "warmup": Wm, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "llama3.1-8b-shape 1 decoder layer + LM head, pure decode",
+                   "batch": B, "ctx": f"U[{CTX_LO},{CTX_HI}] mean {float(np.mean(ctx)):.0f}",
+                   "page_size": 16, "pages": "randomly permuted", "parallelism": f"replicas x{ws}",
+                   "l2": f"inputs larger than L2 ({total_bytes / 1e9:.2f} GB read+written per step)"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": dk["GB_s"], "peak": hbm, "unit": "GB/s",
+                     "frac": dk["hbm_frac"], "traffic": None, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": int(kbytes[dom] / max(1, round(dk["launches_per_step"])))},
+        "step_roofline": {"algorithmic_bytes": total_bytes, "GB_s": round(step_gbs, 1),
+                          "frac": round(step_gbs / hbm, 4)},
+        "kernels": kernels,
+        "gpu_launches": launches * K,
+        "e2e": {"value": round(ws * B * args.e2e_steps / e2e_max, 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * B, "steps": args.e2e_steps},
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec, weights, ctx, tables, mem, args.cpu_sample)
+    print(json.dumps(line))
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def oracle_decode_sample(spec, weights_np, caches, toks):
+    """The oracle's decode step for each request over its cached K/V."""
+    from oracle.decoder import OracleDecoder
+    dec = OracleDecoder(spec, weights_np)
+    return [dec.step(np.array([toks[r]]), cache)[0][0] for r, cache in enumerate(caches)]
+
+
+def cache_from_pages(spec, pages_u16, c):
+    """pages_u16: [layers][n_pages][2][Hkv][16][hd] uint16 -> per-layer (K, V) float64 [c][Hkv][hd]."""
+    from oracle.bf16 import bits_to_f64
+    cache = []
+    for layer in range(spec.n_layers):
+        kv = pages_u16[layer]
+        k = kv[:, 0].transpose(0, 2, 1, 3).reshape(-1, spec.n_kv_heads, spec.head_dim)[:c]
+        v = kv[:, 1].transpose(0, 2, 1, 3).reshape(-1, spec.n_kv_heads, spec.head_dim)[:c]
+        cache.append((bits_to_f64(k), bits_to_f64(v)))
+    return cache
+
+
+def cpu_baseline(spec, weights, ctx, tables, mem, n_req):
+    """Times the oracle (as it stands) on this host for a bounded sample."""
+    from invariant_vd_step_gb300 import synth
+    import torch
+    w_np = synth.weights_to_numpy(weights)
+    pool = mem.view(torch.int16)[: spec.n_layers * (mem.numel() // 2 // spec.n_layers)]
+    pool = pool.view(spec.n_layers, -1, 2, spec.n_kv_heads, 16, spec.head_dim)
+    caches = []
+    for r in range(n_req):
+        c = int(ctx[r])
+        idx = torch.as_tensor(tables[r][:(c + 15) // 16], dtype=torch.long, device=mem.device)
+        pages = pool[:, idx].cpu().numpy().view(np.uint16)
+        caches.append(cache_from_pages(spec, pages, c))
+    toks = synth.make_tokens(n_req, spec.vocab, seed=9)
+    t0 = time.perf_counter()
+    oracle_decode_sample(spec, w_np, caches, toks)
+    dt = time.perf_counter() - t0
+    return {"value": round(n_req / dt, 4), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n_req} decode rows of the same workload (1 layer + LM head, float64 numpy), "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from invariant_vd_step_gb300 import synth
+    from oracle.bf16 import f64_to_bits
+    B = args.batch
+    spec, ctx, tables, num_pages = make_workload(B, 4)
+    weights = synth.make_weights(spec, seed=0)
+    w_np = synth.weights_to_numpy(weights)
+    rng = np.random.default_rng(4)
+    n_req = args.cpu_sample
+    caches = []
+    for r in range(n_req):  # seeded N(0,1) bf16 cached K/V of the sampled requests
+        c = int(ctx[r])
+        shape = (spec.n_layers, (c + 15) // 16, 2, spec.n_kv_heads, 16, spec.head_dim)
+        caches.append(cache_from_pages(spec, f64_to_bits(rng.standard_normal(shape)), c))
+    toks = synth.make_tokens(n_req, spec.vocab, seed=9)
+    for _ in range(args.warmup):
+        oracle_decode_sample(spec, w_np, caches[:1], toks)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_decode_sample(spec, w_np, caches, toks)
+    dt = time.perf_counter() - t0
+    v = round(n_req * args.steps / dt, 4)
+    sample = f"{n_req} of the {B} decode rows per step (1 layer + LM head, float64 numpy)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "llama3.1-8b-shape 1 decoder layer + LM head, pure decode", "batch": B,
+                   "ctx": f"U[{CTX_LO},{CTX_HI}]", "page_size": 16},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--batch", type=int, default=256)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-sample", type=int, default=6)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        args.cpu_sample = min(args.cpu_sample, 2)
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

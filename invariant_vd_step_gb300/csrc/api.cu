@@ -401,20 +401,19 @@ int run_attention(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d, const
   a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(hd)));
   a.status = m->status;
   int rc;
-  {
+  if (d.n_dec) {
     Prof p(m, K_ATTN, s);
-    if (d.n_dec) {
-      a.cls_seq = m->d_desc + d.dec_seq;
-      a.cls_start = m->d_desc + d.dec_start;
-      a.n_cls = d.n_dec;
-      if ((rc = launch_attention(pool->map, a, hd, false, d.items_dec, s))) return rc;
-    }
-    if (d.n_pre) {
-      a.cls_seq = m->d_desc + d.pre_seq;
-      a.cls_start = m->d_desc + d.pre_start;
-      a.n_cls = d.n_pre;
-      if ((rc = launch_attention(pool->map, a, hd, true, d.items_pre, s))) return rc;
-    }
+    a.cls_seq = m->d_desc + d.dec_seq;
+    a.cls_start = m->d_desc + d.dec_start;
+    a.n_cls = d.n_dec;
+    if ((rc = launch_attention(pool->map, a, hd, false, d.items_dec, s))) return rc;
+  }
+  if (d.n_pre) {
+    Prof p(m, K_ATTN, s);
+    a.cls_seq = m->d_desc + d.pre_seq;
+    a.cls_start = m->d_desc + d.pre_start;
+    a.n_cls = d.n_pre;
+    if ((rc = launch_attention(pool->map, a, hd, true, d.items_pre, s))) return rc;
   }
   MergeArgs g{};
   g.part_o = m->part_o;
