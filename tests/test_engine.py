@@ -1,0 +1,103 @@
+"""Host scheduler and block manager on the CPU (oracle-backed paged executor)."""
+
+import numpy as np
+import pytest
+
+from invariant_vd_step_gb300 import engine, synth
+from oracle.decoder import OracleDecoder
+from oracle_executor import OracleExecutor
+
+SPEC = synth.TINY.with_(n_layers=1)
+
+
+@pytest.fixture(scope="module")
+def weights():
+    return synth.weights_to_numpy(synth.make_weights(SPEC, seed=3, gain_std=0.1))
+
+
+def _prompts(n=6, seed=1):
+    return synth.make_prompts(n, 17, 50, SPEC.vocab, seed=seed, shared_prefix=32, n_sharing=4)
+
+
+def _run(weights, prompts, max_new=6, num_pages=64, page_hash=engine.default_page_hash, **kw):
+    box = {}
+    ex = OracleExecutor(SPEC, weights, num_pages,
+                        write_guard=lambda pg: pg not in box["eng"].bm.meta)
+    eng = engine.Engine(ex, num_pages, page_hash=page_hash, **kw)
+    box["eng"] = eng
+    for i, p in enumerate(prompts):
+        eng.add_request(p, max_new, seed=100 + i)
+    while eng.waiting or eng.running:
+        eng.step()
+        eng.bm.check()
+        assert eng.steps < 10000
+    return eng
+
+
+def _cold_check(weights, eng):
+    dec = OracleDecoder(SPEC, weights)
+    for rid, r in eng.requests.items():
+        h = np.asarray(r.history)
+        cold = dec.forward_all(h[:-1])
+        n0 = len(r.prompt) - 1
+        for j, (lg, tok) in enumerate(eng.views[rid]):
+            np.testing.assert_array_equal(lg, cold[n0 + j])  # Theorem 4.1, bitwise
+            assert tok == h[n0 + j + 1]
+
+
+def test_engine_views_equal_cold_forward_with_prefix_reuse(weights):
+    eng = _run(weights, _prompts(), max_batch=3, token_budget=24, placement_seed=5)
+    assert eng.bm.stats["prefix_hit_pages"] > 0
+    _cold_check(weights, eng)
+
+
+def test_forced_hash_collisions_never_cause_reuse(weights):
+    # Every page hashes to the same value: candidates must be rejected by the
+    # exact token / depth / parent check (深入解析 Vosti §五 5.4).
+    prompts = _prompts(seed=2)
+    prompts.append(prompts[0][:20].copy())
+    prompts[-1][17] = (prompts[-1][17] + 1) % SPEC.vocab  # same first page, different second
+    eng = _run(weights, prompts, max_batch=2, token_budget=32, page_hash=lambda ph, t: 7)
+    assert eng.bm.stats["hash_candidates_rejected"] > 0
+    _cold_check(weights, eng)
+
+
+def test_pool_pressure_evicts_leaves_and_recomputes(weights):
+    eng = _run(weights, _prompts(seed=3), max_new=8, num_pages=9, max_batch=4, token_budget=40)
+    assert eng.bm.stats["preempted"] > 0 or eng.bm.stats["evicted"] > 0
+    _cold_check(weights, eng)
+
+
+def test_definition_2_1_prefix_comparable_across_executions(weights):
+    prompts = _prompts(seed=4)
+    base = _run(weights, prompts, max_batch=1, token_budget=64, prefix_reuse=False)
+    variants = [
+        dict(max_batch=6, token_budget=16, placement_seed=1),
+        dict(max_batch=2, token_budget=7, prefix_reuse=True, placement_seed=2),
+        dict(max_batch=3, token_budget=64, num_pages=10),
+    ]
+    for kw in variants:
+        other = _run(weights, prompts, **kw)
+        for rid in base.views:
+            a, b = base.views[rid], other.views[rid]
+            n = min(len(a), len(b))
+            assert n > 0
+            for (la, ta), (lb, tb) in zip(a[:n], b[:n]):
+                np.testing.assert_array_equal(la, lb)
+                assert ta == tb
+
+
+def test_block_manager_leaf_only_eviction_unit():
+    bm = engine.BlockManager(4)
+    toks = np.arange(64)
+    a = bm.allocate(3)
+    h0, c0 = bm.register(a[0], -1, 0, toks[:16], 0)
+    _, c1 = bm.register(a[1], a[0], 1, toks[16:32], h0)
+    assert (c0, c1) == (a[0], a[1])
+    bm.release(a)  # a[2] unregistered -> free; a[1] is a leaf; a[0] has a child
+    assert list(bm.evictable) == [a[1]]
+    got = bm.allocate(3)  # needs 3: 2 free + evict leaf a[1], then a[0] becomes a leaf
+    assert got is not None and a[0] in bm.evictable
+    bm.check()
+    assert bm.match_prefix(toks, 4) == [a[0]]
+    assert bm.match_prefix(np.concatenate([[1], toks[1:]]), 4) == []
