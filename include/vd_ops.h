@@ -55,6 +55,37 @@ int vd_op_rmsnorm(const void* x, const void* w, void* y, int32_t rows, int32_t d
 int vd_op_attention(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, const void* q, void* out,
                     void* stream);
 
+/* vd_op_attention without any allocation: the same kernels, the same
+ * arguments and the same bits, but the split partials go to a fixed device
+ * array inside libvd.so instead of the model's workspace.  (No counterpart
+ * in the paper: this is a deployment convenience of this library.)
+ *
+ * For callers that cannot allocate device memory at call time: a host that
+ * has handed the whole device memory to its own allocator or memory pool
+ * (a cudaMalloc from a library would fail or fragment that pool), and
+ * latency-bound loops that cannot afford cudaMalloc/cudaFree, which may
+ * synchronise the whole device.
+ *
+ * Limits and sharing:
+ *  - scratch = num_tokens * n_heads * S * (head_dim + 2) * 4 bytes, where S
+ *    is the largest number of 512-key splits of any request of the call
+ *    (ceil((cached_len + q_len) / 512)); calls needing more than
+ *    VD_ATTN_STATIC_SCRATCH_BYTES (16 MiB) are rejected with VD_ERR_CAPACITY
+ *    before anything is launched;
+ *  - the array exists once per device (every device that loads libvd.so
+ *    holds it until the process exits) and is shared by all calls: calls
+ *    that may run at the same time on the GPU (different streams, threads
+ *    or models) race on it and must be ordered by the caller;
+ *  - nothing in it needs to start at zero (each call writes every partial
+ *    it reads), so it is never cleared;
+ *  - the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+#define VD_ATTN_STATIC_SCRATCH_BYTES (16u << 20)
+int vd_op_attention_static(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, const void* q,
+                           void* out, void* stream);
+
 /* RoPE + K/V write for `layer` (and per-head QK RMSNorm if the model has
  * it): qkv dev bf16 [T][(Hq+2Hkv) hd] -> q_out dev bf16 [T][Hq][hd]; k and v
  * of token t go to the pool slot of (request, position) via the batch's

@@ -453,6 +453,56 @@ int run_rope(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d, const __nv
   return launch_rope_kv(r, s);
 }
 
+// vd_op_attention with the split partials in caller-independent static
+// scratch (part_o / part_ml, row stride `splits`) instead of the workspace.
+int run_attention_static(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d, const __nv_bfloat16* q,
+                         __nv_bfloat16* out, float* part_o, float* part_ml, int splits, cudaStream_t s) {
+  const vd_model_config& c = m->cfg;
+  const int hd = c.head_dim;
+  const int window = layer_is_local(c, layer) ? c.sliding_window : 0;
+  AttnArgs a{};
+  a.q = q;
+  a.part_o = part_o;
+  a.part_ml = part_ml;
+  a.cu_q = m->d_desc + d.cu_q;
+  a.cached_len = m->d_desc + d.cached;
+  a.page_table = m->d_desc + d.page_table;
+  a.pt_stride = d.stride;
+  a.Hq = c.n_heads;
+  a.Hkv = c.n_kv_heads;
+  a.layer_row0 = static_cast<int>(static_cast<long long>(layer) * pool->num_pages * 2 * c.n_kv_heads * 16);
+  a.pool_rows = static_cast<int>(pool->rows);
+  a.window = window;
+  a.split = m->split;
+  a.max_splits = splits;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(hd)));
+  a.status = m->status;
+  int rc;
+  if (d.n_dec) {
+    a.cls_seq = m->d_desc + d.dec_seq;
+    a.cls_start = m->d_desc + d.dec_start;
+    a.n_cls = d.n_dec;
+    if ((rc = launch_attention(pool->map, a, hd, false, d.items_dec, s))) return rc;
+  }
+  if (d.n_pre) {
+    a.cls_seq = m->d_desc + d.pre_seq;
+    a.cls_start = m->d_desc + d.pre_start;
+    a.n_cls = d.n_pre;
+    if ((rc = launch_attention(pool->map, a, hd, true, d.items_pre, s))) return rc;
+  }
+  MergeArgs g{};
+  g.part_o = part_o;
+  g.part_ml = part_ml;
+  g.out = out;
+  g.positions = m->d_desc + d.positions;
+  g.T = d.T;
+  g.Hq = c.n_heads;
+  g.window = window;
+  g.split = m->split;
+  g.max_splits = splits;
+  return launch_merge(g, hd, s);
+}
+
 int check_model(const vd_model* m) { return m ? VD_OK : fail(VD_ERR_INVALID_ARG, "null model"); }
 
 }  // namespace
@@ -836,6 +886,38 @@ int vd_op_attention(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b
   int rc = upload_desc(m, p, b, false, d, s);
   if (rc || d.T == 0) return rc;
   return run_attention(m, p, layer, d, static_cast<const __nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(out), s);
+}
+
+int vd_op_attention_static(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, const void* q,
+                           void* out, void* stream) {
+  if (check_model(m) || !p || p->m != m || !q || !out || !b) return fail(VD_ERR_INVALID_ARG, "null argument");
+  if (layer < 0 || layer >= m->cfg.n_layers) return fail(VD_ERR_OUT_OF_RANGE, "layer out of range");
+  if (b->num_tokens < 0 || b->num_seqs < 0 || b->num_tokens > m->cfg.max_tokens || b->num_seqs > m->cfg.max_seqs)
+    return fail(VD_ERR_CAPACITY, "step exceeds max_tokens / max_seqs");
+  if (b->num_tokens == 0) return VD_OK;
+  if (!b->cu_q || !b->cached_len) return fail(VD_ERR_INVALID_ARG, "missing descriptor array");
+  // Splits per row stride: the largest split count of any request of the call.
+  int splits = 1;
+  for (int i = 0; i < b->num_seqs; ++i) {
+    const long long kv = static_cast<long long>(b->cached_len[i]) + b->cu_q[i + 1] - b->cu_q[i];
+    if (kv < 1 || kv > m->cfg.max_context) return fail(VD_ERR_INVALID_ARG, "request length out of range");
+    splits = std::max(splits, static_cast<int>((kv - 1) / m->split + 1));
+  }
+  const size_t rows = static_cast<size_t>(b->num_tokens) * m->cfg.n_heads * splits;
+  const size_t need = rows * (m->cfg.head_dim + 2) * sizeof(float);
+  if (need > kAttnStaticScratchBytes)
+    return fail(VD_ERR_CAPACITY, "call needs " + std::to_string(need) + " bytes of split scratch; the static buffer holds " +
+                                     std::to_string(kAttnStaticScratchBytes) + " (fewer tokens or shorter contexts per call)");
+  void* scratch = nullptr;
+  int rc = attn_static_scratch(&scratch);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Desc d;
+  if ((rc = upload_desc(m, p, b, false, d, s)) || d.T == 0) return rc;
+  float* part_o = static_cast<float*>(scratch);
+  float* part_ml = part_o + rows * m->cfg.head_dim;
+  return run_attention_static(m, p, layer, d, static_cast<const __nv_bfloat16*>(q),
+                              static_cast<__nv_bfloat16*>(out), part_o, part_ml, splits, s);
 }
 
 int vd_op_rope_kv(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, const void* qkv, void* q_out,

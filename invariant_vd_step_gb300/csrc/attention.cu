@@ -30,6 +30,8 @@
 // float operation an explicitly rounded intrinsic.
 #include <math.h>
 
+#include <mutex>
+
 #include "vd_device.cuh"
 #include "vd_internal.h"
 
@@ -342,6 +344,33 @@ int launch_attn_t(const CUtensorMap& kvmap, const AttnArgs& a, int n_items, cuda
 }
 
 }  // namespace
+
+// Scratch for vd_op_attention_static: the split partials (o, then m/l) of
+// one call.  It is a fixed device array so that the call needs no
+// allocation; every device that loads the library holds it until exit.
+static __device__ __align__(256) float g_attn_static_scratch[kAttnStaticScratchBytes / sizeof(float)];
+
+int attn_static_scratch(void** ptr) {
+  // Device address of the array on the current device, looked up once per
+  // device (host code cannot take the address of a __device__ symbol).
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  VD_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return fail(VD_ERR_UNSUPPORTED, "device ordinal too large");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+    if (e != cudaSuccess)
+      return fail(VD_ERR_CUDA, std::string("cudaGetSymbolAddress(static attention scratch): ") +
+                                   cudaGetErrorString(e));
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return VD_OK;
+}
 
 int attn_key_tile(int hd) { return hd >= 256 ? AttnCfg<256>::BNK : AttnCfg<128>::BNK; }
 

@@ -82,6 +82,10 @@ int attn_key_tile(int hd);
 int launch_attention(const CUtensorMap& kvmap, const AttnArgs& a, int hd, bool prefill_class, int n_items,
                      cudaStream_t s);
 int launch_merge(const MergeArgs& a, int hd, cudaStream_t s);
+// Fixed-size device scratch of vd_op_attention_static (bytes) and its
+// device address on the current device (looked up once per device).
+constexpr size_t kAttnStaticScratchBytes = static_cast<size_t>(16) << 20;
+int attn_static_scratch(void** ptr);
 
 // ---------------------------------------------------------------- elementwise
 int launch_embed(const void* embed, const int* tokens, void* x, int T, int d, cudaStream_t s);

@@ -89,6 +89,7 @@ _SIGS = {
     "vd_op_rmsnorm": (ctypes.c_int, [_VP, _VP, _VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _VP]),
     "vd_op_attention": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
     "vd_op_rope_kv": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
+    "vd_op_attention_static": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
     "vd_op_philox": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int32, _VP, _VP]),
 }
 
@@ -241,6 +242,11 @@ class Model:
     def attention(self, pool, layer, batch: StepBatch, q, out, stream=None):
         check(lib().vd_op_attention(self.h, pool.h, layer, ctypes.byref(batch.c), _ptr(q), _ptr(out),
                                     _stream(stream)))
+
+    def attention_static(self, pool, layer, batch: StepBatch, q, out, stream=None):
+        """vd_op_attention_static: attention whose scratch is a fixed array in libvd.so (no allocation)."""
+        check(lib().vd_op_attention_static(self.h, pool.h, layer, ctypes.byref(batch.c), _ptr(q), _ptr(out),
+                                           _stream(stream)))
 
     def rope_kv(self, pool, layer, batch: StepBatch, qkv, q_out, stream=None):
         check(lib().vd_op_rope_kv(self.h, pool.h, layer, ctypes.byref(batch.c), _ptr(qkv), _ptr(q_out),
