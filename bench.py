@@ -173,9 +173,15 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     toks = synth.make_tokens(B * total_steps, spec.vocab, seed=1).reshape(total_steps, B)
 
+    width = max(len(t) for t in tables)
+    pt2d = np.zeros((B, width), dtype=np.int32)
+    for i, t in enumerate(tables):
+        pt2d[i, :len(t)] = t
+    cu = np.arange(B + 1, dtype=np.int32)
+    rows = np.arange(B, dtype=np.int32)
+
     def batch_at(step, tok_row):
-        return vd.StepBatch([(tok_row[i:i + 1], int(ctx[i]) + step, tables[i]) for i in range(B)],
-                            logit_rows=range(B))
+        return vd.StepBatch.from_arrays(tok_row, cu, ctx + step, pt2d, rows)
 
     batches = [batch_at(s, toks[s]) for s in range(Wm + K)]
     logits = torch.empty((B, spec.vocab), dtype=torch.float32, device=dev)
@@ -217,7 +223,8 @@ def run_gpu(args):
     t0 = time.perf_counter()
     for s in range(args.e2e_steps):
         b = batch_at(base + s, last)
-        h2d = 4 * (3 * B + 2 * (B + 1) + 2 * B + B * int(b.page_table.shape[1]) + B)
+        need = (int(np.max(ctx)) + base + s + 16) // 16  # page-table columns the library uploads
+        h2d = 4 * (3 * B + 2 * (B + 1) + 3 * B + B * need + B)
         model.step(pool, b, logits, stream)
         model.sample(logits, samplers, out_tok, stream)
         host_tok.copy_(out_tok, non_blocking=True)
@@ -237,16 +244,17 @@ def run_gpu(args):
     total_bytes, kbytes = algorithmic_bytes(spec, ctx, B)
     step_ms = ms_max / K
     kernels = {}
-    for name, (n, tot) in prof.items():
+    for name, (n, nk, tot) in prof.items():
         per_step = tot / K
-        e = {"launches_per_step": n / K, "ms_per_step": round(per_step, 5), "share": round(tot / ms_max, 4)}
+        e = {"launches_per_step": n / K, "kernels_per_step": nk / K, "ms_per_step": round(per_step, 5),
+             "share": round(tot / ms_max, 4)}
         if name in kbytes:
             gbs = kbytes[name] / (per_step * 1e-3) / 1e9
             e.update({"algorithmic_bytes": kbytes[name], "GB_s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)})
         kernels[name] = e
     dom = max((k for k in kernels if k in kbytes), key=lambda k: kernels[k]["ms_per_step"])
     dk = kernels[dom]
-    launches = sum(int(round(v["launches_per_step"])) for v in kernels.values())
+    launches = sum(int(round(v["kernels_per_step"])) for v in kernels.values())
     step_gbs = total_bytes / (step_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(ws * B * K / (ms_max * 1e-3), 1), "unit": UNIT, "n_gpus": ws,
@@ -267,11 +275,93 @@ def run_gpu(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * B, "steps": args.e2e_steps},
         "clocks": clk.summary(),
     }
+    if not args.no_invariance:
+        from invariant_vd_step_gb300 import invariance
+        r = invariance.run_matrix()
+        line["invariance"] = {"pairs": r.pairs, "bitwise_equal": r.equal, "pass_pct": round(r.pass_pct, 3),
+                              "categories": r.categories, "runs": r.runs,
+                              "workload": "tiny llama-style decoder, 8 requests, 16 greedy decode steps"}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, weights, ctx, tables, mem, args.cpu_sample)
     print(json.dumps(line))
     if ws > 1:
         dist.destroy_process_group()
+
+
+def run_prefill(args):
+    """Prefill mode: one step of T new tokens (several requests from an empty
+    cache) through the same layer + LM head; reports prefill tok/s and the
+    GEMMs' TFLOP/s against the measured bf16 tensor peak."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from invariant_vd_step_gb300 import synth, vd
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = synth.LLAMA8B_1L
+    T, nreq = args.tokens, args.prefill_requests
+    per = T // nreq
+    K, Wm = args.steps, args.warmup
+    weights = synth.make_weights(spec, seed=0, device=dev)
+    model = vd.Model(spec, weights, max_tokens=T, max_seqs=nreq, max_logit_rows=nreq, max_context=per + 16)
+    npg = (per + 15) // 16
+    pool = vd.KVPool(model, nreq * npg)
+    toks = synth.make_tokens(T, spec.vocab, seed=1)
+    tables = synth.page_permutation(nreq * npg, seed=2).reshape(nreq, npg)
+    b = vd.StepBatch.from_arrays(toks[:per * nreq], np.arange(nreq + 1, dtype=np.int32) * per,
+                                 np.zeros(nreq, np.int32), tables, np.arange(1, nreq + 1) * per - 1)
+    logits = torch.empty((nreq, spec.vocab), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(Wm):
+        model.step(pool, b, logits, stream)
+    torch.cuda.synchronize()
+    model.profile_collect()
+    model.profile(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        ev0.record(stream)
+        for _ in range(K):
+            model.step(pool, b, logits, stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    model.profile(False)
+    prof = model.profile_collect()
+    ms = ev0.elapsed_time(ev1)
+    hbm, tf_burst, peak_kind = load_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tf_sust = float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        tf_sust = 1700.0
+    d, F = spec.d_model, spec.ffn_dim
+    Tt = per * nreq
+    flops = {"gemm_qkv": 2 * Tt * spec.qkv_dim * d, "gemm_o": 2 * Tt * d * spec.attn_dim,
+             "gemm_gate_up": 2 * Tt * 2 * F * d, "gemm_down": 2 * Tt * d * F,
+             "gemm_lm_head": 2 * nreq * spec.vocab * d}
+    kernels = {}
+    for name, (n, nk, tot) in prof.items():
+        per_step = tot / K
+        e = {"kernels_per_step": nk / K, "ms_per_step": round(per_step, 4), "share": round(tot / ms, 4)}
+        if name in flops:
+            tfs = flops[name] / (per_step * 1e-3) / 1e12
+            e.update({"TFLOP_s": round(tfs, 1), "tensor_frac": round(tfs / tf_sust, 4)})
+        kernels[name] = e
+    dom = max((k for k in kernels if k in flops), key=lambda k: kernels[k]["ms_per_step"])
+    gemm_ms = sum(kernels[k]["ms_per_step"] for k in kernels if k in flops)
+    gemm_tf = sum(flops.values()) / (gemm_ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": "prefill tok/s (Llama-8B shape, 1 GB300)", "value": round(Tt * K / (ms * 1e-3), 1),
+        "unit": "tok/s", "n_gpus": 1, "steps": K, "warmup": Wm, "ms_per_step": round(ms / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "llama3.1-8b-shape 1 decoder layer + LM head, prefill from an empty cache",
+                   "tokens_per_step": Tt, "requests": nreq, "page_size": 16, "pages": "randomly permuted"},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": kernels[dom]["TFLOP_s"], "peak": tf_sust,
+                     "unit": "TFLOP/s", "frac": kernels[dom]["tensor_frac"], "traffic": None,
+                     "peak_source": peak_kind + " (sustained)"},
+        "gemms": {"TFLOP_s": round(gemm_tf, 1), "frac_of_sustained": round(gemm_tf / tf_sust, 4),
+                  "frac_of_burst": round(gemm_tf / tf_burst, 4)},
+        "kernels": kernels, "clocks": clk.summary()}))
 
 
 def oracle_decode_sample(spec, weights_np, caches, toks):
@@ -361,13 +451,19 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-sample", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-invariance", action="store_true")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--mode", default="decode", choices=["decode", "prefill"])
+    ap.add_argument("--tokens", type=int, default=8192, help="prefill mode: tokens per step")
+    ap.add_argument("--prefill-requests", type=int, default=4)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         args.cpu_sample = min(args.cpu_sample, 2)
         run_reference(args)
+    elif args.mode == "prefill":
+        run_prefill(args)
     else:
         run_gpu(args)
 

@@ -136,7 +136,8 @@ typedef struct vd_sampler {
 
 typedef struct vd_kernel_stat {
   char name[32];
-  int32_t launches;
+  int32_t launches;   /* timed regions (event pairs) of this class     */
+  int32_t kernels;    /* kernel launches inside those regions          */
   double total_ms;
 } vd_kernel_stat;
 
@@ -173,7 +174,7 @@ void* vd_kv_pool_data(vd_kv_pool* p);
  * T == 0 is a no-op. */
 int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out, void* stream);
 
-/* Token choice for R rows of dev float32 logits [R][V] -> dev int32 [R]:
+/* Token choice for R rows of dev float32 logits [R][V] (16-byte aligned) -> dev int32 [R]:
  * greedy argmax (lowest index on ties) or Gumbel-max with Philox4x32-10
  * (per-row state in host array per_row[R]). */
 int vd_sample(vd_model* m, const float* logits, int32_t R, const vd_sampler* per_row,

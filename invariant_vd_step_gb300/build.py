@@ -1,6 +1,6 @@
 """Builds libvd.so (the C-ABI library) in-tree for sm_103a with nvcc.
 
-Each .cu file is compiled in parallel to an object under ``_build/`` at the
+Each .cu / .cpp file is compiled in parallel to an object under ``_build/`` at the
 repository root, then linked (static CUDA runtime) into
 ``invariant_vd_step_gb300/libvd.so``.  Rebuilds only when a source or header
 is newer than the library.
@@ -34,7 +34,7 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():

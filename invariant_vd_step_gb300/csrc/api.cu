@@ -85,6 +85,7 @@ constexpr int kSplitKeys = 512;  // S_kv, fixed for every model
 
 struct ProfRec {
   int cls;
+  int kernels;  // kernel launches between the two events
   cudaEvent_t a, b;
 };
 const char* const kKernelNames[] = {"embed",     "rmsnorm",  "gemm_qkv",     "rope_kv",   "attention",
@@ -104,11 +105,13 @@ struct ActBuf {
   int cols = 0;
   std::vector<int> rows;
   std::vector<CUtensorMap> maps;
-  const CUtensorMap& map_for(int T) const {
+  size_t bucket(int T) const {
     for (size_t i = 0; i < rows.size(); ++i)
-      if (rows[i] >= T) return maps[i];
-    return maps.back();
+      if (rows[i] >= T) return i;
+    return rows.size() - 1;
   }
+  const CUtensorMap& map_for(int T) const { return maps[bucket(T)]; }
+  int box_for(int T) const { return std::min(rows[bucket(T)], kGemmBN); }
 };
 
 // Host-side layout of the uploaded step descriptor (int32 offsets).
@@ -148,6 +151,8 @@ struct vd_model {
   int desc_slot = 0;
   size_t desc_cap = 0;
   vd_sampler* d_samp = nullptr;
+  float* samp_part_v = nullptr;  // per-chunk winners of the sampler's first pass
+  int* samp_part_i = nullptr;
   vd_sampler* h_samp = nullptr;
   cudaEvent_t samp_ev = nullptr;
   std::vector<void*> dev_allocs;
@@ -157,6 +162,7 @@ struct vd_model {
   std::vector<cudaEvent_t> ev_pool;
   double prof_ms[K_COUNT] = {};
   int prof_n[K_COUNT] = {};
+  int prof_k[K_COUNT] = {};
 };
 
 struct vd_kv_pool {
@@ -186,6 +192,7 @@ struct Prof {
   int cls;
   cudaStream_t s;
   cudaEvent_t a = nullptr;
+  int kernels = 1;
   Prof(vd_model* m_, int cls_, cudaStream_t s_) : m(m_), cls(cls_), s(s_) {
     if (m->profiling) {
       a = take_event(m);
@@ -196,7 +203,7 @@ struct Prof {
     if (m->profiling) {
       cudaEvent_t b = take_event(m);
       cudaEventRecord(b, s);
-      m->recs.push_back({cls, a, b});
+      m->recs.push_back({cls, kernels, a, b});
     }
   }
 };
@@ -217,7 +224,7 @@ int make_act(vd_model* m, ActBuf& buf, int cap_rows, int cols) {
   for (int r = 1;; r *= 2) {
     const int rows = std::min(r, cap_rows);
     CUtensorMap mp;
-    if ((rc = make_map_2d(&mp, buf.ptr, rows, cols, kGemmBN))) return rc;
+    if ((rc = make_map_2d(&mp, buf.ptr, rows, cols, std::min(rows, kGemmBN)))) return rc;
     buf.rows.push_back(rows);
     buf.maps.push_back(mp);
     if (rows >= cap_rows) break;
@@ -503,6 +510,20 @@ int run_attention_static(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d
   return launch_merge(g, hd, s);
 }
 
+// Status word for the single-kernel ops (they have no model): one int per
+// device, allocated on first use and never freed, so a failed bounded wait
+// in an op makes its remaining CTAs skip their work.
+int* op_status() {
+  static std::mutex mu;
+  static int* words[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!words[dev] && cudaMalloc(reinterpret_cast<void**>(&words[dev]), 256) == cudaSuccess)
+    cudaMemset(words[dev], 0, 256);
+  return words[dev];
+}
+
 int check_model(const vd_model* m) { return m ? VD_OK : fail(VD_ERR_INVALID_ARG, "null model"); }
 
 }  // namespace
@@ -599,6 +620,9 @@ int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_mode
       return bail(fail(VD_ERR_CUDA, "pinned descriptor buffer"));
   }
   if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->d_samp), sizeof(vd_sampler) * c.max_logit_rows))) return bail(rc);
+  const size_t nsp = static_cast<size_t>(c.max_logit_rows) * sample_chunks(c.vocab);
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->samp_part_v), nsp * 4))) return bail(rc);
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->samp_part_i), nsp * 4))) return bail(rc);
   if (cudaMallocHost(reinterpret_cast<void**>(&m->h_samp), sizeof(vd_sampler) * c.max_logit_rows) != cudaSuccess ||
       cudaEventCreateWithFlags(&m->samp_ev, cudaEventDisableTiming) != cudaSuccess)
     return bail(fail(VD_ERR_CUDA, "pinned sampler buffer"));
@@ -710,14 +734,14 @@ int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out,
     }
     {
       Prof p(m, K_GEMM_QKV, s);
-      g.out = m->qkv; g.residual = nullptr; g.K = dm; g.ldo = qkv_dim;
+      g.out = m->qkv; g.residual = nullptr; g.K = dm; g.ldo = qkv_dim; g.b_box_rows = m->a.box_for(T);
       if ((rc = launch_gemm(m->m_qkv[l], m->a.map_for(T), qkv_dim / kGemmBM, g, EPI_BF16, s))) return rc;
     }
     if ((rc = run_rope(m, pool, l, d, m->qkv, m->q, s))) return rc;
     if ((rc = run_attention(m, pool, l, d, m->q, m->o.ptr, s))) return rc;
     {
       Prof p(m, K_GEMM_O, s);
-      g.out = m->x; g.residual = m->x; g.K = c.n_heads * hd; g.ldo = dm;
+      g.out = m->x; g.residual = m->x; g.K = c.n_heads * hd; g.ldo = dm; g.b_box_rows = m->o.box_for(T);
       if ((rc = launch_gemm(m->m_o[l], m->o.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
     }
     {
@@ -726,14 +750,14 @@ int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out,
     }
     {
       Prof p(m, K_GEMM_GU, s);
-      g.out = m->z.ptr; g.residual = nullptr; g.K = dm; g.ldo = F; g.glu_up_row = F;
+      g.out = m->z.ptr; g.residual = nullptr; g.K = dm; g.ldo = F; g.glu_up_row = F; g.b_box_rows = m->a.box_for(T);
       if ((rc = launch_gemm(m->m_gu[l], m->a.map_for(T), F / 64, g,
                             c.act == VD_ACT_GEGLU ? EPI_GEGLU : EPI_SWIGLU, s)))
         return rc;
     }
     {
       Prof p(m, K_GEMM_DOWN, s);
-      g.out = m->x; g.residual = m->x; g.K = F; g.ldo = dm;
+      g.out = m->x; g.residual = m->x; g.K = F; g.ldo = dm; g.b_box_rows = m->z.box_for(T);
       if ((rc = launch_gemm(m->m_down[l], m->z.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
     }
   }
@@ -750,6 +774,7 @@ int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out,
     h.out = logits_out;
     h.K = dm;
     h.ldo = c.vocab;
+    h.b_box_rows = m->ar.box_for(d.R);
     if ((rc = launch_gemm(m->m_lm, m->ar.map_for(d.R), c.vocab / kGemmBM, h, EPI_F32, s))) return rc;
   }
   return VD_OK;
@@ -766,8 +791,10 @@ int vd_sample(vd_model* m, const float* logits, int32_t R, const vd_sampler* per
   memcpy(m->h_samp, per_row, sizeof(vd_sampler) * R);
   VD_CUDA_TRY(cudaMemcpyAsync(m->d_samp, m->h_samp, sizeof(vd_sampler) * R, cudaMemcpyHostToDevice, s));
   VD_CUDA_TRY(cudaEventRecord(m->samp_ev, s));
+  if (reinterpret_cast<uintptr_t>(logits) & 15) return fail(VD_ERR_INVALID_ARG, "logits must be 16-byte aligned");
   Prof p(m, K_SAMPLE, s);
-  return launch_sample(logits, R, m->cfg.vocab, m->d_samp, tokens_out, s);
+  p.kernels = 2;
+  return launch_sample(logits, R, m->cfg.vocab, m->d_samp, m->samp_part_v, m->samp_part_i, tokens_out, s);
 }
 
 int vd_copy_kv(vd_model* m, vd_kv_pool* pool, int32_t layer, const int32_t* page_table, int32_t n_tokens,
@@ -823,6 +850,7 @@ int vd_profile_collect(vd_model* m, vd_kernel_stat* out, int32_t max_out) {
     cudaEventElapsedTime(&ms, r.a, r.b);
     m->prof_ms[r.cls] += ms;
     m->prof_n[r.cls] += 1;
+    m->prof_k[r.cls] += r.kernels;
     m->ev_pool.push_back(r.a);
     m->ev_pool.push_back(r.b);
   }
@@ -834,6 +862,7 @@ int vd_profile_collect(vd_model* m, vd_kernel_stat* out, int32_t max_out) {
       memset(&out[n], 0, sizeof(vd_kernel_stat));
       strncpy(out[n].name, kKernelNames[k], sizeof(out[n].name) - 1);
       out[n].launches = m->prof_n[k];
+      out[n].kernels = m->prof_k[k];
       out[n].total_ms = m->prof_ms[k];
     }
     ++n;
@@ -841,6 +870,7 @@ int vd_profile_collect(vd_model* m, vd_kernel_stat* out, int32_t max_out) {
   for (int k = 0; k < K_COUNT; ++k) {
     m->prof_ms[k] = 0;
     m->prof_n[k] = 0;
+    m->prof_k[k] = 0;
   }
   return n;
 }
@@ -858,7 +888,7 @@ int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int3
   CUtensorMap wm, xm;
   int rc;
   if ((rc = make_map_2d(&wm, W, glu ? 2 * N : N, K, glu ? 64 : kGemmBM))) return rc;
-  if ((rc = make_map_2d(&xm, A, T, K, kGemmBN))) return rc;
+  if ((rc = make_map_2d(&xm, A, T, K, std::min<int>(T, kGemmBN)))) return rc;
   GemmArgs g{};
   g.out = C;
   g.residual = residual;
@@ -866,7 +896,8 @@ int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int3
   g.K = K;
   g.ldo = N;
   g.glu_up_row = N;
-  g.status = nullptr;
+  g.b_box_rows = std::min<int>(T, kGemmBN);
+  g.status = op_status();
   return launch_gemm(wm, xm, glu ? N / 64 : N / kGemmBM, g, epilogue, static_cast<cudaStream_t>(stream));
 }
 

@@ -159,6 +159,13 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + 4 * C::TILE_BYTES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
 
+  // Once any bounded wait has given up, later CTAs skip their work.
+  {
+    __shared__ int skip;  // one read for the whole CTA keeps the exit uniform
+    if (threadIdx.x == 0) skip = a.status ? *reinterpret_cast<volatile int*>(a.status) : 0;
+    __syncthreads();
+    if (skip) return;
+  }
   // ---- work item -> (request, row block, KV head, split)
   const int item = blockIdx.x;
   int lo_i = 0, hi_i = a.n_cls - 1;

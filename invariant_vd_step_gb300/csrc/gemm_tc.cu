@@ -2,10 +2,10 @@
 //
 // acc[t][n] = sum_k X[t][k] * W[n][k], fp32 accumulation in TMEM.  The
 // weight matrix is the MMA's A operand (M = 128 weight rows per tile) and
-// the tokens are its N dimension (N = 128 per tile), so decode batches of
-// any size stream each weight tile exactly once per 128 tokens.  Every
-// launch, whatever the number of tokens T, uses the same instruction shape
-// (M=128, N=128, K=16), the same K order (stage by stage, 4 MMAs of K=16 per
+// the tokens are its N dimension (N = 256 per tile), so decode batches of
+// up to 256 requests stream each weight tile exactly once.  Every launch,
+// whatever the number of tokens T, uses the same instruction shape
+// (M=128, N=256, K=16), the same K order (stage by stage, 4 MMAs of K=16 per
 // 64-wide stage) and no split-K: column t of D depends only on row t of X and
 // on W, which is the matmul contract of 深入解析 Vosti §六 6.1 (row x of a
 // batched run equals the singleton run bit for bit; zero-initialised
@@ -15,6 +15,10 @@
 // owns the TMEM allocation; warp 1 issues tcgen05.mma (one lane); warps 2..5
 // read the accumulator from TMEM (warp w reaches lanes 32*(w%4)..+31) and run
 // the fused epilogue.  Every wait is bounded (see vd_device.cuh).
+//
+// The activation box is as tall as the launch needs (up to 256 rows): rows of
+// the B tile past it keep stale shared-memory contents, which only feed
+// columns that are never stored (a column depends on its own row alone).
 #include "vd_device.cuh"
 #include "vd_internal.h"
 
@@ -60,6 +64,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   constexpr bool kGlu = (EPI == EPI_SWIGLU || EPI == EPI_GEGLU);
+  // Once any bounded wait has given up, later CTAs skip their work instead
+  // of each waiting out the limit (the status word reports the failure).
+  {
+    __shared__ int skip;  // one read for the whole CTA keeps the exit uniform
+    if (threadIdx.x == 0) skip = args.status ? *reinterpret_cast<volatile int*>(args.status) : 0;
+    __syncthreads();
+    if (skip) return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_t = blockIdx.x, tile_n = blockIdx.y;
   const int KB = args.K / kGemmBK;
@@ -90,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % kStages;
         if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, abort_flag, args.status)) break;
-        mbar_arrive_expect_tx(&full[s], kAStageBytes + kBStageBytes);
+        mbar_arrive_expect_tx(&full[s], kAStageBytes + args.b_box_rows * 128);
         uint8_t* a = sA + s * kAStageBytes;
         if (kGlu) {
           tma_load_2d(a, &wmap, &full[s], kb * kGemmBK, tile_n * 64);
@@ -133,19 +145,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt = min(32, args.T - t0);
         if (EPI == EPI_F32) {
           float* out = static_cast<float*>(args.out) + tile_n * kGemmBM + row;
-          for (int j = 0; j < nt; ++j) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
         } else if (EPI == EPI_BF16) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * kGemmBM + row;
-          for (int j = 0; j < nt; ++j) out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(v[j]);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(v[j]);
         } else if (EPI == EPI_RESIDUAL) {
           const size_t col = static_cast<size_t>(tile_n) * kGemmBM + row;
           const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(args.residual) + col;
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + col;
-          for (int j = 0; j < nt; ++j) {
-            const size_t o = static_cast<size_t>(t0 + j) * args.ldo;
-            const float r = __bfloat162float(res[o]);
-            out[o] = __float2bfloat16_rn(__fadd_rn(bf16_round(v[j]), r));
-          }
+          // The residual may alias the output: load the whole chunk first so
+          // the loads are not serialised behind the stores.
+          float r[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            r[j] = (j < nt) ? __bfloat162float(res[static_cast<size_t>(t0 + j) * args.ldo]) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nt)
+              out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fadd_rn(bf16_round(v[j]), r[j]));
         } else {  // GLU: rows 0..63 gate, 64..127 up of the same 64 features
           if (lg >= 2) {
             float* xr = xchg + ((lg - 2) * 32 + lane) * 33;
@@ -156,10 +177,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lg < 2) {
             const float* xr = xchg + (lg * 32 + lane) * 33;
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * 64 + lg * 32 + lane;
-            for (int j = 0; j < nt; ++j) {
-              const float g = bf16_round(v[j]);
-              const float a = (EPI == EPI_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
-              out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fmul_rn(a, xr[j]));
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (j < nt) {
+                const float g = bf16_round(v[j]);
+                const float a = (EPI == EPI_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
+                out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fmul_rn(a, xr[j]));
+              }
             }
           }
           epi_barrier();

@@ -11,7 +11,7 @@
 // Definition 2.1.
 //
 // The reduction picks the unique (largest value, lowest index) pair, which
-// no summation order can change, so the result is fixed by the row alone.
+// no evaluation order can change, so the result is fixed by the row alone.
 #include <limits.h>
 #include <math.h>
 
@@ -44,37 +44,14 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
-constexpr int kSampleThreads = 512;
+// Pass 1: CTA (row, chunk) picks the best (score, index) among kSampleChunk
+// consecutive vocabulary entries with 16-byte loads.  Pass 2: one warp per
+// row picks among the chunk winners.  Both passes select the unique
+// (largest score, lowest index) pair, so the split changes nothing.
+constexpr int kSampleThreads = 256;
+constexpr int kSampleChunk = kSampleThreads * 32;
 
-__global__ void __launch_bounds__(kSampleThreads) sample_kernel(const float* __restrict__ logits, int V,
-                                                               const vd_sampler* __restrict__ params,
-                                                               int* __restrict__ out) {
-  const int r = blockIdx.x;
-  const float* l = logits + static_cast<size_t>(r) * V;
-  const vd_sampler sp = params[r];
-  const bool greedy = !(sp.temperature > 0.f);
-  float bv = -INFINITY;
-  int bi = INT_MAX;
-  for (int blk = threadIdx.x; blk * 4 < V; blk += kSampleThreads) {
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (!greedy) w = philox_block(sp.seed, sp.step, static_cast<uint32_t>(blk));
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = blk * 4 + j;
-      if (i >= V) break;
-      float v = l[i];
-      if (!greedy) {
-        const float u = __fmul_rn(__fadd_rn(static_cast<float>(ws[j] >> 8), 0.5f), 5.9604644775390625e-8f);
-        const float g = -logf(-logf(u));
-        v = __fadd_rn(__fdiv_rn(v, sp.temperature), g);
-      }
-      if (better(v, i, bv, bi)) {
-        bv = v;
-        bi = i;
-      }
-    }
-  }
+__device__ __forceinline__ void warp_best(float& bv, int& bi) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -84,6 +61,42 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const float* __r
       bi = oi;
     }
   }
+}
+
+__global__ void __launch_bounds__(kSampleThreads) sample_partial_kernel(const float* __restrict__ logits, int V,
+                                                                       const vd_sampler* __restrict__ params,
+                                                                       float* __restrict__ part_v,
+                                                                       int* __restrict__ part_i) {
+  const int r = blockIdx.x, chunk = blockIdx.y;
+  const float4* l4 = reinterpret_cast<const float4*>(logits + static_cast<size_t>(r) * V);
+  const vd_sampler sp = params[r];
+  const bool greedy = !(sp.temperature > 0.f);
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  const int blk0 = chunk * (kSampleChunk / 4);
+  const int nblk = min(kSampleChunk / 4, V / 4 - blk0);
+  for (int k = threadIdx.x; k < nblk; k += kSampleThreads) {
+    const int blk = blk0 + k;
+    const float4 x = l4[blk];
+    float v[4] = {x.x, x.y, x.z, x.w};
+    if (!greedy) {
+      const uint4 w = philox_block(sp.seed, sp.step, static_cast<uint32_t>(blk));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float u = __fmul_rn(__fadd_rn(static_cast<float>(ws[j] >> 8), 0.5f), 5.9604644775390625e-8f);
+        const float g = -logf(-logf(u));
+        v[j] = __fadd_rn(__fdiv_rn(v[j], sp.temperature), g);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (better(v[j], blk * 4 + j, bv, bi)) {
+        bv = v[j];
+        bi = blk * 4 + j;
+      }
+  }
+  warp_best(bv, bi);
   __shared__ float sv[kSampleThreads / 32];
   __shared__ int si[kSampleThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -92,14 +105,33 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const float* __r
     si[warp] = bi;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int k = 1; k < kSampleThreads / 32; ++k)
-      if (better(sv[k], si[k], bv, bi)) {
-        bv = sv[k];
-        bi = si[k];
-      }
-    out[r] = (bi == INT_MAX) ? 0 : bi;
+  if (warp == 0) {
+    bv = lane < kSampleThreads / 32 ? sv[lane] : -INFINITY;
+    bi = lane < kSampleThreads / 32 ? si[lane] : INT_MAX;
+    warp_best(bv, bi);
+    if (lane == 0) {
+      part_v[static_cast<size_t>(r) * gridDim.y + chunk] = bv;
+      part_i[static_cast<size_t>(r) * gridDim.y + chunk] = bi;
+    }
   }
+}
+
+__global__ void sample_final_kernel(const float* __restrict__ part_v, const int* __restrict__ part_i, int R,
+                                    int nchunk, int* __restrict__ out) {
+  const int r = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= R) return;
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  for (int c = lane; c < nchunk; c += 32) {
+    const float v = part_v[static_cast<size_t>(r) * nchunk + c];
+    const int i = part_i[static_cast<size_t>(r) * nchunk + c];
+    if (better(v, i, bv, bi)) {
+      bv = v;
+      bi = i;
+    }
+  }
+  warp_best(bv, bi);
+  if (lane == 0) out[r] = (bi == INT_MAX) ? 0 : bi;
 }
 
 __global__ void philox_kernel(uint64_t seed, uint64_t step, int n, uint32_t* out) {
@@ -112,9 +144,16 @@ __global__ void philox_kernel(uint64_t seed, uint64_t step, int n, uint32_t* out
 
 }  // namespace
 
-int launch_sample(const float* logits, int R, int V, const vd_sampler* dev_params, int* out, cudaStream_t s) {
+int sample_chunks(int V) { return (V + kSampleChunk - 1) / kSampleChunk; }
+
+int launch_sample(const float* logits, int R, int V, const vd_sampler* dev_params, float* part_v, int* part_i,
+                  int* out, cudaStream_t s) {
   if (R <= 0) return VD_OK;
-  sample_kernel<<<R, kSampleThreads, 0, s>>>(logits, V, dev_params, out);
+  if (V % 4) return fail(VD_ERR_UNSUPPORTED, "vocab must be a multiple of 4");
+  const int nchunk = sample_chunks(V);
+  sample_partial_kernel<<<dim3(R, nchunk), kSampleThreads, 0, s>>>(logits, V, dev_params, part_v, part_i);
+  VD_CUDA_TRY(cudaGetLastError());
+  sample_final_kernel<<<(R + 3) / 4, 128, 0, s>>>(part_v, part_i, R, nchunk, out);
   VD_CUDA_TRY(cudaGetLastError());
   return VD_OK;
 }

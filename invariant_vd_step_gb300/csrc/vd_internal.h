@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -10,6 +11,7 @@
 
 #include "vd.h"
 #include "vd_ops.h"
+#include "vd_engine.h"
 
 namespace vd {
 
@@ -33,7 +35,7 @@ int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd);
 // ---------------------------------------------------------------- GEMM
 enum Epilogue { EPI_BF16 = 0, EPI_RESIDUAL = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_GEGLU = 4 };
 constexpr int kGemmBM = 128;  // weight rows per tile (MMA M)
-constexpr int kGemmBN = 128;  // tokens per tile (MMA N), one shape for every T
+constexpr int kGemmBN = 256;  // tokens per tile (MMA N), one shape for every T
 constexpr int kGemmBK = 64;   // K per pipeline stage (one 128-byte swizzle row)
 
 struct GemmArgs {
@@ -43,9 +45,10 @@ struct GemmArgs {
   int K;                 // reduction length
   int ldo;               // output row stride (elements)
   int glu_up_row;        // GLU: first row of the up half in the weight matrix (= F)
+  int b_box_rows;        // rows of the activation TMA box (1..kGemmBN)
   int* status;           // device status word
 };
-// A = weight map (box 128 rows, or 64 for GLU), B = activation map (box 128 rows).
+// A = weight map (box 128 rows, or 64 for GLU), B = activation map (box kGemmBN rows).
 int launch_gemm(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, const GemmArgs& a, int epi,
                 cudaStream_t s);
 
@@ -108,7 +111,10 @@ struct RopeArgs {
 int launch_rope_kv(const RopeArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- sampling
-int launch_sample(const float* logits, int R, int V, const vd_sampler* dev_params, int* out, cudaStream_t s);
+// Two passes over [R][V] logits; part_v / part_i hold R * sample_chunks(V) winners.
+int sample_chunks(int V);
+int launch_sample(const float* logits, int R, int V, const vd_sampler* dev_params, float* part_v, int* part_i,
+                  int* out, cudaStream_t s);
 int launch_philox(uint64_t seed, uint64_t step, int n, uint32_t* out, cudaStream_t s);
 
 }  // namespace vd

@@ -65,10 +65,28 @@ class Sampler(ctypes.Structure):
 
 
 class KernelStat(ctypes.Structure):
-    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int32), ("total_ms", ctypes.c_double)]
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int32), ("kernels", ctypes.c_int32),
+                ("total_ms", ctypes.c_double)]
+
+
+class EngineConfig(ctypes.Structure):
+    _fields_ = [("num_pages", ctypes.c_int32), ("max_batch", ctypes.c_int32), ("token_budget", ctypes.c_int32),
+                ("prefix_reuse", ctypes.c_int32), ("placement_seed", ctypes.c_int64),
+                ("hash_mode", ctypes.c_int32), ("pad_", ctypes.c_int32)]
+
+
+class EngineStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in
+                ("steps", "prefix_hit_pages", "registered", "evicted", "preempted", "hash_candidates_rejected")]
+
+
+class PlanOut(ctypes.Structure):
+    _fields_ = [("batch", Batch), ("rids", ctypes.POINTER(ctypes.c_int64)),
+                ("samplers", ctypes.POINTER(Sampler))]
 
 
 _VP = ctypes.c_void_p
+_I64P = ctypes.POINTER(ctypes.c_int64)
 _SIGS = {
     "vd_create_model": (ctypes.c_int, [ctypes.POINTER(ModelConfig), ctypes.POINTER(WeightPtrs), ctypes.POINTER(_VP)]),
     "vd_destroy_model": (None, [_VP]),
@@ -91,6 +109,18 @@ _SIGS = {
     "vd_op_rope_kv": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
     "vd_op_attention_static": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
     "vd_op_philox": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int32, _VP, _VP]),
+    "vd_engine_create": (ctypes.c_int, [ctypes.POINTER(EngineConfig), ctypes.POINTER(_VP)]),
+    "vd_engine_destroy": (None, [_VP]),
+    "vd_engine_add_request": (ctypes.c_int, [_VP, _I32P, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64,
+                                             ctypes.c_float, _I64P]),
+    "vd_engine_plan": (ctypes.c_int, [_VP, ctypes.POINTER(PlanOut)]),
+    "vd_engine_commit": (ctypes.c_int, [_VP, _I32P]),
+    "vd_engine_run_step": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _I64P, _I32P, _I32P, _VP]),
+    "vd_engine_pending": (ctypes.c_int, [_VP]),
+    "vd_engine_get_stats": (ctypes.c_int, [_VP, ctypes.POINTER(EngineStats)]),
+    "vd_engine_check": (ctypes.c_int, [_VP]),
+    "vd_engine_page_info": (ctypes.c_int, [_VP, ctypes.c_int32, _I32P, _I32P]),
+    "vd_engine_history": (ctypes.c_int, [_VP, ctypes.c_int64, _I32P, ctypes.c_int32, _I32P, _I32P]),
 }
 
 _LIB = None
@@ -181,6 +211,29 @@ class StepBatch:
         self.c = Batch(len(self.tokens), len(seqs), len(self.logit_rows), pt_all.shape[1],
                        p_tok, p_pos, p_cu, p_c, p_pt, p_lr)
 
+    @classmethod
+    def from_arrays(cls, token_ids, cu_q, cached_len, page_table, logit_rows=()):
+        """Builds the descriptor from ready numpy arrays (no per-request loop).
+
+        page_table is [B][stride]; positions are derived as cached_len + offset.
+        """
+        self = cls.__new__(cls)
+        self.tokens, p_tok = _i32(token_ids)
+        self.cu_q, p_cu = _i32(cu_q)
+        self.cached, p_c = _i32(cached_len)
+        qlen = np.diff(self.cu_q)
+        seq = np.repeat(np.arange(len(qlen), dtype=np.int32), qlen)
+        self.positions, p_pos = _i32(self.cached[seq] + (np.arange(len(self.tokens), dtype=np.int32)
+                                                         - self.cu_q[:-1][seq]))
+        pt = np.ascontiguousarray(page_table, dtype=np.int32)
+        if pt.ndim == 1:
+            pt = pt.reshape(len(qlen), -1)
+        self.page_table, p_pt = _i32(pt)
+        self.logit_rows, p_lr = _i32(np.asarray(logit_rows, dtype=np.int32))
+        self.c = Batch(len(self.tokens), len(qlen), len(self.logit_rows), pt.shape[1],
+                       p_tok, p_pos, p_cu, p_c, p_pt, p_lr)
+        return self
+
     @property
     def num_tokens(self):
         return int(self.c.num_tokens)
@@ -263,7 +316,8 @@ class Model:
         n = lib().vd_profile_collect(self.h, arr, 32)
         if n < 0:
             check(n)
-        return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms)) for i in range(n)}
+        return {arr[i].name.decode(): (int(arr[i].launches), int(arr[i].kernels), float(arr[i].total_ms))
+                for i in range(n)}
 
 
 class KVPool:

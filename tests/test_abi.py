@@ -52,3 +52,15 @@ def test_ops_validate_arguments(L):
     assert L.vd_op_philox(1, 2, -1, None, None) == 1
     assert L.vd_sample(None, None, 1, None, None, None) == 1
     assert L.vd_step(None, None, None, None, None) == 1
+
+
+def test_step_batch_from_arrays_matches_per_request_builder():
+    import numpy as np
+    seqs = [(np.array([5, 6, 7]), 10, np.array([3, 4])), (np.array([9]), 0, np.array([8]))]
+    a = vd.StepBatch(seqs, logit_rows=[2, 3])
+    b = vd.StepBatch.from_arrays(np.array([5, 6, 7, 9]), np.array([0, 3, 4]), np.array([10, 0]),
+                                 np.array([[3, 4], [8, 0]]), [2, 3])
+    for f in ("tokens", "positions", "cu_q", "cached", "page_table", "logit_rows"):
+        np.testing.assert_array_equal(getattr(a, f), getattr(b, f))
+    assert (a.c.num_tokens, a.c.num_seqs, a.c.num_logit_rows, a.c.page_table_stride) == \
+        (b.c.num_tokens, b.c.num_seqs, b.c.num_logit_rows, b.c.page_table_stride)

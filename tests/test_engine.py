@@ -19,18 +19,20 @@ def _prompts(n=6, seed=1):
     return synth.make_prompts(n, 17, 50, SPEC.vocab, seed=seed, shared_prefix=32, n_sharing=4)
 
 
-def _run(weights, prompts, max_new=6, num_pages=64, page_hash=engine.default_page_hash, **kw):
+def _run(weights, prompts, max_new=6, num_pages=64, **kw):
     box = {}
     ex = OracleExecutor(SPEC, weights, num_pages,
-                        write_guard=lambda pg: pg not in box["eng"].bm.meta)
-    eng = engine.Engine(ex, num_pages, page_hash=page_hash, **kw)
+                        write_guard=lambda pg: not box["eng"].page_info(pg)[1])
+    eng = engine.Engine(ex, num_pages, **kw)
     box["eng"] = eng
     for i, p in enumerate(prompts):
         eng.add_request(p, max_new, seed=100 + i)
-    while eng.waiting or eng.running:
+    n = 0
+    while eng.pending():
         eng.step()
-        eng.bm.check()
-        assert eng.steps < 10000
+        eng.check()
+        n += 1
+        assert n < 10000
     return eng
 
 
@@ -47,7 +49,7 @@ def _cold_check(weights, eng):
 
 def test_engine_views_equal_cold_forward_with_prefix_reuse(weights):
     eng = _run(weights, _prompts(), max_batch=3, token_budget=24, placement_seed=5)
-    assert eng.bm.stats["prefix_hit_pages"] > 0
+    assert eng.stats["prefix_hit_pages"] > 0
     _cold_check(weights, eng)
 
 
@@ -57,14 +59,14 @@ def test_forced_hash_collisions_never_cause_reuse(weights):
     prompts = _prompts(seed=2)
     prompts.append(prompts[0][:20].copy())
     prompts[-1][17] = (prompts[-1][17] + 1) % SPEC.vocab  # same first page, different second
-    eng = _run(weights, prompts, max_batch=2, token_budget=32, page_hash=lambda ph, t: 7)
-    assert eng.bm.stats["hash_candidates_rejected"] > 0
+    eng = _run(weights, prompts, max_batch=2, token_budget=32, hash_mode=1)
+    assert eng.stats["hash_candidates_rejected"] > 0
     _cold_check(weights, eng)
 
 
 def test_pool_pressure_evicts_leaves_and_recomputes(weights):
     eng = _run(weights, _prompts(seed=3), max_new=8, num_pages=9, max_batch=4, token_budget=40)
-    assert eng.bm.stats["preempted"] > 0 or eng.bm.stats["evicted"] > 0
+    assert eng.stats["preempted"] > 0 or eng.stats["evicted"] > 0
     _cold_check(weights, eng)
 
 
@@ -87,17 +89,22 @@ def test_definition_2_1_prefix_comparable_across_executions(weights):
                 assert ta == tb
 
 
-def test_block_manager_leaf_only_eviction_unit():
-    bm = engine.BlockManager(4)
-    toks = np.arange(64)
-    a = bm.allocate(3)
-    h0, c0 = bm.register(a[0], -1, 0, toks[:16], 0)
-    _, c1 = bm.register(a[1], a[0], 1, toks[16:32], h0)
-    assert (c0, c1) == (a[0], a[1])
-    bm.release(a)  # a[2] unregistered -> free; a[1] is a leaf; a[0] has a child
-    assert list(bm.evictable) == [a[1]]
-    got = bm.allocate(3)  # needs 3: 2 free + evict leaf a[1], then a[0] becomes a leaf
-    assert got is not None and a[0] in bm.evictable
-    bm.check()
-    assert bm.match_prefix(toks, 4) == [a[0]]
-    assert bm.match_prefix(np.concatenate([[1], toks[1:]]), 4) == []
+def test_finished_prefix_is_retained_then_evicted_leaf_first(weights):
+    # A finished request's registered pages stay reusable (retain); under
+    # pressure the unreferenced leaves go first, never a parent of a kept page.
+    base = synth.make_tokens(40, SPEC.vocab, seed=21)
+    first = _run(weights, [base], max_new=2, num_pages=8, max_batch=1)
+    assert first.stats["registered"] >= 2
+    ex = OracleExecutor(SPEC, weights, 8)
+    eng = engine.Engine(ex, 8, max_batch=1, token_budget=64)
+    eng.add_request(base, 2, seed=1)
+    eng.run()
+    eng.add_request(base[:36], 2, seed=2)         # same first two pages
+    eng.run()
+    st = eng.stats
+    assert st["prefix_hit_pages"] == 2, st
+    eng.add_request(synth.make_tokens(100, SPEC.vocab, seed=22), 2, seed=3)  # needs 7 of 8 pages
+    eng.run()
+    eng.check()
+    assert eng.stats["evicted"] >= 1
+    _cold_check(weights, eng)
