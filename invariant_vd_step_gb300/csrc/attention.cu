@@ -1,12 +1,13 @@
 // Unified prefill/decode paged attention with a fixed KV split size.
 //
 // Rows.  For request b and KV head g the rows are (token i, query head of
-// the group) pairs, token-major.  A warp owns 16 rows; a CTA owns 16*NW rows
-// of one (request, KV head) and one KV split.  Decode-shaped requests
-// (q_len * Hq/Hkv <= 16) run with NW = 1, longer chunks with NW = 4 so that
-// four warps share each K/V tile.  The per-row instruction sequence is the
-// same in both instantiations (the same `attn_tile` body), so a row's result
-// does not depend on which of them ran it.
+// the group) pairs, token-major.  A CTA owns a block of rows of one
+// (request, KV head) and one KV split.  Decode-shaped requests (q_len *
+// Hq/Hkv <= 16, one block of 16 rows) run with two warps that share the rows
+// and split the head dimension of the P V product; longer chunks run four
+// warps of 16 rows each, sharing every K/V tile.  The per-element instruction
+// sequence is the same in both instantiations (the same `attn_tile` body),
+// so a row's result does not depend on which of them ran it.
 //
 // Traversal (深入解析 Vosti §六 6.2, causal prefix equivalence and the
 // sliding-window traversal; "Deterministic and bit-exact inference",
@@ -26,8 +27,8 @@
 //
 // Numerics: S = Q K^T and O += P V on mma.sync m16n8k16 (bf16 in, fp32
 // accumulate), scores scaled by log2(e)/sqrt(hd), exp2 by ex2.approx,
-// P rounded to bf16 for the P V product and for the row sum, every other
-// float operation an explicitly rounded intrinsic.
+// P split into bf16 hi + lo terms for the P V product (fp32 for the row
+// sum), every other float operation an explicitly rounded intrinsic.
 #include <math.h>
 
 #include <mutex>
@@ -56,17 +57,20 @@ __device__ __forceinline__ uint32_t kv_off(int key, int chunk) {
   return pg * AttnCfg<HD>::PAGE_BYTES + lr * 128 + (((chunk & 7) ^ (lr & 7)) << 4);
 }
 
-template <int HD>
+template <int ND>
 struct RowState {
   float m[2], l[2];     // rows g and g+8 of the warp
-  float o[HD / 8][4];   // mma C fragments
+  float o[ND / 8][4];   // mma C fragments of the ND output dims this warp owns
 };
 
-// One key tile for the 16 rows of a warp.
-template <int HD, int BNK>
-__device__ __forceinline__ void attn_tile(RowState<HD>& st, const uint32_t (&qf)[HD / 16][4], uint32_t kbase,
+// One key tile for the 16 rows of a warp, which accumulates output dims
+// [dim0, dim0 + ND).  S and the softmax state are computed over the full
+// head either way, so every output element gets the same instruction chain
+// whether one warp owns all dims or several warps share them.
+template <int HD, int BNK, int ND>
+__device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)[HD / 16][4], uint32_t kbase,
                                           uint32_t vbase, int key0, const int (&pos)[2], const int (&lo)[2],
-                                          float scale_log2, int lane) {
+                                          float scale_log2, int lane, int dim0) {
   const int t4 = lane & 3, mi = lane >> 3, r8 = lane & 7;
   float s[BNK / 8][4];
 #pragma unroll
@@ -104,20 +108,27 @@ __device__ __forceinline__ void attn_tile(RowState<HD>& st, const uint32_t (&qf)
     mnew[r] = rv[r] ? fmaxf(st.m[r], mx[r]) : st.m[r];
     alpha[r] = rv[r] ? ex2(__fsub_rn(st.m[r], mnew[r])) : 1.0f;
   }
-  uint32_t pa[BNK / 16][4];
+  // P enters the P V product as two bf16 terms, hi = bf16(p) and
+  // lo = bf16(p - hi) (p - hi is exact in fp32), so the weights carry about
+  // 16 significant bits; the row sum uses the fp32 weights.
+  uint32_t pa[BNK / 16][4], pl[BNK / 16][4];
   float rs[2] = {0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < BNK / 8; ++j) {
-    float p[4];
+    float p[4], h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int r = e >> 1;
-      p[e] = (s[j][e] == -INFINITY) ? 0.f : bf16_round(ex2(__fsub_rn(s[j][e], mnew[r])));
+      p[e] = (s[j][e] == -INFINITY) ? 0.f : ex2(__fsub_rn(s[j][e], mnew[r]));
+      h[e] = bf16_round(p[e]);
+      l[e] = __fsub_rn(p[e], h[e]);
     }
     rs[0] = __fadd_rn(__fadd_rn(rs[0], p[0]), p[1]);
     rs[1] = __fadd_rn(__fadd_rn(rs[1], p[2]), p[3]);
-    pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p[0], p[1]);
-    pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p[2], p[3]);
+    pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(h[0], h[1]);
+    pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(h[2], h[3]);
+    pl[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(l[0], l[1]);
+    pl[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(l[2], l[3]);
   }
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -127,20 +138,23 @@ __device__ __forceinline__ void attn_tile(RowState<HD>& st, const uint32_t (&qf)
     st.m[r] = mnew[r];
   }
 #pragma unroll
-  for (int n = 0; n < HD / 8; ++n) {
+  for (int n = 0; n < ND / 8; ++n) {
     st.o[n][0] = __fmul_rn(st.o[n][0], alpha[0]);
     st.o[n][1] = __fmul_rn(st.o[n][1], alpha[0]);
     st.o[n][2] = __fmul_rn(st.o[n][2], alpha[1]);
     st.o[n][3] = __fmul_rn(st.o[n][3], alpha[1]);
   }
+  const int np0 = dim0 / 16;
 #pragma unroll
   for (int ks = 0; ks < BNK / 16; ++ks) {
 #pragma unroll
-    for (int np = 0; np < HD / 16; ++np) {
+    for (int np = 0; np < ND / 16; ++np) {
       uint32_t b[4];
-      ldmatrix_x4_trans(b, vbase + kv_off<HD>(ks * 16 + (mi & 1) * 8 + r8, np * 2 + (mi >> 1)));
+      ldmatrix_x4_trans(b, vbase + kv_off<HD>(ks * 16 + (mi & 1) * 8 + r8, (np0 + np) * 2 + (mi >> 1)));
       mma_bf16_16816(st.o[2 * np], pa[ks], b);
+      mma_bf16_16816(st.o[2 * np], pl[ks], b);
       mma_bf16_16816(st.o[2 * np + 1], pa[ks], b + 2);
+      mma_bf16_16816(st.o[2 * np + 1], pl[ks], b + 2);
     }
   }
 }
@@ -151,9 +165,14 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (globaltimer() - t0 > kWaitLimitNs) return;
 }
 
-template <int HD, int NW>
+// NW warps per CTA; groups of DS warps own the same 16 rows and split the
+// head dimension between them (DS = 2 for decode-shaped CTAs, which have one
+// row block only; DS = 1 for prefill CTAs).
+template <int HD, int NW, int DS>
 __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ CUtensorMap kvmap, AttnArgs a) {
   using C = AttnCfg<HD>;
+  constexpr int RB = 16 * NW / DS;  // rows per CTA
+  constexpr int ND = HD / DS;       // output dims per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + 4 * C::TILE_BYTES);
@@ -184,8 +203,8 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   const int kvh = local % a.Hkv;
   const int rb = local / a.Hkv;
   const int rows = qlen * G;
-  const int r0 = rb * 16 * NW;
-  const int r_end = min(rows, r0 + 16 * NW);
+  const int r0 = rb * RB;
+  const int r_end = min(rows, r0 + RB);
   const int p_min = cached + r0 / G, p_max = cached + (r_end - 1) / G;
   const int lo_min = a.window > 0 ? max(0, p_min - a.window + 1) : 0;
   const int key_lo = max(sidx * a.split, lo_min);
@@ -234,11 +253,12 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   // ---- this warp's rows
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, t4 = lane & 3;
+  const int dim0 = (warp % DS) * ND;
   int pos[2], lo[2], tok[2], hq[2];
   bool valid[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    const int row = r0 + warp * 16 + gq + 8 * r;
+    const int row = r0 + (warp / DS) * 16 + gq + 8 * r;
     valid[r] = row < rows;
     tok[r] = row / G;
     hq[r] = kvh * G + row % G;
@@ -255,14 +275,14 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
       qf[kk][2 + r] = valid[r] ? *reinterpret_cast<const uint32_t*>(qr + kk * 16 + 8 + t4 * 2) : 0u;
     }
   }
-  RowState<HD> st;
+  RowState<ND> st;
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     st.m[r] = -INFINITY;
     st.l[r] = 0.f;
   }
 #pragma unroll
-  for (int n = 0; n < HD / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
+  for (int n = 0; n < ND / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
 
   bool ok = true;
   int it = 0;
@@ -276,7 +296,7 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
     mine = __any_sync(0xffffffffu, mine);
     if (ok && mine) {
       const uint32_t kb = smem_u32(smem + stg * 2 * C::TILE_BYTES);
-      attn_tile<HD, C::BNK>(st, qf, kb, kb + C::TILE_BYTES, key0, pos, lo, a.scale_log2, lane);
+      attn_tile<HD, C::BNK, ND>(st, qf, kb, kb + C::TILE_BYTES, key0, pos, lo, a.scale_log2, lane, dim0);
     }
     if (__syncthreads_or(!ok)) break;
     if (threadIdx.x == 0 && it + 2 < ntiles) {
@@ -295,13 +315,13 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   for (int r = 0; r < 2; ++r) {
     if (!valid[r] || st.m[r] == -INFINITY) continue;
     const size_t base = (static_cast<size_t>(q0 + tok[r]) * a.Hq + hq[r]) * a.max_splits + sidx;
-    if (t4 == 0) {
+    if (t4 == 0 && dim0 == 0) {
       a.part_ml[base * 2] = st.m[r];
       a.part_ml[base * 2 + 1] = st.l[r];
     }
-    float* po = a.part_o + base * HD;
+    float* po = a.part_o + base * HD + dim0;
 #pragma unroll
-    for (int n = 0; n < HD / 8; ++n)
+    for (int n = 0; n < ND / 8; ++n)
       *reinterpret_cast<float2*>(po + n * 8 + t4 * 2) = make_float2(st.o[n][2 * r], st.o[n][2 * r + 1]);
   }
 }
@@ -337,15 +357,15 @@ __global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
   for (int i = 0; i < PER; ++i) out[i] = __float2bfloat16_rn(__fdiv_rn(O[i], L));
 }
 
-template <int HD, int NW>
+template <int HD, int NW, int DS>
 int launch_attn_t(const CUtensorMap& kvmap, const AttnArgs& a, int n_items, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
-    VD_CUDA_TRY(cudaFuncSetAttribute(attn_kernel<HD, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    VD_CUDA_TRY(cudaFuncSetAttribute(attn_kernel<HD, NW, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      AttnCfg<HD>::SMEM));
     configured = true;
   }
-  attn_kernel<HD, NW><<<n_items, NW * 32, AttnCfg<HD>::SMEM, s>>>(kvmap, a);
+  attn_kernel<HD, NW, DS><<<n_items, NW * 32, AttnCfg<HD>::SMEM, s>>>(kvmap, a);
   VD_CUDA_TRY(cudaGetLastError());
   return VD_OK;
 }
@@ -384,9 +404,9 @@ int attn_key_tile(int hd) { return hd >= 256 ? AttnCfg<256>::BNK : AttnCfg<128>:
 int launch_attention(const CUtensorMap& kvmap, const AttnArgs& a, int hd, bool prefill_class, int n_items,
                      cudaStream_t s) {
   if (n_items <= 0) return VD_OK;
-  if (hd == 64) return prefill_class ? launch_attn_t<64, 4>(kvmap, a, n_items, s) : launch_attn_t<64, 1>(kvmap, a, n_items, s);
-  if (hd == 128) return prefill_class ? launch_attn_t<128, 4>(kvmap, a, n_items, s) : launch_attn_t<128, 1>(kvmap, a, n_items, s);
-  if (hd == 256) return prefill_class ? launch_attn_t<256, 4>(kvmap, a, n_items, s) : launch_attn_t<256, 1>(kvmap, a, n_items, s);
+  if (hd == 64) return prefill_class ? launch_attn_t<64, 4, 1>(kvmap, a, n_items, s) : launch_attn_t<64, 2, 2>(kvmap, a, n_items, s);
+  if (hd == 128) return prefill_class ? launch_attn_t<128, 4, 1>(kvmap, a, n_items, s) : launch_attn_t<128, 2, 2>(kvmap, a, n_items, s);
+  if (hd == 256) return prefill_class ? launch_attn_t<256, 4, 1>(kvmap, a, n_items, s) : launch_attn_t<256, 2, 2>(kvmap, a, n_items, s);
   return fail(VD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
 }
 

@@ -46,6 +46,7 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* _
   uint4* yr = reinterpret_cast<uint4*>(y + static_cast<size_t>(r) * d);
   const int d8 = d >> 3;
   float ss = 0.f;
+#pragma unroll 4
   for (int c = lane; c < d8; c += 32) {
     float f[8];
     unpack8(xr[c], f);

@@ -11,14 +11,17 @@
 // batched run equals the singleton run bit for bit; zero-initialised
 // accumulator, same iteration order).
 //
-// Warp roles (192 threads): warp 0 issues TMA loads (one elected lane) and
-// owns the TMEM allocation; warp 1 issues tcgen05.mma (one lane); warps 2..5
-// read the accumulator from TMEM (warp w reaches lanes 32*(w%4)..+31) and run
-// the fused epilogue.  Every wait is bounded (see vd_device.cuh).
+// Warp roles (192 threads, one persistent CTA per SM): warp 0 issues TMA
+// loads (one elected lane) and owns the TMEM allocation; warp 1 issues
+// tcgen05.mma (one lane) into one of two TMEM accumulators; warps 2..5 read
+// the other accumulator (warp w reaches lanes 32*(w%4)..+31) and run the
+// fused epilogue.  Every wait is bounded (see vd_device.cuh).
 //
 // The activation box is as tall as the launch needs (up to 256 rows): rows of
 // the B tile past it keep stale shared-memory contents, which only feed
 // columns that are never stored (a column depends on its own row alone).
+#include <algorithm>
+
 #include "vd_device.cuh"
 #include "vd_internal.h"
 
@@ -49,6 +52,71 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (globaltimer() - t0 > kWaitLimitNs) return;
 }
 
+// Epilogue of one tile: accumulator columns [c*32, c*32+32) are tokens
+// t0.. of the tile; TMEM lane = weight row of the tile.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tacc, int tile_t, int tile_n, int lg,
+                                              int lane, float* xchg) {
+  const int row = lg * 32 + lane;  // tile row == TMEM lane
+  const uint32_t taddr = tacc + (static_cast<uint32_t>(lg * 32) << 16);
+  for (int c = 0; c < kGemmBN / 32; ++c) {
+    const int t0 = tile_t * kGemmBN + c * 32;
+    if (t0 >= args.T) break;  // uniform over the four epilogue warps
+    float v[32];
+    tmem_ld32(taddr + c * 32, v);
+    const int nt = min(32, args.T - t0);
+    if (EPI == EPI_F32) {
+      float* out = static_cast<float*>(args.out) + tile_n * kGemmBM + row;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
+    } else if (EPI == EPI_BF16) {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * kGemmBM + row;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(v[j]);
+    } else if (EPI == EPI_RESIDUAL) {
+      const size_t col = static_cast<size_t>(tile_n) * kGemmBM + row;
+      const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(args.residual) + col;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + col;
+      // The residual may alias the output: load the whole chunk first so
+      // the loads are not serialised behind the stores.
+      float r[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        r[j] = (j < nt) ? __bfloat162float(res[static_cast<size_t>(t0 + j) * args.ldo]) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nt)
+          out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fadd_rn(bf16_round(v[j]), r[j]));
+    } else {  // GLU: rows 0..63 gate, 64..127 up of the same 64 features
+      if (lg >= 2) {
+        float* xr = xchg + ((lg - 2) * 32 + lane) * 33;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xr[j] = bf16_round(v[j]);
+      }
+      epi_barrier();
+      if (lg < 2) {
+        const float* xr = xchg + (lg * 32 + lane) * 33;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * 64 + lg * 32 + lane;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j < nt) {
+            const float g = bf16_round(v[j]);
+            const float a = (EPI == EPI_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
+            out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fmul_rn(a, xr[j]));
+          }
+        }
+      }
+      epi_barrier();
+    }
+  }
+}
+
+// Persistent: CTA b handles tiles b, b + gridDim.x, ...; tile i = (token
+// tile i % n_tok_tiles, weight tile i / n_tok_tiles).  Two TMEM accumulators
+// (2 x 256 columns) let the MMAs of one tile run while the epilogue warps
+// drain the previous one.
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, GemmArgs args) {
@@ -59,8 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* xchg = reinterpret_cast<float*>(sB + kStages * kBStageBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(xchg + kXchgFloats);
   uint64_t* empty = full + kStages;
-  uint64_t* accum = empty + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* acc_full = empty + kStages;   // [2] MMAs of a tile done
+  uint64_t* acc_empty = acc_full + 2;     // [2] epilogue finished reading
+  uint64_t* mma_done = acc_empty + 2;     // every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   constexpr bool kGlu = (EPI == EPI_SWIGLU || EPI == EPI_GEGLU);
@@ -73,22 +143,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (skip) return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile_t = blockIdx.x, tile_n = blockIdx.y;
   const int KB = args.K / kGemmBK;
+  const int ntt = (args.T + kGemmBN - 1) / kGemmBN;
+  const int ntiles = ntt * args.n_wtiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&wmap);
     tma_prefetch_desc(&xmap);
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, kGemmBN);
+    tmem_alloc(tmem_slot, 2 * kGemmBN);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -96,140 +171,115 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  int issued = 0;  // producer: stages loaded so far
+  int issued = 0;  // producer: stages loaded so far (all tiles)
   if (warp == 0) {
     if (lane == 0) {
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % kStages;
-        if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, abort_flag, args.status)) break;
-        mbar_arrive_expect_tx(&full[s], kAStageBytes + args.b_box_rows * 128);
-        uint8_t* a = sA + s * kAStageBytes;
-        if (kGlu) {
-          tma_load_2d(a, &wmap, &full[s], kb * kGemmBK, tile_n * 64);
-          tma_load_2d(a + 64 * 128, &wmap, &full[s], kb * kGemmBK, args.glu_up_row + tile_n * 64);
-        } else {
-          tma_load_2d(a, &wmap, &full[s], kb * kGemmBK, tile_n * kGemmBM);
+      int g = 0;
+      for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+        const int tile_t = tile % ntt, tile_n = tile / ntt;
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) - 1) & 1, abort_flag, args.status)) break;
+          mbar_arrive_expect_tx(&full[s], kAStageBytes + args.b_box_rows * 128);
+          uint8_t* a = sA + s * kAStageBytes;
+          if (kGlu) {
+            tma_load_2d(a, &wmap, &full[s], kb * kGemmBK, tile_n * 64);
+            tma_load_2d(a + 64 * 128, &wmap, &full[s], kb * kGemmBK, args.glu_up_row + tile_n * 64);
+          } else {
+            tma_load_2d(a, &wmap, &full[s], kb * kGemmBK, tile_n * kGemmBM);
+          }
+          tma_load_2d(sB + s * kBStageBytes, &xmap, &full[s], kb * kGemmBK, tile_t * kGemmBN);
+          issued = g + 1;
         }
-        tma_load_2d(sB + s * kBStageBytes, &xmap, &full[s], kb * kGemmBK, tile_t * kGemmBN);
-        issued = kb + 1;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(kGemmBM, kGemmBN);
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % kStages;
-        if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag, args.status)) break;
+      int g = 0, i = 0;
+      for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x, ++i) {
+        const int b = i & 1;
+        if (i >= 2 && !mbar_wait(&acc_empty[b], ((i >> 1) - 1) & 1, abort_flag, args.status)) break;
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + s * kAStageBytes);
-        const uint32_t b0 = smem_u32(sB + s * kBStageBytes);
+        const uint32_t tacc = tmem + b * kGemmBN;
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int s = g % kStages;
+          if (!mbar_wait(&full[s], (g / kStages) & 1, abort_flag, args.status)) break;
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * kAStageBytes);
+          const uint32_t b0 = smem_u32(sB + s * kBStageBytes);
 #pragma unroll
-        for (int kk = 0; kk < kGemmBK / 16; ++kk)
-          umma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (kb | kk) != 0);
-        umma_commit(&empty[s]);
+          for (int kk = 0; kk < kGemmBK / 16; ++kk)
+            umma_bf16(tacc, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (kb | kk) != 0);
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&acc_full[b]);
       }
-      umma_commit(accum);  // fires once every issued MMA has completed
+      umma_commit(mma_done);  // fires once every issued MMA has completed
     }
   } else {
     const int lg = warp & 3;  // TMEM lane group reachable by this warp
-    const bool ok = mbar_wait(accum, 0, abort_flag, args.status);
-    tc_fence_after();
-    if (ok) {
-      const int row = lg * 32 + lane;  // tile row == TMEM lane
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(lg * 32) << 16);
-      for (int c = 0; c < kGemmBN / 32; ++c) {
-        const int t0 = tile_t * kGemmBN + c * 32;
-        if (t0 >= args.T) break;  // uniform over the four epilogue warps
-        float v[32];
-        tmem_ld32(taddr + c * 32, v);
-        const int nt = min(32, args.T - t0);
-        if (EPI == EPI_F32) {
-          float* out = static_cast<float*>(args.out) + tile_n * kGemmBM + row;
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
-        } else if (EPI == EPI_BF16) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * kGemmBM + row;
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(v[j]);
-        } else if (EPI == EPI_RESIDUAL) {
-          const size_t col = static_cast<size_t>(tile_n) * kGemmBM + row;
-          const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(args.residual) + col;
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + col;
-          // The residual may alias the output: load the whole chunk first so
-          // the loads are not serialised behind the stores.
-          float r[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            r[j] = (j < nt) ? __bfloat162float(res[static_cast<size_t>(t0 + j) * args.ldo]) : 0.f;
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nt)
-              out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fadd_rn(bf16_round(v[j]), r[j]));
-        } else {  // GLU: rows 0..63 gate, 64..127 up of the same 64 features
-          if (lg >= 2) {
-            float* xr = xchg + ((lg - 2) * 32 + lane) * 33;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) xr[j] = bf16_round(v[j]);
-          }
-          epi_barrier();
-          if (lg < 2) {
-            const float* xr = xchg + (lg * 32 + lane) * 33;
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * 64 + lg * 32 + lane;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j < nt) {
-                const float g = bf16_round(v[j]);
-                const float a = (EPI == EPI_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
-                out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fmul_rn(a, xr[j]));
-              }
-            }
-          }
-          epi_barrier();
-        }
-      }
+    int i = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+      const int b = i & 1;
+      if (!mbar_wait(&acc_full[b], (i >> 1) & 1, abort_flag, args.status)) break;
+      tc_fence_after();
+      epilogue_tile<EPI>(args, tmem + b * kGemmBN, tile % ntt, tile / ntt, lg, lane, xchg);
+      tc_fence_before();
+      mbar_arrive(&acc_empty[b]);
     }
   }
 
   // Teardown: let in-flight TMA copies land and issued MMAs finish, then
   // release TMEM.  On the normal path these waits return at once.
   if (warp == 0 && lane == 0 && *abort_flag) {
-    for (int kb = max(0, issued - kStages); kb < issued; ++kb) drain_wait(&full[kb % kStages], (kb / kStages) & 1);
+    for (int g = max(0, issued - kStages); g < issued; ++g) drain_wait(&full[g % kStages], (g / kStages) & 1);
   }
-  if (warp == 1 && lane == 0 && *abort_flag) drain_wait(accum, 0);
+  if (warp == 1 && lane == 0) drain_wait(mma_done, 0);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kGemmBN);
+    tmem_dealloc(tmem, 2 * kGemmBN);
   }
 }
 
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
 template <int EPI>
-int launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, const GemmArgs& a, cudaStream_t s) {
+int launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const GemmArgs& a, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
     VD_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
     configured = true;
   }
-  dim3 grid((a.T + kGemmBN - 1) / kGemmBN, n_tiles);
-  gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(wmap, xmap, a);
+  const int tiles = ((a.T + kGemmBN - 1) / kGemmBN) * a.n_wtiles;
+  gemm_kernel<EPI><<<std::min(tiles, sm_count()), kThreads, kSmemBytes, s>>>(wmap, xmap, a);
   VD_CUDA_TRY(cudaGetLastError());
   return VD_OK;
 }
 
 }  // namespace
 
-int launch_gemm(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, const GemmArgs& a, int epi,
+int launch_gemm(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, const GemmArgs& a0, int epi,
                 cudaStream_t s) {
-  if (a.T <= 0) return VD_OK;
+  if (a0.T <= 0) return VD_OK;
+  GemmArgs a = a0;
+  a.n_wtiles = n_tiles;
   switch (epi) {
-    case EPI_BF16: return launch_one<EPI_BF16>(wmap, xmap, n_tiles, a, s);
-    case EPI_RESIDUAL: return launch_one<EPI_RESIDUAL>(wmap, xmap, n_tiles, a, s);
-    case EPI_F32: return launch_one<EPI_F32>(wmap, xmap, n_tiles, a, s);
-    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(wmap, xmap, n_tiles, a, s);
-    case EPI_GEGLU: return launch_one<EPI_GEGLU>(wmap, xmap, n_tiles, a, s);
+    case EPI_BF16: return launch_one<EPI_BF16>(wmap, xmap, a, s);
+    case EPI_RESIDUAL: return launch_one<EPI_RESIDUAL>(wmap, xmap, a, s);
+    case EPI_F32: return launch_one<EPI_F32>(wmap, xmap, a, s);
+    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(wmap, xmap, a, s);
+    case EPI_GEGLU: return launch_one<EPI_GEGLU>(wmap, xmap, a, s);
     default: return fail(VD_ERR_INVALID_ARG, "unknown GEMM epilogue");
   }
 }

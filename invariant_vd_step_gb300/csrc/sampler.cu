@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_partial_kernel(const fl
   int bi = INT_MAX;
   const int blk0 = chunk * (kSampleChunk / 4);
   const int nblk = min(kSampleChunk / 4, V / 4 - blk0);
+#pragma unroll 4
   for (int k = threadIdx.x; k < nblk; k += kSampleThreads) {
     const int blk = blk0 + k;
     const float4 x = l4[blk];

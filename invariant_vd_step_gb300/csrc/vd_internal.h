@@ -46,6 +46,7 @@ struct GemmArgs {
   int ldo;               // output row stride (elements)
   int glu_up_row;        // GLU: first row of the up half in the weight matrix (= F)
   int b_box_rows;        // rows of the activation TMA box (1..kGemmBN)
+  int n_wtiles;          // weight tiles (set by launch_gemm)
   int* status;           // device status word
 };
 // A = weight map (box 128 rows, or 64 for GLU), B = activation map (box kGemmBN rows).

@@ -145,8 +145,11 @@ class Engine:
         return self.views
 
     def run_native(self, model, pool, logits, tokens_dev, keep_logits: bool = False, stream=None,
-                   max_steps: int = 1000000):
-        """Runs to completion with whole steps inside libvd (plan, step, sample, commit)."""
+                   max_steps: int = 1000000, on_step=None):
+        """Runs to completion with whole steps inside libvd (plan, step, sample, commit).
+
+        ``on_step(rids, logits_rows, tokens)`` is called after every step that
+        emitted rows (logits_rows: the first n rows of ``logits``)."""
         cap = int(tokens_dev.shape[0])
         rids = np.zeros(cap, dtype=np.int64)
         toks = np.zeros(cap, dtype=np.int32)
@@ -159,6 +162,8 @@ class Engine:
                                                ctypes.byref(n), s))
             for i in range(n.value):
                 self.views[int(rids[i])].append((logits[i].clone() if keep_logits else None, int(toks[i])))
+            if on_step is not None and n.value:
+                on_step(rids[:n.value].copy(), logits[:n.value], toks[:n.value].copy())
             steps += 1
         return self.views
 
