@@ -3,11 +3,12 @@
 // kernel sequence of one engine step.
 //
 // Fixed kernel choices (深入解析 Vosti §三 3.2): every constant that shapes a
-// reduction -- GEMM tile 128x128x64, attention key tile B_N (64 keys, 32 for
-// hd 256), KV split size S_kv (512 keys), RMSNorm lane layout -- is chosen
-// here from (dims, dtype, head geometry, page size) and never from a batch.
-// What varies per step (grid sizes, which TMA map bucket covers the T
-// activation rows, NW of the attention CTA) changes no row's arithmetic.
+// reduction -- GEMM tile 128 weight rows x 256 tokens x 64 (MMA 128x256x16),
+// attention key tile B_N (32 keys), KV split size S_kv (512 keys), RMSNorm
+// lane layout -- is chosen here from (dims, dtype, head geometry, page size)
+// and never from a batch.  What varies per step (grid sizes, which TMA map
+// bucket covers the T activation rows, the attention CTA shape) changes no
+// row's arithmetic.
 #include <math.h>
 #include <string.h>
 

@@ -41,7 +41,7 @@ namespace {
 
 template <int HD>
 struct AttnCfg {
-  static constexpr int BNK = (HD >= 256) ? 32 : 64;  // keys per tile
+  static constexpr int BNK = 32;                     // keys per tile
   static constexpr int PAGES = BNK / 16;             // 16-token pages per tile
   static constexpr int PAGE_BYTES = 16 * HD * 2;     // one page of one KV head
   static constexpr int TILE_BYTES = BNK * HD * 2;
@@ -400,6 +400,7 @@ int attn_static_scratch(void** ptr) {
 }
 
 int attn_key_tile(int hd) { return hd >= 256 ? AttnCfg<256>::BNK : AttnCfg<128>::BNK; }
+static_assert(512 % AttnCfg<64>::BNK == 0 && 512 % AttnCfg<256>::BNK == 0, "splits must hold whole key tiles");
 
 int launch_attention(const CUtensorMap& kvmap, const AttnArgs& a, int hd, bool prefill_class, int n_items,
                      cudaStream_t s) {
