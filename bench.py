@@ -123,6 +123,18 @@ def make_workload(B: int, steps: int, seed_ctx: int = 3):
     return spec, ctx, tables, num_pages
 
 
+def traffic_of(kernel, alg_bytes_per_launch):
+    """DRAM bytes of one launch, scaled from the committed ncu capture of a
+    smaller launch of the same kernel (traffic grows with the bytes
+    streamed); None when no capture covers the kernel."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)[kernel]
+        return int(round(t["dram_over_algorithmic"] * alg_bytes_per_launch))
+    except Exception:
+        return None
+
+
 def algorithmic_bytes(spec, ctx_lens, B):
     """Per decode step: weights + KV read/write + activations, and per kernel."""
     d, hd, Hq, Hkv, F, V = spec.d_model, spec.head_dim, spec.n_heads, spec.n_kv_heads, spec.ffn_dim, spec.vocab
@@ -265,7 +277,8 @@ def run_gpu(args):
                    "page_size": 16, "pages": "randomly permuted", "parallelism": f"replicas x{ws}",
                    "l2": f"inputs larger than L2 ({total_bytes / 1e9:.2f} GB read+written per step)"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dk["GB_s"], "peak": hbm, "unit": "GB/s",
-                     "frac": dk["hbm_frac"], "traffic": None, "peak_source": peak_kind,
+                     "frac": dk["hbm_frac"], "traffic": traffic_of(dom, kbytes[dom] / max(1, round(dk["launches_per_step"]))),
+                     "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": int(kbytes[dom] / max(1, round(dk["launches_per_step"])))},
         "step_roofline": {"algorithmic_bytes": total_bytes, "GB_s": round(step_gbs, 1),
                           "frac": round(step_gbs / hbm, 4)},
