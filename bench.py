@@ -204,11 +204,10 @@ def run_gpu(args):
         model.step(pool, batches[s], logits, stream)
         model.sample(logits, samplers, out_tok, stream)
 
+    model.set_graph_mode(args.graphs)  # 0: eager launches
     for s in range(Wm):
         one(s)
     torch.cuda.synchronize()
-    model.profile_collect()
-    model.profile(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         dist.barrier()
@@ -221,9 +220,21 @@ def run_gpu(args):
         torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    graph_stats = model.graph_stats()
+    # Per-kernel times: the same K steps again, eager, with events around
+    # every kernel class (profiling forces eager launches).
+    model.profile_collect()
+    model.profile(True)
+    ep0, ep1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ep0.record(stream)
+    for s in range(Wm, Wm + K):
+        one(s)
+    ep1.record(stream)
+    torch.cuda.synchronize()
     model.profile(False)
     prof = model.profile_collect()
-    ms = ev0.elapsed_time(ev1)
+    prof_ms = ep0.elapsed_time(ep1)
     assert model.device_status() == 0, "a bounded on-device wait timed out"
 
     # ---- end to end: host descriptor + tokens fed back, D2H of sampled tokens each step
@@ -236,6 +247,8 @@ def run_gpu(args):
     for s in range(args.e2e_steps):
         b = batch_at(base + s, last)
         need = (int(np.max(ctx)) + base + s + 16) // 16  # page-table columns the library uploads
+        if args.graphs:  # graph mode rounds the stride up to 64 pages
+            need = min((need + 63) // 64 * 64, (CTX_HI + total_steps + 16 + 15) // 16)
         h2d = 4 * (3 * B + 2 * (B + 1) + 3 * B + B * need + B)
         model.step(pool, b, logits, stream)
         model.sample(logits, samplers, out_tok, stream)
@@ -259,7 +272,7 @@ def run_gpu(args):
     for name, (n, nk, tot) in prof.items():
         per_step = tot / K
         e = {"launches_per_step": n / K, "kernels_per_step": nk / K, "ms_per_step": round(per_step, 5),
-             "share": round(tot / ms_max, 4)}
+             "share": round(tot / prof_ms, 4)}
         if name in kbytes:
             gbs = kbytes[name] / (per_step * 1e-3) / 1e9
             e.update({"algorithmic_bytes": kbytes[name], "GB_s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)})
@@ -275,6 +288,7 @@ def run_gpu(args):
         "config": {"workload": "llama3.1-8b-shape 1 decoder layer + LM head, pure decode",
                    "batch": B, "ctx": f"U[{CTX_LO},{CTX_HI}] mean {float(np.mean(ctx)):.0f}",
                    "page_size": 16, "pages": "randomly permuted", "parallelism": f"replicas x{ws}",
+                   "launch": f"CUDA graph replay (<= {args.graphs} graphs)" if args.graphs else "eager launches",
                    "l2": f"inputs larger than L2 ({total_bytes / 1e9:.2f} GB read+written per step)"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dk["GB_s"], "peak": hbm, "unit": "GB/s",
                      "frac": dk["hbm_frac"], "traffic": traffic_of(dom, kbytes[dom] / max(1, round(dk["launches_per_step"]))),
@@ -284,6 +298,8 @@ def run_gpu(args):
                           "frac": round(step_gbs / hbm, 4)},
         "kernels": kernels,
         "gpu_launches": launches * K,
+        "graphs": {"max_graphs": args.graphs, **graph_stats,
+                   "eager_profiled_ms_per_step": round(prof_ms / K, 4)},
         "e2e": {"value": round(ws * B * args.e2e_steps / e2e_max, 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * B, "steps": args.e2e_steps},
         "clocks": clk.summary(),
@@ -462,6 +478,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--batch", type=int, default=256)
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--graphs", type=int, default=64,
+                    help="decode: keep up to N captured step graphs (0 = eager launches)")
     ap.add_argument("--cpu-sample", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-invariance", action="store_true")

@@ -174,6 +174,26 @@ void* vd_kv_pool_data(vd_kv_pool* p);
  * T == 0 is a no-op. */
 int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out, void* stream);
 
+/* Graph replay of steps (an engineering addition; the pages' design has no
+ * counterpart).  With max_graphs > 0, vd_step keeps the descriptor upload as
+ * an ordinary copy on the stream and replays the step's kernel sequence as
+ * one CUDA graph, captured the first time its key is seen.  The key is
+ * (pool, logits_out address, T, B, R, page-table stride, number of decode-
+ * and prefill-class requests, attention grid sizes); in this mode the
+ * stride is rounded up to 64 pages and each attention grid to a 1/16
+ * quantum of its item count (extra CTAs exit at once), so steady decode
+ * steps share a graph.  The kernels, their arguments and every row's
+ * arithmetic are those of the eager path: logits are bitwise identical.
+ * At most max_graphs executables are kept (least recently replayed goes
+ * first); 0 turns the mode off and frees them.  Profiling (vd_profile_enable)
+ * forces the eager path.  A capture costs milliseconds of host time.  Not
+ * thread-safe: one host thread drives a model.
+ * Errors: VD_ERR_INVALID_ARG (null model, max_graphs < 0). */
+int vd_set_graph_mode(vd_model* m, int32_t max_graphs);
+/* out3[0] = graphs captured, out3[1] = replays of a cached graph, out3[2] =
+ * graphs currently cached (host int64 [3]). */
+int vd_graph_stats(const vd_model* m, int64_t* out3);
+
 /* Token choice for R rows of dev float32 logits [R][V] (16-byte aligned) -> dev int32 [R]:
  * greedy argmax (lowest index on ties) or Gumbel-max with Philox4x32-10
  * (per-row state in host array per_row[R]). */

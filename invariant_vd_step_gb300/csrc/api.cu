@@ -13,6 +13,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <unordered_set>
@@ -120,7 +121,25 @@ struct Desc {
   int T = 0, B = 0, R = 0, stride = 0;
   int tokens, positions, slot_page, cu_q, cached, page_table, logit_rows, dec_seq, dec_start, pre_seq, pre_start;
   int n_dec = 0, n_pre = 0, items_dec = 0, items_pre = 0;
+  int grid_dec = 0, grid_pre = 0;  // attention CTAs launched (>= items; extra CTAs exit)
   int total = 0;
+};
+
+// What a captured step graph depends on beyond the model: every kernel
+// argument and grid size of a step is a function of these fields.
+struct GraphKey {
+  unsigned long long pool_id = 0;
+  const void* logits = nullptr;
+  int T = 0, B = 0, R = 0, stride = 0, n_dec = 0, n_pre = 0, grid_dec = 0, grid_pre = 0;
+  bool operator==(const GraphKey& o) const {
+    return pool_id == o.pool_id && logits == o.logits && T == o.T && B == o.B && R == o.R && stride == o.stride &&
+           n_dec == o.n_dec && n_pre == o.n_pre && grid_dec == o.grid_dec && grid_pre == o.grid_pre;
+  }
+};
+struct GraphEntry {
+  GraphKey key;
+  cudaGraphExec_t exec = nullptr;
+  long long used = 0;
 };
 
 }  // namespace
@@ -164,10 +183,16 @@ struct vd_model {
   double prof_ms[K_COUNT] = {};
   int prof_n[K_COUNT] = {};
   int prof_k[K_COUNT] = {};
+  // graph replay of steps
+  int graph_max = 0;
+  cudaStream_t cap_stream = nullptr;
+  std::vector<GraphEntry> graphs;
+  long long graph_clock = 0, graph_captures = 0, graph_replays = 0;
 };
 
 struct vd_kv_pool {
   vd_model* m = nullptr;
+  unsigned long long id = 0;  // never reused, unlike the host address
   int num_pages = 0;
   void* data = nullptr;
   bool owned = false;
@@ -267,7 +292,22 @@ int attn_items(int qlen, int kv_len, int G, int Hkv, int rows_per_cta) {
 }
 
 // Validates a step descriptor and builds the upload image in h.
-int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_tokens, Desc& d, int* h) {
+// Highest power of two <= n, divided by 16, is the rounding quantum: at most
+// 1/16 of the CTAs are extra, and the rounded count changes rarely as
+// contexts grow.
+int bucket_items(int n) {
+  if (n <= 16) return n;
+  int p = 1;
+  while (p <= n / 2) p *= 2;
+  const int q = p / 16;
+  return (n + q - 1) / q * q;
+}
+
+// graph_shape rounds the page-table stride up to 64 pages and the attention
+// grids with bucket_items(), so that consecutive decode steps share one
+// captured graph; neither changes any row's arithmetic.
+int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_tokens, Desc& d, int* h,
+               bool graph_shape = false) {
   const vd_model_config& c = m->cfg;
   if (!b) return fail(VD_ERR_INVALID_ARG, "null batch");
   const int T = b->num_tokens, B = b->num_seqs, R = b->num_logit_rows;
@@ -294,6 +334,7 @@ int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_token
     if (np > b->page_table_stride) return fail(VD_ERR_OUT_OF_RANGE, "page table narrower than the request");
     stride = std::max(stride, np);
   }
+  if (graph_shape) stride = std::min((stride + 63) / 64 * 64, (c.max_context + 15) / 16);
   d.T = T;
   d.B = B;
   d.R = R;
@@ -371,15 +412,18 @@ int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_token
   d.n_pre = npre;
   d.items_dec = idec;
   d.items_pre = ipre;
+  d.grid_dec = graph_shape ? bucket_items(idec) : idec;
+  d.grid_pre = graph_shape ? bucket_items(ipre) : ipre;
   return VD_OK;
 }
 
-int upload_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_tokens, Desc& d, cudaStream_t s) {
+int upload_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_tokens, Desc& d, cudaStream_t s,
+                bool graph_shape = false) {
   const int slot = m->desc_slot;
   m->desc_slot ^= 1;
   VD_CUDA_TRY(cudaEventSynchronize(m->desc_ev[slot]));  // previous upload from this staging slot is done
   int* h = m->h_desc[slot];
-  int rc = build_desc(m, pool, b, need_tokens, d, h);
+  int rc = build_desc(m, pool, b, need_tokens, d, h, graph_shape);
   if (rc || d.T == 0) return rc;
   VD_CUDA_TRY(cudaMemcpyAsync(m->d_desc, h, static_cast<size_t>(d.total) * 4, cudaMemcpyHostToDevice, s));
   VD_CUDA_TRY(cudaEventRecord(m->desc_ev[slot], s));
@@ -414,14 +458,14 @@ int run_attention(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d, const
     a.cls_seq = m->d_desc + d.dec_seq;
     a.cls_start = m->d_desc + d.dec_start;
     a.n_cls = d.n_dec;
-    if ((rc = launch_attention(pool->map, a, hd, false, d.items_dec, s))) return rc;
+    if ((rc = launch_attention(pool->map, a, hd, false, d.grid_dec, s))) return rc;
   }
   if (d.n_pre) {
     Prof p(m, K_ATTN, s);
     a.cls_seq = m->d_desc + d.pre_seq;
     a.cls_start = m->d_desc + d.pre_start;
     a.n_cls = d.n_pre;
-    if ((rc = launch_attention(pool->map, a, hd, true, d.items_pre, s))) return rc;
+    if ((rc = launch_attention(pool->map, a, hd, true, d.grid_pre, s))) return rc;
   }
   MergeArgs g{};
   g.part_o = m->part_o;
@@ -526,6 +570,127 @@ int* op_status() {
 }
 
 int check_model(const vd_model* m) { return m ? VD_OK : fail(VD_ERR_INVALID_ARG, "null model"); }
+
+// The kernel sequence of one step (descriptor already uploaded).
+int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out, cudaStream_t s) {
+  int rc;
+  const vd_model_config& c = m->cfg;
+  const int T = d.T, dm = c.d_model, hd = c.head_dim, F = c.ffn_dim;
+  const int qkv_dim = (c.n_heads + 2 * c.n_kv_heads) * hd;
+  {
+    Prof p(m, K_EMBED, s);
+    if ((rc = launch_embed(m->embed, m->d_desc + d.tokens, m->x, T, dm, s))) return rc;
+  }
+  GemmArgs g{};
+  g.status = m->status;
+  g.T = T;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const vd_layer_weights& L = m->layers[l];
+    {
+      Prof p(m, K_RMSNORM, s);
+      if ((rc = launch_rmsnorm(m->x, nullptr, L.attn_norm, m->a.ptr, T, dm, c.rms_eps, s))) return rc;
+    }
+    {
+      Prof p(m, K_GEMM_QKV, s);
+      g.out = m->qkv; g.residual = nullptr; g.K = dm; g.ldo = qkv_dim; g.b_box_rows = m->a.box_for(T);
+      if ((rc = launch_gemm(m->m_qkv[l], m->a.map_for(T), qkv_dim / kGemmBM, g, EPI_BF16, s))) return rc;
+    }
+    if ((rc = run_rope(m, pool, l, d, m->qkv, m->q, s))) return rc;
+    if ((rc = run_attention(m, pool, l, d, m->q, m->o.ptr, s))) return rc;
+    {
+      Prof p(m, K_GEMM_O, s);
+      g.out = m->x; g.residual = m->x; g.K = c.n_heads * hd; g.ldo = dm; g.b_box_rows = m->o.box_for(T);
+      if ((rc = launch_gemm(m->m_o[l], m->o.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
+    }
+    {
+      Prof p(m, K_RMSNORM, s);
+      if ((rc = launch_rmsnorm(m->x, nullptr, L.ffn_norm, m->a.ptr, T, dm, c.rms_eps, s))) return rc;
+    }
+    {
+      Prof p(m, K_GEMM_GU, s);
+      g.out = m->z.ptr; g.residual = nullptr; g.K = dm; g.ldo = F; g.glu_up_row = F; g.b_box_rows = m->a.box_for(T);
+      if ((rc = launch_gemm(m->m_gu[l], m->a.map_for(T), F / 64, g,
+                            c.act == VD_ACT_GEGLU ? EPI_GEGLU : EPI_SWIGLU, s)))
+        return rc;
+    }
+    {
+      Prof p(m, K_GEMM_DOWN, s);
+      g.out = m->x; g.residual = m->x; g.K = F; g.ldo = dm; g.b_box_rows = m->z.box_for(T);
+      if ((rc = launch_gemm(m->m_down[l], m->z.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
+    }
+  }
+  if (d.R > 0) {
+    {
+      Prof p(m, K_FINAL_NORM, s);
+      if ((rc = launch_rmsnorm(m->x, m->d_desc + d.logit_rows, m->final_norm, m->ar.ptr, d.R, dm, c.rms_eps, s)))
+        return rc;
+    }
+    Prof p(m, K_GEMM_LM, s);
+    GemmArgs h{};
+    h.status = m->status;
+    h.T = d.R;
+    h.out = logits_out;
+    h.K = dm;
+    h.ldo = c.vocab;
+    h.b_box_rows = m->ar.box_for(d.R);
+    if ((rc = launch_gemm(m->m_lm, m->ar.map_for(d.R), c.vocab / kGemmBM, h, EPI_F32, s))) return rc;
+  }
+  return VD_OK;
+}
+
+// Replays the graph captured for d's key, capturing it first if new.
+// Capture runs on a private stream (the legacy default stream cannot be
+// captured); the replay is launched on s, after the descriptor upload.
+int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out, cudaStream_t s) {
+  GraphKey k;
+  k.pool_id = pool->id;
+  k.logits = logits_out;
+  k.T = d.T;
+  k.B = d.B;
+  k.R = d.R;
+  k.stride = d.stride;
+  k.n_dec = d.n_dec;
+  k.n_pre = d.n_pre;
+  k.grid_dec = d.grid_dec;
+  k.grid_pre = d.grid_pre;
+  for (GraphEntry& e : m->graphs)
+    if (e.key == k) {
+      e.used = ++m->graph_clock;
+      ++m->graph_replays;
+      VD_CUDA_TRY(cudaGraphLaunch(e.exec, s));
+      return VD_OK;
+    }
+  if (!m->cap_stream) VD_CUDA_TRY(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
+  VD_CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeRelaxed));
+  const int rc = enqueue_step(m, pool, d, logits_out, m->cap_stream);
+  cudaGraph_t g = nullptr;
+  const cudaError_t ce = cudaStreamEndCapture(m->cap_stream, &g);
+  if (rc || ce != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return rc ? rc : fail(VD_ERR_CUDA, std::string("step capture: ") + cudaGetErrorString(ce));
+  }
+  cudaGraphExec_t x = nullptr;
+  const cudaError_t ie = cudaGraphInstantiate(&x, g, 0);
+  cudaGraphDestroy(g);
+  if (ie != cudaSuccess) return fail(VD_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(ie));
+  if (static_cast<int>(m->graphs.size()) >= m->graph_max) {  // drop the least recently replayed
+    auto lru = std::min_element(m->graphs.begin(), m->graphs.end(),
+                                [](const GraphEntry& a, const GraphEntry& b) { return a.used < b.used; });
+    cudaGraphExecDestroy(lru->exec);  // freed after any launch still in flight
+    m->graphs.erase(lru);
+  }
+  m->graphs.push_back({k, x, ++m->graph_clock});
+  ++m->graph_captures;
+  VD_CUDA_TRY(cudaGraphLaunch(x, s));
+  return VD_OK;
+}
+
+void drop_graphs(vd_model* m) {
+  for (GraphEntry& e : m->graphs) cudaGraphExecDestroy(e.exec);
+  m->graphs.clear();
+}
+
 
 }  // namespace
 
@@ -635,6 +800,8 @@ int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_mode
 void vd_destroy_model(vd_model* m) {
   if (!m) return;
   cudaDeviceSynchronize();
+  drop_graphs(m);
+  if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
   for (void* p : m->dev_allocs) cudaFree(p);
   for (int k = 0; k < 2; ++k) {
     if (m->h_desc[k]) cudaFreeHost(m->h_desc[k]);
@@ -664,8 +831,10 @@ int vd_kv_pool_alloc(vd_model* m, int32_t num_pages, void* dev_mem, size_t bytes
   const vd_model_config& c = m->cfg;
   const long long rows = static_cast<long long>(c.n_layers) * num_pages * 2 * c.n_kv_heads * 16;
   if (rows + 16 > 0x7fffffffLL) return fail(VD_ERR_CAPACITY, "pool too large for 32-bit TMA row coordinates");
+  static std::atomic<unsigned long long> next_id{1};
   vd_kv_pool* p = new vd_kv_pool();
   p->m = m;
+  p->id = next_id++;
   p->num_pages = num_pages;
   p->rows = rows;
   if (dev_mem) {
@@ -714,70 +883,29 @@ int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out,
   if (check_model(m) || !pool || pool->m != m) return fail(VD_ERR_INVALID_ARG, "null or foreign model/pool");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (b && b->num_logit_rows > 0 && !logits_out) return fail(VD_ERR_INVALID_ARG, "null logits_out");
+  const bool graph = m->graph_max > 0 && !m->profiling;
   Desc d;
-  int rc = upload_desc(m, pool, b, true, d, s);
+  int rc = upload_desc(m, pool, b, true, d, s, graph);
   if (rc || d.T == 0) return rc;
-  const vd_model_config& c = m->cfg;
-  const int T = d.T, dm = c.d_model, hd = c.head_dim, F = c.ffn_dim;
-  const int qkv_dim = (c.n_heads + 2 * c.n_kv_heads) * hd;
-  {
-    Prof p(m, K_EMBED, s);
-    if ((rc = launch_embed(m->embed, m->d_desc + d.tokens, m->x, T, dm, s))) return rc;
+  return graph ? replay_step(m, pool, d, logits_out, s) : enqueue_step(m, pool, d, logits_out, s);
+}
+
+int vd_set_graph_mode(vd_model* m, int32_t max_graphs) {
+  if (check_model(m)) return VD_ERR_INVALID_ARG;
+  if (max_graphs < 0) return fail(VD_ERR_INVALID_ARG, "max_graphs must be >= 0");
+  m->graph_max = max_graphs;
+  while (static_cast<int>(m->graphs.size()) > max_graphs) {
+    cudaGraphExecDestroy(m->graphs.front().exec);
+    m->graphs.erase(m->graphs.begin());
   }
-  GemmArgs g{};
-  g.status = m->status;
-  g.T = T;
-  for (int l = 0; l < c.n_layers; ++l) {
-    const vd_layer_weights& L = m->layers[l];
-    {
-      Prof p(m, K_RMSNORM, s);
-      if ((rc = launch_rmsnorm(m->x, nullptr, L.attn_norm, m->a.ptr, T, dm, c.rms_eps, s))) return rc;
-    }
-    {
-      Prof p(m, K_GEMM_QKV, s);
-      g.out = m->qkv; g.residual = nullptr; g.K = dm; g.ldo = qkv_dim; g.b_box_rows = m->a.box_for(T);
-      if ((rc = launch_gemm(m->m_qkv[l], m->a.map_for(T), qkv_dim / kGemmBM, g, EPI_BF16, s))) return rc;
-    }
-    if ((rc = run_rope(m, pool, l, d, m->qkv, m->q, s))) return rc;
-    if ((rc = run_attention(m, pool, l, d, m->q, m->o.ptr, s))) return rc;
-    {
-      Prof p(m, K_GEMM_O, s);
-      g.out = m->x; g.residual = m->x; g.K = c.n_heads * hd; g.ldo = dm; g.b_box_rows = m->o.box_for(T);
-      if ((rc = launch_gemm(m->m_o[l], m->o.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
-    }
-    {
-      Prof p(m, K_RMSNORM, s);
-      if ((rc = launch_rmsnorm(m->x, nullptr, L.ffn_norm, m->a.ptr, T, dm, c.rms_eps, s))) return rc;
-    }
-    {
-      Prof p(m, K_GEMM_GU, s);
-      g.out = m->z.ptr; g.residual = nullptr; g.K = dm; g.ldo = F; g.glu_up_row = F; g.b_box_rows = m->a.box_for(T);
-      if ((rc = launch_gemm(m->m_gu[l], m->a.map_for(T), F / 64, g,
-                            c.act == VD_ACT_GEGLU ? EPI_GEGLU : EPI_SWIGLU, s)))
-        return rc;
-    }
-    {
-      Prof p(m, K_GEMM_DOWN, s);
-      g.out = m->x; g.residual = m->x; g.K = F; g.ldo = dm; g.b_box_rows = m->z.box_for(T);
-      if ((rc = launch_gemm(m->m_down[l], m->z.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
-    }
-  }
-  if (d.R > 0) {
-    {
-      Prof p(m, K_FINAL_NORM, s);
-      if ((rc = launch_rmsnorm(m->x, m->d_desc + d.logit_rows, m->final_norm, m->ar.ptr, d.R, dm, c.rms_eps, s)))
-        return rc;
-    }
-    Prof p(m, K_GEMM_LM, s);
-    GemmArgs h{};
-    h.status = m->status;
-    h.T = d.R;
-    h.out = logits_out;
-    h.K = dm;
-    h.ldo = c.vocab;
-    h.b_box_rows = m->ar.box_for(d.R);
-    if ((rc = launch_gemm(m->m_lm, m->ar.map_for(d.R), c.vocab / kGemmBM, h, EPI_F32, s))) return rc;
-  }
+  return VD_OK;
+}
+
+int vd_graph_stats(const vd_model* m, int64_t* out3) {
+  if (check_model(m) || !out3) return fail(VD_ERR_INVALID_ARG, "null argument");
+  out3[0] = m->graph_captures;
+  out3[1] = m->graph_replays;
+  out3[2] = static_cast<int64_t>(m->graphs.size());
   return VD_OK;
 }
 

@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   }
   // ---- work item -> (request, row block, KV head, split)
   const int item = blockIdx.x;
+  if (item >= a.cls_start[a.n_cls]) return;  // grid rounded up past the class's items
   int lo_i = 0, hi_i = a.n_cls - 1;
   while (lo_i < hi_i) {  // last j with cls_start[j] <= item
     const int mid = (lo_i + hi_i + 1) >> 1;

@@ -98,6 +98,8 @@ _SIGS = {
     "vd_sample": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Sampler), _VP, _VP]),
     "vd_copy_kv": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, _I32P, ctypes.c_int32, _VP, _VP, _VP]),
     "vd_device_status": (ctypes.c_int, [_VP]),
+    "vd_set_graph_mode": (ctypes.c_int, [_VP, ctypes.c_int32]),
+    "vd_graph_stats": (ctypes.c_int, [_VP, _I64P]),
     "vd_profile_enable": (ctypes.c_int, [_VP, ctypes.c_int32]),
     "vd_profile_collect": (ctypes.c_int, [_VP, ctypes.POINTER(KernelStat), ctypes.c_int32]),
     "vd_last_error": (ctypes.c_char_p, []),
@@ -310,6 +312,15 @@ class Model:
 
     def profile(self, on: bool):
         check(lib().vd_profile_enable(self.h, int(on)))
+
+    def set_graph_mode(self, max_graphs: int):
+        """Replay steps as captured CUDA graphs (0 = eager launches)."""
+        check(lib().vd_set_graph_mode(self.h, int(max_graphs)))
+
+    def graph_stats(self) -> dict:
+        out = (ctypes.c_int64 * 3)()
+        check(lib().vd_graph_stats(self.h, out))
+        return {"captures": int(out[0]), "replays": int(out[1]), "cached": int(out[2])}
 
     def profile_collect(self) -> dict:
         arr = (KernelStat * 32)()
