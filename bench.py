@@ -201,8 +201,7 @@ def run_gpu(args):
     samplers = [(1000 + i, 0, 0.0) for i in range(B)]
 
     def one(s):
-        model.step(pool, batches[s], logits, stream)
-        model.sample(logits, samplers, out_tok, stream)
+        model.step_sample(pool, batches[s], samplers, logits, out_tok, stream)
 
     model.set_graph_mode(args.graphs)  # 0: eager launches
     for s in range(Wm):
@@ -249,9 +248,8 @@ def run_gpu(args):
         need = (int(np.max(ctx)) + base + s + 16) // 16  # page-table columns the library uploads
         if args.graphs:  # graph mode rounds the stride up to 64 pages
             need = min((need + 63) // 64 * 64, (CTX_HI + total_steps + 16 + 15) // 16)
-        h2d = 4 * (3 * B + 2 * (B + 1) + 3 * B + B * need + B)
-        model.step(pool, b, logits, stream)
-        model.sample(logits, samplers, out_tok, stream)
+        h2d = 4 * (3 * B + 2 * (B + 1) + 3 * B + B * need + B) + 24 * B  # descriptor + sampler states
+        model.step_sample(pool, b, samplers, logits, out_tok, stream)
         host_tok.copy_(out_tok, non_blocking=True)
         stream.synchronize()
         last = host_tok.numpy().copy()

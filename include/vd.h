@@ -200,6 +200,18 @@ int vd_graph_stats(const vd_model* m, int64_t* out3);
 int vd_sample(vd_model* m, const float* logits, int32_t R, const vd_sampler* per_row,
               int32_t* tokens_out, void* stream);
 
+/* One engine step with the token choice fused into the LM-head GEMM
+ * [B §二 Definition 2.1: per-request sampler_0; Theorem 4.1 for the logits].
+ * Same validation, errors and logits as vd_step (logits_out may be NULL:
+ * then logits are computed but not stored), and tokens_out (dev int32 [R])
+ * holds exactly what vd_sample would choose from those logits: the GEMM
+ * epilogue scores each 32-row vocabulary group per token (greedy or
+ * Gumbel-max, per-row state in host per_row[R]) and a second kernel picks
+ * the (largest score, lowest index) winner, so the logits are never read
+ * back.  per_row is copied before the call returns. */
+int vd_step_sample(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const vd_sampler* per_row,
+                   float* logits_out, int32_t* tokens_out, void* stream);
+
 /* Debug: copies the K and V of `layer` for logical positions [0, n_tokens)
  * of one request (host page table) into dev bf16 out_k / out_v
  * [n_tokens][Hkv][hd], for bitwise checks of the KV-value invariant

@@ -12,7 +12,7 @@
  * (深入解析 Vosti §二 Theorem 4.1).
  *
  * Use: vd_engine_add_request() any number of times, then repeat either
- * vd_engine_run_step() (plan, vd_step, vd_sample, copy tokens back, commit),
+ * vd_engine_run_step() (plan, vd_step_sample, copy tokens back, commit),
  * or vd_engine_plan() / execute the returned vd_batch yourself /
  * vd_engine_commit(tokens), until vd_engine_pending() is 0.  Host-only except
  * vd_engine_run_step.  An engine is not thread-safe.  Errors as in vd.h.
@@ -67,7 +67,7 @@ int vd_engine_plan(vd_engine* e, vd_engine_plan_out* out);
 /* Commits the planned step: tokens (host [num_logit_rows]) are appended to the
  * requests of the logit rows; finished requests release their pages. */
 int vd_engine_commit(vd_engine* e, const int32_t* tokens);
-/* Plan + vd_step + vd_sample + token copy to the host + commit.  logits: dev
+/* Plan + vd_step_sample + token copy to the host + commit.  logits: dev
  * fp32 [>= rows][V]; tokens_dev: dev int32 [>= rows]; rids_out / tokens_out:
  * host arrays [>= rows] or null; *n_out = rows emitted.  Synchronises the stream. */
 int vd_engine_run_step(vd_engine* e, vd_model* m, vd_kv_pool* pool, float* logits, int32_t* tokens_dev,

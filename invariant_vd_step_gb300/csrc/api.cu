@@ -10,6 +10,7 @@
 // bucket covers the T activation rows, the attention CTA shape) changes no
 // row's arithmetic.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -25,6 +26,14 @@
 #include "vd_internal.h"
 
 namespace vd {
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("VD_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
 
 static thread_local std::string g_err;
 void set_error(const std::string& msg) { g_err = msg; }
@@ -130,9 +139,10 @@ struct Desc {
 struct GraphKey {
   unsigned long long pool_id = 0;
   const void* logits = nullptr;
+  const void* tokens = nullptr;  // fused token choice (vd_step_sample) or null
   int T = 0, B = 0, R = 0, stride = 0, n_dec = 0, n_pre = 0, grid_dec = 0, grid_pre = 0;
   bool operator==(const GraphKey& o) const {
-    return pool_id == o.pool_id && logits == o.logits && T == o.T && B == o.B && R == o.R && stride == o.stride &&
+    return pool_id == o.pool_id && logits == o.logits && tokens == o.tokens && T == o.T && B == o.B && R == o.R && stride == o.stride &&
            n_dec == o.n_dec && n_pre == o.n_pre && grid_dec == o.grid_dec && grid_pre == o.grid_pre;
   }
 };
@@ -173,6 +183,8 @@ struct vd_model {
   vd_sampler* d_samp = nullptr;
   float* samp_part_v = nullptr;  // per-chunk winners of the sampler's first pass
   int* samp_part_i = nullptr;
+  float* fused_part_v = nullptr;  // per-32-row-group winners of the fused LM-head epilogue
+  int* fused_part_i = nullptr;
   vd_sampler* h_samp = nullptr;
   cudaEvent_t samp_ev = nullptr;
   std::vector<void*> dev_allocs;
@@ -572,7 +584,7 @@ int* op_status() {
 int check_model(const vd_model* m) { return m ? VD_OK : fail(VD_ERR_INVALID_ARG, "null model"); }
 
 // The kernel sequence of one step (descriptor already uploaded).
-int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out, cudaStream_t s) {
+int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out, int* tokens_out, cudaStream_t s) {
   int rc;
   const vd_model_config& c = m->cfg;
   const int T = d.T, dm = c.d_model, hd = c.head_dim, F = c.ffn_dim;
@@ -625,15 +637,29 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
       if ((rc = launch_rmsnorm(m->x, m->d_desc + d.logit_rows, m->final_norm, m->ar.ptr, d.R, dm, c.rms_eps, s)))
         return rc;
     }
-    Prof p(m, K_GEMM_LM, s);
-    GemmArgs h{};
-    h.status = m->status;
-    h.T = d.R;
-    h.out = logits_out;
-    h.K = dm;
-    h.ldo = c.vocab;
-    h.b_box_rows = m->ar.box_for(d.R);
-    if ((rc = launch_gemm(m->m_lm, m->ar.map_for(d.R), c.vocab / kGemmBM, h, EPI_F32, s))) return rc;
+    {
+      Prof p(m, K_GEMM_LM, s);
+      GemmArgs h{};
+      h.status = m->status;
+      h.T = d.R;
+      h.out = logits_out;
+      h.K = dm;
+      h.ldo = c.vocab;
+      h.b_box_rows = m->ar.box_for(d.R);
+      if (tokens_out) {
+        h.samp = m->d_samp;
+        h.part_v = m->fused_part_v;
+        h.part_i = m->fused_part_i;
+        h.part_stride = c.vocab / 32;
+      }
+      if ((rc = launch_gemm(m->m_lm, m->ar.map_for(d.R), c.vocab / kGemmBM, h, tokens_out ? EPI_F32_SAMPLE : EPI_F32,
+                            s)))
+        return rc;
+    }
+    if (tokens_out) {
+      Prof p(m, K_SAMPLE, s);
+      if ((rc = launch_sample_final(m->fused_part_v, m->fused_part_i, d.R, c.vocab / 32, tokens_out, s))) return rc;
+    }
   }
   return VD_OK;
 }
@@ -641,10 +667,11 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
 // Replays the graph captured for d's key, capturing it first if new.
 // Capture runs on a private stream (the legacy default stream cannot be
 // captured); the replay is launched on s, after the descriptor upload.
-int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out, cudaStream_t s) {
+int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out, int* tokens_out, cudaStream_t s) {
   GraphKey k;
   k.pool_id = pool->id;
   k.logits = logits_out;
+  k.tokens = tokens_out;
   k.T = d.T;
   k.B = d.B;
   k.R = d.R;
@@ -662,7 +689,7 @@ int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out,
     }
   if (!m->cap_stream) VD_CUDA_TRY(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
   VD_CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeRelaxed));
-  const int rc = enqueue_step(m, pool, d, logits_out, m->cap_stream);
+  const int rc = enqueue_step(m, pool, d, logits_out, tokens_out, m->cap_stream);
   cudaGraph_t g = nullptr;
   const cudaError_t ce = cudaStreamEndCapture(m->cap_stream, &g);
   if (rc || ce != cudaSuccess) {
@@ -789,6 +816,9 @@ int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_mode
   const size_t nsp = static_cast<size_t>(c.max_logit_rows) * sample_chunks(c.vocab);
   if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->samp_part_v), nsp * 4))) return bail(rc);
   if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->samp_part_i), nsp * 4))) return bail(rc);
+  const size_t nfp = static_cast<size_t>(c.max_logit_rows) * (c.vocab / 32);
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->fused_part_v), nfp * 4))) return bail(rc);
+  if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->fused_part_i), nfp * 4))) return bail(rc);
   if (cudaMallocHost(reinterpret_cast<void**>(&m->h_samp), sizeof(vd_sampler) * c.max_logit_rows) != cudaSuccess ||
       cudaEventCreateWithFlags(&m->samp_ev, cudaEventDisableTiming) != cudaSuccess)
     return bail(fail(VD_ERR_CUDA, "pinned sampler buffer"));
@@ -887,7 +917,28 @@ int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out,
   Desc d;
   int rc = upload_desc(m, pool, b, true, d, s, graph);
   if (rc || d.T == 0) return rc;
-  return graph ? replay_step(m, pool, d, logits_out, s) : enqueue_step(m, pool, d, logits_out, s);
+  return graph ? replay_step(m, pool, d, logits_out, nullptr, s) : enqueue_step(m, pool, d, logits_out, nullptr, s);
+}
+
+int vd_step_sample(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const vd_sampler* per_row, float* logits_out,
+                   int32_t* tokens_out, void* stream) {
+  if (check_model(m) || !pool || pool->m != m) return fail(VD_ERR_INVALID_ARG, "null or foreign model/pool");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int R = b ? b->num_logit_rows : 0;
+  if (R > 0 && (!per_row || !tokens_out)) return fail(VD_ERR_INVALID_ARG, "null per_row or tokens_out");
+  if (R > m->cfg.max_logit_rows) return fail(VD_ERR_CAPACITY, "step exceeds max_logit_rows");
+  const bool graph = m->graph_max > 0 && !m->profiling;
+  Desc d;
+  int rc = upload_desc(m, pool, b, true, d, s, graph);
+  if (rc || d.T == 0) return rc;
+  if (d.R > 0) {
+    VD_CUDA_TRY(cudaEventSynchronize(m->samp_ev));  // the staging buffer's previous copy is done
+    memcpy(m->h_samp, per_row, sizeof(vd_sampler) * d.R);
+    VD_CUDA_TRY(cudaMemcpyAsync(m->d_samp, m->h_samp, sizeof(vd_sampler) * d.R, cudaMemcpyHostToDevice, s));
+    VD_CUDA_TRY(cudaEventRecord(m->samp_ev, s));
+  }
+  int* tok = d.R > 0 ? tokens_out : nullptr;
+  return graph ? replay_step(m, pool, d, logits_out, tok, s) : enqueue_step(m, pool, d, logits_out, tok, s);
 }
 
 int vd_set_graph_mode(vd_model* m, int32_t max_graphs) {

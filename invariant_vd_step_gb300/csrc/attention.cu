@@ -45,7 +45,9 @@ struct AttnCfg {
   static constexpr int PAGES = BNK / 16;             // 16-token pages per tile
   static constexpr int PAGE_BYTES = 16 * HD * 2;     // one page of one KV head
   static constexpr int TILE_BYTES = BNK * HD * 2;
-  static constexpr int SMEM = 1024 + 2 * 2 * TILE_BYTES + 64;
+  static constexpr int MAX_STAGES = 8;
+  // K + V tiles of `stages` pipeline stages, their barriers, the abort flag
+  static constexpr int smem(int stages) { return 1024 + stages * 2 * TILE_BYTES + MAX_STAGES * 8 + 16; }
 };
 
 // Byte offset of (key, 16-byte chunk along hd) inside a K or V tile staged
@@ -175,9 +177,12 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   constexpr int ND = HD / DS;       // output dims per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 4 * C::TILE_BYTES);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+  const int NS = a.stages;  // tiles in flight; changes when copies are issued, never the fold order
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * 2 * C::TILE_BYTES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + C::MAX_STAGES);
 
+  pdl_wait();
+  pdl_trigger();
   // Once any bounded wait has given up, later CTAs skip their work.
   {
     __shared__ int skip;  // one read for the whole CTA keeps the exit uniform
@@ -215,15 +220,13 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   const int ntiles = key_hi / C::BNK - tile_lo + 1;
 
   if (threadIdx.x == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int k = 0; k < NS; ++k) mbar_init(&full[k], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
-  auto issue = [&](int it) {
-    const int stg = it & 1;
+  auto issue = [&](int it, int stg) {
     uint8_t* sk = smem + stg * 2 * C::TILE_BYTES;
     uint8_t* sv = sk + C::TILE_BYTES;
     mbar_arrive_expect_tx(&full[stg], 2 * C::TILE_BYTES);
@@ -243,12 +246,8 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   };
   int issued = 0;
   if (threadIdx.x == 0) {
-    issue(0);
-    issued = 1;
-    if (ntiles > 1) {
-      issue(1);
-      issued = 2;
-    }
+    issued = min(NS, ntiles);
+    for (int k = 0; k < issued; ++k) issue(k, k);
   }
 
   // ---- this warp's rows
@@ -286,10 +285,10 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   for (int n = 0; n < ND / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
 
   bool ok = true;
-  int it = 0;
+  int it = 0, stg = 0;
+  uint32_t ph = 0;  // tile it sits in stage it % NS, round it / NS
   for (; it < ntiles; ++it) {
-    const int stg = it & 1;
-    if (!mbar_wait(&full[stg], (it >> 1) & 1, abort_flag, a.status)) ok = false;
+    if (!mbar_wait(&full[stg], ph, abort_flag, a.status)) ok = false;
     const int key0 = (tile_lo + it) * C::BNK;
     bool mine = false;  // any row of this warp sees a key of this tile
 #pragma unroll
@@ -300,14 +299,18 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
       attn_tile<HD, C::BNK, ND>(st, qf, kb, kb + C::TILE_BYTES, key0, pos, lo, a.scale_log2, lane, dim0);
     }
     if (__syncthreads_or(!ok)) break;
-    if (threadIdx.x == 0 && it + 2 < ntiles) {
-      issue(it + 2);
-      issued = it + 3;
+    if (threadIdx.x == 0 && it + NS < ntiles) {
+      issue(it + NS, stg);
+      issued = it + NS + 1;
+    }
+    if (++stg == NS) {
+      stg = 0;
+      ph ^= 1u;
     }
   }
   if (it < ntiles) {  // gave up: let copies in flight land before leaving
     if (threadIdx.x == 0)
-      for (int k = it; k < issued; ++k) drain_wait(&full[k & 1], (k >> 1) & 1);
+      for (int k = it; k < issued; ++k) drain_wait(&full[k % NS], (k / NS) & 1);
     return;
   }
 
@@ -327,10 +330,35 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   }
 }
 
-// Left-to-right fold of a row's split partials, then o / l -> bf16.
+// Left-to-right fold of a row's split partials, then o / l -> bf16.  The
+// loop is unrolled so that the loads of later splits are in flight while
+// earlier ones are folded; the fold itself stays strictly left to right.
+template <int PER>
+__device__ __forceinline__ void load_part(const float* p, float* o) {
+  if constexpr (PER % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < PER; i += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(p + i);
+      o[i] = v.x;
+      o[i + 1] = v.y;
+      o[i + 2] = v.z;
+      o[i + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < PER; i += 2) {
+      const float2 v = *reinterpret_cast<const float2*>(p + i);
+      o[i] = v.x;
+      o[i + 1] = v.y;
+    }
+  }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
   constexpr int PER = HD / 32;
+  pdl_wait();
+  pdl_trigger();
   const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (w >= a.T * a.Hq) return;
   const int tok = w / a.Hq, h = w % a.Hq;
@@ -340,34 +368,64 @@ __global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
   const size_t base = (static_cast<size_t>(tok) * a.Hq + h) * a.max_splits;
   float M = a.part_ml[(base + s0) * 2], L = a.part_ml[(base + s0) * 2 + 1];
   float O[PER];
-  const float* po = a.part_o + (base + s0) * HD + lane * PER;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) O[i] = po[i];
+  load_part<PER>(a.part_o + (base + s0) * HD + lane * PER, O);
+#pragma unroll 4
   for (int s = s0 + 1; s <= s1; ++s) {
-    const float m = a.part_ml[(base + s) * 2], l = a.part_ml[(base + s) * 2 + 1];
-    const float mn = fmaxf(M, m);
-    const float ca = ex2(__fsub_rn(M, mn)), cb = ex2(__fsub_rn(m, mn));
-    L = __fadd_rn(__fmul_rn(L, ca), __fmul_rn(l, cb));
-    const float* ps = a.part_o + (base + s) * HD + lane * PER;
+    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + (base + s) * 2);
+    float P[PER];
+    load_part<PER>(a.part_o + (base + s) * HD + lane * PER, P);
+    const float mn = fmaxf(M, ml.x);
+    const float ca = ex2(__fsub_rn(M, mn)), cb = ex2(__fsub_rn(ml.x, mn));
+    L = __fadd_rn(__fmul_rn(L, ca), __fmul_rn(ml.y, cb));
 #pragma unroll
-    for (int i = 0; i < PER; ++i) O[i] = __fadd_rn(__fmul_rn(O[i], ca), __fmul_rn(ps[i], cb));
+    for (int i = 0; i < PER; ++i) O[i] = __fadd_rn(__fmul_rn(O[i], ca), __fmul_rn(P[i], cb));
     M = mn;
   }
   __nv_bfloat16* out = a.out + (static_cast<size_t>(tok) * a.Hq + h) * HD + lane * PER;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) out[i] = __float2bfloat16_rn(__fdiv_rn(O[i], L));
+  for (int i = 0; i < PER; i += 2)
+    *reinterpret_cast<uint32_t*>(out + i) = pack_bf16x2(__fdiv_rn(O[i], L), __fdiv_rn(O[i + 1], L));
+}
+
+int sm_count_attn() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
+// Pipeline depth of one launch: the deepest (up to 8 stages) whose CTAs all
+// fit on the GPU at once, so that few work items (small batches) keep as many
+// key tiles in flight per SM as a full wave of 2-stage CTAs does.
+template <int HD>
+int attn_stages(int n_items) {
+  using C = AttnCfg<HD>;
+  constexpr int kSmemPerSM = 228 * 1024, kSmemPerCTA = 227 * 1024;
+  for (int ns = C::MAX_STAGES; ns > 2; --ns) {
+    if (C::smem(ns) > kSmemPerCTA) continue;
+    const long long slots = static_cast<long long>(sm_count_attn()) * (kSmemPerSM / (C::smem(ns) + 1024));
+    if (slots >= n_items) return ns;
+  }
+  return 2;
 }
 
 template <int HD, int NW, int DS>
-int launch_attn_t(const CUtensorMap& kvmap, const AttnArgs& a, int n_items, cudaStream_t s) {
+int launch_attn_t(const CUtensorMap& kvmap, const AttnArgs& a0, int n_items, cudaStream_t s) {
+  using C = AttnCfg<HD>;
   static bool configured = false;
   if (!configured) {
+    int max_ns = C::MAX_STAGES;
+    while (C::smem(max_ns) > 227 * 1024) --max_ns;
     VD_CUDA_TRY(cudaFuncSetAttribute(attn_kernel<HD, NW, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     AttnCfg<HD>::SMEM));
+                                     C::smem(max_ns)));
     configured = true;
   }
-  attn_kernel<HD, NW, DS><<<n_items, NW * 32, AttnCfg<HD>::SMEM, s>>>(kvmap, a);
-  VD_CUDA_TRY(cudaGetLastError());
+  AttnArgs a = a0;
+  a.stages = attn_stages<HD>(n_items);
+  VD_CUDA_TRY(launch_k(attn_kernel<HD, NW, DS>, dim3(n_items), dim3(NW * 32), C::smem(a.stages), s, kvmap, a));
   return VD_OK;
 }
 
@@ -416,11 +474,9 @@ int launch_merge(const MergeArgs& a, int hd, cudaStream_t s) {
   const int warps = a.T * a.Hq;
   if (warps <= 0) return VD_OK;
   const int blocks = (warps + 3) / 4;
-  if (hd == 64) merge_kernel<64><<<blocks, 128, 0, s>>>(a);
-  else if (hd == 128) merge_kernel<128><<<blocks, 128, 0, s>>>(a);
-  else if (hd == 256) merge_kernel<256><<<blocks, 128, 0, s>>>(a);
-  else return fail(VD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
-  VD_CUDA_TRY(cudaGetLastError());
+  auto k = hd == 64 ? merge_kernel<64> : hd == 128 ? merge_kernel<128> : hd == 256 ? merge_kernel<256> : nullptr;
+  if (!k) return fail(VD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+  VD_CUDA_TRY(launch_k(k, dim3(blocks), dim3(128), 0, s, a));
   return VD_OK;
 }
 

@@ -14,8 +14,11 @@ namespace {
 
 __global__ void embed_kernel(const uint4* __restrict__ E, const int* __restrict__ tok, uint4* __restrict__ x,
                              int d8) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const size_t src = static_cast<size_t>(tok[t]) * d8;
+#pragma unroll 4
   for (int c = threadIdx.x; c < d8; c += blockDim.x) x[static_cast<size_t>(t) * d8 + c] = E[src + c];
 }
 
@@ -35,9 +38,17 @@ __device__ __forceinline__ float warp_sum_fixed(float v) {
 }
 
 // y[r] = bf16(x[row_idx[r]] * (1 / sqrt(mean(x^2) + eps)) * w)
+//
+// CH > 0: the row's CH chunks per lane are loaded into registers before the
+// sum (all loads in flight at once) and reused for the output; CH == 0 is
+// the streaming form for rows longer than 32 * 16 chunks.  Both sum the same
+// terms in the same order.
+template <int CH>
 __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ row_idx,
                                const __nv_bfloat16* __restrict__ w, __nv_bfloat16* __restrict__ y, int rows, int d,
                                float eps) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (r >= rows) return;
   const int src = row_idx ? row_idx[r] : r;
@@ -45,19 +56,9 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* _
   const uint4* wr = reinterpret_cast<const uint4*>(w);
   uint4* yr = reinterpret_cast<uint4*>(y + static_cast<size_t>(r) * d);
   const int d8 = d >> 3;
-  float ss = 0.f;
-#pragma unroll 4
-  for (int c = lane; c < d8; c += 32) {
-    float f[8];
-    unpack8(xr[c], f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(f[i], f[i]));
-  }
-  ss = warp_sum_fixed(ss);
-  const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(d)), eps)));
-  for (int c = lane; c < d8; c += 32) {
+  auto out8 = [&](const uint4& xv, int c, float inv) {
     float f[8], g[8];
-    unpack8(xr[c], f);
+    unpack8(xv, f);
     unpack8(wr[c], g);
     uint4 o;
     o.x = pack_bf16x2(__fmul_rn(__fmul_rn(f[0], inv), g[0]), __fmul_rn(__fmul_rn(f[1], inv), g[1]));
@@ -65,6 +66,34 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* _
     o.z = pack_bf16x2(__fmul_rn(__fmul_rn(f[4], inv), g[4]), __fmul_rn(__fmul_rn(f[5], inv), g[5]));
     o.w = pack_bf16x2(__fmul_rn(__fmul_rn(f[6], inv), g[6]), __fmul_rn(__fmul_rn(f[7], inv), g[7]));
     yr[c] = o;
+  };
+  auto add8 = [](float ss, const uint4& xv) {
+    float f[8];
+    unpack8(xv, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(f[i], f[i]));
+    return ss;
+  };
+  float ss = 0.f;
+  if constexpr (CH > 0) {
+    uint4 xv[CH];
+#pragma unroll
+    for (int k = 0; k < CH; ++k)
+      if (lane + 32 * k < d8) xv[k] = xr[lane + 32 * k];
+#pragma unroll
+    for (int k = 0; k < CH; ++k)
+      if (lane + 32 * k < d8) ss = add8(ss, xv[k]);
+    ss = warp_sum_fixed(ss);
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(d)), eps)));
+#pragma unroll
+    for (int k = 0; k < CH; ++k)
+      if (lane + 32 * k < d8) out8(xv[k], lane + 32 * k, inv);
+  } else {
+#pragma unroll 4
+    for (int c = lane; c < d8; c += 32) ss = add8(ss, xr[c]);
+    ss = warp_sum_fixed(ss);
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(d)), eps)));
+    for (int c = lane; c < d8; c += 32) out8(xr[c], c, inv);
   }
 }
 
@@ -73,6 +102,8 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* _
 // slot, v heads -> pool V slot of the token's (page, position % 16).
 constexpr int kRopeWarps = 8;
 __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_kernel(RopeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const int head = blockIdx.y * kRopeWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int nh = a.Hq + 2 * a.Hkv;
@@ -140,18 +171,25 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_kernel(RopeArgs a) {
 
 int launch_embed(const void* embed, const int* tokens, void* x, int T, int d, cudaStream_t s) {
   if (T <= 0) return VD_OK;
-  embed_kernel<<<T, 128, 0, s>>>(static_cast<const uint4*>(embed), tokens, static_cast<uint4*>(x), d / 8);
-  VD_CUDA_TRY(cudaGetLastError());
+  VD_CUDA_TRY(launch_k(embed_kernel, dim3(T), dim3(128), 0, s, static_cast<const uint4*>(embed), tokens,
+                       static_cast<uint4*>(x), d / 8));
   return VD_OK;
 }
 
 int launch_rmsnorm(const void* x, const int* row_idx, const void* w, void* y, int rows, int d, float eps,
                    cudaStream_t s) {
   if (rows <= 0) return VD_OK;
-  rmsnorm_kernel<<<(rows + 3) / 4, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(x), row_idx,
-                                                static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(y),
-                                                rows, d, eps);
-  VD_CUDA_TRY(cudaGetLastError());
+  const auto* xp = static_cast<const __nv_bfloat16*>(x);
+  const auto* wp = static_cast<const __nv_bfloat16*>(w);
+  auto* yp = static_cast<__nv_bfloat16*>(y);
+  const int per_lane = (d / 8 + 31) / 32, blocks = (rows + 3) / 4;
+  auto k = per_lane <= 1    ? rmsnorm_kernel<1>
+           : per_lane <= 2  ? rmsnorm_kernel<2>
+           : per_lane <= 4  ? rmsnorm_kernel<4>
+           : per_lane <= 8  ? rmsnorm_kernel<8>
+           : per_lane <= 16 ? rmsnorm_kernel<16>
+                            : rmsnorm_kernel<0>;
+  VD_CUDA_TRY(launch_k(k, dim3(blocks), dim3(128), 0, s, xp, row_idx, wp, yp, rows, d, eps));
   return VD_OK;
 }
 
@@ -159,8 +197,7 @@ int launch_rope_kv(const RopeArgs& a, cudaStream_t s) {
   if (a.T <= 0) return VD_OK;
   const int nh = a.Hq + 2 * a.Hkv;
   dim3 grid(a.T, (nh + kRopeWarps - 1) / kRopeWarps);
-  rope_kv_kernel<<<grid, kRopeWarps * 32, 0, s>>>(a);
-  VD_CUDA_TRY(cudaGetLastError());
+  VD_CUDA_TRY(launch_k(rope_kv_kernel, grid, dim3(kRopeWarps * 32), 0, s, a));
   return VD_OK;
 }
 

@@ -466,9 +466,8 @@ int vd_engine_run_step(vd_engine* e, vd_model* m, vd_kv_pool* pool, float* logit
   if (rc) return rc;
   if (p.batch.num_tokens == 0) return VD_OK;
   const int R = p.batch.num_logit_rows;
-  if ((rc = vd_step(m, pool, &p.batch, logits, stream))) return rc;
+  if ((rc = vd_step_sample(m, pool, &p.batch, p.samplers, logits, tokens_dev, stream))) return rc;
   if (R > 0) {
-    if ((rc = vd_sample(m, logits, R, p.samplers, tokens_dev, stream))) return rc;
     if (e->h_tokens_cap < static_cast<size_t>(R)) {
       if (e->h_tokens) cudaFreeHost(e->h_tokens);
       e->h_tokens = nullptr;

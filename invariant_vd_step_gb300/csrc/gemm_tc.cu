@@ -20,6 +20,17 @@
 // The activation box is as tall as the launch needs (up to 256 rows): rows of
 // the B tile past it keep stale shared-memory contents, which only feed
 // columns that are never stored (a column depends on its own row alone).
+//
+// Pipeline depth follows the box: a 192 KB ring holds S stages of A tiles
+// (16 KB each) followed by S B tiles spaced b_stride = box bytes rounded up to
+// 1 KB, S being the most for which the last B tile plus the 32 KB the MMA
+// reads from it still ends inside the ring (4 stages at 256 rows, 9 at <= 16).
+// Short boxes thus keep up to 144 KB of weights in flight per SM, which is
+// what a decode GEMM with few weight tiles needs to approach HBM bandwidth.
+// The depth changes only when copies are issued, never the MMA sequence.
+#include <limits.h>
+#include <math.h>
+
 #include <algorithm>
 
 #include "vd_device.cuh"
@@ -28,12 +39,16 @@
 namespace vd {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kMaxStages = 9;
 constexpr int kThreads = 192;
 constexpr int kAStageBytes = kGemmBM * kGemmBK * 2;
-constexpr int kBStageBytes = kGemmBN * kGemmBK * 2;
-constexpr int kXchgFloats = 64 * 33;  // GLU: up-half values handed to the gate-half warps
-constexpr int kSmemBytes = 1024 + kStages * (kAStageBytes + kBStageBytes) + kXchgFloats * 4 + 256;
+constexpr int kBStageBytes = kGemmBN * kGemmBK * 2;  // what one MMA reads of B
+constexpr int kRingBytes = 4 * (kAStageBytes + kBStageBytes);
+// Epilogue exchange: GLU hands the up half (64 x 33) to the gate-half warps;
+// the sampling epilogue transposes each warp's 32 x 32 block (4 x 32 x 33).
+constexpr int kXchgFloats = 128 * 33;
+constexpr int kSmemBytes = 1024 + kRingBytes + kXchgFloats * 4 + 256;
+static_assert((2 * kMaxStages + 5) * 8 + 8 <= 256, "barrier block");
 
 __device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
 __device__ __forceinline__ float gelu_tanh_f(float g) {
@@ -70,6 +85,50 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tac
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
+    } else if (EPI == EPI_F32_SAMPLE) {
+      if (args.out) {
+        float* out = static_cast<float*>(args.out) + tile_n * kGemmBM + row;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
+      }
+      // Transpose the warp's block (lane = vocabulary row, j = token) so that
+      // lane j scans token t0 + j over the warp's 32 consecutive rows, one
+      // Philox block per 4 rows, exactly as the standalone sampler does.
+      float* xs = xchg + lg * 32 * 33;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) xs[lane * 33 + j] = v[j];
+      __syncwarp();
+      if (lane < nt) {
+        const int t = t0 + lane;
+        const vd_sampler sp = args.samp[t];
+        const bool greedy = !(sp.temperature > 0.f);
+        const int n0 = tile_n * kGemmBM + lg * 32;
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int r4 = 0; r4 < 32; r4 += 4) {
+          float sc[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) sc[q] = xs[(r4 + q) * 33 + lane];
+          if (!greedy) {
+            const uint4 w = philox_block(sp.seed, sp.step, static_cast<uint32_t>((n0 + r4) >> 2));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sc[q] = gumbel_score(sc[q], ws[q], sp.temperature);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (better(sc[q], n0 + r4 + q, bv, bi)) {
+              bv = sc[q];
+              bi = n0 + r4 + q;
+            }
+        }
+        const size_t pi = static_cast<size_t>(t) * args.part_stride + tile_n * 4 + lg;
+        args.part_v[pi] = bv;
+        args.part_i[pi] = bi;
+      }
+      __syncwarp();
     } else if (EPI == EPI_BF16) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * kGemmBM + row;
 #pragma unroll
@@ -122,33 +181,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const int S = args.stages, b_stride = args.b_stride;
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kAStageBytes;
-  float* xchg = reinterpret_cast<float*>(sB + kStages * kBStageBytes);
+  uint8_t* sB = smem + S * kAStageBytes;
+  float* xchg = reinterpret_cast<float*>(smem + kRingBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(xchg + kXchgFloats);
-  uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;   // [2] MMAs of a tile done
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* acc_full = empty + kMaxStages;  // [2] MMAs of a tile done
   uint64_t* acc_empty = acc_full + 2;     // [2] epilogue finished reading
   uint64_t* mma_done = acc_empty + 2;     // every MMA issued has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   constexpr bool kGlu = (EPI == EPI_SWIGLU || EPI == EPI_GEGLU);
-  // Once any bounded wait has given up, later CTAs skip their work instead
-  // of each waiting out the limit (the status word reports the failure).
-  {
-    __shared__ int skip;  // one read for the whole CTA keeps the exit uniform
-    if (threadIdx.x == 0) skip = args.status ? *reinterpret_cast<volatile int*>(args.status) : 0;
-    __syncthreads();
-    if (skip) return;
-  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = args.K / kGemmBK;
   const int ntt = (args.T + kGemmBN - 1) / kGemmBN;
   const int ntiles = ntt * args.n_wtiles;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -166,20 +218,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, 2 * kGemmBN);
     tmem_relinquish();
   }
+  // The prologue above touches no global memory; everything below may read
+  // what the previous kernel of the stream writes.
+  pdl_wait();
+  // Once any bounded wait has given up, later CTAs skip their work instead
+  // of each waiting out the limit (the status word reports the failure).
+  __shared__ int skip;  // one read for the whole CTA keeps the exit uniform
+  if (threadIdx.x == 0) skip = args.status ? *reinterpret_cast<volatile int*>(args.status) : 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();
   const uint32_t tmem = *tmem_slot;
 
   int issued = 0;  // producer: stages loaded so far (all tiles)
-  if (warp == 0) {
+  if (skip) {
+    // nothing issued: fall through to the teardown
+  } else if (warp == 0) {
     if (lane == 0) {
-      int g = 0;
+      int g = 0, s = 0;  // stage g lives in slot s = g % S, round g / S
+      uint32_t ph = 0;     // parity of round g / S
       for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
         const int tile_t = tile % ntt, tile_n = tile / ntt;
         for (int kb = 0; kb < KB; ++kb, ++g) {
-          const int s = g % kStages;
-          if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) - 1) & 1, abort_flag, args.status)) break;
+          if (g >= S && !mbar_wait(&empty[s], ph ^ 1u, abort_flag, args.status)) break;
           mbar_arrive_expect_tx(&full[s], kAStageBytes + args.b_box_rows * 128);
           uint8_t* a = sA + s * kAStageBytes;
           if (kGlu) {
@@ -188,30 +250,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_2d(a, &wmap, &full[s], kb * kGemmBK, tile_n * kGemmBM);
           }
-          tma_load_2d(sB + s * kBStageBytes, &xmap, &full[s], kb * kGemmBK, tile_t * kGemmBN);
+          tma_load_2d(sB + s * b_stride, &xmap, &full[s], kb * kGemmBK, tile_t * kGemmBN);
           issued = g + 1;
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(kGemmBM, kGemmBN);
-      int g = 0, i = 0;
+      int i = 0, s = 0;
+      uint32_t ph = 0;
       for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x, ++i) {
         const int b = i & 1;
         if (i >= 2 && !mbar_wait(&acc_empty[b], ((i >> 1) - 1) & 1, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t tacc = tmem + b * kGemmBN;
-        for (int kb = 0; kb < KB; ++kb, ++g) {
-          const int s = g % kStages;
-          if (!mbar_wait(&full[s], (g / kStages) & 1, abort_flag, args.status)) break;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[s], ph, abort_flag, args.status)) break;
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + s * kAStageBytes);
-          const uint32_t b0 = smem_u32(sB + s * kBStageBytes);
+          const uint32_t b0 = smem_u32(sB + s * b_stride);
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)
             umma_bf16(tacc, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (kb | kk) != 0);
           umma_commit(&empty[s]);
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         umma_commit(&acc_full[b]);
       }
@@ -233,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Teardown: let in-flight TMA copies land and issued MMAs finish, then
   // release TMEM.  On the normal path these waits return at once.
   if (warp == 0 && lane == 0 && *abort_flag) {
-    for (int g = max(0, issued - kStages); g < issued; ++g) drain_wait(&full[g % kStages], (g / kStages) & 1);
+    for (int g = max(0, issued - S); g < issued; ++g) drain_wait(&full[g % S], (g / S) & 1);
   }
-  if (warp == 1 && lane == 0) drain_wait(mma_done, 0);
+  if (!skip && warp == 1 && lane == 0) drain_wait(mma_done, 0);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -262,8 +332,8 @@ int launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const GemmArgs&
     configured = true;
   }
   const int tiles = ((a.T + kGemmBN - 1) / kGemmBN) * a.n_wtiles;
-  gemm_kernel<EPI><<<std::min(tiles, sm_count()), kThreads, kSmemBytes, s>>>(wmap, xmap, a);
-  VD_CUDA_TRY(cudaGetLastError());
+  VD_CUDA_TRY(launch_k(gemm_kernel<EPI>, dim3(std::min(tiles, sm_count())), dim3(kThreads), kSmemBytes, s, wmap, xmap,
+                       a));
   return VD_OK;
 }
 
@@ -274,10 +344,19 @@ int launch_gemm(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, c
   if (a0.T <= 0) return VD_OK;
   GemmArgs a = a0;
   a.n_wtiles = n_tiles;
+  if (a.b_box_rows < 1 || a.b_box_rows > kGemmBN) return fail(VD_ERR_INVALID_ARG, "activation box rows out of range");
+  a.b_stride = std::max(1024, (a.b_box_rows * 128 + 1023) / 1024 * 1024);
+  a.stages = std::min(kMaxStages, (kRingBytes - (kBStageBytes - a.b_stride)) / (kAStageBytes + a.b_stride));
+  // the MMA reads kBStageBytes from the last stage's B tile: keep that in the ring
+  if (a.stages < 2 || a.stages * kAStageBytes + (a.stages - 1) * a.b_stride + kBStageBytes > kRingBytes)
+    return fail(VD_ERR_INVALID_ARG, "GEMM pipeline layout");
   switch (epi) {
     case EPI_BF16: return launch_one<EPI_BF16>(wmap, xmap, a, s);
     case EPI_RESIDUAL: return launch_one<EPI_RESIDUAL>(wmap, xmap, a, s);
     case EPI_F32: return launch_one<EPI_F32>(wmap, xmap, a, s);
+    case EPI_F32_SAMPLE:
+      if (!a.samp || !a.part_v || !a.part_i) return fail(VD_ERR_INVALID_ARG, "sampling epilogue without buffers");
+      return launch_one<EPI_F32_SAMPLE>(wmap, xmap, a, s);
     case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(wmap, xmap, a, s);
     case EPI_GEGLU: return launch_one<EPI_GEGLU>(wmap, xmap, a, s);
     default: return fail(VD_ERR_INVALID_ARG, "unknown GEMM epilogue");

@@ -21,31 +21,8 @@
 namespace vd {
 namespace {
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    if (r) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-  }
-  return c;
-}
-
-__device__ __forceinline__ uint4 philox_block(uint64_t seed, uint64_t step, uint32_t blk) {
-  return philox4x32_10(make_uint4(blk, static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32), 0x5644u),
-                       static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
-}
-
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
-
 // Pass 1: CTA (row, chunk) picks the best (score, index) among kSampleChunk
-// consecutive vocabulary entries with 16-byte loads.  Pass 2: one warp per
+// consecutive vocabulary entries with 16-byte loads.  Pass 2: one CTA per
 // row picks among the chunk winners.  Both passes select the unique
 // (largest score, lowest index) pair, so the split changes nothing.
 constexpr int kSampleThreads = 256;
@@ -67,6 +44,8 @@ __global__ void __launch_bounds__(kSampleThreads) sample_partial_kernel(const fl
                                                                        const vd_sampler* __restrict__ params,
                                                                        float* __restrict__ part_v,
                                                                        int* __restrict__ part_i) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x, chunk = blockIdx.y;
   const float4* l4 = reinterpret_cast<const float4*>(logits + static_cast<size_t>(r) * V);
   const vd_sampler sp = params[r];
@@ -75,20 +54,25 @@ __global__ void __launch_bounds__(kSampleThreads) sample_partial_kernel(const fl
   int bi = INT_MAX;
   const int blk0 = chunk * (kSampleChunk / 4);
   const int nblk = min(kSampleChunk / 4, V / 4 - blk0);
-#pragma unroll 4
-  for (int k = threadIdx.x; k < nblk; k += kSampleThreads) {
+  constexpr int kPer = kSampleChunk / 4 / kSampleThreads;  // float4 loads per thread, all issued first
+  float4 xs[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int k = threadIdx.x + q * kSampleThreads;
+    if (k < nblk) xs[q] = l4[blk0 + k];
+  }
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int k = threadIdx.x + q * kSampleThreads;
+    if (k >= nblk) break;
     const int blk = blk0 + k;
-    const float4 x = l4[blk];
+    const float4 x = xs[q];
     float v[4] = {x.x, x.y, x.z, x.w};
     if (!greedy) {
       const uint4 w = philox_block(sp.seed, sp.step, static_cast<uint32_t>(blk));
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float u = __fmul_rn(__fadd_rn(static_cast<float>(ws[j] >> 8), 0.5f), 5.9604644775390625e-8f);
-        const float g = -logf(-logf(u));
-        v[j] = __fadd_rn(__fdiv_rn(v[j], sp.temperature), g);
-      }
+      for (int j = 0; j < 4; ++j) v[j] = gumbel_score(v[j], ws[j], sp.temperature);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -117,13 +101,17 @@ __global__ void __launch_bounds__(kSampleThreads) sample_partial_kernel(const fl
   }
 }
 
-__global__ void sample_final_kernel(const float* __restrict__ part_v, const int* __restrict__ part_i, int R,
-                                    int nchunk, int* __restrict__ out) {
-  const int r = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (r >= R) return;
+// Pass 2: one CTA per row picks the best of the row's chunk winners.
+constexpr int kFinalThreads = 256;
+__global__ void __launch_bounds__(kFinalThreads) sample_final_kernel(const float* __restrict__ part_v,
+                                                                     const int* __restrict__ part_i, int R, int nchunk,
+                                                                     int* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x;
   float bv = -INFINITY;
   int bi = INT_MAX;
-  for (int c = lane; c < nchunk; c += 32) {
+  for (int c = threadIdx.x; c < nchunk; c += kFinalThreads) {
     const float v = part_v[static_cast<size_t>(r) * nchunk + c];
     const int i = part_i[static_cast<size_t>(r) * nchunk + c];
     if (better(v, i, bv, bi)) {
@@ -132,10 +120,25 @@ __global__ void sample_final_kernel(const float* __restrict__ part_v, const int*
     }
   }
   warp_best(bv, bi);
-  if (lane == 0) out[r] = (bi == INT_MAX) ? 0 : bi;
+  __shared__ float sv[kFinalThreads / 32];
+  __shared__ int si[kFinalThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sv[warp] = bv;
+    si[warp] = bi;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    bv = lane < kFinalThreads / 32 ? sv[lane] : -INFINITY;
+    bi = lane < kFinalThreads / 32 ? si[lane] : INT_MAX;
+    warp_best(bv, bi);
+    if (lane == 0) out[r] = (bi == INT_MAX) ? 0 : bi;
+  }
 }
 
 __global__ void philox_kernel(uint64_t seed, uint64_t step, int n, uint32_t* out) {
+  pdl_wait();
+  pdl_trigger();
   const int blk = blockIdx.x * blockDim.x + threadIdx.x;
   if (blk * 4 >= n) return;
   const uint4 w = philox_block(seed, step, static_cast<uint32_t>(blk));
@@ -152,18 +155,23 @@ int launch_sample(const float* logits, int R, int V, const vd_sampler* dev_param
   if (R <= 0) return VD_OK;
   if (V % 4) return fail(VD_ERR_UNSUPPORTED, "vocab must be a multiple of 4");
   const int nchunk = sample_chunks(V);
-  sample_partial_kernel<<<dim3(R, nchunk), kSampleThreads, 0, s>>>(logits, V, dev_params, part_v, part_i);
-  VD_CUDA_TRY(cudaGetLastError());
-  sample_final_kernel<<<(R + 3) / 4, 128, 0, s>>>(part_v, part_i, R, nchunk, out);
-  VD_CUDA_TRY(cudaGetLastError());
+  VD_CUDA_TRY(launch_k(sample_partial_kernel, dim3(R, nchunk), dim3(kSampleThreads), 0, s, logits, V, dev_params,
+                       part_v, part_i));
+  VD_CUDA_TRY(launch_k(sample_final_kernel, dim3(R), dim3(kFinalThreads), 0, s, static_cast<const float*>(part_v),
+                       static_cast<const int*>(part_i), R, nchunk, out));
+  return VD_OK;
+}
+
+int launch_sample_final(const float* part_v, const int* part_i, int R, int nchunk, int* out, cudaStream_t s) {
+  if (R <= 0) return VD_OK;
+  VD_CUDA_TRY(launch_k(sample_final_kernel, dim3(R), dim3(kFinalThreads), 0, s, part_v, part_i, R, nchunk, out));
   return VD_OK;
 }
 
 int launch_philox(uint64_t seed, uint64_t step, int n, uint32_t* out, cudaStream_t s) {
   if (n <= 0) return VD_OK;
   const int blocks = (n + 4 * 256 - 1) / (4 * 256);
-  philox_kernel<<<blocks, 256, 0, s>>>(seed, step, n, out);
-  VD_CUDA_TRY(cudaGetLastError());
+  VD_CUDA_TRY(launch_k(philox_kernel, dim3(blocks), dim3(256), 0, s, seed, step, n, out));
   return VD_OK;
 }
 

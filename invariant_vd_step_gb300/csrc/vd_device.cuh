@@ -28,6 +28,15 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// pdl_wait returns once the grids this one depends on have completed and
+// their writes are visible (a no-op for a launch without the programmatic
+// attribute); every kernel calls it before touching memory that an earlier
+// kernel of the stream writes or reads.  pdl_trigger lets the next kernel of
+// the stream be scheduled (it still waits for this grid in its own pdl_wait).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -191,5 +200,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// ------------------------------------------------------------------ token choice
+// Philox4x32-10 of Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers:
+// As Easy as 1, 2, 3" (SC'11).  Vocabulary index i at sampler state
+// (seed, step) uses word i % 4 of block (i / 4, step lo, step hi, 0x5644)
+// under key (seed lo, seed hi).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+__device__ __forceinline__ uint4 philox_block(uint64_t seed, uint64_t step, uint32_t blk) {
+  return philox4x32_10(make_uint4(blk, static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32), 0x5644u),
+                       static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+}
+// Gumbel-max score of logit v: v / T + G with G = -log(-log(u)),
+// u = ((word >> 8) + 0.5) * 2^-24 (exact in fp32, never 0 or 1).
+__device__ __forceinline__ float gumbel_score(float v, uint32_t word, float temperature) {
+  const float u = __fmul_rn(__fadd_rn(static_cast<float>(word >> 8), 0.5f), 5.9604644775390625e-8f);
+  const float g = -logf(-logf(u));
+  return __fadd_rn(__fdiv_rn(v, temperature), g);
+}
+// (v, i) beats (bv, bi): larger score, then lower index.  The winner of any
+// set is unique, so no evaluation order changes it.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
 
 }  // namespace vd

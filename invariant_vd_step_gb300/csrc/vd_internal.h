@@ -25,6 +25,27 @@ int fail(int code, const std::string& msg);
       return ::vd::fail(VD_ERR_CUDA, std::string(#expr) + ": " + cudaGetErrorString(e_)); \
   } while (0)
 
+// ---------------------------------------------------------------- launches
+// Every kernel of the library is launched with the programmatic-stream-
+// serialisation attribute, so it may be scheduled while the previous kernel
+// of the stream drains; each kernel waits (griddepcontrol.wait) before it
+// touches memory.  VD_PDL=0 in the environment launches without it.
+bool pdl_enabled();
+template <typename... Exp, typename... Act>
+cudaError_t launch_k(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Act&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
+}
+
 // ---------------------------------------------------------------- TMA maps
 // 2-D bf16 map over a row-major [rows][cols] matrix; box = box_rows x 64
 // columns (128 bytes), 128-byte swizzle, zero fill outside the matrix.
@@ -33,7 +54,9 @@ int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols
 int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd);
 
 // ---------------------------------------------------------------- GEMM
-enum Epilogue { EPI_BF16 = 0, EPI_RESIDUAL = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_GEGLU = 4 };
+// EPI_F32_SAMPLE: fp32 logits (stored unless out is null) plus, per token and
+// 32-row vocabulary group, the best (score, index) of the token choice.
+enum Epilogue { EPI_BF16 = 0, EPI_RESIDUAL = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_GEGLU = 4, EPI_F32_SAMPLE = 5 };
 constexpr int kGemmBM = 128;  // weight rows per tile (MMA M)
 constexpr int kGemmBN = 256;  // tokens per tile (MMA N), one shape for every T
 constexpr int kGemmBK = 64;   // K per pipeline stage (one 128-byte swizzle row)
@@ -47,6 +70,12 @@ struct GemmArgs {
   int glu_up_row;        // GLU: first row of the up half in the weight matrix (= F)
   int b_box_rows;        // rows of the activation TMA box (1..kGemmBN)
   int n_wtiles;          // weight tiles (set by launch_gemm)
+  const vd_sampler* samp;  // EPI_F32_SAMPLE: per-token sampler state [T]
+  float* part_v;           // EPI_F32_SAMPLE: [T][part_stride] group winners' scores
+  int* part_i;             //                 and indices
+  int part_stride;         //                 = vocab / 32
+  int stages;            // pipeline depth (set by launch_gemm from b_box_rows)
+  int b_stride;          // bytes between the B tiles of two stages (set by launch_gemm)
   int* status;           // device status word
 };
 // A = weight map (box 128 rows, or 64 for GLU), B = activation map (box kGemmBN rows).
@@ -72,6 +101,7 @@ struct AttnArgs {
   int split;               // S_kv keys
   int max_splits;
   float scale_log2;        // log2(e) / sqrt(hd)
+  int stages;              // K/V tiles in flight (set by launch_attention)
   int* status;
 };
 struct MergeArgs {
@@ -116,6 +146,8 @@ int launch_rope_kv(const RopeArgs& a, cudaStream_t s);
 int sample_chunks(int V);
 int launch_sample(const float* logits, int R, int V, const vd_sampler* dev_params, float* part_v, int* part_i,
                   int* out, cudaStream_t s);
+// Second pass alone: per row, the best of nchunk (score, index) partials.
+int launch_sample_final(const float* part_v, const int* part_i, int R, int nchunk, int* out, cudaStream_t s);
 int launch_philox(uint64_t seed, uint64_t step, int n, uint32_t* out, cudaStream_t s);
 
 }  // namespace vd

@@ -96,6 +96,7 @@ _SIGS = {
     "vd_kv_pool_data": (_VP, [_VP]),
     "vd_step": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(Batch), _VP, _VP]),
     "vd_sample": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Sampler), _VP, _VP]),
+    "vd_step_sample": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(Batch), ctypes.POINTER(Sampler), _VP, _VP, _VP]),
     "vd_copy_kv": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, _I32P, ctypes.c_int32, _VP, _VP, _VP]),
     "vd_device_status": (ctypes.c_int, [_VP]),
     "vd_set_graph_mode": (ctypes.c_int, [_VP, ctypes.c_int32]),
@@ -289,6 +290,16 @@ class Model:
         for i, (seed, step, temp) in enumerate(samplers):
             arr[i] = Sampler(seed, step, temp, 0.0)
         check(lib().vd_sample(self.h, _ptr(logits), R, arr, _ptr(tokens_out), _stream(stream)))
+
+    def step_sample(self, pool: "KVPool", batch: StepBatch, samplers, logits, tokens_out: torch.Tensor,
+                    stream=None):
+        """vd_step_sample: one step with the token choice fused into the LM head (logits may be None)."""
+        R = len(samplers)
+        arr = (Sampler * max(R, 1))()
+        for i, (seed, step, temp) in enumerate(samplers):
+            arr[i] = Sampler(seed, step, temp, 0.0)
+        check(lib().vd_step_sample(self.h, pool.h, ctypes.byref(batch.c), arr, _ptr(logits), _ptr(tokens_out),
+                                   _stream(stream)))
 
     def copy_kv(self, pool: "KVPool", layer: int, page_table, n_tokens: int, out_k, out_v, stream=None):
         pt, p = _i32(page_table)
