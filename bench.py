@@ -169,7 +169,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     B, K, Wm = args.batch, args.steps, args.warmup
-    total_steps = Wm + K + args.e2e_steps + 2
+    total_steps = Wm + K + 2 * args.e2e_steps + 2  # warm-up, timed, synchronous and pipelined e2e
     spec, ctx, tables, num_pages = make_workload(B, total_steps)
     weights = synth.make_weights(spec, seed=0, device=dev)
     model = vd.Model(spec, weights, max_tokens=max(B, 16), max_seqs=B, max_logit_rows=B,
@@ -236,29 +236,59 @@ def run_gpu(args):
     prof_ms = ep0.elapsed_time(ep1)
     assert model.device_status() == 0, "a bounded on-device wait timed out"
 
-    # ---- end to end: host descriptor + tokens fed back, D2H of sampled tokens each step
-    host_tok = torch.empty(B, dtype=torch.int32, pin_memory=True)
+    # ---- end to end through the C ABI from host buffers: every step uploads its
+    # descriptor and sampler states from pinned host memory and reads its sampled
+    # tokens back.  Synchronous loop: tokens go to the host and back each step.
+    # Pipelined loop: step s+1 takes step s's tokens on the device
+    # (vd_step_sample_fed) and is enqueued before step s's tokens are read.
+    host_tok = torch.empty((2, B), dtype=torch.int32, pin_memory=True)
     last = toks[Wm + K - 1].astype(np.int32)
     base = Wm + K
-    h2d = 0
+    max_pages = (CTX_HI + total_steps + 16 + 15) // 16
+
+    def h2d_bytes(step):
+        need = (int(np.max(ctx)) + step + 16) // 16  # page-table columns the library uploads
+        if args.graphs:  # graph mode rounds the stride up to 64 pages
+            need = min((need + 63) // 64 * 64, max_pages)
+        return 4 * (3 * B + 2 * (B + 1) + 3 * B + B * need + B) + 24 * B  # descriptor + sampler states
+
+    E = args.e2e_steps
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for s in range(args.e2e_steps):
-        b = batch_at(base + s, last)
-        need = (int(np.max(ctx)) + base + s + 16) // 16  # page-table columns the library uploads
-        if args.graphs:  # graph mode rounds the stride up to 64 pages
-            need = min((need + 63) // 64 * 64, (CTX_HI + total_steps + 16 + 15) // 16)
-        h2d = 4 * (3 * B + 2 * (B + 1) + 3 * B + B * need + B) + 24 * B  # descriptor + sampler states
-        model.step_sample(pool, b, samplers, logits, out_tok, stream)
-        host_tok.copy_(out_tok, non_blocking=True)
+    for s in range(E):
+        model.step_sample(pool, batch_at(base + s, last), samplers, logits, out_tok, stream)
+        host_tok[0].copy_(out_tok, non_blocking=True)
         stream.synchronize()
-        last = host_tok.numpy().copy()
+        last = host_tok[0].numpy().copy()
+    e2e_sync_s = time.perf_counter() - t0
+    base += E
+    feed_idx = np.arange(B, dtype=np.int32)
+    zeros = np.zeros(B, dtype=np.int32)
+    evs = [torch.cuda.Event(), torch.cuda.Event()]
+    emitted = []
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(E):
+        if s == 0:
+            model.step_sample(pool, batch_at(base, last), samplers, logits, out_tok, stream)
+        else:
+            model.step_sample_fed(pool, batch_at(base + s, zeros), feed_idx, out_tok, samplers, logits, out_tok,
+                                  stream)
+        host_tok[s % 2].copy_(out_tok, non_blocking=True)
+        evs[s % 2].record(stream)
+        if s >= 1:
+            evs[(s - 1) % 2].synchronize()
+            emitted.append(host_tok[(s - 1) % 2].numpy().copy())
+    evs[(E - 1) % 2].synchronize()
+    emitted.append(host_tok[(E - 1) % 2].numpy().copy())
     e2e_s = time.perf_counter() - t0
+    h2d = h2d_bytes(base + E - 1)
+    assert len(emitted) == E and model.device_status() == 0
 
-    t = torch.tensor([ms, e2e_s], dtype=torch.float64, device=dev if ws > 1 else "cpu")
+    t = torch.tensor([ms, e2e_s, e2e_sync_s], dtype=torch.float64, device=dev if ws > 1 else "cpu")
     if ws > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max, e2e_max = float(t[0]), float(t[1])
+    ms_max, e2e_max, e2e_sync_max = float(t[0]), float(t[1]), float(t[2])
     if rank != 0:
         if ws > 1:
             dist.destroy_process_group()
@@ -299,7 +329,10 @@ def run_gpu(args):
         "graphs": {"max_graphs": args.graphs, **graph_stats,
                    "eager_profiled_ms_per_step": round(prof_ms / K, 4)},
         "e2e": {"value": round(ws * B * args.e2e_steps / e2e_max, 1), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * B, "steps": args.e2e_steps},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * B, "steps": args.e2e_steps,
+                "loop": "pipelined: step s+1 takes step s's tokens on the device and is enqueued before "
+                        "step s's tokens are read back",
+                "synchronous_value": round(ws * B * args.e2e_steps / e2e_sync_max, 1)},
         "clocks": clk.summary(),
     }
     if not args.no_invariance:

@@ -212,6 +212,21 @@ int vd_sample(vd_model* m, const float* logits, int32_t R, const vd_sampler* per
 int vd_step_sample(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const vd_sampler* per_row,
                    float* logits_out, int32_t* tokens_out, void* stream);
 
+/* vd_step_sample with device-side token feedback (an engineering addition;
+ * the pages have no counterpart).  feed_index: host int32 [num_tokens]; for
+ * each t with feed_index[t] >= 0 the step's token t is feed_tokens[feed_index[t]]
+ * (dev int32, typically an earlier step's tokens_out; it may be this call's
+ * own tokens_out), read on the device when the step runs, and token_ids[t] is
+ * ignored; -1 takes token_ids[t] as usual.  A host can thus enqueue step s+1
+ * before it has read step s's tokens back.  The caller keeps every index
+ * inside its feed buffer.  A fed id outside [0, V) is not read: the step
+ * records VD_ERR_OUT_OF_RANGE in the device status word (vd_device_status)
+ * and the rest of the step is skipped.  Host-side errors as vd_step_sample,
+ * plus VD_ERR_INVALID_ARG for entries below -1 or a null feed_tokens. */
+int vd_step_sample_fed(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const int32_t* feed_index,
+                       const int32_t* feed_tokens, const vd_sampler* per_row, float* logits_out,
+                       int32_t* tokens_out, void* stream);
+
 /* Debug: copies the K and V of `layer` for logical positions [0, n_tokens)
  * of one request (host page table) into dev bf16 out_k / out_v
  * [n_tokens][Hkv][hd], for bitwise checks of the KV-value invariant
@@ -219,8 +234,9 @@ int vd_step_sample(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const vd_sa
 int vd_copy_kv(vd_model* m, vd_kv_pool* pool, int32_t layer, const int32_t* page_table,
                int32_t n_tokens, void* out_k, void* out_v, void* stream);
 
-/* Reads (synchronising the device) the on-device status word: VD_OK, or
- * VD_ERR_TIMEOUT if a bounded wait in a kernel gave up; clears it. */
+/* Reads (synchronising the device) the on-device status word: VD_OK,
+ * VD_ERR_TIMEOUT if a bounded wait in a kernel gave up, or VD_ERR_OUT_OF_RANGE
+ * if a token fed on the device was outside the vocabulary; clears it. */
 int vd_device_status(vd_model* m);
 
 /* Per-kernel timing with CUDA events on the launching stream. */

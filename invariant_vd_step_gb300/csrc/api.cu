@@ -132,6 +132,7 @@ struct Desc {
   int n_dec = 0, n_pre = 0, items_dec = 0, items_pre = 0;
   int grid_dec = 0, grid_pre = 0;  // attention CTAs launched (>= items; extra CTAs exit)
   int total = 0;
+  const int* feed = nullptr;  // device tokens that entries -(1 + i) of `tokens` refer to
 };
 
 // What a captured step graph depends on beyond the model: every kernel
@@ -140,9 +141,10 @@ struct GraphKey {
   unsigned long long pool_id = 0;
   const void* logits = nullptr;
   const void* tokens = nullptr;  // fused token choice (vd_step_sample) or null
+  const void* feed = nullptr;    // device-side token feedback or null
   int T = 0, B = 0, R = 0, stride = 0, n_dec = 0, n_pre = 0, grid_dec = 0, grid_pre = 0;
   bool operator==(const GraphKey& o) const {
-    return pool_id == o.pool_id && logits == o.logits && tokens == o.tokens && T == o.T && B == o.B && R == o.R && stride == o.stride &&
+    return pool_id == o.pool_id && logits == o.logits && tokens == o.tokens && feed == o.feed && T == o.T && B == o.B && R == o.R && stride == o.stride &&
            n_dec == o.n_dec && n_pre == o.n_pre && grid_dec == o.grid_dec && grid_pre == o.grid_pre;
   }
 };
@@ -318,8 +320,11 @@ int bucket_items(int n) {
 // graph_shape rounds the page-table stride up to 64 pages and the attention
 // grids with bucket_items(), so that consecutive decode steps share one
 // captured graph; neither changes any row's arithmetic.
+// feed_index (host [T] or null): token t with feed_index[t] >= 0 is taken on
+// the device from the step's feed buffer; its descriptor entry is
+// -(1 + feed_index[t]).
 int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_tokens, Desc& d, int* h,
-               bool graph_shape = false) {
+               bool graph_shape = false, const int32_t* feed_index = nullptr) {
   const vd_model_config& c = m->cfg;
   if (!b) return fail(VD_ERR_INVALID_ARG, "null batch");
   const int T = b->num_tokens, B = b->num_seqs, R = b->num_logit_rows;
@@ -385,12 +390,14 @@ int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_token
     for (int i = 0; i < ql; ++i) {
       const int t = q0 + i, p = cached + i;
       if (b->positions[t] != p) return fail(VD_ERR_INVALID_ARG, "positions[t] must equal cached_len + offset");
-      if (need_tokens && (b->token_ids[t] < 0 || b->token_ids[t] >= V))
+      const bool fed = feed_index && feed_index[t] >= 0;
+      if (feed_index && feed_index[t] < -1) return fail(VD_ERR_INVALID_ARG, "feed_index entries must be >= -1");
+      if (need_tokens && !fed && (b->token_ids[t] < 0 || b->token_ids[t] >= V))
         return fail(VD_ERR_OUT_OF_RANGE, "token id out of range");
       const int pg = h[d.page_table + s * stride + p / 16];
       if (!slots.insert(static_cast<long long>(pg) * 16 + (p & 15)).second)
         return fail(VD_ERR_INVALID_ARG, "two new tokens of the step write the same KV slot");
-      h[d.tokens + t] = need_tokens ? b->token_ids[t] : 0;
+      h[d.tokens + t] = fed ? -1 - feed_index[t] : need_tokens ? b->token_ids[t] : 0;
       h[d.positions + t] = p;
       h[d.slot_page + t] = pg;
     }
@@ -430,12 +437,12 @@ int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_token
 }
 
 int upload_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_tokens, Desc& d, cudaStream_t s,
-                bool graph_shape = false) {
+                bool graph_shape = false, const int32_t* feed_index = nullptr) {
   const int slot = m->desc_slot;
   m->desc_slot ^= 1;
   VD_CUDA_TRY(cudaEventSynchronize(m->desc_ev[slot]));  // previous upload from this staging slot is done
   int* h = m->h_desc[slot];
-  int rc = build_desc(m, pool, b, need_tokens, d, h, graph_shape);
+  int rc = build_desc(m, pool, b, need_tokens, d, h, graph_shape, feed_index);
   if (rc || d.T == 0) return rc;
   VD_CUDA_TRY(cudaMemcpyAsync(m->d_desc, h, static_cast<size_t>(d.total) * 4, cudaMemcpyHostToDevice, s));
   VD_CUDA_TRY(cudaEventRecord(m->desc_ev[slot], s));
@@ -591,7 +598,7 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
   const int qkv_dim = (c.n_heads + 2 * c.n_kv_heads) * hd;
   {
     Prof p(m, K_EMBED, s);
-    if ((rc = launch_embed(m->embed, m->d_desc + d.tokens, m->x, T, dm, s))) return rc;
+    if ((rc = launch_embed(m->embed, m->d_desc + d.tokens, d.feed, c.vocab, m->status, m->x, T, dm, s))) return rc;
   }
   GemmArgs g{};
   g.status = m->status;
@@ -672,6 +679,7 @@ int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out,
   k.pool_id = pool->id;
   k.logits = logits_out;
   k.tokens = tokens_out;
+  k.feed = d.feed;
   k.T = d.T;
   k.B = d.B;
   k.R = d.R;
@@ -920,17 +928,23 @@ int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out,
   return graph ? replay_step(m, pool, d, logits_out, nullptr, s) : enqueue_step(m, pool, d, logits_out, nullptr, s);
 }
 
-int vd_step_sample(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const vd_sampler* per_row, float* logits_out,
-                   int32_t* tokens_out, void* stream) {
+namespace {
+int step_sample_impl(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const int32_t* feed_index,
+                     const int32_t* feed_tokens, const vd_sampler* per_row, float* logits_out, int32_t* tokens_out,
+                     void* stream) {
   if (check_model(m) || !pool || pool->m != m) return fail(VD_ERR_INVALID_ARG, "null or foreign model/pool");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int R = b ? b->num_logit_rows : 0;
   if (R > 0 && (!per_row || !tokens_out)) return fail(VD_ERR_INVALID_ARG, "null per_row or tokens_out");
   if (R > m->cfg.max_logit_rows) return fail(VD_ERR_CAPACITY, "step exceeds max_logit_rows");
+  if (feed_index && !feed_tokens && b)
+    for (int t = 0; t < b->num_tokens; ++t)
+      if (feed_index[t] >= 0) return fail(VD_ERR_INVALID_ARG, "feed_index without feed_tokens");
   const bool graph = m->graph_max > 0 && !m->profiling;
   Desc d;
-  int rc = upload_desc(m, pool, b, true, d, s, graph);
+  int rc = upload_desc(m, pool, b, true, d, s, graph, feed_index);
   if (rc || d.T == 0) return rc;
+  d.feed = feed_index ? feed_tokens : nullptr;
   if (d.R > 0) {
     VD_CUDA_TRY(cudaEventSynchronize(m->samp_ev));  // the staging buffer's previous copy is done
     memcpy(m->h_samp, per_row, sizeof(vd_sampler) * d.R);
@@ -939,6 +953,19 @@ int vd_step_sample(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const vd_sa
   }
   int* tok = d.R > 0 ? tokens_out : nullptr;
   return graph ? replay_step(m, pool, d, logits_out, tok, s) : enqueue_step(m, pool, d, logits_out, tok, s);
+}
+}  // namespace
+
+int vd_step_sample(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const vd_sampler* per_row, float* logits_out,
+                   int32_t* tokens_out, void* stream) {
+  return step_sample_impl(m, pool, b, nullptr, nullptr, per_row, logits_out, tokens_out, stream);
+}
+
+int vd_step_sample_fed(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const int32_t* feed_index,
+                       const int32_t* feed_tokens, const vd_sampler* per_row, float* logits_out, int32_t* tokens_out,
+                       void* stream) {
+  if (!feed_index) return fail(VD_ERR_INVALID_ARG, "null feed_index");
+  return step_sample_impl(m, pool, b, feed_index, feed_tokens, per_row, logits_out, tokens_out, stream);
 }
 
 int vd_set_graph_mode(vd_model* m, int32_t max_graphs) {
@@ -1012,6 +1039,7 @@ int vd_device_status(vd_model* m) {
   VD_CUDA_TRY(cudaDeviceSynchronize());
   VD_CUDA_TRY(cudaMemcpy(&v, m->status, 4, cudaMemcpyDeviceToHost));
   VD_CUDA_TRY(cudaMemset(m->status, 0, 4));
+  if (v == VD_ERR_OUT_OF_RANGE) return fail(VD_ERR_OUT_OF_RANGE, "a token read on the device was outside the vocabulary");
   if (v) return fail(VD_ERR_TIMEOUT, "a bounded on-device wait gave up");
   return VD_OK;
 }

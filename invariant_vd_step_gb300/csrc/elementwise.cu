@@ -12,12 +12,23 @@
 namespace vd {
 namespace {
 
-__global__ void embed_kernel(const uint4* __restrict__ E, const int* __restrict__ tok, uint4* __restrict__ x,
-                             int d8) {
+// Token t's id is tok[t], or feed[-1 - tok[t]] for an entry below zero (a
+// token produced on the device by an earlier step).  A fed id outside the
+// vocabulary is recorded in the status word and row 0 is read instead.
+__global__ void embed_kernel(const uint4* __restrict__ E, const int* __restrict__ tok, const int* __restrict__ feed,
+                             int V, int* status, uint4* __restrict__ x, int d8) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
-  const size_t src = static_cast<size_t>(tok[t]) * d8;
+  int id = tok[t];
+  if (id < 0) {
+    id = feed ? feed[-1 - id] : -1;
+    if (id < 0 || id >= V) {
+      if (threadIdx.x == 0 && status) atomicCAS(status, 0, static_cast<int>(VD_ERR_OUT_OF_RANGE));
+      id = 0;
+    }
+  }
+  const size_t src = static_cast<size_t>(id) * d8;
 #pragma unroll 4
   for (int c = threadIdx.x; c < d8; c += blockDim.x) x[static_cast<size_t>(t) * d8 + c] = E[src + c];
 }
@@ -169,10 +180,11 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_kernel(RopeArgs a) {
 
 }  // namespace
 
-int launch_embed(const void* embed, const int* tokens, void* x, int T, int d, cudaStream_t s) {
+int launch_embed(const void* embed, const int* tokens, const int* feed, int V, int* status, void* x, int T, int d,
+                 cudaStream_t s) {
   if (T <= 0) return VD_OK;
-  VD_CUDA_TRY(launch_k(embed_kernel, dim3(T), dim3(128), 0, s, static_cast<const uint4*>(embed), tokens,
-                       static_cast<uint4*>(x), d / 8));
+  VD_CUDA_TRY(launch_k(embed_kernel, dim3(T), dim3(128), 0, s, static_cast<const uint4*>(embed), tokens, feed, V,
+                       status, static_cast<uint4*>(x), d / 8));
   return VD_OK;
 }
 

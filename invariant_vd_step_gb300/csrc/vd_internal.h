@@ -122,7 +122,9 @@ constexpr size_t kAttnStaticScratchBytes = static_cast<size_t>(16) << 20;
 int attn_static_scratch(void** ptr);
 
 // ---------------------------------------------------------------- elementwise
-int launch_embed(const void* embed, const int* tokens, void* x, int T, int d, cudaStream_t s);
+// tokens[t] < 0 refers to feed[-1 - tokens[t]] (device tokens of an earlier step).
+int launch_embed(const void* embed, const int* tokens, const int* feed, int V, int* status, void* x, int T, int d,
+                 cudaStream_t s);
 int launch_rmsnorm(const void* x, const int* row_idx, const void* w, void* y, int rows, int d, float eps,
                    cudaStream_t s);
 struct RopeArgs {

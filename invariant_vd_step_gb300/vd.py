@@ -19,6 +19,8 @@ from . import build as _build
 VD_OK = 0
 ERRORS = {1: "VD_ERR_INVALID_ARG", 2: "VD_ERR_UNSUPPORTED", 3: "VD_ERR_OUT_OF_RANGE",
           4: "VD_ERR_CAPACITY", 5: "VD_ERR_CUDA", 6: "VD_ERR_TIMEOUT"}
+(VD_ERR_INVALID_ARG, VD_ERR_UNSUPPORTED, VD_ERR_OUT_OF_RANGE, VD_ERR_CAPACITY, VD_ERR_CUDA,
+ VD_ERR_TIMEOUT) = range(1, 7)
 EPI_BF16, EPI_RESIDUAL, EPI_F32, EPI_SWIGLU, EPI_GEGLU = range(5)
 
 
@@ -97,6 +99,8 @@ _SIGS = {
     "vd_step": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(Batch), _VP, _VP]),
     "vd_sample": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Sampler), _VP, _VP]),
     "vd_step_sample": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(Batch), ctypes.POINTER(Sampler), _VP, _VP, _VP]),
+    "vd_step_sample_fed": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(Batch), _I32P, _VP, ctypes.POINTER(Sampler), _VP,
+                                          _VP, _VP]),
     "vd_copy_kv": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, _I32P, ctypes.c_int32, _VP, _VP, _VP]),
     "vd_device_status": (ctypes.c_int, [_VP]),
     "vd_set_graph_mode": (ctypes.c_int, [_VP, ctypes.c_int32]),
@@ -300,6 +304,17 @@ class Model:
             arr[i] = Sampler(seed, step, temp, 0.0)
         check(lib().vd_step_sample(self.h, pool.h, ctypes.byref(batch.c), arr, _ptr(logits), _ptr(tokens_out),
                                    _stream(stream)))
+
+    def step_sample_fed(self, pool: "KVPool", batch: StepBatch, feed_index, feed_tokens: torch.Tensor, samplers,
+                        logits, tokens_out: torch.Tensor, stream=None):
+        """vd_step_sample_fed: tokens with feed_index[t] >= 0 come from feed_tokens on the device."""
+        R = len(samplers)
+        arr = (Sampler * max(R, 1))()
+        for i, (seed, step, temp) in enumerate(samplers):
+            arr[i] = Sampler(seed, step, temp, 0.0)
+        fi, fip = _i32(feed_index)
+        check(lib().vd_step_sample_fed(self.h, pool.h, ctypes.byref(batch.c), fip,
+                                       _ptr(feed_tokens), arr, _ptr(logits), _ptr(tokens_out), _stream(stream)))
 
     def copy_kv(self, pool: "KVPool", layer: int, page_table, n_tokens: int, out_k, out_v, stream=None):
         pt, p = _i32(page_table)

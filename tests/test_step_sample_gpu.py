@@ -93,3 +93,56 @@ def test_step_sample_validation():
     rows = vd.StepBatch([(np.arange(4, dtype=np.int32), 0, np.array([1], np.int32))], logit_rows=[])
     tw.m.step_sample(tw.pa, rows, [], None, None)  # no logit rows: nothing to choose
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("graphs", [0, 8])
+def test_device_fed_tokens_match_host_fed(graphs):
+    """Decode steps whose tokens come from the previous step's device output
+    equal steps fed the same tokens from the host, logits and tokens bitwise."""
+    ready()
+    tw = Twin(WIDE, graphs=graphs)
+    prompts = synth.make_prompts(5, 16, 40, WIDE.vocab, seed=21)
+    tables = [np.arange(8 * r, 8 * r + 8, dtype=np.int32) for r in range(5)]
+    lens = [len(p) for p in prompts]
+    rows = list(np.cumsum(lens) - 1)
+    pre = vd.StepBatch([(p, 0, tables[r]) for r, p in enumerate(prompts)], logit_rows=rows)
+    samp = _samplers(5, 4)
+    # prefill both pools; tokens of the last prompt positions seed the decode loop
+    tw.m.step_sample(tw.pa, pre, samp, tw.la, tw.ta)
+    tw.m.step_sample(tw.pb, pre, samp, tw.lb, tw.tb)
+    torch.cuda.synchronize()
+    host_tok = tw.ta[:5].cpu().numpy()
+    fed_logits = []
+    ctx = list(lens)
+    for step in range(6):
+        zeros = [(np.zeros(1, np.int32), ctx[r], tables[r]) for r in range(5)]
+        b_host = vd.StepBatch([(np.array([host_tok[r]], np.int32), ctx[r], tables[r]) for r in range(5)],
+                              logit_rows=range(5))
+        b_fed = vd.StepBatch(zeros, logit_rows=range(5))
+        samp = _samplers(5, 10 + step)
+        # fed path: never read back inside the loop; feed buffer = its own tokens_out
+        lb = torch.empty(5, WIDE.vocab, device="cuda")
+        tw.m.step_sample_fed(tw.pb, b_fed, np.arange(5), tw.tb, samp, lb, tw.tb)
+        fed_logits.append(lb)
+        tw.m.step_sample(tw.pa, b_host, samp, tw.la, tw.ta)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(tw.la[:5]), bits(lb)), f"step {step}: fed logits differ"
+        host_tok = tw.ta[:5].cpu().numpy()
+        assert np.array_equal(host_tok, tw.tb[:5].cpu().numpy())
+        ctx = [c + 1 for c in ctx]
+    assert tw.m.device_status() == 0
+
+
+def test_fed_token_outside_vocabulary_is_reported():
+    ready()
+    tw = Twin(synth.TINY)
+    seqs = [(np.array([1, 2, 3], np.int32), 0, np.array([3], np.int32))]
+    feed = torch.tensor([synth.TINY.vocab + 5, 7], dtype=torch.int32, device="cuda")
+    b = vd.StepBatch(seqs, logit_rows=[2])
+    tw.m.step_sample_fed(tw.pa, b, [-1, 0, -1], feed, [(1, 0, 0.0)], tw.la, tw.ta)
+    assert tw.m.device_status() == vd.VD_ERR_OUT_OF_RANGE
+    assert tw.m.device_status() == 0  # reading clears it
+    tw.m.step_sample_fed(tw.pa, b, [-1, 1, -1], feed, [(1, 0, 0.0)], tw.la, tw.ta)
+    assert tw.m.device_status() == 0
+    with pytest.raises(vd.VDError):
+        tw.m.step_sample_fed(tw.pa, b, [-2, 0, -1], feed, [(1, 0, 0.0)], tw.la, tw.ta)
