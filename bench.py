@@ -424,6 +424,125 @@ def run_prefill(args):
         "kernels": kernels, "clocks": clk.summary()}))
 
 
+def step_roofline_s(spec, seqs, R, hbm_gbs, tf_peak):
+    """Roofline time of one engine step: max(algorithmic bytes / HBM, flops / tensor peak).
+
+    seqs: (cached_len, q_len) per request.  Bytes: every layer's weights, the
+    LM head and fp32 logits when rows are returned, each request's visible
+    K/V read once per layer, its new K/V written.  Flops: the GEMMs over the
+    step's tokens plus 4 * Hq * hd per (query, visible key) pair."""
+    L, d, F, V = spec.n_layers, spec.d_model, spec.ffn_dim, spec.vocab
+    per_layer = spec.qkv_dim * d + d * spec.attn_dim + 3 * F * d
+    T = sum(q for _, q in seqs)
+    kvb = 2 * spec.n_kv_heads * spec.head_dim * 2
+    byts = L * per_layer * 2 + (V * d * 2 + R * V * 4 if R else 0)
+    flops = 2 * per_layer * T * L + 2 * V * d * R
+    for c, q in seqs:
+        for i in range(L):
+            w = spec.layer_window(i)
+            vis_last = min(c + q, w) if w else c + q
+            byts += vis_last * kvb + q * kvb
+            if w:
+                pairs = sum(min(t + 1, w) for t in range(c, c + q)) if q < 64 else q * min(c + q, w)
+            else:
+                pairs = q * c + q * (q + 1) // 2
+            flops += 4 * spec.n_heads * spec.head_dim * pairs
+    return max(byts / (hbm_gbs * 1e9), flops / (tf_peak * 1e12)), T
+
+
+def run_serve(args):
+    """Serving workloads through the native engine (plan -> vd_step_sample ->
+    tokens to the host -> commit), full 32-layer Llama-3.1-8B shape:
+
+    c3: 64 requests, prompts U[1024, 4096], 256 decode tokens each, chunk
+        budget --budget (2048 or 8192), prefill and decode rows mixed.
+    c5: agentic sessions: a shared 4096-token prefix; every turn appends
+        U[200, 800] tokens and decodes U[128, 512]; --sessions x --turns at
+        --concurrency sessions in flight; prefix reuse on and a pool of half of
+        concurrency x mean final session length, which forces evictions and
+        recomputation.
+
+    A step that carries prompt tokens counts as prefill (its tokens minus its
+    decode rows are prefill tokens); a step of decode rows only counts as
+    decode.  Reports tok/s of each kind over its own steps, all computed
+    tokens over the wall clock, and the wall-clock roofline fraction (sum of
+    per-step roofline times / time)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from invariant_vd_step_gb300 import engine, sessions, synth, vd
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = synth.LLAMA8B
+    V = spec.vocab
+    budget = args.budget
+    if args.workload == "c3":
+        prompts = synth.make_prompts(64, 1024, 4096, V, seed=1)
+        work = sessions.SessionWorkload(V, 64, 1, decode_lo=256, decode_hi=256, prompts=prompts)
+        conc = 64
+        pages = sum((len(p) + 256 + 15) // 16 for p in prompts) + 64
+    else:
+        conc = args.concurrency
+        work = sessions.SessionWorkload(V, args.sessions, args.turns, 200, 800, 128, 512,
+                                        prefix=synth.make_tokens(4096, V, seed=11), seed=args.seed)
+        mean_final = 4096 + args.turns * (500 + 320)
+        pages = max(int(0.5 * conc * mean_final / 16), work.max_context() // 16 + 64)
+    weights = synth.make_weights(spec, seed=0, device=dev)
+    model = vd.Model(spec, weights, max_tokens=budget, max_seqs=conc, max_logit_rows=conc,
+                     max_context=work.max_context())
+    model.set_graph_mode(args.graphs)
+    pool = vd.KVPool(model, pages)
+    eng = engine.Engine(None, pages, max_batch=conc, token_budget=budget, prefix_reuse=True, placement_seed=2)
+    stream = torch.cuda.current_stream(dev)
+    logits = torch.empty((conc, V), dtype=torch.float32, device=dev)
+    tok_dev = torch.empty(conc, dtype=torch.int32, device=dev)
+    hbm, tf_burst, peak_kind = load_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tf_sust = float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        tf_sust = 1700.0
+    torch.cuda.synchronize()
+    t_start = time.perf_counter()
+    with Clocks(local) as clk:
+        res = sessions.run_sessions(work, model, pool, eng, conc, logits, tok_dev, stream)
+    wall = time.perf_counter() - t_start
+    assert model.device_status() == 0
+    t_pre = t_dec = roof_pre = roof_dec = 0.0
+    n_pre_tok = n_dec_tok = total_T = 0
+    for st in res.steps:
+        T = sum(q for _, q in st.seqs)
+        total_T += T
+        roof, _ = step_roofline_s(spec, st.seqs, st.rows, hbm, tf_sust)
+        if T > st.rows:  # the step carries prompt tokens
+            t_pre += st.seconds
+            roof_pre += roof
+            n_pre_tok += T - sum(1 for c, q in st.seqs if q == 1 and c > 0)
+        else:
+            t_dec += st.seconds
+            roof_dec += roof
+            n_dec_tok += st.rows
+    gen = sum(len(t) for outs in res.outputs.values() for t in outs)
+    print(json.dumps({
+        "metric": f"serving tok/s ({args.workload}, Llama-3.1-8B shape 32 layers, 1 GB300)",
+        "value": round(total_T / wall, 1), "unit": "tok/s (tokens computed: prefill chunks + decode)",
+        "generated_tok_s": round(gen / wall, 1),
+        "n_gpus": 1, "higher_is_better": True, "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": spec.n_layers, "budget": budget, "max_batch": conc,
+                   "sessions": work.n_sessions, "turns": work.turns, "pool_pages": pages, "graphs": args.graphs},
+        "steps": len(res.steps), "wall_s": round(wall, 3),
+        "prefill": {"tok_s": round(n_pre_tok / max(t_pre, 1e-9), 1), "steps_s": round(t_pre, 3),
+                    "roofline_frac": round(roof_pre / max(t_pre, 1e-9), 4)},
+        "decode": {"tok_s": round(n_dec_tok / max(t_dec, 1e-9), 1), "steps_s": round(t_dec, 3),
+                   "roofline_frac": round(roof_dec / max(t_dec, 1e-9), 4)},
+        "roofline_frac": round((roof_pre + roof_dec) / wall, 4),
+        "tokens": {"prompt_submitted": res.submitted, "computed": total_T, "generated": gen},
+        "engine": eng.stats, "graphs": model.graph_stats(), "clocks": clk.summary(),
+        "peaks": {"hbm_gbs": hbm, "bf16_tflops_sustained": tf_sust, "source": peak_kind},
+    }))
+
+
 def oracle_decode_sample(spec, weights_np, caches, toks):
     """The oracle's decode step for each request over its cached K/V."""
     from oracle.decoder import OracleDecoder
@@ -515,7 +634,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-invariance", action="store_true")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--mode", default="decode", choices=["decode", "prefill"])
+    ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "serve"])
+    ap.add_argument("--workload", default="c3", choices=["c3", "c5"], help="serve mode workload")
+    ap.add_argument("--budget", type=int, default=2048, help="serve mode: chunked-prefill token budget")
+    ap.add_argument("--sessions", type=int, default=128, help="serve c5: sessions")
+    ap.add_argument("--turns", type=int, default=8, help="serve c5: turns per session")
+    ap.add_argument("--concurrency", type=int, default=64, help="serve c5: sessions in flight")
+    ap.add_argument("--seed", type=int, default=7, help="serve c5: turn-length seed")
     ap.add_argument("--tokens", type=int, default=8192, help="prefill mode: tokens per step")
     ap.add_argument("--prefill-requests", type=int, default=4)
     args = ap.parse_args()
@@ -526,6 +651,8 @@ def main():
         run_reference(args)
     elif args.mode == "prefill":
         run_prefill(args)
+    elif args.mode == "serve":
+        run_serve(args)
     else:
         run_gpu(args)
 

@@ -177,7 +177,8 @@ int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out,
 /* Graph replay of steps (an engineering addition; the pages' design has no
  * counterpart).  With max_graphs > 0, vd_step keeps the descriptor upload as
  * an ordinary copy on the stream and replays the step's kernel sequence as
- * one CUDA graph, captured the first time its key is seen.  The key is
+ * one CUDA graph, captured the second time its key is seen (the first time
+ * runs eagerly, so one-off shapes never pay for a capture).  The key is
  * (pool, logits_out address, T, B, R, page-table stride, number of decode-
  * and prefill-class requests, attention grid sizes); in this mode the
  * stride is rounded up to 64 pages and each attention grid to a 1/16
@@ -190,9 +191,10 @@ int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out,
  * thread-safe: one host thread drives a model.
  * Errors: VD_ERR_INVALID_ARG (null model, max_graphs < 0). */
 int vd_set_graph_mode(vd_model* m, int32_t max_graphs);
-/* out3[0] = graphs captured, out3[1] = replays of a cached graph, out3[2] =
- * graphs currently cached (host int64 [3]). */
-int vd_graph_stats(const vd_model* m, int64_t* out3);
+/* out4[0] = graphs captured, out4[1] = replays of a cached graph, out4[2] =
+ * graphs currently cached, out4[3] = steps run eagerly because their key was
+ * new (a key is captured the second time it is seen) (host int64 [4]). */
+int vd_graph_stats(const vd_model* m, int64_t* out4);
 
 /* Token choice for R rows of dev float32 logits [R][V] (16-byte aligned) -> dev int32 [R]:
  * greedy argmax (lowest index on ties) or Gumbel-max with Philox4x32-10

@@ -201,7 +201,7 @@ struct vd_model {
   int graph_max = 0;
   cudaStream_t cap_stream = nullptr;
   std::vector<GraphEntry> graphs;
-  long long graph_clock = 0, graph_captures = 0, graph_replays = 0;
+  long long graph_clock = 0, graph_captures = 0, graph_replays = 0, graph_eager = 0;
 };
 
 struct vd_kv_pool {
@@ -671,9 +671,12 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
   return VD_OK;
 }
 
-// Replays the graph captured for d's key, capturing it first if new.
-// Capture runs on a private stream (the legacy default stream cannot be
-// captured); the replay is launched on s, after the descriptor upload.
+// Replays the graph captured for d's key.  A key seen for the first time
+// runs eagerly and is remembered; the second time it is captured, so one-off
+// shapes (continuous batching with requests joining and leaving) never pay
+// for a capture.  Capture runs on a private stream (the legacy default
+// stream cannot be captured); the replay is launched on s, after the
+// descriptor upload.
 int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out, int* tokens_out, cudaStream_t s) {
   GraphKey k;
   k.pool_id = pool->id;
@@ -688,13 +691,29 @@ int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out,
   k.n_pre = d.n_pre;
   k.grid_dec = d.grid_dec;
   k.grid_pre = d.grid_pre;
+  GraphEntry* seen = nullptr;
   for (GraphEntry& e : m->graphs)
     if (e.key == k) {
       e.used = ++m->graph_clock;
-      ++m->graph_replays;
-      VD_CUDA_TRY(cudaGraphLaunch(e.exec, s));
-      return VD_OK;
+      if (e.exec) {
+        ++m->graph_replays;
+        VD_CUDA_TRY(cudaGraphLaunch(e.exec, s));
+        return VD_OK;
+      }
+      seen = &e;
+      break;
     }
+  if (!seen) {  // first sight: remember the key, run eagerly
+    if (static_cast<int>(m->graphs.size()) >= m->graph_max) {
+      auto lru = std::min_element(m->graphs.begin(), m->graphs.end(),
+                                  [](const GraphEntry& a, const GraphEntry& b) { return a.used < b.used; });
+      if (lru->exec) cudaGraphExecDestroy(lru->exec);  // freed after any launch still in flight
+      m->graphs.erase(lru);
+    }
+    m->graphs.push_back({k, nullptr, ++m->graph_clock});
+    ++m->graph_eager;
+    return enqueue_step(m, pool, d, logits_out, tokens_out, s);
+  }
   if (!m->cap_stream) VD_CUDA_TRY(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
   VD_CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeRelaxed));
   const int rc = enqueue_step(m, pool, d, logits_out, tokens_out, m->cap_stream);
@@ -709,20 +728,15 @@ int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out,
   const cudaError_t ie = cudaGraphInstantiate(&x, g, 0);
   cudaGraphDestroy(g);
   if (ie != cudaSuccess) return fail(VD_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(ie));
-  if (static_cast<int>(m->graphs.size()) >= m->graph_max) {  // drop the least recently replayed
-    auto lru = std::min_element(m->graphs.begin(), m->graphs.end(),
-                                [](const GraphEntry& a, const GraphEntry& b) { return a.used < b.used; });
-    cudaGraphExecDestroy(lru->exec);  // freed after any launch still in flight
-    m->graphs.erase(lru);
-  }
-  m->graphs.push_back({k, x, ++m->graph_clock});
+  seen->exec = x;
   ++m->graph_captures;
   VD_CUDA_TRY(cudaGraphLaunch(x, s));
   return VD_OK;
 }
 
 void drop_graphs(vd_model* m) {
-  for (GraphEntry& e : m->graphs) cudaGraphExecDestroy(e.exec);
+  for (GraphEntry& e : m->graphs)
+    if (e.exec) cudaGraphExecDestroy(e.exec);
   m->graphs.clear();
 }
 
@@ -973,17 +987,20 @@ int vd_set_graph_mode(vd_model* m, int32_t max_graphs) {
   if (max_graphs < 0) return fail(VD_ERR_INVALID_ARG, "max_graphs must be >= 0");
   m->graph_max = max_graphs;
   while (static_cast<int>(m->graphs.size()) > max_graphs) {
-    cudaGraphExecDestroy(m->graphs.front().exec);
+    if (m->graphs.front().exec) cudaGraphExecDestroy(m->graphs.front().exec);
     m->graphs.erase(m->graphs.begin());
   }
   return VD_OK;
 }
 
-int vd_graph_stats(const vd_model* m, int64_t* out3) {
-  if (check_model(m) || !out3) return fail(VD_ERR_INVALID_ARG, "null argument");
-  out3[0] = m->graph_captures;
-  out3[1] = m->graph_replays;
-  out3[2] = static_cast<int64_t>(m->graphs.size());
+int vd_graph_stats(const vd_model* m, int64_t* out4) {
+  if (check_model(m) || !out4) return fail(VD_ERR_INVALID_ARG, "null argument");
+  out4[0] = m->graph_captures;
+  out4[1] = m->graph_replays;
+  int64_t cached = 0;
+  for (const GraphEntry& e : m->graphs) cached += e.exec != nullptr;
+  out4[2] = cached;
+  out4[3] = m->graph_eager;
   return VD_OK;
 }
 

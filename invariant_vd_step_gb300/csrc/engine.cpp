@@ -70,6 +70,7 @@ struct BlockManager {
   std::unordered_map<int, PageMeta> meta;
   std::unordered_map<uint64_t, std::vector<int>> index;
   std::list<int> lru;  // evictable leaves, oldest first
+  int idle = 0;        // registered pages with no reference (all evictable, leaves first)
   std::unordered_map<int, std::list<int>::iterator> lru_pos;
   vd_engine_stats stats{};
 
@@ -116,7 +117,10 @@ struct BlockManager {
   }
   void acquire(const std::vector<int>& pages) {
     for (int p : pages) {
-      if (ref[p] == 0) lru_del(p);
+      if (ref[p] == 0) {
+        lru_del(p);
+        if (meta.count(p)) idle--;
+      }
       ref[p]++;
     }
   }
@@ -126,6 +130,7 @@ struct BlockManager {
       if (ref[p] == 0) {
         auto it = meta.find(p);
         if (it != meta.end()) {
+          idle++;
           if (it->second.children == 0) lru_add(p);
         } else {
           free_list.push_back(p);
@@ -133,12 +138,18 @@ struct BlockManager {
       }
     }
   }
+  // Pages obtainable without preempting anyone: free ones plus every
+  // registered page nobody references.  A request references its whole
+  // chain, so an unreferenced page's subtree is unreferenced too and leaf-
+  // first eviction reaches all of them.
+  int reclaimable() const { return static_cast<int>(free_list.size()) + idle; }
   bool evict_one() {
     if (lru.empty()) return false;
     const int p = lru.front();
     lru_del(p);
     const PageMeta m = meta.at(p);
     meta.erase(p);
+    idle--;
     auto& v = index[m.hash];
     v.erase(std::find(v.begin(), v.end(), p));
     if (v.empty()) index.erase(m.hash);
@@ -198,6 +209,9 @@ struct BlockManager {
     }
     for (int p : lru)
       if (ref[p] != 0 || meta.at(p).children != 0) return fail(VD_ERR_INVALID_ARG, "evictable page in use");
+    int n_idle = 0;
+    for (const auto& kv : meta) n_idle += ref[kv.first] == 0;
+    if (n_idle != idle) return fail(VD_ERR_INVALID_ARG, "idle page count mismatch");
     return VD_OK;
   }
 };
@@ -240,12 +254,22 @@ struct vd_engine {
 
 namespace {
 
+// Admission (running < max_batch) takes the waiting queue in order while the
+// pool can hold the next request's uncached prompt plus one page; with
+// nothing running the front request is admitted unconditionally.
 void admit(vd_engine* e) {
   while (!e->waiting.empty() && static_cast<int>(e->running.size()) < e->cfg.max_batch) {
     Request* r = e->waiting.front();
-    e->waiting.pop_front();
+    const int hist_pages = (static_cast<int>(r->history.size()) + kPage - 1) / kPage;
     const int max_pages = (static_cast<int>(r->history.size()) - 1) / kPage;
     std::vector<int> hits = e->bm.match_prefix(r->history.data(), max_pages);
+    if (!e->running.empty()) {
+      int idle_hits = 0;  // hit pages now evictable: acquiring them removes them from the reclaimable set
+      for (int p : hits) idle_hits += e->bm.ref[p] == 0;
+      const int need = hist_pages - static_cast<int>(hits.size()) + 1;
+      if (need > e->bm.reclaimable() - idle_hits) break;
+    }
+    e->waiting.pop_front();
     e->bm.acquire(hits);
     r->pages = hits;
     r->canon = hits;
@@ -280,9 +304,17 @@ bool ensure_pages(vd_engine* e, Request* r, int upto) {
   return e->bm.allocate(need, r->pages);
 }
 
-void make_plan(vd_engine* e) {
+// Plans one step.  Decode rows first, then prompt chunks in admission order,
+// within the token budget; a request that cannot get its pages this step
+// waits.  If nothing fits, the newest running request is preempted (its
+// pages released, its K/V recomputed later) and nothing is admitted for the
+// rest of this planning pass, so the victim cannot take its pages straight
+// back; this repeats until something fits.  A request that cannot get its
+// pages while running alone does not fit in the pool: VD_ERR_CAPACITY.
+int make_plan(vd_engine* e) {
+  bool allow_admit = true;
   for (;;) {
-    admit(e);
+    if (allow_admit || e->running.empty()) admit(e);
     e->plan.clear();
     int budget = e->cfg.token_budget;
     std::vector<Request*> order(e->running);
@@ -299,11 +331,12 @@ void make_plan(vd_engine* e) {
       e->plan.push_back({r, n});
       budget -= n;
     }
-    if (!e->plan.empty() || e->running.empty()) return;
+    if (!e->plan.empty() || e->running.empty()) return VD_OK;
+    if (e->running.size() == 1) return fail(VD_ERR_CAPACITY, "a request does not fit in the KV pool on its own");
     Request* victim = *std::max_element(e->running.begin(), e->running.end(),
                                         [](const Request* a, const Request* b) { return a->rid < b->rid; });
     preempt(e, victim);
-    if (e->running.empty() && e->waiting.empty()) return;
+    allow_admit = false;
   }
 }
 
@@ -383,8 +416,8 @@ int vd_engine_add_request(vd_engine* e, const int32_t* prompt, int32_t len, int3
 int vd_engine_plan(vd_engine* e, vd_engine_plan_out* out) {
   if (!e || !out) return fail(VD_ERR_INVALID_ARG, "null argument");
   if (e->planned) return fail(VD_ERR_INVALID_ARG, "previous plan not committed");
-  make_plan(e);
   memset(out, 0, sizeof(*out));
+  if (const int rc = make_plan(e)) return rc;
   if (e->plan.empty()) return VD_OK;
   e->tok.clear();
   e->pos.clear();

@@ -344,9 +344,9 @@ class Model:
         check(lib().vd_set_graph_mode(self.h, int(max_graphs)))
 
     def graph_stats(self) -> dict:
-        out = (ctypes.c_int64 * 3)()
+        out = (ctypes.c_int64 * 4)()
         check(lib().vd_graph_stats(self.h, out))
-        return {"captures": int(out[0]), "replays": int(out[1]), "cached": int(out[2])}
+        return {"captures": int(out[0]), "replays": int(out[1]), "cached": int(out[2]), "eager": int(out[3])}
 
     def profile_collect(self) -> dict:
         arr = (KernelStat * 32)()

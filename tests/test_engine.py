@@ -108,3 +108,79 @@ def test_finished_prefix_is_retained_then_evicted_leaf_first(weights):
     eng.check()
     assert eng.stats["evicted"] >= 1
     _cold_check(weights, eng)
+
+
+class _NoCompute:
+    """Executor stand-in for scheduling-only tests: token = (rid-independent) 7."""
+
+    def step(self, seqs, rows):
+        return np.zeros((len(rows), 1))
+
+    def sample(self, logits, samplers):
+        return np.full(len(samplers), 7, dtype=np.int32)
+
+
+@pytest.mark.parametrize("num_pages", [40, 48, 64, 96])
+def test_multi_turn_sessions_under_pressure_make_progress(num_pages):
+    """Sessions with a shared prefix resubmitting their whole history every turn,
+    under a pool far smaller than their working set: every plan makes progress
+    (preemption never re-admits its victim in the same pass), the block
+    manager stays consistent, and everything finishes."""
+    rng = np.random.default_rng(num_pages)
+    prefix = synth.make_tokens(96, SPEC.vocab, seed=5)
+    eng = engine.Engine(_NoCompute(), num_pages, max_batch=8, token_budget=64, placement_seed=1)
+    hist, live, emitted = {}, {}, {}
+
+    def submit(s, k):
+        base = prefix if k == 0 else hist[s]
+        hist[s] = np.concatenate([base, synth.make_tokens(int(rng.integers(10, 60)), SPEC.vocab, seed=100 * s + k)])
+        max_new = int(rng.integers(4, 20))
+        rid = eng.add_request(hist[s], max_new, seed=s)
+        live[rid] = (s, k, max_new)
+        emitted[rid] = 0
+
+    for s in range(10):
+        submit(s, 0)
+    steps = 0
+    while eng.pending():
+        rec = eng.step()
+        eng.check()
+        steps += 1
+        assert steps < 5000, "scheduler stopped making progress"
+        for rid in rec:
+            emitted[rid] += 1
+        for rid in [r for r in live if emitted[r] == live[r][2]]:
+            s, k, _ = live.pop(rid)
+            hist[s] = np.asarray(eng.history(rid).history, dtype=np.int32)
+            if k + 1 < 3:
+                submit(s, k + 1)
+    assert not live
+    assert eng.stats["evicted"] > 0 or num_pages >= 96
+
+
+def test_decode_growth_preempts_newest_and_finishes():
+    """Requests admitted when their prompts fit, then outgrowing the pool while
+    decoding: the newest is preempted and recomputed, nothing livelocks, and
+    every request emits all of its tokens."""
+    eng = engine.Engine(_NoCompute(), 24, max_batch=8, token_budget=64, prefix_reuse=False)
+    want = {}
+    for i in range(8):
+        want[eng.add_request(synth.make_tokens(20, SPEC.vocab, seed=i), 60, seed=i)] = 60
+    got = {r: 0 for r in want}
+    steps = 0
+    while eng.pending():
+        for rid in eng.step():
+            got[rid] += 1
+        eng.check()
+        steps += 1
+        assert steps < 5000, "scheduler stopped making progress"
+    assert got == want
+    assert eng.stats["preempted"] > 0
+
+
+def test_request_larger_than_the_pool_is_reported():
+    eng = engine.Engine(_NoCompute(), 4, max_batch=2, token_budget=64)
+    eng.add_request(synth.make_tokens(100, SPEC.vocab, seed=1), 4)
+    with pytest.raises(Exception, match="VD_ERR_CAPACITY"):
+        for _ in range(4):  # the first 64-token chunk fits in the 4 pages, the rest cannot
+            eng.step()
