@@ -49,6 +49,12 @@ class ModelSpec:
     sliding_window: int = 0  # 0: no local layers
     local_global_period: int = 0  # 0: every layer global
     page_size: int = 16
+    # Gemma-3 block: embeddings times bf16(sqrt(d)); RMSNorm gains (1 + w);
+    # sandwich norms (a norm on the attention and FFN outputs before each
+    # residual add, weights post_attn_norm / post_ffn_norm).
+    embed_scale: bool = False
+    norm_offset: bool = False
+    sandwich_norm: bool = False
 
     @property
     def qkv_dim(self) -> int:
@@ -83,11 +89,13 @@ LLAMA8B = ModelSpec("llama3.1-8b-shape", 32, 4096, 32, 8, 128, 14336, 128256,
 # One decoder layer of the 8B shape plus the LM head (decode sweep workload).
 LLAMA8B_1L = LLAMA8B.with_(name="llama3.1-8b-shape-1layer", n_layers=1)
 
-# Gemma-3-4B shape: QK-RMSNorm, GeGLU, 5 local (window 1024) : 1 global.
+# Gemma-3-4B shape: QK-RMSNorm, GeGLU, 5 local (window 1024) : 1 global,
+# and the Gemma-3 block (embedding scale, (1 + w) norm gains, sandwich norms).
 GEMMA3_4B = ModelSpec("gemma3-4b-shape", 34, 2560, 8, 4, 256, 10240, 262144,
                       act="geglu", qk_norm=True, rope_theta=1e6,
                       rope_theta_local=1e4, sliding_window=1024,
-                      local_global_period=6)
+                      local_global_period=6, rms_eps=1e-6, embed_scale=True,
+                      norm_offset=True, sandwich_norm=True)
 
 SPECS = {s.name: s for s in (TINY, LLAMA8B, LLAMA8B_1L, GEMMA3_4B)}
 
@@ -109,6 +117,9 @@ def weight_shapes(spec: ModelSpec) -> dict:
             shapes[p + "q_norm"] = (hd,)
             shapes[p + "k_norm"] = (hd,)
         shapes[p + "wo"] = (d, spec.attn_dim)
+        if spec.sandwich_norm:
+            shapes[p + "post_attn_norm"] = (d,)
+            shapes[p + "post_ffn_norm"] = (d,)
         shapes[p + "ffn_norm"] = (d,)
         shapes[p + "w_gate_up"] = (2 * F, d)  # rows 0..F-1 gate, F..2F-1 up
         shapes[p + "w_down"] = (d, F)
@@ -124,7 +135,9 @@ def make_weights(spec: ModelSpec, seed: int = 0, device="cpu", std: float = 0.02
     """Random-init bf16 weights, one independent generator stream per tensor.
 
     Matrices ~ N(0, std) rounded to bf16; norm gains are 1 + N(0, gain_std)
-    (exactly 1.0 for gain_std == 0).  ``zero=True`` gives the all-zero model.
+    (exactly 1.0 for gain_std == 0).  With ``spec.norm_offset`` the stored
+    weight w is the gain minus one, N(0, gain_std).  ``zero=True`` gives the
+    all-zero model.
     """
     out = {}
     for name, shape in weight_shapes(spec).items():
@@ -134,7 +147,7 @@ def make_weights(spec: ModelSpec, seed: int = 0, device="cpu", std: float = 0.02
         g = torch.Generator(device=device)
         g.manual_seed(_subseed(seed, name))
         if _is_gain(name):
-            t = torch.ones(shape, dtype=torch.float32, device=device)
+            t = torch.full(shape, 0.0 if spec.norm_offset else 1.0, dtype=torch.float32, device=device)
             if gain_std > 0:
                 t += gain_std * torch.randn(shape, generator=g, device=device)
         else:

@@ -16,12 +16,17 @@ Per decoder layer (Llama block; Gemma deltas QK-RMSNorm, GeGLU and local
 sliding-window layers as named by the model configuration):
 
     a = rms(x) ; q,k,v = bf16(a Wqkv^T) ; [q,k = bf16(rms_head(q,k))]
-    q,k = bf16(rope(q,k)) ; o = bf16(attention) ; x = bf16(x + bf16(o Wo^T))
-    a = rms(x) ; g,u = bf16(a Wgu^T) ; z = bf16(act(g) u)
-    x = bf16(x + bf16(z Wd^T))
+    q,k = bf16(rope(q,k)) ; o = bf16(attention) ; h = bf16(o Wo^T)
+    [h = rms_post_attn(h)] ; x = bf16(x + h)
+    a = rms(x) ; g,u = bf16(a Wgu^T) ; z = bf16(act(g) u) ; h = bf16(z Wd^T)
+    [h = rms_post_ffn(h)] ; x = bf16(x + h)
     logits = rms(x_last) W_lm^T           (float64, not rounded)
 
-``rms(x) = bf16(x / sqrt(mean(x^2) + eps) * w)``; RoPE rotates the pairs
+``rms(x) = bf16(x / sqrt(mean(x^2) + eps) * g)`` with gain g = w, or
+g = 1 + w for the Gemma-3 block, which also scales the embeddings by
+bf16(sqrt(d)) and adds the bracketed sandwich norms.  The pages name the
+Gemma3-4B model but not its block; these three deltas are the published
+Gemma 3 architecture, taken as a reading.  RoPE rotates the pairs
 (i, i + hd/2) ("rotate half") by angle ``p * theta**(-2i/hd)``; attention
 of a row at position p sees keys ``[lo, p]`` with ``lo = 0`` for global
 layers and ``max(0, p - w + 1)`` for a window of w keys (深入解析 Vosti
@@ -47,11 +52,11 @@ import numpy as np
 from .bf16 import bits_to_f64, round_bf16
 
 
-def rmsnorm(x, w, eps):
-    """bf16(x / sqrt(mean(x^2) + eps) * w) over the last axis, float64 inside."""
+def rmsnorm(x, w, eps, offset=0.0):
+    """bf16(x / sqrt(mean(x^2) + eps) * (w + offset)) over the last axis, float64 inside."""
     x = np.asarray(x, dtype=np.float64)
     ms = np.mean(x * x, axis=-1, keepdims=True)
-    return round_bf16(x * (1.0 / np.sqrt(ms + eps)) * w)
+    return round_bf16(x * (1.0 / np.sqrt(ms + eps)) * (w + offset))
 
 
 def rope(x, positions, theta):
@@ -109,6 +114,12 @@ class OracleDecoder:
         self.w = weights_u16
         self.chunk_rows = chunk_rows
         self._vec = {}
+        self.offset = 1.0 if getattr(spec, "norm_offset", False) else 0.0
+        self.embed_scale = bool(getattr(spec, "embed_scale", False))
+        self.sandwich = bool(getattr(spec, "sandwich_norm", False))
+
+    def rms(self, x, name):
+        return rmsnorm(x, self.vec(name), self.spec.rms_eps, self.offset)
 
     # -- weights ---------------------------------------------------------
     def vec(self, name):
@@ -147,17 +158,19 @@ class OracleDecoder:
         positions = start + np.arange(n)
         Hq, Hkv, hd, F = s.n_heads, s.n_kv_heads, s.head_dim, s.ffn_dim
         x = bits_to_f64(self.w["embed"][tokens])
+        if self.embed_scale:
+            x = round_bf16(x * round_bf16(math.sqrt(s.d_model)))
         new_cache = []
         for i in range(s.n_layers):
             p = f"layers.{i}."
-            a = rmsnorm(x, self.vec(p + "attn_norm"), s.rms_eps)
+            a = self.rms(x, p + "attn_norm")
             qkv = round_bf16(self.linear(p + "wqkv", a))
             q = qkv[:, :Hq * hd].reshape(n, Hq, hd)
             k = qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(n, Hkv, hd)
             v = qkv[:, (Hq + Hkv) * hd:].reshape(n, Hkv, hd)
             if s.qk_norm:
-                q = rmsnorm(q, self.vec(p + "q_norm"), s.rms_eps)
-                k = rmsnorm(k, self.vec(p + "k_norm"), s.rms_eps)
+                q = self.rms(q, p + "q_norm")
+                k = self.rms(k, p + "k_norm")
             theta = s.layer_theta(i)
             q = rope(q, positions, theta)
             k = rope(k, positions, theta)
@@ -165,15 +178,21 @@ class OracleDecoder:
             V = np.concatenate([cache[i][1], v], axis=0)
             new_cache.append((K, V))
             o = attention(q, K, V, positions, s.layer_window(i)).reshape(n, Hq * hd)
-            x = round_bf16(x + round_bf16(self.linear(p + "wo", o)))
-            a = rmsnorm(x, self.vec(p + "ffn_norm"), s.rms_eps)
+            h = round_bf16(self.linear(p + "wo", o))
+            if self.sandwich:
+                h = self.rms(h, p + "post_attn_norm")
+            x = round_bf16(x + h)
+            a = self.rms(x, p + "ffn_norm")
             gu = round_bf16(self.linear(p + "w_gate_up", a))
             g, u = gu[:, :F], gu[:, F:]
             act = gelu_tanh(g) if s.act == "geglu" else silu(g)
             z = round_bf16(act * u)
-            x = round_bf16(x + round_bf16(self.linear(p + "w_down", z)))
+            h = round_bf16(self.linear(p + "w_down", z))
+            if self.sandwich:
+                h = self.rms(h, p + "post_ffn_norm")
+            x = round_bf16(x + h)
         rows = [n - 1] if logit_rows is None else list(logit_rows)
-        h = rmsnorm(x[rows], self.vec("final_norm"), s.rms_eps)
+        h = self.rms(x[rows], "final_norm")
         return self.linear("lm_head", h), new_cache
 
     def forward(self, history):

@@ -295,3 +295,66 @@ def test_two_token_one_layer_attention_wiring():
     x2 = bf(x1 + bf(T["layers.0.w_down"] @ bf(torch.nn.functional.silu(g) * u)))
     want = T["lm_head"] @ bf(x2 * torch.rsqrt((x2 * x2).mean() + spec.rms_eps))
     np.testing.assert_allclose(dec.forward(toks), want.numpy(), rtol=0, atol=1e-9)
+
+
+# ---------------------------------------------------------------- Gemma-3 block
+GEMMA_BLOCK = dict(act="geglu", qk_norm=True, embed_scale=True, norm_offset=True, sandwich_norm=True,
+                   rms_eps=1e-6)
+
+
+def test_rmsnorm_offset_gain_closed_form():
+    # Gemma-style gains: g = 1 + w.  A constant row c with w = 0 gives c/sqrt(c^2+eps);
+    # with w = -1 the gain is exactly 0.
+    for c in (0.5, -3.0, 7.25):
+        x = np.full((1, 32), c)
+        want = round_bf16(np.array(c / math.sqrt(c * c + 1e-6)))
+        np.testing.assert_array_equal(od.rmsnorm(x, np.zeros(32), 1e-6, offset=1.0), np.full((1, 32), want))
+        np.testing.assert_array_equal(od.rmsnorm(x, -np.ones(32), 1e-6, offset=1.0), np.zeros((1, 32)))
+
+
+def test_gemma_block_zero_model_gives_zero_logits():
+    spec = synth.TINY.with_(**GEMMA_BLOCK)
+    W = synth.make_weights(spec, zero=True)
+    dec = od.OracleDecoder(spec, synth.weights_to_numpy(W))
+    assert np.all(dec.forward(synth.make_tokens(9, spec.vocab)) == 0)
+
+
+def test_gemma_block_one_token_forward_reduces_to_library_ops():
+    # One token attends to itself only, so attention returns v; the rest is
+    # torch float64 ops written from the block's definition: embeddings times
+    # bf16(sqrt(d)), (1 + w) gains, a norm on each sub-layer output before the
+    # residual add, GeGLU with the tanh GELU.
+    spec, W, dec = _tiny(seed=4, gain_std=0.1, **GEMMA_BLOCK)
+    assert "layers.0.post_attn_norm" in W and "layers.1.post_ffn_norm" in W
+    tok = 29
+    T = {k: v.to(torch.float64) for k, v in W.items()}
+    bf = lambda t: t.to(torch.bfloat16).to(torch.float64)
+    def rms(x, w):
+        return bf(x * torch.rsqrt((x * x).mean() + spec.rms_eps) * (1.0 + w))
+    x = bf(T["embed"][tok] * bf(torch.tensor(math.sqrt(spec.d_model), dtype=torch.float64)))
+    Hq, Hkv, hd, F = spec.n_heads, spec.n_kv_heads, spec.head_dim, spec.ffn_dim
+    for i in range(spec.n_layers):
+        p = f"layers.{i}."
+        a = rms(x, T[p + "attn_norm"])
+        v = bf(T[p + "wqkv"][(Hq + Hkv) * hd:] @ a).reshape(Hkv, hd)
+        o = v.repeat_interleave(Hq // Hkv, dim=0).reshape(-1)
+        x = bf(x + rms(bf(T[p + "wo"] @ o), T[p + "post_attn_norm"]))
+        a = rms(x, T[p + "ffn_norm"])
+        g = bf(T[p + "w_gate_up"][:F] @ a)
+        u = bf(T[p + "w_gate_up"][F:] @ a)
+        z = bf(torch.nn.functional.gelu(g, approximate="tanh") * u)
+        x = bf(x + rms(bf(T[p + "w_down"] @ z), T[p + "post_ffn_norm"]))
+    want = T["lm_head"] @ rms(x, T["final_norm"])
+    got = dec.forward(np.array([tok]))
+    np.testing.assert_allclose(got, want.numpy(), rtol=0, atol=1e-12)
+
+
+def test_gemma_block_incremental_equals_cold_forward_bitwise():
+    spec, W, dec = _tiny(seed=6, gain_std=0.1, **GEMMA_BLOCK)
+    h = synth.make_tokens(30, spec.vocab, seed=12)
+    cold = dec.forward_all(h)
+    cache, parts = dec.empty_cache(), []
+    for a, b in ((0, 11), (11, 12), (12, 30)):
+        lg, cache = dec.step(h[a:b], cache, logit_rows=range(b - a))
+        parts.append(lg)
+    np.testing.assert_array_equal(np.concatenate(parts), cold)
