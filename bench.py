@@ -155,6 +155,55 @@ def algorithmic_bytes(spec, ctx_lens, B):
     return total, kernels
 
 
+def decode_sweep_point(spec, weights, B, K, Wm, graphs, dev, hbm):
+    """One point of the decode batch sweep: the bench workload at batch B
+    (contexts U[512, 8192], permuted pages, random cached K/V), K timed steps
+    of vd_step_sample after Wm warm-up steps, graph replay; device time."""
+    import torch
+    from invariant_vd_step_gb300 import synth, vd
+    spec_, ctx, tables, num_pages = make_workload(B, Wm + K + 1)
+    model = vd.Model(spec, weights, max_tokens=max(B, 16), max_seqs=B, max_logit_rows=B,
+                     max_context=CTX_HI + Wm + K + 32)
+    mem = torch.empty(model.pool_bytes(num_pages), dtype=torch.uint8, device=dev)
+    pool = vd.KVPool(model, num_pages, memory=mem)
+    g = torch.Generator(device=dev)
+    g.manual_seed(4)
+    pv = mem.view(torch.bfloat16)
+    for i in range(0, pv.numel(), 1 << 28):
+        n = min(1 << 28, pv.numel() - i)
+        pv[i:i + n] = torch.randn(n, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    width = max(len(t) for t in tables)
+    pt2d = np.zeros((B, width), dtype=np.int32)
+    for i, t in enumerate(tables):
+        pt2d[i, :len(t)] = t
+    toks = synth.make_tokens(B * (Wm + K), spec.vocab, seed=1).reshape(Wm + K, B)
+    cu, rows = np.arange(B + 1, dtype=np.int32), np.arange(B, dtype=np.int32)
+    batches = [vd.StepBatch.from_arrays(toks[s], cu, ctx + s, pt2d, rows) for s in range(Wm + K)]
+    logits = torch.empty((B, spec.vocab), dtype=torch.float32, device=dev)
+    out_tok = torch.empty(B, dtype=torch.int32, device=dev)
+    samplers = [(1000 + i, 0, 0.0) for i in range(B)]
+    stream = torch.cuda.current_stream(dev)
+    model.set_graph_mode(graphs)
+    for s in range(Wm):
+        model.step_sample(pool, batches[s], samplers, logits, out_tok, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(Wm, Wm + K):
+        model.step_sample(pool, batches[s], samplers, logits, out_tok, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    assert model.device_status() == 0
+    total, _ = algorithmic_bytes(spec, ctx + Wm, B)
+    pool.close()
+    model.close()
+    del mem
+    roof_ms = total / (hbm * 1e9) * 1e3
+    return {"batch": B, "tok_s": round(B / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
+            "step_roofline_frac": round(roof_ms / ms, 4), "roofline_tok_s": round(B / (roof_ms * 1e-3), 1)}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -343,6 +392,9 @@ def run_gpu(args):
                               "workload": "tiny llama-style decoder, 8 requests, 16 greedy decode steps"}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, weights, ctx, tables, mem, args.cpu_sample)
+    if args.sweep:
+        line["sweep"] = [decode_sweep_point(spec, weights, b, 10, 3, args.graphs, dev, hbm)
+                         for b in (1, 2, 4, 8, 16, 32, 64, 128, 256)]
     print(json.dumps(line))
     if ws > 1:
         dist.destroy_process_group()
@@ -633,6 +685,7 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-invariance", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="decode: add the batch sweep 1..256 to the line")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "serve"])
     ap.add_argument("--workload", default="c3", choices=["c3", "c5"], help="serve mode workload")

@@ -84,6 +84,12 @@ typedef struct vd_model_config {
   int32_t max_seqs;          /* max requests per step                         */
   int32_t max_logit_rows;    /* max rows returning logits per step            */
   int32_t max_context;       /* max cached + new tokens of one request        */
+  /* Gemma-3 block (the published Gemma 3 architecture; the pages name the
+   * model, not its block): */
+  int32_t embed_scale;       /* 1: embeddings times bf16(sqrt(d_model))       */
+  int32_t norm_offset;       /* 1: every RMSNorm gain is (1 + w), fp32        */
+  int32_t sandwich_norm;     /* 1: x = x + rms_post(sub-layer output), both
+                                sub-layers (post_attn_norm, post_ffn_norm)    */
 } vd_model_config;
 
 /* Per-layer weights: bf16 device pointers, borrowed (caller keeps them
@@ -97,6 +103,8 @@ typedef struct vd_layer_weights {
   const void* ffn_norm;    /* [d]                                             */
   const void* w_gate_up;   /* [2F][d]; rows 0..F-1 gate, F..2F-1 up           */
   const void* w_down;      /* [d][F]                                          */
+  const void* post_attn_norm; /* [d] (only if sandwich_norm)                  */
+  const void* post_ffn_norm;  /* [d] (only if sandwich_norm)                  */
 } vd_layer_weights;
 
 typedef struct vd_weight_ptrs {

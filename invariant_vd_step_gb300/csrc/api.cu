@@ -174,6 +174,9 @@ struct vd_model {
   ActBuf a, o, z, ar;
   // workspace
   __nv_bfloat16 *x = nullptr, *qkv = nullptr, *q = nullptr;
+  __nv_bfloat16* hsub = nullptr;  // sandwich norms: a sub-layer's output before its norm
+  float embed_scale = 0.f;        // 0: none, else bf16(sqrt(d)) as float
+  float gain_offset = 0.f;        // RMSNorm gains are w + gain_offset
   float *part_o = nullptr, *part_ml = nullptr;
   float *cos_g = nullptr, *sin_g = nullptr, *cos_l = nullptr, *sin_l = nullptr;
   int* status = nullptr;
@@ -515,6 +518,7 @@ int run_rope(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d, const __nv
   r.q_norm = c.qk_norm ? static_cast<const __nv_bfloat16*>(m->layers[layer].q_norm) : nullptr;
   r.k_norm = c.qk_norm ? static_cast<const __nv_bfloat16*>(m->layers[layer].k_norm) : nullptr;
   r.eps = c.rms_eps;
+  r.gain_offset = m->gain_offset;
   r.T = d.T;
   r.Hq = c.n_heads;
   r.Hkv = c.n_kv_heads;
@@ -596,18 +600,22 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
   const vd_model_config& c = m->cfg;
   const int T = d.T, dm = c.d_model, hd = c.head_dim, F = c.ffn_dim;
   const int qkv_dim = (c.n_heads + 2 * c.n_kv_heads) * hd;
+  const float off = m->gain_offset;
+  const bool sandwich = c.sandwich_norm != 0;
   {
     Prof p(m, K_EMBED, s);
-    if ((rc = launch_embed(m->embed, m->d_desc + d.tokens, d.feed, c.vocab, m->status, m->x, T, dm, s))) return rc;
+    if ((rc = launch_embed(m->embed, m->d_desc + d.tokens, d.feed, c.vocab, m->status, m->embed_scale, m->x, T, dm,
+                           s)))
+      return rc;
   }
   GemmArgs g{};
   g.status = m->status;
   g.T = T;
   for (int l = 0; l < c.n_layers; ++l) {
     const vd_layer_weights& L = m->layers[l];
-    {
+    if (l == 0 || !sandwich) {  // with sandwich norms the previous layer's last kernel produced it
       Prof p(m, K_RMSNORM, s);
-      if ((rc = launch_rmsnorm(m->x, nullptr, L.attn_norm, m->a.ptr, T, dm, c.rms_eps, s))) return rc;
+      if ((rc = launch_rmsnorm(m->x, nullptr, L.attn_norm, m->a.ptr, T, dm, c.rms_eps, off, s))) return rc;
     }
     {
       Prof p(m, K_GEMM_QKV, s);
@@ -616,14 +624,25 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
     }
     if ((rc = run_rope(m, pool, l, d, m->qkv, m->q, s))) return rc;
     if ((rc = run_attention(m, pool, l, d, m->q, m->o.ptr, s))) return rc;
-    {
-      Prof p(m, K_GEMM_O, s);
-      g.out = m->x; g.residual = m->x; g.K = c.n_heads * hd; g.ldo = dm; g.b_box_rows = m->o.box_for(T);
-      if ((rc = launch_gemm(m->m_o[l], m->o.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
-    }
-    {
+    if (sandwich) {
+      // h = bf16(o Wo^T); x = bf16(x + rms_post(h)); a = rms_ffn(x)
+      {
+        Prof p(m, K_GEMM_O, s);
+        g.out = m->hsub; g.residual = nullptr; g.K = c.n_heads * hd; g.ldo = dm; g.b_box_rows = m->o.box_for(T);
+        if ((rc = launch_gemm(m->m_o[l], m->o.map_for(T), dm / kGemmBM, g, EPI_BF16, s))) return rc;
+      }
       Prof p(m, K_RMSNORM, s);
-      if ((rc = launch_rmsnorm(m->x, nullptr, L.ffn_norm, m->a.ptr, T, dm, c.rms_eps, s))) return rc;
+      if ((rc = launch_postnorm_residual(m->hsub, m->x, L.post_attn_norm, L.ffn_norm, m->a.ptr, T, dm, c.rms_eps,
+                                         off, s)))
+        return rc;
+    } else {
+      {
+        Prof p(m, K_GEMM_O, s);
+        g.out = m->x; g.residual = m->x; g.K = c.n_heads * hd; g.ldo = dm; g.b_box_rows = m->o.box_for(T);
+        if ((rc = launch_gemm(m->m_o[l], m->o.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
+      }
+      Prof p(m, K_RMSNORM, s);
+      if ((rc = launch_rmsnorm(m->x, nullptr, L.ffn_norm, m->a.ptr, T, dm, c.rms_eps, off, s))) return rc;
     }
     {
       Prof p(m, K_GEMM_GU, s);
@@ -632,7 +651,19 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
                             c.act == VD_ACT_GEGLU ? EPI_GEGLU : EPI_SWIGLU, s)))
         return rc;
     }
-    {
+    if (sandwich) {
+      // h = bf16(z Wd^T); x = bf16(x + rms_post(h)); a = rms_attn of the next layer (none after the last)
+      {
+        Prof p(m, K_GEMM_DOWN, s);
+        g.out = m->hsub; g.residual = nullptr; g.K = F; g.ldo = dm; g.b_box_rows = m->z.box_for(T);
+        if ((rc = launch_gemm(m->m_down[l], m->z.map_for(T), dm / kGemmBM, g, EPI_BF16, s))) return rc;
+      }
+      const void* next_norm = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : nullptr;
+      Prof p(m, K_RMSNORM, s);
+      if ((rc = launch_postnorm_residual(m->hsub, m->x, L.post_ffn_norm, next_norm, m->a.ptr, T, dm, c.rms_eps, off,
+                                         s)))
+        return rc;
+    } else {
       Prof p(m, K_GEMM_DOWN, s);
       g.out = m->x; g.residual = m->x; g.K = F; g.ldo = dm; g.b_box_rows = m->z.box_for(T);
       if ((rc = launch_gemm(m->m_down[l], m->z.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
@@ -641,7 +672,7 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
   if (d.R > 0) {
     {
       Prof p(m, K_FINAL_NORM, s);
-      if ((rc = launch_rmsnorm(m->x, m->d_desc + d.logit_rows, m->final_norm, m->ar.ptr, d.R, dm, c.rms_eps, s)))
+      if ((rc = launch_rmsnorm(m->x, m->d_desc + d.logit_rows, m->final_norm, m->ar.ptr, d.R, dm, c.rms_eps, off, s)))
         return rc;
     }
     {
@@ -771,8 +802,10 @@ int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_mode
   for (int i = 0; i < c.n_layers; ++i) {
     const vd_layer_weights& L = w->layers[i];
     if (!L.attn_norm || !L.wqkv || !L.wo || !L.ffn_norm || !L.w_gate_up || !L.w_down ||
-        (c.qk_norm && (!L.q_norm || !L.k_norm)))
+        (c.qk_norm && (!L.q_norm || !L.k_norm)) || (c.sandwich_norm && (!L.post_attn_norm || !L.post_ffn_norm)))
       return fail(VD_ERR_INVALID_ARG, "null layer weight");
+    if (c.sandwich_norm && (!aligned16(L.post_attn_norm) || !aligned16(L.post_ffn_norm)))
+      return fail(VD_ERR_INVALID_ARG, "weights must be 16-byte aligned");
     if (!aligned16(L.wqkv) || !aligned16(L.wo) || !aligned16(L.w_gate_up) || !aligned16(L.w_down) ||
         !aligned16(L.attn_norm) || !aligned16(L.ffn_norm))
       return fail(VD_ERR_INVALID_ARG, "weights must be 16-byte aligned");
@@ -788,6 +821,9 @@ int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_mode
   m->lm_head = static_cast<const __nv_bfloat16*>(w->lm_head);
   m->layers.assign(w->layers, w->layers + c.n_layers);
   m->G = c.n_heads / c.n_kv_heads;
+  if (c.embed_scale)  // the scale itself rounded to bf16, as a bf16 model multiplies by it
+    m->embed_scale = __bfloat162float(__float2bfloat16_rn(static_cast<float>(sqrt(static_cast<double>(c.d_model)))));
+  m->gain_offset = c.norm_offset ? 1.0f : 0.0f;
   m->key_tile = attn_key_tile(c.head_dim);
   m->split = kSplitKeys;
   m->max_splits = (c.max_context - 1) / m->split + 1;
@@ -819,6 +855,9 @@ int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_mode
   if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->x), static_cast<size_t>(TM) * d * 2))) return bail(rc);
   if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->qkv), static_cast<size_t>(TM) * qkv_dim * 2))) return bail(rc);
   if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->q), static_cast<size_t>(TM) * attn_dim * 2))) return bail(rc);
+  if (c.sandwich_norm &&
+      (rc = dev_alloc(m, reinterpret_cast<void**>(&m->hsub), static_cast<size_t>(TM) * d * 2)))
+    return bail(rc);
   const size_t np = static_cast<size_t>(TM) * c.n_heads * m->max_splits;
   if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->part_o), np * hd * 4))) return bail(rc);
   if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->part_ml), np * 2 * 4))) return bail(rc);
@@ -1130,7 +1169,7 @@ int vd_op_rmsnorm(const void* x, const void* w, void* y, int32_t rows, int32_t d
   if (!x || !w || !y) return fail(VD_ERR_INVALID_ARG, "null pointer");
   if (rows < 0 || d < 8 || d % 8) return fail(VD_ERR_INVALID_ARG, "d must be a positive multiple of 8");
   if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return fail(VD_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-  return launch_rmsnorm(x, nullptr, w, y, rows, d, eps, static_cast<cudaStream_t>(stream));
+  return launch_rmsnorm(x, nullptr, w, y, rows, d, eps, 0.f, static_cast<cudaStream_t>(stream));
 }
 
 int vd_op_attention(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, const void* q, void* out,

@@ -16,7 +16,7 @@ namespace {
 // token produced on the device by an earlier step).  A fed id outside the
 // vocabulary is recorded in the status word and row 0 is read instead.
 __global__ void embed_kernel(const uint4* __restrict__ E, const int* __restrict__ tok, const int* __restrict__ feed,
-                             int V, int* status, uint4* __restrict__ x, int d8) {
+                             int V, int* status, float scale, uint4* __restrict__ x, int d8) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
@@ -29,8 +29,20 @@ __global__ void embed_kernel(const uint4* __restrict__ E, const int* __restrict_
     }
   }
   const size_t src = static_cast<size_t>(id) * d8;
+  if (scale == 0.f) {
 #pragma unroll 4
-  for (int c = threadIdx.x; c < d8; c += blockDim.x) x[static_cast<size_t>(t) * d8 + c] = E[src + c];
+    for (int c = threadIdx.x; c < d8; c += blockDim.x) x[static_cast<size_t>(t) * d8 + c] = E[src + c];
+  } else {
+#pragma unroll 4
+    for (int c = threadIdx.x; c < d8; c += blockDim.x) {
+      const uint4 v = E[src + c];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(__fmul_rn(bf16_lo(w[i]), scale), __fmul_rn(bf16_hi(w[i]), scale));
+      x[static_cast<size_t>(t) * d8 + c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
 }
 
 __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
@@ -57,7 +69,7 @@ __device__ __forceinline__ float warp_sum_fixed(float v) {
 template <int CH>
 __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ row_idx,
                                const __nv_bfloat16* __restrict__ w, __nv_bfloat16* __restrict__ y, int rows, int d,
-                               float eps) {
+                               float eps, float off) {
   pdl_wait();
   pdl_trigger();
   const int r = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -71,6 +83,10 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* _
     float f[8], g[8];
     unpack8(xv, f);
     unpack8(wr[c], g);
+    if (off != 0.f) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = __fadd_rn(g[i], off);
+    }
     uint4 o;
     o.x = pack_bf16x2(__fmul_rn(__fmul_rn(f[0], inv), g[0]), __fmul_rn(__fmul_rn(f[1], inv), g[1]));
     o.y = pack_bf16x2(__fmul_rn(__fmul_rn(f[2], inv), g[2]), __fmul_rn(__fmul_rn(f[3], inv), g[3]));
@@ -105,6 +121,108 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* _
     ss = warp_sum_fixed(ss);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(d)), eps)));
     for (int c = lane; c < d8; c += 32) out8(xr[c], c, inv);
+  }
+}
+
+// Sandwich norm of a sub-layer output h, residual add, and (optionally) the
+// next pre-norm, one warp per row:
+//   x = bf16(x + bf16(h * (1 / sqrt(mean(h^2) + eps)) * g_post))
+//   y = bf16(x * (1 / sqrt(mean(x^2) + eps)) * g_pre)        (if w_pre)
+// Both sums run in the lane-strided order of rmsnorm_kernel, so y equals what
+// rmsnorm_kernel gives for the new x.  CH as in rmsnorm_kernel.
+template <int CH>
+__global__ void postnorm_residual_kernel(const __nv_bfloat16* __restrict__ h, __nv_bfloat16* __restrict__ x,
+                                         const __nv_bfloat16* __restrict__ w_post,
+                                         const __nv_bfloat16* __restrict__ w_pre, __nv_bfloat16* __restrict__ y,
+                                         int rows, int d, float eps, float off) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const uint4* hr = reinterpret_cast<const uint4*>(h + static_cast<size_t>(r) * d);
+  uint4* xr = reinterpret_cast<uint4*>(x + static_cast<size_t>(r) * d);
+  uint4* yr = reinterpret_cast<uint4*>(y + static_cast<size_t>(r) * d);
+  const uint4* wp = reinterpret_cast<const uint4*>(w_post);
+  const uint4* wq = reinterpret_cast<const uint4*>(w_pre);
+  const int d8 = d >> 3;
+  auto add8 = [](float ss, const uint4& v) {
+    float f[8];
+    unpack8(v, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(f[i], f[i]));
+    return ss;
+  };
+  auto gains8 = [&](const uint4* w, int c, float* g) {
+    unpack8(w[c], g);
+    if (off != 0.f) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = __fadd_rn(g[i], off);
+    }
+  };
+  auto inv_of = [&](float ss) {
+    ss = warp_sum_fixed(ss);
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(d)), eps)));
+  };
+  // x + bf16(h * inv * g) for one chunk, rounded to bf16
+  auto resid8 = [&](const uint4& hv, const uint4& xv, int c, float inv) {
+    float fh[8], fx[8], g[8], o[8];
+    unpack8(hv, fh);
+    unpack8(xv, fx);
+    gains8(wp, c, g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = __fadd_rn(fx[i], bf16_round(__fmul_rn(__fmul_rn(fh[i], inv), g[i])));
+    return make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+  };
+  auto norm8 = [&](const uint4& xv, int c, float inv) {
+    float f[8], g[8];
+    unpack8(xv, f);
+    gains8(wq, c, g);
+    return make_uint4(pack_bf16x2(__fmul_rn(__fmul_rn(f[0], inv), g[0]), __fmul_rn(__fmul_rn(f[1], inv), g[1])),
+                      pack_bf16x2(__fmul_rn(__fmul_rn(f[2], inv), g[2]), __fmul_rn(__fmul_rn(f[3], inv), g[3])),
+                      pack_bf16x2(__fmul_rn(__fmul_rn(f[4], inv), g[4]), __fmul_rn(__fmul_rn(f[5], inv), g[5])),
+                      pack_bf16x2(__fmul_rn(__fmul_rn(f[6], inv), g[6]), __fmul_rn(__fmul_rn(f[7], inv), g[7])));
+  };
+  if constexpr (CH > 0) {
+    uint4 hv[CH], xv[CH];
+#pragma unroll
+    for (int k = 0; k < CH; ++k)
+      if (lane + 32 * k < d8) {
+        hv[k] = hr[lane + 32 * k];
+        xv[k] = xr[lane + 32 * k];
+      }
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < CH; ++k)
+      if (lane + 32 * k < d8) ss = add8(ss, hv[k]);
+    const float inv = inv_of(ss);
+#pragma unroll
+    for (int k = 0; k < CH; ++k)
+      if (lane + 32 * k < d8) {
+        xv[k] = resid8(hv[k], xv[k], lane + 32 * k, inv);
+        xr[lane + 32 * k] = xv[k];
+      }
+    if (!w_pre) return;
+    float s2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < CH; ++k)
+      if (lane + 32 * k < d8) s2 = add8(s2, xv[k]);
+    const float inv2 = inv_of(s2);
+#pragma unroll
+    for (int k = 0; k < CH; ++k)
+      if (lane + 32 * k < d8) yr[lane + 32 * k] = norm8(xv[k], lane + 32 * k, inv2);
+  } else {
+    float ss = 0.f;
+    for (int c = lane; c < d8; c += 32) ss = add8(ss, hr[c]);
+    const float inv = inv_of(ss);
+    float s2 = 0.f;
+    for (int c = lane; c < d8; c += 32) {
+      const uint4 xn = resid8(hr[c], xr[c], c, inv);
+      xr[c] = xn;
+      s2 = add8(s2, xn);
+    }
+    if (!w_pre) return;
+    const float inv2 = inv_of(s2);
+    for (int c = lane; c < d8; c += 32) yr[c] = norm8(xr[c], c, inv2);
   }
 }
 
@@ -153,8 +271,13 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_kernel(RopeArgs a) {
     for (int k = 0; k < 4; ++k) {
       const int i = lane + 32 * k;
       if (k < np && i < half) {
-        x1[k] = bf16_round(__fmul_rn(__fmul_rn(x1[k], inv), __bfloat162float(nw[i])));
-        x2[k] = bf16_round(__fmul_rn(__fmul_rn(x2[k], inv), __bfloat162float(nw[i + half])));
+        float g1 = __bfloat162float(nw[i]), g2 = __bfloat162float(nw[i + half]);
+        if (a.gain_offset != 0.f) {
+          g1 = __fadd_rn(g1, a.gain_offset);
+          g2 = __fadd_rn(g2, a.gain_offset);
+        }
+        x1[k] = bf16_round(__fmul_rn(__fmul_rn(x1[k], inv), g1));
+        x2[k] = bf16_round(__fmul_rn(__fmul_rn(x2[k], inv), g2));
       }
     }
   }
@@ -180,16 +303,16 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_kernel(RopeArgs a) {
 
 }  // namespace
 
-int launch_embed(const void* embed, const int* tokens, const int* feed, int V, int* status, void* x, int T, int d,
-                 cudaStream_t s) {
+int launch_embed(const void* embed, const int* tokens, const int* feed, int V, int* status, float scale, void* x,
+                 int T, int d, cudaStream_t s) {
   if (T <= 0) return VD_OK;
   VD_CUDA_TRY(launch_k(embed_kernel, dim3(T), dim3(128), 0, s, static_cast<const uint4*>(embed), tokens, feed, V,
-                       status, static_cast<uint4*>(x), d / 8));
+                       status, scale, static_cast<uint4*>(x), d / 8));
   return VD_OK;
 }
 
 int launch_rmsnorm(const void* x, const int* row_idx, const void* w, void* y, int rows, int d, float eps,
-                   cudaStream_t s) {
+                   float gain_offset, cudaStream_t s) {
   if (rows <= 0) return VD_OK;
   const auto* xp = static_cast<const __nv_bfloat16*>(x);
   const auto* wp = static_cast<const __nv_bfloat16*>(w);
@@ -201,7 +324,26 @@ int launch_rmsnorm(const void* x, const int* row_idx, const void* w, void* y, in
            : per_lane <= 8  ? rmsnorm_kernel<8>
            : per_lane <= 16 ? rmsnorm_kernel<16>
                             : rmsnorm_kernel<0>;
-  VD_CUDA_TRY(launch_k(k, dim3(blocks), dim3(128), 0, s, xp, row_idx, wp, yp, rows, d, eps));
+  VD_CUDA_TRY(launch_k(k, dim3(blocks), dim3(128), 0, s, xp, row_idx, wp, yp, rows, d, eps, gain_offset));
+  return VD_OK;
+}
+
+int launch_postnorm_residual(const void* h, void* x, const void* w_post, const void* w_pre, void* y, int rows, int d,
+                             float eps, float gain_offset, cudaStream_t s) {
+  if (rows <= 0) return VD_OK;
+  const auto* hp = static_cast<const __nv_bfloat16*>(h);
+  auto* xp = static_cast<__nv_bfloat16*>(x);
+  const auto* wp = static_cast<const __nv_bfloat16*>(w_post);
+  const auto* wq = static_cast<const __nv_bfloat16*>(w_pre);
+  auto* yp = static_cast<__nv_bfloat16*>(y);
+  const int per_lane = (d / 8 + 31) / 32, blocks = (rows + 3) / 4;
+  auto k = per_lane <= 1    ? postnorm_residual_kernel<1>
+           : per_lane <= 2  ? postnorm_residual_kernel<2>
+           : per_lane <= 4  ? postnorm_residual_kernel<4>
+           : per_lane <= 8  ? postnorm_residual_kernel<8>
+           : per_lane <= 16 ? postnorm_residual_kernel<16>
+                            : postnorm_residual_kernel<0>;
+  VD_CUDA_TRY(launch_k(k, dim3(blocks), dim3(128), 0, s, hp, xp, wp, wq, yp, rows, d, eps, gain_offset));
   return VD_OK;
 }
 

@@ -123,10 +123,16 @@ int attn_static_scratch(void** ptr);
 
 // ---------------------------------------------------------------- elementwise
 // tokens[t] < 0 refers to feed[-1 - tokens[t]] (device tokens of an earlier step).
-int launch_embed(const void* embed, const int* tokens, const int* feed, int V, int* status, void* x, int T, int d,
-                 cudaStream_t s);
+// scale != 0: x = bf16(E[token] * scale) (Gemma-3 embedding scale).
+int launch_embed(const void* embed, const int* tokens, const int* feed, int V, int* status, float scale, void* x,
+                 int T, int d, cudaStream_t s);
+// y[r] = bf16(x[row_idx[r]] * (1 / sqrt(mean(x^2) + eps)) * (w + gain_offset)).
 int launch_rmsnorm(const void* x, const int* row_idx, const void* w, void* y, int rows, int d, float eps,
-                   cudaStream_t s);
+                   float gain_offset, cudaStream_t s);
+// Sandwich norm + residual (+ the next pre-norm): x = bf16(x + rms(h; w_post));
+// then, if w_pre is not null, y = rms(x; w_pre).  Gains are w + gain_offset.
+int launch_postnorm_residual(const void* h, void* x, const void* w_post, const void* w_pre, void* y, int rows, int d,
+                             float eps, float gain_offset, cudaStream_t s);
 struct RopeArgs {
   const __nv_bfloat16* qkv;   // [T][(Hq+2Hkv) hd]
   __nv_bfloat16* q_out;       // [T][Hq][hd]
@@ -138,6 +144,7 @@ struct RopeArgs {
   const __nv_bfloat16* q_norm;  // nullable
   const __nv_bfloat16* k_norm;
   float eps;
+  float gain_offset;          // QK-norm gains are w + gain_offset
   int T, Hq, Hkv, hd;
   long long layer_elem0;      // first element of this layer in the pool
 };

@@ -38,12 +38,14 @@ class ModelConfig(ctypes.Structure):
                 ("rope_theta_local", ctypes.c_float), ("sliding_window", ctypes.c_int32),
                 ("local_global_period", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("max_tokens", ctypes.c_int32), ("max_seqs", ctypes.c_int32),
-                ("max_logit_rows", ctypes.c_int32), ("max_context", ctypes.c_int32)]
+                ("max_logit_rows", ctypes.c_int32), ("max_context", ctypes.c_int32),
+                ("embed_scale", ctypes.c_int32), ("norm_offset", ctypes.c_int32), ("sandwich_norm", ctypes.c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("attn_norm", "wqkv", "q_norm", "k_norm", "wo", "ffn_norm", "w_gate_up", "w_down")]
+                ("attn_norm", "wqkv", "q_norm", "k_norm", "wo", "ffn_norm", "w_gate_up", "w_down",
+                 "post_attn_norm", "post_ffn_norm")]
 
 
 class WeightPtrs(ctypes.Structure):
@@ -186,7 +188,9 @@ def config_of(spec, max_tokens: int, max_seqs: int, max_logit_rows: int, max_con
         act=1 if spec.act == "geglu" else 0, qk_norm=int(spec.qk_norm), rope_theta=spec.rope_theta,
         rope_theta_local=spec.rope_theta_local, sliding_window=spec.sliding_window,
         local_global_period=spec.local_global_period, page_size=spec.page_size, max_tokens=max_tokens,
-        max_seqs=max_seqs, max_logit_rows=max_logit_rows, max_context=max_context)
+        max_seqs=max_seqs, max_logit_rows=max_logit_rows, max_context=max_context,
+        embed_scale=int(getattr(spec, "embed_scale", False)), norm_offset=int(getattr(spec, "norm_offset", False)),
+        sandwich_norm=int(getattr(spec, "sandwich_norm", False)))
 
 
 class StepBatch:
@@ -264,7 +268,7 @@ class Model:
             p = f"layers.{i}."
             g = lambda n: _ptr(weights.get(p + n))
             layers[i] = LayerWeights(g("attn_norm"), g("wqkv"), g("q_norm"), g("k_norm"), g("wo"), g("ffn_norm"),
-                                     g("w_gate_up"), g("w_down"))
+                                     g("w_gate_up"), g("w_down"), g("post_attn_norm"), g("post_ffn_norm"))
         self._layers = layers
         w = WeightPtrs(_ptr(weights["embed"]), layers, _ptr(weights["final_norm"]), _ptr(weights["lm_head"]))
         h = ctypes.c_void_p()

@@ -35,6 +35,7 @@ def test_create_model_rejects_unsupported_shapes_before_any_cuda_call(L):
         (synth.TINY.with_(page_size=32), 2),                     # page size
         (synth.TINY.with_(d_model=200), 2),                      # no GEMM tiling
         (synth.TINY.with_(n_kv_heads=3), 1),                     # Hq % Hkv
+        (synth.TINY.with_(sandwich_norm=True), 1),               # post-sub-layer norms missing
     ]
     for spec, code in bad:
         cfg = vd.config_of(spec, 64, 4, 8, 256)

@@ -149,3 +149,48 @@ def test_gemma3_4b_batch_and_budget_invariance():
         _assert_views_equal(ref, got)
     alone, _ = _run_engine(spec, W, prompts[:4], 128, 4096, 1, pages, mc, seed=9)
     _assert_views_equal(alone, {r: ref[r] for r in alone})
+
+
+def test_gemma_block_32k_context_prefill_decode_pairs():
+    """Prefill–decode pairs at a 32,768-token context on the Gemma-3 block
+    (embedding scale, (1 + w) gains, sandwich norms, QK-norm, GeGLU, 5:1
+    local/global with window 1024): logits of the last positions computed
+    inside prefill chunks equal those computed by single-token decode steps
+    over the same history, bitwise, under two chunk budgets."""
+    ready()
+    spec = synth.GEMMA3_4B.with_(name="gemma3-4b-shape-2layer", n_layers=2, local_global_period=2)
+    n = 32768
+    hist = synth.make_tokens(n, spec.vocab, seed=21)
+    W = synth.make_weights(spec, seed=0, gain_std=0.1, device="cuda")
+    tail = [n - 4, n - 3, n - 2, n - 1]
+    pages = (n + 15) // 16
+    table = np.arange(pages, dtype=np.int32)[::-1].copy()  # pages in reverse order
+
+    def run(budget, decode_tail):
+        model = vd.Model(spec, W, max_tokens=budget, max_seqs=1, max_logit_rows=budget, max_context=n + 16)
+        pool = vd.KVPool(model, pages)
+        logits = torch.empty((budget, spec.vocab), device="cuda")
+        out = {}
+        end = n - 4 if decode_tail else n
+        for a in range(0, end, budget):
+            b = min(end, a + budget)
+            rows = [p - a for p in tail if a <= p < b]
+            model.step(pool, vd.StepBatch([(hist[a:b], a, table)], logit_rows=rows), logits)
+            for j, p in enumerate(p for p in tail if a <= p < b):
+                out[p] = logits[j].clone()
+        if decode_tail:
+            for p in tail:
+                model.step(pool, vd.StepBatch([(hist[p:p + 1], p, table)], logit_rows=[0]), logits)
+                out[p] = logits[0].clone()
+        torch.cuda.synchronize()
+        assert model.device_status() == 0
+        del pool
+        model.close()
+        return {p: bits(v) for p, v in out.items()}
+
+    pre = run(4096, False)
+    dec = run(4096, True)
+    other = run(2048, True)
+    for p in tail:
+        assert np.array_equal(pre[p], dec[p]), f"position {p}: prefill and decode logits differ"
+        assert np.array_equal(dec[p], other[p]), f"position {p}: budgets 4096 and 2048 differ"

@@ -11,7 +11,8 @@ from oracle.decoder import OracleDecoder
 pytestmark = pytest.mark.gpu
 
 GEMMA_TINY = synth.ModelSpec("gemma-tiny", 3, 256, 2, 1, 256, 512, 512, act="geglu", qk_norm=True,
-                             rope_theta=1e6, rope_theta_local=1e4, sliding_window=24, local_global_period=2)
+                             rope_theta=1e6, rope_theta_local=1e4, sliding_window=24, local_global_period=2,
+                             rms_eps=1e-6, embed_scale=True, norm_offset=True, sandwich_norm=True)
 LLAMA_TINY128 = synth.ModelSpec("llama-tiny-128", 2, 512, 8, 2, 128, 1024, 1024, rope_theta=5e5,
                                 rope_theta_local=5e5)
 
