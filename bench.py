@@ -253,6 +253,7 @@ def run_gpu(args):
         model.step_sample(pool, batches[s], samplers, logits, out_tok, stream)
 
     model.set_graph_mode(args.graphs)  # 0: eager launches
+    model.set_attention_fold(args.attention_fold)
     for s in range(Wm):
         one(s)
     torch.cuda.synchronize()
@@ -366,6 +367,7 @@ def run_gpu(args):
                    "batch": B, "ctx": f"U[{CTX_LO},{CTX_HI}] mean {float(np.mean(ctx)):.0f}",
                    "page_size": 16, "pages": "randomly permuted", "parallelism": f"replicas x{ws}",
                    "launch": f"CUDA graph replay (<= {args.graphs} graphs)" if args.graphs else "eager launches",
+                   "attention_fold": ["default (split)", "fold", "split"][args.attention_fold],
                    "l2": f"inputs larger than L2 ({total_bytes / 1e9:.2f} GB read+written per step)"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dk["GB_s"], "peak": hbm, "unit": "GB/s",
                      "frac": dk["hbm_frac"], "traffic": traffic_of(dom, kbytes[dom] / max(1, round(dk["launches_per_step"]))),
@@ -686,6 +688,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-invariance", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="decode: add the batch sweep 1..256 to the line")
+    ap.add_argument("--ctx", default="512,8192", help="decode: context lengths U[lo, hi] (lo,hi)")
+    ap.add_argument("--attention-fold", type=int, default=0, choices=[0, 1, 2],
+                    help="decode attention mapping: 0 default (one CTA per split), 1 fold splits in one CTA, 2 split")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "serve"])
     ap.add_argument("--workload", default="c3", choices=["c3", "c5"], help="serve mode workload")
@@ -697,6 +702,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=8192, help="prefill mode: tokens per step")
     ap.add_argument("--prefill-requests", type=int, default=4)
     args = ap.parse_args()
+    global CTX_LO, CTX_HI  # the decode workload's context range
+    CTX_LO, CTX_HI = (int(v) for v in args.ctx.split(","))
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

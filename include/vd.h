@@ -182,6 +182,22 @@ void* vd_kv_pool_data(vd_kv_pool* p);
  * T == 0 is a no-op. */
 int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out, void* stream);
 
+/* Workload-dependent decode attention mapping [B §八 8.1: one SM per
+ * sequence for full waves, several SMs for partially filled waves, both with
+ * the same accumulation order; named there as future work that needs a
+ * cross-kernel bitwise check].  Decode-class rows
+ * (q_len * Hq/Hkv <= 16) normally get one CTA per (request, KV head, split)
+ * and a merge kernel folds the split partials.  In fold mode one CTA per
+ * (request, KV head) walks all its splits and folds them itself, with the
+ * merge kernel's arithmetic and order, writing the output directly: no
+ * partials round trip and no merge launch for those rows.  Logits are bitwise
+ * identical in both modes.  mode 0 (default) and 2: split mode; 1: fold
+ * mode.  On GB300 fold mode measured slower or equal (a fold CTA walks its
+ * splits serially, so a long request sets the launch's critical path, and
+ * the merged state costs registers), so the default does not use it.
+ * Head dimensions above 128 never fold.  Errors: VD_ERR_INVALID_ARG. */
+int vd_set_attention_fold(vd_model* m, int32_t mode);
+
 /* Graph replay of steps (an engineering addition; the pages' design has no
  * counterpart).  With max_graphs > 0, vd_step keeps the descriptor upload as
  * an ordinary copy on the stream and replays the step's kernel sequence as

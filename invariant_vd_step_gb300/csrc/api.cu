@@ -129,7 +129,10 @@ struct ActBuf {
 struct Desc {
   int T = 0, B = 0, R = 0, stride = 0;
   int tokens, positions, slot_page, cu_q, cached, page_table, logit_rows, dec_seq, dec_start, pre_seq, pre_start;
+  // (merge_tok: offset of the token list the merge kernel folds)
   int n_dec = 0, n_pre = 0, items_dec = 0, items_pre = 0;
+  bool fold = false;  // decode class in fold mode
+  int merge_tok = 0, n_merge = 0;
   int grid_dec = 0, grid_pre = 0;  // attention CTAs launched (>= items; extra CTAs exit)
   int total = 0;
   const int* feed = nullptr;  // device tokens that entries -(1 + i) of `tokens` refer to
@@ -142,10 +145,11 @@ struct GraphKey {
   const void* logits = nullptr;
   const void* tokens = nullptr;  // fused token choice (vd_step_sample) or null
   const void* feed = nullptr;    // device-side token feedback or null
-  int T = 0, B = 0, R = 0, stride = 0, n_dec = 0, n_pre = 0, grid_dec = 0, grid_pre = 0;
+  int T = 0, B = 0, R = 0, stride = 0, n_dec = 0, n_pre = 0, grid_dec = 0, grid_pre = 0, fold = 0, n_merge = 0;
   bool operator==(const GraphKey& o) const {
     return pool_id == o.pool_id && logits == o.logits && tokens == o.tokens && feed == o.feed && T == o.T && B == o.B && R == o.R && stride == o.stride &&
-           n_dec == o.n_dec && n_pre == o.n_pre && grid_dec == o.grid_dec && grid_pre == o.grid_pre;
+           n_dec == o.n_dec && n_pre == o.n_pre && grid_dec == o.grid_dec && grid_pre == o.grid_pre &&
+           fold == o.fold && n_merge == o.n_merge;
   }
 };
 struct GraphEntry {
@@ -176,6 +180,8 @@ struct vd_model {
   __nv_bfloat16 *x = nullptr, *qkv = nullptr, *q = nullptr;
   __nv_bfloat16* hsub = nullptr;  // sandwich norms: a sub-layer's output before its norm
   float embed_scale = 0.f;        // 0: none, else bf16(sqrt(d)) as float
+  int fold_mode = 0;              // 0: default (split mode), 1: fold the decode class whenever legal, 2: never
+  std::vector<int> scratch_dec;   // host scratch of build_desc
   float gain_offset = 0.f;        // RMSNorm gains are w + gain_offset
   float *part_o = nullptr, *part_ml = nullptr;
   float *cos_g = nullptr, *sin_g = nullptr, *cos_l = nullptr, *sin_l = nullptr;
@@ -376,6 +382,7 @@ int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_token
   d.dec_start = take(B + 1);
   d.pre_seq = take(B);
   d.pre_start = take(B + 1);
+  d.merge_tok = take(T);
   d.total = off;
   if (static_cast<size_t>(off) > m->desc_cap) return fail(VD_ERR_CAPACITY, "descriptor exceeds capacity");
   std::unordered_set<long long> slots;
@@ -413,13 +420,13 @@ int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_token
     h[d.logit_rows + j] = b->logit_rows[j];
   }
   // attention work classes: decode-shaped requests (one warp of rows) and the rest
-  int nd = 0, npre = 0, idec = 0, ipre = 0;
+  int nd = 0, npre = 0, ipre = 0;
+  std::vector<int>& dec = m->scratch_dec;
+  dec.clear();
   for (int s = 0; s < B; ++s) {
     const int ql = b->cu_q[s + 1] - b->cu_q[s], kv = b->cached_len[s] + ql;
     if (ql * m->G <= 16) {
-      h[d.dec_seq + nd] = s;
-      h[d.dec_start + nd] = idec;
-      idec += attn_items(ql, kv, m->G, c.n_kv_heads, 16);
+      dec.push_back(s);
       ++nd;
     } else {
       h[d.pre_seq + npre] = s;
@@ -427,6 +434,23 @@ int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_token
       ipre += attn_items(ql, kv, m->G, c.n_kv_heads, 64);
       ++npre;
     }
+  }
+  // Fold mode (one CTA per request and KV head, folding its splits itself)
+  // only on request: on this GPU it never beat split mode (a fold CTA walks
+  // its splits one after another, so a long request sets the launch's
+  // critical path, and its merged state costs registers).  In fold mode the
+  // longest requests go first.  Neither mode changes a row's arithmetic.
+  d.fold = nd > 0 && c.head_dim <= 128 && m->fold_mode == 1;
+  if (d.fold)
+    std::stable_sort(dec.begin(), dec.end(), [&](int x, int y) {
+      return b->cached_len[x] + b->cu_q[x + 1] - b->cu_q[x] > b->cached_len[y] + b->cu_q[y + 1] - b->cu_q[y];
+    });
+  int idec = 0;
+  for (int k = 0; k < nd; ++k) {
+    const int s = dec[k], ql = b->cu_q[s + 1] - b->cu_q[s], kv = b->cached_len[s] + ql;
+    h[d.dec_seq + k] = s;
+    h[d.dec_start + k] = idec;
+    idec += d.fold ? c.n_kv_heads : attn_items(ql, kv, m->G, c.n_kv_heads, 16);
   }
   h[d.dec_start + nd] = idec;
   h[d.pre_start + npre] = ipre;
@@ -436,6 +460,15 @@ int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_token
   d.items_pre = ipre;
   d.grid_dec = graph_shape ? bucket_items(idec) : idec;
   d.grid_pre = graph_shape ? bucket_items(ipre) : ipre;
+  // tokens the merge kernel folds: all of them, or only the prefill class's
+  d.n_merge = T;
+  if (d.fold) {
+    d.n_merge = 0;
+    for (int k = 0; k < npre; ++k) {
+      const int s = h[d.pre_seq + k];
+      for (int t = b->cu_q[s]; t < b->cu_q[s + 1]; ++t) h[d.merge_tok + d.n_merge++] = t;
+    }
+  }
   return VD_OK;
 }
 
@@ -480,7 +513,10 @@ int run_attention(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d, const
     a.cls_seq = m->d_desc + d.dec_seq;
     a.cls_start = m->d_desc + d.dec_start;
     a.n_cls = d.n_dec;
+    a.fold = d.fold;
+    a.out = out;
     if ((rc = launch_attention(pool->map, a, hd, false, d.grid_dec, s))) return rc;
+    a.fold = 0;
   }
   if (d.n_pre) {
     Prof p(m, K_ATTN, s);
@@ -489,12 +525,14 @@ int run_attention(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d, const
     a.n_cls = d.n_pre;
     if ((rc = launch_attention(pool->map, a, hd, true, d.grid_pre, s))) return rc;
   }
+  if (d.n_merge == 0) return VD_OK;  // every row was folded inside the attention kernel
   MergeArgs g{};
   g.part_o = m->part_o;
   g.part_ml = m->part_ml;
   g.out = out;
   g.positions = m->d_desc + d.positions;
-  g.T = d.T;
+  g.tokens = d.fold ? m->d_desc + d.merge_tok : nullptr;
+  g.T = d.n_merge;
   g.Hq = c.n_heads;
   g.window = window;
   g.split = m->split;
@@ -557,7 +595,10 @@ int run_attention_static(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d
     a.cls_seq = m->d_desc + d.dec_seq;
     a.cls_start = m->d_desc + d.dec_start;
     a.n_cls = d.n_dec;
+    a.fold = d.fold;
+    a.out = out;
     if ((rc = launch_attention(pool->map, a, hd, false, d.items_dec, s))) return rc;
+    a.fold = 0;
   }
   if (d.n_pre) {
     a.cls_seq = m->d_desc + d.pre_seq;
@@ -565,12 +606,14 @@ int run_attention_static(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d
     a.n_cls = d.n_pre;
     if ((rc = launch_attention(pool->map, a, hd, true, d.items_pre, s))) return rc;
   }
+  if (d.n_merge == 0) return VD_OK;
   MergeArgs g{};
   g.part_o = part_o;
   g.part_ml = part_ml;
   g.out = out;
   g.positions = m->d_desc + d.positions;
-  g.T = d.T;
+  g.tokens = d.fold ? m->d_desc + d.merge_tok : nullptr;
+  g.T = d.n_merge;
   g.Hq = c.n_heads;
   g.window = window;
   g.split = m->split;
@@ -722,6 +765,8 @@ int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out,
   k.n_pre = d.n_pre;
   k.grid_dec = d.grid_dec;
   k.grid_pre = d.grid_pre;
+  k.fold = d.fold;
+  k.n_merge = d.n_merge;
   GraphEntry* seen = nullptr;
   for (GraphEntry& e : m->graphs)
     if (e.key == k) {
@@ -865,7 +910,7 @@ int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_mode
   if ((rc = rope_table(m, c.rope_theta_local, hd, &m->cos_l, &m->sin_l))) return bail(rc);
   if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->status), 256))) return bail(rc);
   const int max_pages = (c.max_context + 15) / 16;
-  m->desc_cap = 3 * static_cast<size_t>(TM) + 6 * static_cast<size_t>(c.max_seqs) + 8 +
+  m->desc_cap = 4 * static_cast<size_t>(TM) + 6 * static_cast<size_t>(c.max_seqs) + 8 +
                 static_cast<size_t>(c.max_seqs) * max_pages + c.max_logit_rows;
   if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->d_desc), m->desc_cap * 4))) return bail(rc);
   for (int k = 0; k < 2; ++k) {
@@ -1019,6 +1064,13 @@ int vd_step_sample_fed(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const i
                        void* stream) {
   if (!feed_index) return fail(VD_ERR_INVALID_ARG, "null feed_index");
   return step_sample_impl(m, pool, b, feed_index, feed_tokens, per_row, logits_out, tokens_out, stream);
+}
+
+int vd_set_attention_fold(vd_model* m, int32_t mode) {
+  if (check_model(m)) return VD_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 2) return fail(VD_ERR_INVALID_ARG, "mode must be 0 (auto), 1 (always) or 2 (never)");
+  m->fold_mode = mode;
+  return VD_OK;
 }
 
 int vd_set_graph_mode(vd_model* m, int32_t max_graphs) {

@@ -170,7 +170,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // NW warps per CTA; groups of DS warps own the same 16 rows and split the
 // head dimension between them (DS = 2 for decode-shaped CTAs, which have one
 // row block only; DS = 1 for prefill CTAs).
-template <int HD, int NW, int DS>
+template <int HD, int NW, int DS, bool FOLD>
 __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ CUtensorMap kvmap, AttnArgs a) {
   using C = AttnCfg<HD>;
   constexpr int RB = 16 * NW / DS;  // rows per CTA
@@ -203,7 +203,10 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   const int q0 = a.cu_q[b], qlen = a.cu_q[b + 1] - q0, cached = a.cached_len[b];
   const int kv_len = cached + qlen;
   const int G = a.Hq / a.Hkv;
-  const int nsplit = (kv_len - 1) / a.split + 1;
+  // Split mode: one CTA per split.  Fold mode: one CTA walks every split of
+  // its rows (the same tiles, split by split) and folds the split states
+  // itself, with the merge kernel's arithmetic and order.
+  const int nsplit = FOLD ? 1 : (kv_len - 1) / a.split + 1;
   const int sidx = local % nsplit;
   local /= nsplit;
   const int kvh = local % a.Hkv;
@@ -213,8 +216,8 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   const int r_end = min(rows, r0 + RB);
   const int p_min = cached + r0 / G, p_max = cached + (r_end - 1) / G;
   const int lo_min = a.window > 0 ? max(0, p_min - a.window + 1) : 0;
-  const int key_lo = max(sidx * a.split, lo_min);
-  const int key_hi = min((sidx + 1) * a.split - 1, p_max);
+  const int key_lo = FOLD ? lo_min : max(sidx * a.split, lo_min);
+  const int key_hi = FOLD ? p_max : min((sidx + 1) * a.split - 1, p_max);
   if (key_lo > key_hi) return;  // no visible key of these rows in this split
   const int tile_lo = key_lo / C::BNK;
   const int ntiles = key_hi / C::BNK - tile_lo + 1;
@@ -284,6 +287,13 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
 #pragma unroll
   for (int n = 0; n < ND / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
 
+  // fold mode: the merged state of the splits seen so far (rows g, g+8)
+  float fm[2] = {-INFINITY, -INFINITY}, fl[2] = {0.f, 0.f};
+  float fo[FOLD ? ND / 8 : 1][4];
+  if constexpr (FOLD) {
+#pragma unroll
+    for (int n = 0; n < ND / 8; ++n) fo[n][0] = fo[n][1] = fo[n][2] = fo[n][3] = 0.f;
+  }
   bool ok = true;
   int it = 0, stg = 0;
   uint32_t ph = 0;  // tile it sits in stage it % NS, round it / NS
@@ -297,6 +307,38 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
     if (ok && mine) {
       const uint32_t kb = smem_u32(smem + stg * 2 * C::TILE_BYTES);
       attn_tile<HD, C::BNK, ND>(st, qf, kb, kb + C::TILE_BYTES, key0, pos, lo, a.scale_log2, lane, dim0);
+    }
+    if (FOLD && ((key0 + C::BNK) % a.split == 0 || it == ntiles - 1)) {
+      // end of a split: fold it into the merged state of every row that saw a
+      // key in it (merge order: splits left to right, the first one taken as is)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        if (st.m[r] != -INFINITY) {
+          if (fm[r] == -INFINITY) {
+            fm[r] = st.m[r];
+            fl[r] = st.l[r];
+#pragma unroll
+            for (int n = 0; n < ND / 8; ++n) {
+              fo[n][2 * r] = st.o[n][2 * r];
+              fo[n][2 * r + 1] = st.o[n][2 * r + 1];
+            }
+          } else {
+            const float mn = fmaxf(fm[r], st.m[r]);
+            const float ca = ex2(__fsub_rn(fm[r], mn)), cb = ex2(__fsub_rn(st.m[r], mn));
+            fl[r] = __fadd_rn(__fmul_rn(fl[r], ca), __fmul_rn(st.l[r], cb));
+#pragma unroll
+            for (int n = 0; n < ND / 8; ++n) {
+              fo[n][2 * r] = __fadd_rn(__fmul_rn(fo[n][2 * r], ca), __fmul_rn(st.o[n][2 * r], cb));
+              fo[n][2 * r + 1] = __fadd_rn(__fmul_rn(fo[n][2 * r + 1], ca), __fmul_rn(st.o[n][2 * r + 1], cb));
+            }
+            fm[r] = mn;
+          }
+        }
+        st.m[r] = -INFINITY;
+        st.l[r] = 0.f;
+      }
+#pragma unroll
+      for (int n = 0; n < ND / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
     }
     if (__syncthreads_or(!ok)) break;
     if (threadIdx.x == 0 && it + NS < ntiles) {
@@ -314,6 +356,18 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
     return;
   }
 
+  if constexpr (FOLD) {  // o / l of every row -> bf16, as the merge kernel writes it
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (!valid[r] || fm[r] == -INFINITY) continue;
+      __nv_bfloat16* out = a.out + (static_cast<size_t>(q0 + tok[r]) * a.Hq + hq[r]) * HD + dim0;
+#pragma unroll
+      for (int n = 0; n < ND / 8; ++n)
+        *reinterpret_cast<uint32_t*>(out + n * 8 + t4 * 2) =
+            pack_bf16x2(__fdiv_rn(fo[n][2 * r], fl[r]), __fdiv_rn(fo[n][2 * r + 1], fl[r]));
+    }
+    return;
+  }
   // ---- split partial of every row that saw a key here
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -361,7 +415,7 @@ __global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
   pdl_trigger();
   const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (w >= a.T * a.Hq) return;
-  const int tok = w / a.Hq, h = w % a.Hq;
+  const int tok = a.tokens ? a.tokens[w / a.Hq] : w / a.Hq, h = w % a.Hq;
   const int p = a.positions[tok];
   const int lo = a.window > 0 ? max(0, p - a.window + 1) : 0;
   const int s0 = lo / a.split, s1 = p / a.split;
@@ -412,20 +466,21 @@ int attn_stages(int n_items) {
   return 2;
 }
 
-template <int HD, int NW, int DS>
+template <int HD, int NW, int DS, bool FOLD>
 int launch_attn_t(const CUtensorMap& kvmap, const AttnArgs& a0, int n_items, cudaStream_t s) {
   using C = AttnCfg<HD>;
   static bool configured = false;
   if (!configured) {
     int max_ns = C::MAX_STAGES;
     while (C::smem(max_ns) > 227 * 1024) --max_ns;
-    VD_CUDA_TRY(cudaFuncSetAttribute(attn_kernel<HD, NW, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    VD_CUDA_TRY(cudaFuncSetAttribute(attn_kernel<HD, NW, DS, FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::smem(max_ns)));
     configured = true;
   }
   AttnArgs a = a0;
   a.stages = attn_stages<HD>(n_items);
-  VD_CUDA_TRY(launch_k(attn_kernel<HD, NW, DS>, dim3(n_items), dim3(NW * 32), C::smem(a.stages), s, kvmap, a));
+  VD_CUDA_TRY(
+      launch_k(attn_kernel<HD, NW, DS, FOLD>, dim3(n_items), dim3(NW * 32), C::smem(a.stages), s, kvmap, a));
   return VD_OK;
 }
 
@@ -464,9 +519,16 @@ static_assert(512 % AttnCfg<64>::BNK == 0 && 512 % AttnCfg<256>::BNK == 0, "spli
 int launch_attention(const CUtensorMap& kvmap, const AttnArgs& a, int hd, bool prefill_class, int n_items,
                      cudaStream_t s) {
   if (n_items <= 0) return VD_OK;
-  if (hd == 64) return prefill_class ? launch_attn_t<64, 4, 1>(kvmap, a, n_items, s) : launch_attn_t<64, 2, 2>(kvmap, a, n_items, s);
-  if (hd == 128) return prefill_class ? launch_attn_t<128, 4, 1>(kvmap, a, n_items, s) : launch_attn_t<128, 2, 2>(kvmap, a, n_items, s);
-  if (hd == 256) return prefill_class ? launch_attn_t<256, 4, 1>(kvmap, a, n_items, s) : launch_attn_t<256, 2, 2>(kvmap, a, n_items, s);
+  if (prefill_class && a.fold) return fail(VD_ERR_INVALID_ARG, "split folding is for decode-class CTAs");
+#define VD_ATTN_LAUNCH(HD_)                                                                     \
+  if (hd == HD_)                                                                              \
+    return prefill_class ? launch_attn_t<HD_, 4, 1, false>(kvmap, a, n_items, s)               \
+           : a.fold      ? launch_attn_t<HD_, 2, 2, true>(kvmap, a, n_items, s)                \
+                         : launch_attn_t<HD_, 2, 2, false>(kvmap, a, n_items, s);
+  VD_ATTN_LAUNCH(64)
+  VD_ATTN_LAUNCH(128)
+  VD_ATTN_LAUNCH(256)
+#undef VD_ATTN_LAUNCH
   return fail(VD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
 }
 

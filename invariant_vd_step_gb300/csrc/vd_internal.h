@@ -102,6 +102,9 @@ struct AttnArgs {
   int max_splits;
   float scale_log2;        // log2(e) / sqrt(hd)
   int stages;              // K/V tiles in flight (set by launch_attention)
+  int fold;                // decode class: 1 = a CTA walks all splits of its rows and folds them,
+                           // writing out directly (no partials); 0 = one CTA per split
+  __nv_bfloat16* out;      // [T][Hq][hd] (fold mode)
   int* status;
 };
 struct MergeArgs {
@@ -109,6 +112,7 @@ struct MergeArgs {
   const float* part_ml;
   __nv_bfloat16* out;      // [T][Hq][hd]
   const int* positions;    // [T]
+  const int* tokens;       // tokens to merge (T of them), or null for 0..T-1
   int T, Hq, window, split, max_splits;
 };
 int attn_key_tile(int hd);

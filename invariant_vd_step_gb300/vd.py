@@ -106,6 +106,7 @@ _SIGS = {
     "vd_copy_kv": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, _I32P, ctypes.c_int32, _VP, _VP, _VP]),
     "vd_device_status": (ctypes.c_int, [_VP]),
     "vd_set_graph_mode": (ctypes.c_int, [_VP, ctypes.c_int32]),
+    "vd_set_attention_fold": (ctypes.c_int, [_VP, ctypes.c_int32]),
     "vd_graph_stats": (ctypes.c_int, [_VP, _I64P]),
     "vd_profile_enable": (ctypes.c_int, [_VP, ctypes.c_int32]),
     "vd_profile_collect": (ctypes.c_int, [_VP, ctypes.POINTER(KernelStat), ctypes.c_int32]),
@@ -342,6 +343,10 @@ class Model:
 
     def profile(self, on: bool):
         check(lib().vd_profile_enable(self.h, int(on)))
+
+    def set_attention_fold(self, mode: int):
+        """Decode attention mapping: 0 default (one CTA per split), 1 fold all splits in one CTA, 2 split."""
+        check(lib().vd_set_attention_fold(self.h, int(mode)))
 
     def set_graph_mode(self, max_graphs: int):
         """Replay steps as captured CUDA graphs (0 = eager launches)."""
