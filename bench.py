@@ -51,6 +51,17 @@ def load_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def max_over_ranks(values, ws, device="cpu"):
+    """Elementwise maximum of per-rank floats over all ranks: the slowest
+    replica sets the job's time (a collective only when ws > 1)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -335,10 +346,8 @@ def run_gpu(args):
     h2d = h2d_bytes(base + E - 1)
     assert len(emitted) == E and model.device_status() == 0
 
-    t = torch.tensor([ms, e2e_s, e2e_sync_s], dtype=torch.float64, device=dev if ws > 1 else "cpu")
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max, e2e_max, e2e_sync_max = float(t[0]), float(t[1]), float(t[2])
+    ms_max, e2e_max, e2e_sync_max = max_over_ranks([ms, e2e_s, e2e_sync_s], ws,
+                                                   dev if ws > 1 and dist.get_backend() == "nccl" else "cpu")
     if rank != 0:
         if ws > 1:
             dist.destroy_process_group()

@@ -54,3 +54,44 @@ def test_bf16_flip_cascade_reaches_the_stated_tolerance(layer, monkeypatch):
     monkeypatch.setattr(od, "attention", exact_attention)
     d = np.abs(alt - ref)
     assert 5e-3 < d.max() < 5e-2, d.max()
+
+
+def test_gemma_block_flip_cascade_is_wider(monkeypatch):
+    """The same measurement on the Gemma-3-4B-shaped block (2 layers, one
+    local window-1024 and one global; embedding scale, (1 + w) gains,
+    sandwich norms, vocab 262144).  One 1e-5 disagreement already puts about
+    one logit in ten thousand beyond the stated tolerance (30 of 262144 here),
+    more than the 8B check's 99.99 % allows, which is why the full-size Gemma
+    check asks for 99.9 % (and twice the tolerance everywhere)."""
+    spec = synth.GEMMA3_4B.with_(name="gemma3-4b-shape-2layer", n_layers=2, local_global_period=2)
+    dec = od.OracleDecoder(spec, synth.weights_to_numpy(synth.make_weights(spec, seed=0, gain_std=0.1)))
+    rng = np.random.default_rng(4)
+    c = 4000
+    cache = [(round_bf16(rng.standard_normal((c, spec.n_kv_heads, spec.head_dim))),
+              round_bf16(rng.standard_normal((c, spec.n_kv_heads, spec.head_dim)))) for _ in range(2)]
+    ref, _ = dec.step(np.array([1234]), cache)
+    exact_attention = od.attention
+
+    def perturbed(q, Kf, Vf, positions, window):
+        n, Hq, hd = q.shape
+        rep = Hq // Kf.shape[1]
+        out = np.empty((n, Hq, hd))
+        for t in range(n):
+            p = int(positions[t])
+            lo = max(0, p - window + 1) if window > 0 else 0
+            for h in range(Hq):
+                s = (Kf[lo:p + 1, h // rep] @ q[t, h]) / math.sqrt(hd)
+                e = np.exp(s - s.max())
+                out[t, h] = (e / e.sum()) @ Vf[lo:p + 1, h // rep]
+        out *= 1 + 1e-5 * np.random.default_rng(99).standard_normal(out.shape)
+        return round_bf16(out)
+
+    monkeypatch.setattr(od, "attention", perturbed)
+    alt, _ = dec.step(np.array([1234]), cache)
+    monkeypatch.setattr(od, "attention", exact_attention)
+    d = np.abs(alt - ref)[0]
+    tol = 2e-2 + 1e-2 * np.abs(ref[0])
+    beyond = int((d > tol).sum())
+    assert 1e-2 < d.max() < 5e-2, d.max()
+    assert 0.5e-4 * d.size < beyond < 1e-3 * d.size, beyond
+    assert np.all(d <= 2 * tol)
