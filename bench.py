@@ -606,6 +606,92 @@ def run_serve(args):
     }))
 
 
+def run_llm42(args):
+    """Decode-verify-rollback against plain invariant decoding on the decode
+    workload (Llama-3.1-8B-shaped layer + LM head, contexts U[lo, hi], random
+    cached K/V, permuted pages): both loops emit --new-tokens tokens per
+    request, one host sync per step; tok/s of released tokens."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from invariant_vd_step_gb300 import llm42, synth, vd
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B, N, Wn = args.batch, args.new_tokens, args.window
+    spec, ctx, tables, num_pages = make_workload(B, N + Wn + 8)
+    weights = synth.make_weights(spec, seed=0, device=dev)
+    model = vd.Model(spec, weights, max_tokens=max(B * Wn, 16), max_seqs=B, max_logit_rows=B * Wn,
+                     max_context=CTX_HI + N + Wn + 32)
+    mem = torch.empty(model.pool_bytes(num_pages), dtype=torch.uint8, device=dev)
+    pool = vd.KVPool(model, num_pages, memory=mem)
+    g = torch.Generator(device=dev)
+    g.manual_seed(4)
+    pv = mem.view(torch.bfloat16)
+    for i in range(0, pv.numel(), 1 << 28):
+        n = min(1 << 28, pv.numel() - i)
+        pv[i:i + n] = torch.randn(n, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    snapshot = mem.clone()  # both loops start from the same cached K/V
+    first = synth.make_tokens(B, spec.vocab, seed=1)
+    model.set_graph_mode(args.graphs)
+
+    def plain():
+        model.set_reduction_mode(0)
+        lg = torch.empty((B, spec.vocab), dtype=torch.float32, device=dev)
+        tok = torch.empty(B, dtype=torch.int32, device=dev)
+        last, out = first.copy(), [[] for _ in range(B)]
+        cu, rows = np.arange(B + 1, dtype=np.int32), np.arange(B, dtype=np.int32)
+        width = max(len(t) for t in tables)
+        pt = np.zeros((B, width), dtype=np.int32)
+        for i, t in enumerate(tables):
+            pt[i, :len(t)] = t
+        for i in range(N):
+            b = vd.StepBatch.from_arrays(last, cu, ctx + i, pt, rows)
+            model.step_sample(pool, b, [(1000 + r, i, 0.0) for r in range(B)], lg, tok)
+            last = tok.cpu().numpy()
+            for r in range(B):
+                out[r].append(int(last[r]))
+        return out
+
+    def selective():
+        dec = llm42.SelectiveDecoder(model, pool, pages=[], window=Wn, max_batch=B)
+        for r in range(B):
+            dec.add_cached(int(ctx[r]), int(first[r]), tables[r], N, seed=1000 + r)
+        got = dec.run()
+        return [got[r] for r in range(B)], dec.stats
+
+    for _ in range(2):  # warm-up both loops (graphs, split-K buffer)
+        mem.copy_(snapshot)
+        plain()
+        mem.copy_(snapshot)
+        selective()
+    mem.copy_(snapshot)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ref = plain()
+    t_plain = time.perf_counter() - t0
+    mem.copy_(snapshot)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    got, st = selective()
+    t_sel = time.perf_counter() - t0
+    assert model.device_status() == 0
+    same = sum(int(a == b) for a, b in zip(got, ref))
+    print(json.dumps({
+        "metric": "decode tok/s with decode-verify-rollback (Llama-8B shape, 1 GB300)",
+        "value": round(B * N / t_sel, 1), "unit": "tok/s (released tokens)", "n_gpus": 1,
+        "higher_is_better": True, "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "llama3.1-8b-shape 1 decoder layer + LM head, greedy decode from cached K/V",
+                   "batch": B, "new_tokens": N, "window": Wn, "ctx": f"U[{CTX_LO},{CTX_HI}]",
+                   "graphs": args.graphs},
+        "invariant_decode_tok_s": round(B * N / t_plain, 1),
+        "speedup": round(t_plain / t_sel, 3),
+        "requests_identical_to_invariant_decoding": f"{same}/{B}",
+        "fast_steps": st.fast_steps, "verify_steps": st.verify_steps, "candidates": st.candidates,
+        "accepted": st.accepted, "rolled_back": st.rolled_back,
+    }))
+
+
 def oracle_decode_sample(spec, weights_np, caches, toks):
     """The oracle's decode step for each request over its cached K/V."""
     from oracle.decoder import OracleDecoder
@@ -701,7 +787,9 @@ def main():
     ap.add_argument("--attention-fold", type=int, default=0, choices=[0, 1, 2],
                     help="decode attention mapping: 0 default (one CTA per split), 1 fold splits in one CTA, 2 split")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "serve"])
+    ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "serve", "llm42"])
+    ap.add_argument("--window", type=int, default=8, help="llm42 mode: verification window")
+    ap.add_argument("--new-tokens", type=int, default=64, help="llm42 mode: tokens per request")
     ap.add_argument("--workload", default="c3", choices=["c3", "c5"], help="serve mode workload")
     ap.add_argument("--budget", type=int, default=2048, help="serve mode: chunked-prefill token budget")
     ap.add_argument("--sessions", type=int, default=128, help="serve c5: sessions")
@@ -722,6 +810,8 @@ def main():
         run_prefill(args)
     elif args.mode == "serve":
         run_serve(args)
+    elif args.mode == "llm42":
+        run_llm42(args)
     else:
         run_gpu(args)
 

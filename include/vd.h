@@ -21,6 +21,8 @@
  *   [T]  "Deterministic and bit-exact inference" (catalogue record M-0002),
  *        technical section: fixed KV split *size*, batch-invariant RMSNorm,
  *        matmul and attention.
+ *   [L]  "LLM-42: Enabling Determinism in LLM Inference with Verified
+ *        Speculation" (arXiv 2601.17768), §4 decode-verify-rollback.
  *
  * Conventions for every entry point:
  *   - Return value: VD_OK (0) or a VD_ERR_* code; vd_last_error() then gives
@@ -181,6 +183,17 @@ void* vd_kv_pool_data(vd_kv_pool* p);
  * VD_ERR_INVALID_ARG, VD_ERR_OUT_OF_RANGE, VD_ERR_CAPACITY, VD_ERR_CUDA.
  * T == 0 is a no-op. */
 int vd_step(vd_model* m, vd_kv_pool* pool, const vd_batch* b, float* logits_out, void* stream);
+
+/* Reduction mode (the fast path of LLM-42's decode-verify-rollback [L, design:
+ * a non-invariant fast path verified by fixed-shape replay]).  mode 0
+ * (default): every step is batch-invariant.  mode 1: GEMMs with fewer weight
+ * tiles than SMs split K across CTAs (fp32 partials summed in split order,
+ * then the same epilogue) when a step has at most 256 tokens; logits then
+ * depend on the batch and are not guaranteed to equal the invariant path's.
+ * Use mode 1 only for candidates that an invariant step verifies.  Switching
+ * is cheap (the partial buffer is allocated on first use).
+ * Errors: VD_ERR_INVALID_ARG, VD_ERR_CUDA. */
+int vd_set_reduction_mode(vd_model* m, int32_t mode);
 
 /* Workload-dependent decode attention mapping [B §八 8.1: one SM per
  * sequence for full waves, several SMs for partially filled waves, both with

@@ -146,10 +146,11 @@ struct GraphKey {
   const void* tokens = nullptr;  // fused token choice (vd_step_sample) or null
   const void* feed = nullptr;    // device-side token feedback or null
   int T = 0, B = 0, R = 0, stride = 0, n_dec = 0, n_pre = 0, grid_dec = 0, grid_pre = 0, fold = 0, n_merge = 0;
+  int fast = 0;
   bool operator==(const GraphKey& o) const {
     return pool_id == o.pool_id && logits == o.logits && tokens == o.tokens && feed == o.feed && T == o.T && B == o.B && R == o.R && stride == o.stride &&
            n_dec == o.n_dec && n_pre == o.n_pre && grid_dec == o.grid_dec && grid_pre == o.grid_pre &&
-           fold == o.fold && n_merge == o.n_merge;
+           fold == o.fold && n_merge == o.n_merge && fast == o.fast;
   }
 };
 struct GraphEntry {
@@ -181,6 +182,11 @@ struct vd_model {
   __nv_bfloat16* hsub = nullptr;  // sandwich norms: a sub-layer's output before its norm
   float embed_scale = 0.f;        // 0: none, else bf16(sqrt(d)) as float
   int fold_mode = 0;              // 0: default (split mode), 1: fold the decode class whenever legal, 2: never
+  // fast (non-invariant) path: split-K for GEMMs with too few weight tiles
+  int fast = 0;
+  int n_sm = 0;
+  float* splitk_part = nullptr;
+  size_t splitk_cap = 0;          // floats
   std::vector<int> scratch_dec;   // host scratch of build_desc
   float gain_offset = 0.f;        // RMSNorm gains are w + gain_offset
   float *part_o = nullptr, *part_ml = nullptr;
@@ -637,6 +643,47 @@ int* op_status() {
 
 int check_model(const vd_model* m) { return m ? VD_OK : fail(VD_ERR_INVALID_ARG, "null model"); }
 
+// Fast path only: tokens per step up to which narrow GEMMs split K.
+constexpr int kFastMaxTokens = 256;
+
+// K splits of a GEMM on the fast path: enough tiles for every SM, at most 8,
+// at least two K blocks per split; 1 (no split) on the invariant path.
+int fast_splits(const vd_model* m, int T, int n_wtiles, int K) {
+  if (!m->fast || T > kFastMaxTokens) return 1;
+  const int ntt = (T + kGemmBN - 1) / kGemmBN;
+  const int ks = std::min({8, m->n_sm / (ntt * n_wtiles), K / kGemmBK / 2});
+  return ks >= 2 ? ks : 1;
+}
+
+// One GEMM of the step.  The invariant path fuses the epilogue; the fast
+// path may split K (fp32 partials, then a reduction kernel applying the same
+// epilogue), which is not batch-invariant.
+int gemm_step(vd_model* m, const CUtensorMap& wmap, const ActBuf& xb, int T, int n_wtiles, int K, int ldo, void* out,
+              const void* residual, int epi, int glu_up_row, Prof& p, cudaStream_t s) {
+  GemmArgs g{};
+  g.status = m->status;
+  g.T = T;
+  g.K = K;
+  g.ldo = ldo;
+  g.out = out;
+  g.residual = residual;
+  g.glu_up_row = glu_up_row;
+  g.b_box_rows = xb.box_for(T);
+  const bool glu = epi == EPI_SWIGLU || epi == EPI_GEGLU;
+  const int ks = fast_splits(m, T, n_wtiles, K);
+  const int np = glu ? 2 * glu_up_row : ldo;  // width of the partial sums
+  if (ks == 1 || static_cast<size_t>(ks) * T * np > m->splitk_cap) return launch_gemm(wmap, xb.map_for(T), n_wtiles, g, epi, s);
+  g.out = m->splitk_part;
+  g.ldo = np;
+  g.residual = nullptr;
+  g.k_splits = ks;
+  g.glu = glu;
+  int rc;
+  if ((rc = launch_gemm(wmap, xb.map_for(T), n_wtiles, g, EPI_PARTIAL, s))) return rc;
+  p.kernels = 2;
+  return launch_splitk_reduce(m->splitk_part, ks, T, np, epi, out, residual, s);
+}
+
 // The kernel sequence of one step (descriptor already uploaded).
 int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out, int* tokens_out, cudaStream_t s) {
   int rc;
@@ -651,9 +698,6 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
                            s)))
       return rc;
   }
-  GemmArgs g{};
-  g.status = m->status;
-  g.T = T;
   for (int l = 0; l < c.n_layers; ++l) {
     const vd_layer_weights& L = m->layers[l];
     if (l == 0 || !sandwich) {  // with sandwich norms the previous layer's last kernel produced it
@@ -662,8 +706,8 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
     }
     {
       Prof p(m, K_GEMM_QKV, s);
-      g.out = m->qkv; g.residual = nullptr; g.K = dm; g.ldo = qkv_dim; g.b_box_rows = m->a.box_for(T);
-      if ((rc = launch_gemm(m->m_qkv[l], m->a.map_for(T), qkv_dim / kGemmBM, g, EPI_BF16, s))) return rc;
+      if ((rc = gemm_step(m, m->m_qkv[l], m->a, T, qkv_dim / kGemmBM, dm, qkv_dim, m->qkv, nullptr, EPI_BF16, 0, p, s)))
+        return rc;
     }
     if ((rc = run_rope(m, pool, l, d, m->qkv, m->q, s))) return rc;
     if ((rc = run_attention(m, pool, l, d, m->q, m->o.ptr, s))) return rc;
@@ -671,8 +715,9 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
       // h = bf16(o Wo^T); x = bf16(x + rms_post(h)); a = rms_ffn(x)
       {
         Prof p(m, K_GEMM_O, s);
-        g.out = m->hsub; g.residual = nullptr; g.K = c.n_heads * hd; g.ldo = dm; g.b_box_rows = m->o.box_for(T);
-        if ((rc = launch_gemm(m->m_o[l], m->o.map_for(T), dm / kGemmBM, g, EPI_BF16, s))) return rc;
+        if ((rc = gemm_step(m, m->m_o[l], m->o, T, dm / kGemmBM, c.n_heads * hd, dm, m->hsub, nullptr, EPI_BF16, 0, p,
+                            s)))
+          return rc;
       }
       Prof p(m, K_RMSNORM, s);
       if ((rc = launch_postnorm_residual(m->hsub, m->x, L.post_attn_norm, L.ffn_norm, m->a.ptr, T, dm, c.rms_eps,
@@ -681,25 +726,25 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
     } else {
       {
         Prof p(m, K_GEMM_O, s);
-        g.out = m->x; g.residual = m->x; g.K = c.n_heads * hd; g.ldo = dm; g.b_box_rows = m->o.box_for(T);
-        if ((rc = launch_gemm(m->m_o[l], m->o.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
+        if ((rc = gemm_step(m, m->m_o[l], m->o, T, dm / kGemmBM, c.n_heads * hd, dm, m->x, m->x, EPI_RESIDUAL, 0, p,
+                            s)))
+          return rc;
       }
       Prof p(m, K_RMSNORM, s);
       if ((rc = launch_rmsnorm(m->x, nullptr, L.ffn_norm, m->a.ptr, T, dm, c.rms_eps, off, s))) return rc;
     }
     {
       Prof p(m, K_GEMM_GU, s);
-      g.out = m->z.ptr; g.residual = nullptr; g.K = dm; g.ldo = F; g.glu_up_row = F; g.b_box_rows = m->a.box_for(T);
-      if ((rc = launch_gemm(m->m_gu[l], m->a.map_for(T), F / 64, g,
-                            c.act == VD_ACT_GEGLU ? EPI_GEGLU : EPI_SWIGLU, s)))
+      if ((rc = gemm_step(m, m->m_gu[l], m->a, T, F / 64, dm, F, m->z.ptr, nullptr,
+                          c.act == VD_ACT_GEGLU ? EPI_GEGLU : EPI_SWIGLU, F, p, s)))
         return rc;
     }
     if (sandwich) {
       // h = bf16(z Wd^T); x = bf16(x + rms_post(h)); a = rms_attn of the next layer (none after the last)
       {
         Prof p(m, K_GEMM_DOWN, s);
-        g.out = m->hsub; g.residual = nullptr; g.K = F; g.ldo = dm; g.b_box_rows = m->z.box_for(T);
-        if ((rc = launch_gemm(m->m_down[l], m->z.map_for(T), dm / kGemmBM, g, EPI_BF16, s))) return rc;
+        if ((rc = gemm_step(m, m->m_down[l], m->z, T, dm / kGemmBM, F, dm, m->hsub, nullptr, EPI_BF16, 0, p, s)))
+          return rc;
       }
       const void* next_norm = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : nullptr;
       Prof p(m, K_RMSNORM, s);
@@ -708,8 +753,7 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
         return rc;
     } else {
       Prof p(m, K_GEMM_DOWN, s);
-      g.out = m->x; g.residual = m->x; g.K = F; g.ldo = dm; g.b_box_rows = m->z.box_for(T);
-      if ((rc = launch_gemm(m->m_down[l], m->z.map_for(T), dm / kGemmBM, g, EPI_RESIDUAL, s))) return rc;
+      if ((rc = gemm_step(m, m->m_down[l], m->z, T, dm / kGemmBM, F, dm, m->x, m->x, EPI_RESIDUAL, 0, p, s))) return rc;
     }
   }
   if (d.R > 0) {
@@ -767,6 +811,7 @@ int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out,
   k.grid_pre = d.grid_pre;
   k.fold = d.fold;
   k.n_merge = d.n_merge;
+  k.fast = m->fast;
   GraphEntry* seen = nullptr;
   for (GraphEntry& e : m->graphs)
     if (e.key == k) {
@@ -869,6 +914,8 @@ int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_mode
   if (c.embed_scale)  // the scale itself rounded to bf16, as a bf16 model multiplies by it
     m->embed_scale = __bfloat162float(__float2bfloat16_rn(static_cast<float>(sqrt(static_cast<double>(c.d_model)))));
   m->gain_offset = c.norm_offset ? 1.0f : 0.0f;
+  if (cudaDeviceGetAttribute(&m->n_sm, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess || m->n_sm <= 0)
+    m->n_sm = 148;
   m->key_tile = attn_key_tile(c.head_dim);
   m->split = kSplitKeys;
   m->max_splits = (c.max_context - 1) / m->split + 1;
@@ -1064,6 +1111,28 @@ int vd_step_sample_fed(vd_model* m, vd_kv_pool* pool, const vd_batch* b, const i
                        void* stream) {
   if (!feed_index) return fail(VD_ERR_INVALID_ARG, "null feed_index");
   return step_sample_impl(m, pool, b, feed_index, feed_tokens, per_row, logits_out, tokens_out, stream);
+}
+
+int vd_set_reduction_mode(vd_model* m, int32_t mode) {
+  if (check_model(m)) return VD_ERR_INVALID_ARG;
+  if (mode != 0 && mode != 1) return fail(VD_ERR_INVALID_ARG, "mode must be 0 (invariant) or 1 (fast)");
+  if (mode == 1 && !m->splitk_part) {  // partial sums of the largest split GEMM at kFastMaxTokens
+    const vd_model_config& c = m->cfg;
+    const int T = std::min(kFastMaxTokens, c.max_tokens), dm = c.d_model, F = c.ffn_dim;
+    const int qkv_dim = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+    m->fast = 1;
+    size_t cap = 0;
+    cap = std::max(cap, static_cast<size_t>(fast_splits(m, T, qkv_dim / kGemmBM, dm)) * T * qkv_dim);
+    cap = std::max(cap, static_cast<size_t>(fast_splits(m, T, dm / kGemmBM, c.n_heads * c.head_dim)) * T * dm);
+    cap = std::max(cap, static_cast<size_t>(fast_splits(m, T, F / 64, dm)) * T * 2 * F);
+    cap = std::max(cap, static_cast<size_t>(fast_splits(m, T, dm / kGemmBM, F)) * T * dm);
+    m->fast = 0;
+    int rc;
+    if ((rc = dev_alloc(m, reinterpret_cast<void**>(&m->splitk_part), cap * 4))) return rc;
+    m->splitk_cap = cap;
+  }
+  m->fast = mode;
+  return VD_OK;
 }
 
 int vd_set_attention_fold(vd_model* m, int32_t mode) {

@@ -71,7 +71,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // t0.. of the tile; TMEM lane = weight row of the tile.
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tacc, int tile_t, int tile_n, int lg,
-                                              int lane, float* xchg) {
+                                              int lane, float* xchg, int ksplit) {
   const int row = lg * 32 + lane;  // tile row == TMEM lane
   const uint32_t taddr = tacc + (static_cast<uint32_t>(lg * 32) << 16);
   for (int c = 0; c < kGemmBN / 32; ++c) {
@@ -80,7 +80,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tac
     float v[32];
     tmem_ld32(taddr + c * 32, v);
     const int nt = min(32, args.T - t0);
-    if (EPI == EPI_F32) {
+    if (EPI == EPI_PARTIAL) {
+      // fp32 partial of K split `ksplit`: part[ksplit][t][n], n the row of the
+      // full output (gate rows then up rows for a GLU matrix)
+      const int n = args.glu ? (row < 64 ? tile_n * 64 + row : args.glu_up_row + tile_n * 64 + row - 64)
+                             : tile_n * kGemmBM + row;
+      float* out = static_cast<float*>(args.out) + (static_cast<size_t>(ksplit) * args.T) * args.ldo + n;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
+    } else if (EPI == EPI_F32) {
       float* out = static_cast<float*>(args.out) + tile_n * kGemmBM + row;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
@@ -193,11 +202,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  constexpr bool kGlu = (EPI == EPI_SWIGLU || EPI == EPI_GEGLU);
+  // a GLU weight tile: gate rows and up rows of the same 64 features, two boxes
+  const bool kGlu = EPI == EPI_SWIGLU || EPI == EPI_GEGLU || (EPI == EPI_PARTIAL && args.glu);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = args.K / kGemmBK;
   const int ntt = (args.T + kGemmBN - 1) / kGemmBN;
-  const int ntiles = ntt * args.n_wtiles;
+  const int KS = args.k_splits;  // 1 on the invariant path
+  const int ntiles = ntt * args.n_wtiles * KS;
+  // tile -> (K split, token tile, weight tile); a split covers K blocks [kb_lo, kb_hi)
+  auto kb_lo = [&](int tile) { return (tile % KS) * KB / KS; };
+  auto kb_hi = [&](int tile) { return (tile % KS + 1) * KB / KS; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -239,8 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0, s = 0;  // stage g lives in slot s = g % S, round g / S
       uint32_t ph = 0;     // parity of round g / S
       for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
-        const int tile_t = tile % ntt, tile_n = tile / ntt;
-        for (int kb = 0; kb < KB; ++kb, ++g) {
+        const int tile_t = (tile / KS) % ntt, tile_n = (tile / KS) / ntt;
+        for (int kb = kb_lo(tile); kb < kb_hi(tile); ++kb, ++g) {
           if (g >= S && !mbar_wait(&empty[s], ph ^ 1u, abort_flag, args.status)) break;
           mbar_arrive_expect_tx(&full[s], kAStageBytes + args.b_box_rows * 128);
           uint8_t* a = sA + s * kAStageBytes;
@@ -269,14 +283,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i >= 2 && !mbar_wait(&acc_empty[b], ((i >> 1) - 1) & 1, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t tacc = tmem + b * kGemmBN;
-        for (int kb = 0; kb < KB; ++kb) {
+        const int kb0 = kb_lo(tile);
+        for (int kb = kb0; kb < kb_hi(tile); ++kb) {
           if (!mbar_wait(&full[s], ph, abort_flag, args.status)) break;
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + s * kAStageBytes);
           const uint32_t b0 = smem_u32(sB + s * b_stride);
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)
-            umma_bf16(tacc, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (kb | kk) != 0);
+            umma_bf16(tacc, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (kb - kb0) | kk);
           umma_commit(&empty[s]);
           if (++s == S) {
             s = 0;
@@ -294,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = i & 1;
       if (!mbar_wait(&acc_full[b], (i >> 1) & 1, abort_flag, args.status)) break;
       tc_fence_after();
-      epilogue_tile<EPI>(args, tmem + b * kGemmBN, tile % ntt, tile / ntt, lg, lane, xchg);
+      epilogue_tile<EPI>(args, tmem + b * kGemmBN, (tile / KS) % ntt, (tile / KS) / ntt, lg, lane, xchg, tile % KS);
       tc_fence_before();
       mbar_arrive(&acc_empty[b]);
     }
@@ -311,6 +326,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 2 * kGemmBN);
+  }
+}
+
+// Fast path: sum the K-split partials in split order and apply the epilogue
+// the invariant path fuses into the GEMM (same roundings; only the sum's
+// association differs).  One thread per output element.
+template <int EPI>
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int KS, int T, int N,
+                                     __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ res) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr bool kGluOut = EPI == EPI_SWIGLU || EPI == EPI_GEGLU;
+  const int outN = kGluOut ? N / 2 : N;
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<size_t>(T) * outN) return;
+  const int t = static_cast<int>(i / outN), n = static_cast<int>(i % outN);
+  const size_t plane = static_cast<size_t>(T) * N;
+  float acc = 0.f, up = 0.f;
+  for (int k = 0; k < KS; ++k) {
+    acc = __fadd_rn(acc, part[k * plane + static_cast<size_t>(t) * N + n]);
+    if (kGluOut) up = __fadd_rn(up, part[k * plane + static_cast<size_t>(t) * N + outN + n]);
+  }
+  if (EPI == EPI_BF16) {
+    out[i] = __float2bfloat16_rn(acc);
+  } else if (EPI == EPI_RESIDUAL) {
+    out[i] = __float2bfloat16_rn(__fadd_rn(bf16_round(acc), __bfloat162float(res[i])));
+  } else {
+    const float g = bf16_round(acc);
+    const float a = (EPI == EPI_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
+    out[i] = __float2bfloat16_rn(__fmul_rn(a, bf16_round(up)));
   }
 }
 
@@ -331,7 +376,7 @@ int launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const GemmArgs&
     VD_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
     configured = true;
   }
-  const int tiles = ((a.T + kGemmBN - 1) / kGemmBN) * a.n_wtiles;
+  const int tiles = ((a.T + kGemmBN - 1) / kGemmBN) * a.n_wtiles * a.k_splits;
   VD_CUDA_TRY(launch_k(gemm_kernel<EPI>, dim3(std::min(tiles, sm_count())), dim3(kThreads), kSmemBytes, s, wmap, xmap,
                        a));
   return VD_OK;
@@ -339,11 +384,31 @@ int launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const GemmArgs&
 
 }  // namespace
 
+int launch_splitk_reduce(const float* part, int k_splits, int T, int N, int epi, void* out, const void* residual,
+                         cudaStream_t s) {
+  if (T <= 0) return VD_OK;
+  const int outN = (epi == EPI_SWIGLU || epi == EPI_GEGLU) ? N / 2 : N;
+  const dim3 grid(static_cast<unsigned>((static_cast<size_t>(T) * outN + 255) / 256));
+  auto* o = static_cast<__nv_bfloat16*>(out);
+  const auto* r = static_cast<const __nv_bfloat16*>(residual);
+  switch (epi) {
+    case EPI_BF16: VD_CUDA_TRY(launch_k(splitk_reduce_kernel<EPI_BF16>, grid, dim3(256), 0, s, part, k_splits, T, N, o, r)); break;
+    case EPI_RESIDUAL: VD_CUDA_TRY(launch_k(splitk_reduce_kernel<EPI_RESIDUAL>, grid, dim3(256), 0, s, part, k_splits, T, N, o, r)); break;
+    case EPI_SWIGLU: VD_CUDA_TRY(launch_k(splitk_reduce_kernel<EPI_SWIGLU>, grid, dim3(256), 0, s, part, k_splits, T, N, o, r)); break;
+    case EPI_GEGLU: VD_CUDA_TRY(launch_k(splitk_reduce_kernel<EPI_GEGLU>, grid, dim3(256), 0, s, part, k_splits, T, N, o, r)); break;
+    default: return fail(VD_ERR_INVALID_ARG, "split-K reduction epilogue");
+  }
+  return VD_OK;
+}
+
 int launch_gemm(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, const GemmArgs& a0, int epi,
                 cudaStream_t s) {
   if (a0.T <= 0) return VD_OK;
   GemmArgs a = a0;
   a.n_wtiles = n_tiles;
+  if (a.k_splits < 1) a.k_splits = 1;
+  if ((a.k_splits > 1) != (epi == EPI_PARTIAL) || a.k_splits > a.K / kGemmBK)
+    return fail(VD_ERR_INVALID_ARG, "K splits need the partial epilogue and at most one split per K block");
   if (a.b_box_rows < 1 || a.b_box_rows > kGemmBN) return fail(VD_ERR_INVALID_ARG, "activation box rows out of range");
   a.b_stride = std::max(1024, (a.b_box_rows * 128 + 1023) / 1024 * 1024);
   a.stages = std::min(kMaxStages, (kRingBytes - (kBStageBytes - a.b_stride)) / (kAStageBytes + a.b_stride));
@@ -354,6 +419,7 @@ int launch_gemm(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, c
     case EPI_BF16: return launch_one<EPI_BF16>(wmap, xmap, a, s);
     case EPI_RESIDUAL: return launch_one<EPI_RESIDUAL>(wmap, xmap, a, s);
     case EPI_F32: return launch_one<EPI_F32>(wmap, xmap, a, s);
+    case EPI_PARTIAL: return launch_one<EPI_PARTIAL>(wmap, xmap, a, s);
     case EPI_F32_SAMPLE:
       if (!a.samp || !a.part_v || !a.part_i) return fail(VD_ERR_INVALID_ARG, "sampling epilogue without buffers");
       return launch_one<EPI_F32_SAMPLE>(wmap, xmap, a, s);

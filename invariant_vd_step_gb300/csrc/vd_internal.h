@@ -56,7 +56,11 @@ int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd);
 // ---------------------------------------------------------------- GEMM
 // EPI_F32_SAMPLE: fp32 logits (stored unless out is null) plus, per token and
 // 32-row vocabulary group, the best (score, index) of the token choice.
-enum Epilogue { EPI_BF16 = 0, EPI_RESIDUAL = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_GEGLU = 4, EPI_F32_SAMPLE = 5 };
+// EPI_PARTIAL: fp32 partial sums of one K split (the fast, non-invariant path;
+// splitk_reduce applies the real epilogue).
+enum Epilogue {
+  EPI_BF16 = 0, EPI_RESIDUAL = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_GEGLU = 4, EPI_F32_SAMPLE = 5, EPI_PARTIAL = 6
+};
 constexpr int kGemmBM = 128;  // weight rows per tile (MMA M)
 constexpr int kGemmBN = 256;  // tokens per tile (MMA N), one shape for every T
 constexpr int kGemmBK = 64;   // K per pipeline stage (one 128-byte swizzle row)
@@ -74,10 +78,17 @@ struct GemmArgs {
   float* part_v;           // EPI_F32_SAMPLE: [T][part_stride] group winners' scores
   int* part_i;             //                 and indices
   int part_stride;         //                 = vocab / 32
+  int k_splits;          // K splits (1: the invariant path; > 1 only with EPI_PARTIAL)
+  int glu;               // EPI_PARTIAL over a GLU weight matrix (gate/up tile layout)
   int stages;            // pipeline depth (set by launch_gemm from b_box_rows)
   int b_stride;          // bytes between the B tiles of two stages (set by launch_gemm)
   int* status;           // device status word
 };
+// Fast path: out = epilogue(sum over ks of part[ks][t][n]) for the T x N
+// output (N = 2F for GLU: z[t][f] = act(bf16(gate)) * bf16(up)), summed in
+// split order.  epi: EPI_BF16, EPI_RESIDUAL, EPI_SWIGLU or EPI_GEGLU.
+int launch_splitk_reduce(const float* part, int k_splits, int T, int N, int epi, void* out, const void* residual,
+                         cudaStream_t s);
 // A = weight map (box 128 rows, or 64 for GLU), B = activation map (box kGemmBN rows).
 int launch_gemm(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, const GemmArgs& a, int epi,
                 cudaStream_t s);

@@ -107,6 +107,7 @@ _SIGS = {
     "vd_device_status": (ctypes.c_int, [_VP]),
     "vd_set_graph_mode": (ctypes.c_int, [_VP, ctypes.c_int32]),
     "vd_set_attention_fold": (ctypes.c_int, [_VP, ctypes.c_int32]),
+    "vd_set_reduction_mode": (ctypes.c_int, [_VP, ctypes.c_int32]),
     "vd_graph_stats": (ctypes.c_int, [_VP, _I64P]),
     "vd_profile_enable": (ctypes.c_int, [_VP, ctypes.c_int32]),
     "vd_profile_collect": (ctypes.c_int, [_VP, ctypes.POINTER(KernelStat), ctypes.c_int32]),
@@ -343,6 +344,10 @@ class Model:
 
     def profile(self, on: bool):
         check(lib().vd_profile_enable(self.h, int(on)))
+
+    def set_reduction_mode(self, mode: int):
+        """0: batch-invariant steps (default); 1: fast split-K steps (not invariant; verify them)."""
+        check(lib().vd_set_reduction_mode(self.h, int(mode)))
 
     def set_attention_fold(self, mode: int):
         """Decode attention mapping: 0 default (one CTA per split), 1 fold all splits in one CTA, 2 split."""
