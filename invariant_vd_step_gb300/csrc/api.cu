@@ -72,6 +72,21 @@ int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols
   return VD_OK;
 }
 
+int make_map_glu(CUtensorMap* map, const void* base, uint64_t F, uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return fail(VD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16) return fail(VD_ERR_INVALID_ARG, "TMA base/stride not 16-byte aligned");
+  cuuint64_t dims[3] = {cols, 2, F};
+  cuuint64_t strides[2] = {F * cols * 2, cols * 2};  // half, feature
+  cuuint32_t box[3] = {64, 2, 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(VD_ERR_CUDA, "cuTensorMapEncodeTiled(glu) failed: " + std::to_string(r));
+  return VD_OK;
+}
+
 int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd) {
   auto fn = encode_fn();
   if (!fn) return fail(VD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
@@ -933,7 +948,7 @@ int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_mode
     m->m_qkv.push_back(mp);
     if ((rc = make_map_2d(&mp, L.wo, d, attn_dim, kGemmBM))) return bail(rc);
     m->m_o.push_back(mp);
-    if ((rc = make_map_2d(&mp, L.w_gate_up, 2 * F, d, 64))) return bail(rc);
+    if ((rc = make_map_glu(&mp, L.w_gate_up, F, d))) return bail(rc);
     m->m_gu.push_back(mp);
     if ((rc = make_map_2d(&mp, L.w_down, d, F, kGemmBM))) return bail(rc);
     m->m_down.push_back(mp);
@@ -1272,7 +1287,7 @@ int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int3
   if (!aligned16(A) || !aligned16(W) || !aligned16(C)) return fail(VD_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
   CUtensorMap wm, xm;
   int rc;
-  if ((rc = make_map_2d(&wm, W, glu ? 2 * N : N, K, glu ? 64 : kGemmBM))) return rc;
+  if ((rc = glu ? make_map_glu(&wm, W, N, K) : make_map_2d(&wm, W, N, K, kGemmBM))) return rc;
   if ((rc = make_map_2d(&xm, A, T, K, std::min<int>(T, kGemmBN)))) return rc;
   GemmArgs g{};
   g.out = C;

@@ -44,8 +44,8 @@ constexpr int kThreads = 192;
 constexpr int kAStageBytes = kGemmBM * kGemmBK * 2;
 constexpr int kBStageBytes = kGemmBN * kGemmBK * 2;  // what one MMA reads of B
 constexpr int kRingBytes = 4 * (kAStageBytes + kBStageBytes);
-// Epilogue exchange: GLU hands the up half (64 x 33) to the gate-half warps;
-// the sampling epilogue transposes each warp's 32 x 32 block (4 x 32 x 33).
+// Epilogue exchange: the sampling epilogue transposes each warp's 32 x 32
+// block (4 x 32 x 33).
 constexpr int kXchgFloats = 128 * 33;
 constexpr int kSmemBytes = 1024 + kRingBytes + kXchgFloats * 4 + 256;
 static_assert((2 * kMaxStages + 5) * 8 + 8 <= 256, "barrier block");
@@ -56,8 +56,6 @@ __device__ __forceinline__ float gelu_tanh_f(float g) {
   const float inner = __fmul_rn(0.7978845608028654f, __fadd_rn(g, __fmul_rn(0.044715f, g3)));
   return __fmul_rn(__fmul_rn(0.5f, g), __fadd_rn(1.0f, tanhf(inner)));
 }
-
-__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Waits without looking at the abort flag (used only on the teardown path to
 // let copies and MMAs already in flight finish before the CTA exits).
@@ -83,7 +81,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tac
     if (EPI == EPI_PARTIAL) {
       // fp32 partial of K split `ksplit`: part[ksplit][t][n], n the row of the
       // full output (gate rows then up rows for a GLU matrix)
-      const int n = args.glu ? (row < 64 ? tile_n * 64 + row : args.glu_up_row + tile_n * 64 + row - 64)
+      const int n = args.glu ? ((row & 1) ? args.glu_up_row : 0) + tile_n * 64 + (row >> 1)
                              : tile_n * kGemmBM + row;
       float* out = static_cast<float*>(args.out) + (static_cast<size_t>(ksplit) * args.T) * args.ldo + n;
 #pragma unroll
@@ -157,26 +155,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tac
       for (int j = 0; j < 32; ++j)
         if (j < nt)
           out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fadd_rn(bf16_round(v[j]), r[j]));
-    } else {  // GLU: rows 0..63 gate, 64..127 up of the same 64 features
-      if (lg >= 2) {
-        float* xr = xchg + ((lg - 2) * 32 + lane) * 33;
+    } else {  // GLU: TMEM lane 2f holds gate, 2f+1 up of feature f (the 3-D weight box interleaves them)
+      const bool gate_lane = (lane & 1) == 0;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * 64 + lg * 16 + (lane >> 1);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) xr[j] = bf16_round(v[j]);
-      }
-      epi_barrier();
-      if (lg < 2) {
-        const float* xr = xchg + (lg * 32 + lane) * 33;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * 64 + lg * 32 + lane;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j < nt) {
-            const float g = bf16_round(v[j]);
-            const float a = (EPI == EPI_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
-            out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fmul_rn(a, xr[j]));
-          }
+      for (int j = 0; j < 32; ++j) {
+        const float u = __shfl_xor_sync(0xffffffffu, bf16_round(v[j]), 1);  // the neighbour's up value
+        if (gate_lane && j < nt) {
+          const float g = bf16_round(v[j]);
+          const float a = (EPI == EPI_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
+          out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fmul_rn(a, u));
         }
       }
-      epi_barrier();
     }
   }
 }
@@ -258,9 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g >= S && !mbar_wait(&empty[s], ph ^ 1u, abort_flag, args.status)) break;
           mbar_arrive_expect_tx(&full[s], kAStageBytes + args.b_box_rows * 128);
           uint8_t* a = sA + s * kAStageBytes;
-          if (kGlu) {
-            tma_load_2d(a, &wmap, &full[s], kb * kGemmBK, tile_n * 64);
-            tma_load_2d(a + 64 * 128, &wmap, &full[s], kb * kGemmBK, args.glu_up_row + tile_n * 64);
+          if (kGlu) {  // rows (feature, half) of 64 features: gate and up of a feature side by side
+            tma_load_3d(a, &wmap, &full[s], kb * kGemmBK, 0, tile_n * 64);
           } else {
             tma_load_2d(a, &wmap, &full[s], kb * kGemmBK, tile_n * kGemmBM);
           }

@@ -50,6 +50,10 @@ cudaError_t launch_k(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
 // 2-D bf16 map over a row-major [rows][cols] matrix; box = box_rows x 64
 // columns (128 bytes), 128-byte swizzle, zero fill outside the matrix.
 int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// 3-D bf16 map over a gate/up matrix [2F][cols] (gate rows 0..F-1, up rows
+// F..2F-1) as (cols, half, feature): a box (64, 2, 64) stages 64 features with
+// each gate row next to its up row.
+int make_map_glu(CUtensorMap* map, const void* base, uint64_t F, uint64_t cols);
 // 3-D bf16 map for the KV pool: dims (64, hd/64, rows), box (64, hd/64, 16).
 int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd);
 
