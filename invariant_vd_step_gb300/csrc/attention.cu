@@ -520,10 +520,15 @@ int launch_attention(const CUtensorMap& kvmap, const AttnArgs& a, int hd, bool p
                      cudaStream_t s) {
   if (n_items <= 0) return VD_OK;
   if (prefill_class && a.fold) return fail(VD_ERR_INVALID_ARG, "split folding is for decode-class CTAs");
+  // Decode CTAs split the head dimension of P V over 2 warps, or over 4 when
+  // the launch has at most one CTA per SM (small batches); every
+  // output element keeps the same instruction chain either way.
+  const bool wide = !prefill_class && !a.fold && n_items <= sm_count_attn();
 #define VD_ATTN_LAUNCH(HD_)                                                                     \
   if (hd == HD_)                                                                              \
     return prefill_class ? launch_attn_t<HD_, 4, 1, false>(kvmap, a, n_items, s)               \
            : a.fold      ? launch_attn_t<HD_, 2, 2, true>(kvmap, a, n_items, s)                \
+           : wide        ? launch_attn_t<HD_, 4, 4, false>(kvmap, a, n_items, s)               \
                          : launch_attn_t<HD_, 2, 2, false>(kvmap, a, n_items, s);
   VD_ATTN_LAUNCH(64)
   VD_ATTN_LAUNCH(128)
