@@ -105,3 +105,30 @@ def test_decode_verify_rollback_releases_the_invariant_tokens(window, corrupt):
     if corrupt:
         assert st.rolled_back > 0
     assert m.device_status() == 0
+
+
+def test_a_changed_reduction_strategy_is_visible_in_the_bits():
+    """Negative check for the first failure source the pages list (a kernel
+    whose reduction strategy follows something other than the row): the same
+    rows computed with split-K GEMMs differ from the invariant rows in their
+    bits, though they agree within the stated tolerance, so the bitwise
+    comparisons of the invariance tests do detect such a change."""
+    ready()
+    spec = synth.LLAMA8B_1L
+    W = synth.make_weights(spec, seed=0, device="cuda")
+    m = vd.Model(spec, W, max_tokens=256, max_seqs=8, max_logit_rows=8, max_context=1024)
+    pool = vd.KVPool(m, 64)
+    toks = synth.make_tokens(8 * 30, spec.vocab, seed=2).reshape(8, 30)  # 240 tokens: the fast path splits K
+    seqs = [(toks[i], 0, np.arange(2 * i, 2 * i + 2, dtype=np.int32)) for i in range(8)]
+    rows = [30 * i + 29 for i in range(8)]
+    out = []
+    for mode in (0, 1, 0):
+        m.set_reduction_mode(mode)
+        lg = torch.empty(8, spec.vocab, device="cuda")
+        m.step(pool, vd.StepBatch(seqs, logit_rows=rows), lg)
+        torch.cuda.synchronize()
+        out.append(lg)
+    assert np.array_equal(bits(out[0]), bits(out[2]))           # the invariant path repeats itself
+    assert not np.array_equal(bits(out[0]), bits(out[1]))       # split-K changes bits
+    d = (out[0] - out[1]).abs().max().item()
+    assert d < 5e-2, d                                           # but computes the same model (noise floor)
