@@ -29,8 +29,11 @@ enum {
 
 /* Batch-invariant bf16 GEMM [B §六 6.1 matmul contract: row x of a batched
  * run equals the singleton run bit for bit].  acc[t][n] = sum_k A[t][k] W[n][k]
- * in fp32 on tcgen05 tensor cores, tile 128 (weight rows) x 128 (tokens) x 64,
- * one tile shape for every T, K traversed in one fixed order, no split-K.
+ * in fp32 on tcgen05 tensor cores.  Every element of acc is one chain of
+ * K = 16 MMA steps in ascending K order into a zeroed accumulator, with no
+ * split-K, whatever T; the tile (BM weight rows x BN tokens, chosen per
+ * launch, see vd_set_gemm_plan) sets only the instruction's M and N, which
+ * leave each element's arithmetic unchanged.
  * A: dev bf16 [T][K]; W: dev bf16 [N][K] (GLU: [2F][K], rows F.. are "up",
  * N = F); C: dev [T][N] bf16 (float32 for VD_EPI_F32); residual: dev bf16
  * [T][N] or null.  Requires N % 128 == 0 (GLU: F % 64 == 0), K % 64 == 0,
@@ -38,6 +41,19 @@ enum {
  * VD_ERR_UNSUPPORTED, VD_ERR_CUDA. */
 int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int32_t K, int32_t epilogue,
                const void* residual, void* stream);
+
+/* GEMM launch shape override, process-wide, for every later GEMM launch
+ * (vd_op_gemm and the GEMMs of vd_step / vd_step_sample): bm = weight rows
+ * per tile (64 or 128), bn = tokens per tile (16, 32, 64, 128 or 256), kpo =
+ * 64-wide K blocks per weight copy (1, 2 or 4); 0 leaves a field to the
+ * per-launch choice.  A field a launch cannot take is left to that choice
+ * too (bm 64 for the fused token choice of the LM head; a kpo that does not
+ * divide K / 64; kpo is halved while two pipeline stages do not fit).  The
+ * plan changes speed only, never a bit of the result: it exists to test that
+ * and to measure each shape.  Step graphs captured under another override are
+ * not replayed.  (An engineering addition; the pages have no counterpart.)
+ * Errors: VD_ERR_INVALID_ARG for values outside those sets. */
+int vd_set_gemm_plan(int32_t bm, int32_t bn, int32_t kpo);
 
 /* Batch-invariant RMSNorm [T technical: batch-invariant RMSNorm]:
  * y[r] = bf16(x[r] / sqrt(mean(x[r]^2) + eps) * w), one warp per row, fixed

@@ -14,6 +14,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <array>
 #include <atomic>
 #include <mutex>
 #include <string>
@@ -72,18 +73,40 @@ int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols
   return VD_OK;
 }
 
-int make_map_glu(CUtensorMap* map, const void* base, uint64_t F, uint64_t cols) {
+int make_weight_maps(WeightMaps* w, const void* base, uint64_t rows, uint64_t K, bool glu) {
   auto fn = encode_fn();
   if (!fn) return fail(VD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-  if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16) return fail(VD_ERR_INVALID_ARG, "TMA base/stride not 16-byte aligned");
-  cuuint64_t dims[3] = {cols, 2, F};
-  cuuint64_t strides[2] = {F * cols * 2, cols * 2};  // half, feature
-  cuuint32_t box[3] = {64, 2, 64};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(VD_ERR_CUDA, "cuTensorMapEncodeTiled(glu) failed: " + std::to_string(r));
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || K % kGemmBK || (glu && rows % 2))
+    return fail(VD_ERR_INVALID_ARG, "weight matrix: base not 16-byte aligned or K not a multiple of 64");
+  *w = WeightMaps{};
+  w->rows = static_cast<int>(rows);
+  w->K = static_cast<int>(K);
+  w->glu = glu;
+  const uint64_t KB = K / kGemmBK, F = rows / 2;
+  for (int bi = 0; bi < 2; ++bi)
+    for (int ki = 0; ki < kNumKpo; ++ki) {
+      const uint32_t bm = bi ? kGemmBM / 2 : kGemmBM, kpo = 1u << ki;
+      if (KB % kpo) continue;  // never used: a plan's kpo divides the K blocks
+      CUresult r;
+      if (!glu) {  // (64, row, K block)
+        cuuint64_t dims[3] = {64, rows, KB};
+        cuuint64_t strides[2] = {K * 2, 128};
+        cuuint32_t box[3] = {64, bm, kpo};
+        cuuint32_t estr[3] = {1, 1, 1};
+        r = fn(&w->m[bi][ki], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      } else {  // (64, half, feature, K block): gate rows 0..F-1, up rows F..2F-1
+        cuuint64_t dims[4] = {64, 2, F, KB};
+        cuuint64_t strides[3] = {F * K * 2, K * 2, 128};
+        cuuint32_t box[4] = {64, 2, bm / 2, kpo};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = fn(&w->m[bi][ki], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      }
+      if (r != CUDA_SUCCESS) return fail(VD_ERR_CUDA, "cuTensorMapEncodeTiled(weights) failed: " + std::to_string(r));
+    }
   return VD_OK;
 }
 
@@ -123,21 +146,26 @@ enum KernelClass {
 };
 
 // Activation buffer with TMA maps for row counts 1, 2, 4, ... (capped at
-// the capacity): a GEMM over T rows uses the smallest map covering T, so
-// rows past T are either never fetched or (within the bucket) computed and
-// discarded -- a GEMM column depends on its own row only.
+// the capacity), each in every token tile width: a GEMM over T rows uses the
+// smallest row count covering T, so rows past T are either never fetched or
+// (within the bucket) computed and discarded -- a GEMM column depends on its
+// own row only.
 struct ActBuf {
   __nv_bfloat16* ptr = nullptr;
   int cols = 0;
   std::vector<int> rows;
-  std::vector<CUtensorMap> maps;
+  std::vector<std::array<CUtensorMap, kNumBn>> maps;
   size_t bucket(int T) const {
     for (size_t i = 0; i < rows.size(); ++i)
       if (rows[i] >= T) return i;
     return rows.size() - 1;
   }
-  const CUtensorMap& map_for(int T) const { return maps[bucket(T)]; }
-  int box_for(int T) const { return std::min(rows[bucket(T)], kGemmBN); }
+  ActMaps view(int T) const {
+    ActMaps v;
+    v.maps = maps[bucket(T)].data();
+    v.rows = rows[bucket(T)];
+    return v;
+  }
 };
 
 // Host-side layout of the uploaded step descriptor (int32 offsets).
@@ -162,10 +190,12 @@ struct GraphKey {
   const void* feed = nullptr;    // device-side token feedback or null
   int T = 0, B = 0, R = 0, stride = 0, n_dec = 0, n_pre = 0, grid_dec = 0, grid_pre = 0, fold = 0, n_merge = 0;
   int fast = 0;
+  unsigned plan_epoch = 0;  // GEMM plan override in force
   bool operator==(const GraphKey& o) const {
     return pool_id == o.pool_id && logits == o.logits && tokens == o.tokens && feed == o.feed && T == o.T && B == o.B && R == o.R && stride == o.stride &&
            n_dec == o.n_dec && n_pre == o.n_pre && grid_dec == o.grid_dec && grid_pre == o.grid_pre &&
-           fold == o.fold && n_merge == o.n_merge && fast == o.fast;
+           fold == o.fold && n_merge == o.n_merge && fast == o.fast &&
+           plan_epoch == o.plan_epoch;
   }
 };
 struct GraphEntry {
@@ -189,8 +219,8 @@ struct vd_model {
   int max_splits = 0;
   int G = 1;
   // TMA maps
-  std::vector<CUtensorMap> m_qkv, m_o, m_gu, m_down;
-  CUtensorMap m_lm{};
+  std::vector<WeightMaps> m_qkv, m_o, m_gu, m_down;
+  WeightMaps m_lm{};
   ActBuf a, o, z, ar;
   // workspace
   __nv_bfloat16 *x = nullptr, *qkv = nullptr, *q = nullptr;
@@ -293,8 +323,9 @@ int make_act(vd_model* m, ActBuf& buf, int cap_rows, int cols) {
   buf.cols = cols;
   for (int r = 1;; r *= 2) {
     const int rows = std::min(r, cap_rows);
-    CUtensorMap mp;
-    if ((rc = make_map_2d(&mp, buf.ptr, rows, cols, std::min(rows, kGemmBN)))) return rc;
+    std::array<CUtensorMap, kNumBn> mp;
+    for (int i = 0; i < kNumBn; ++i)
+      if ((rc = make_map_2d(&mp[i], buf.ptr, rows, cols, std::min(rows, 16 << i)))) return rc;
     buf.rows.push_back(rows);
     buf.maps.push_back(mp);
     if (rows >= cap_rows) break;
@@ -673,28 +704,27 @@ int fast_splits(const vd_model* m, int T, int n_wtiles, int K) {
 // One GEMM of the step.  The invariant path fuses the epilogue; the fast
 // path may split K (fp32 partials, then a reduction kernel applying the same
 // epilogue), which is not batch-invariant.
-int gemm_step(vd_model* m, const CUtensorMap& wmap, const ActBuf& xb, int T, int n_wtiles, int K, int ldo, void* out,
-              const void* residual, int epi, int glu_up_row, Prof& p, cudaStream_t s) {
+int gemm_step(vd_model* m, const WeightMaps& w, const ActBuf& xb, int T, int ldo, void* out, const void* residual,
+              int epi, int glu_up_row, Prof& p, cudaStream_t s) {
   GemmArgs g{};
   g.status = m->status;
   g.T = T;
-  g.K = K;
+  g.K = w.K;
   g.ldo = ldo;
   g.out = out;
   g.residual = residual;
   g.glu_up_row = glu_up_row;
-  g.b_box_rows = xb.box_for(T);
   const bool glu = epi == EPI_SWIGLU || epi == EPI_GEGLU;
-  const int ks = fast_splits(m, T, n_wtiles, K);
+  const int ks = fast_splits(m, T, w.rows / kGemmBM, w.K);
   const int np = glu ? 2 * glu_up_row : ldo;  // width of the partial sums
-  if (ks == 1 || static_cast<size_t>(ks) * T * np > m->splitk_cap) return launch_gemm(wmap, xb.map_for(T), n_wtiles, g, epi, s);
+  if (ks == 1 || static_cast<size_t>(ks) * T * np > m->splitk_cap) return launch_gemm(w, xb.view(T), g, epi, s);
   g.out = m->splitk_part;
   g.ldo = np;
   g.residual = nullptr;
   g.k_splits = ks;
   g.glu = glu;
   int rc;
-  if ((rc = launch_gemm(wmap, xb.map_for(T), n_wtiles, g, EPI_PARTIAL, s))) return rc;
+  if ((rc = launch_gemm(w, xb.view(T), g, EPI_PARTIAL, s))) return rc;
   p.kernels = 2;
   return launch_splitk_reduce(m->splitk_part, ks, T, np, epi, out, residual, s);
 }
@@ -721,7 +751,7 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
     }
     {
       Prof p(m, K_GEMM_QKV, s);
-      if ((rc = gemm_step(m, m->m_qkv[l], m->a, T, qkv_dim / kGemmBM, dm, qkv_dim, m->qkv, nullptr, EPI_BF16, 0, p, s)))
+      if ((rc = gemm_step(m, m->m_qkv[l], m->a, T, qkv_dim, m->qkv, nullptr, EPI_BF16, 0, p, s)))
         return rc;
     }
     if ((rc = run_rope(m, pool, l, d, m->qkv, m->q, s))) return rc;
@@ -730,8 +760,7 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
       // h = bf16(o Wo^T); x = bf16(x + rms_post(h)); a = rms_ffn(x)
       {
         Prof p(m, K_GEMM_O, s);
-        if ((rc = gemm_step(m, m->m_o[l], m->o, T, dm / kGemmBM, c.n_heads * hd, dm, m->hsub, nullptr, EPI_BF16, 0, p,
-                            s)))
+        if ((rc = gemm_step(m, m->m_o[l], m->o, T, dm, m->hsub, nullptr, EPI_BF16, 0, p, s)))
           return rc;
       }
       Prof p(m, K_RMSNORM, s);
@@ -741,8 +770,7 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
     } else {
       {
         Prof p(m, K_GEMM_O, s);
-        if ((rc = gemm_step(m, m->m_o[l], m->o, T, dm / kGemmBM, c.n_heads * hd, dm, m->x, m->x, EPI_RESIDUAL, 0, p,
-                            s)))
+        if ((rc = gemm_step(m, m->m_o[l], m->o, T, dm, m->x, m->x, EPI_RESIDUAL, 0, p, s)))
           return rc;
       }
       Prof p(m, K_RMSNORM, s);
@@ -750,7 +778,7 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
     }
     {
       Prof p(m, K_GEMM_GU, s);
-      if ((rc = gemm_step(m, m->m_gu[l], m->a, T, F / 64, dm, F, m->z.ptr, nullptr,
+      if ((rc = gemm_step(m, m->m_gu[l], m->a, T, F, m->z.ptr, nullptr,
                           c.act == VD_ACT_GEGLU ? EPI_GEGLU : EPI_SWIGLU, F, p, s)))
         return rc;
     }
@@ -758,7 +786,7 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
       // h = bf16(z Wd^T); x = bf16(x + rms_post(h)); a = rms_attn of the next layer (none after the last)
       {
         Prof p(m, K_GEMM_DOWN, s);
-        if ((rc = gemm_step(m, m->m_down[l], m->z, T, dm / kGemmBM, F, dm, m->hsub, nullptr, EPI_BF16, 0, p, s)))
+        if ((rc = gemm_step(m, m->m_down[l], m->z, T, dm, m->hsub, nullptr, EPI_BF16, 0, p, s)))
           return rc;
       }
       const void* next_norm = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : nullptr;
@@ -768,7 +796,7 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
         return rc;
     } else {
       Prof p(m, K_GEMM_DOWN, s);
-      if ((rc = gemm_step(m, m->m_down[l], m->z, T, dm / kGemmBM, F, dm, m->x, m->x, EPI_RESIDUAL, 0, p, s))) return rc;
+      if ((rc = gemm_step(m, m->m_down[l], m->z, T, dm, m->x, m->x, EPI_RESIDUAL, 0, p, s))) return rc;
     }
   }
   if (d.R > 0) {
@@ -785,14 +813,13 @@ int enqueue_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out
       h.out = logits_out;
       h.K = dm;
       h.ldo = c.vocab;
-      h.b_box_rows = m->ar.box_for(d.R);
       if (tokens_out) {
         h.samp = m->d_samp;
         h.part_v = m->fused_part_v;
         h.part_i = m->fused_part_i;
         h.part_stride = c.vocab / 32;
       }
-      if ((rc = launch_gemm(m->m_lm, m->ar.map_for(d.R), c.vocab / kGemmBM, h, tokens_out ? EPI_F32_SAMPLE : EPI_F32,
+      if ((rc = launch_gemm(m->m_lm, m->ar.view(d.R), h, tokens_out ? EPI_F32_SAMPLE : EPI_F32,
                             s)))
         return rc;
     }
@@ -827,6 +854,7 @@ int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out,
   k.fold = d.fold;
   k.n_merge = d.n_merge;
   k.fast = m->fast;
+  k.plan_epoch = gemm_plan_epoch();
   GraphEntry* seen = nullptr;
   for (GraphEntry& e : m->graphs)
     if (e.key == k) {
@@ -942,18 +970,18 @@ int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_mode
     return r;
   };
   for (int i = 0; i < c.n_layers; ++i) {
-    CUtensorMap mp;
+    WeightMaps mp;
     const vd_layer_weights& L = m->layers[i];
-    if ((rc = make_map_2d(&mp, L.wqkv, qkv_dim, d, kGemmBM))) return bail(rc);
+    if ((rc = make_weight_maps(&mp, L.wqkv, qkv_dim, d, false))) return bail(rc);
     m->m_qkv.push_back(mp);
-    if ((rc = make_map_2d(&mp, L.wo, d, attn_dim, kGemmBM))) return bail(rc);
+    if ((rc = make_weight_maps(&mp, L.wo, d, attn_dim, false))) return bail(rc);
     m->m_o.push_back(mp);
-    if ((rc = make_map_glu(&mp, L.w_gate_up, F, d))) return bail(rc);
+    if ((rc = make_weight_maps(&mp, L.w_gate_up, 2 * static_cast<uint64_t>(F), d, true))) return bail(rc);
     m->m_gu.push_back(mp);
-    if ((rc = make_map_2d(&mp, L.w_down, d, F, kGemmBM))) return bail(rc);
+    if ((rc = make_weight_maps(&mp, L.w_down, d, F, false))) return bail(rc);
     m->m_down.push_back(mp);
   }
-  if ((rc = make_map_2d(&m->m_lm, w->lm_head, V, d, kGemmBM))) return bail(rc);
+  if ((rc = make_weight_maps(&m->m_lm, w->lm_head, V, d, false))) return bail(rc);
   const int TM = c.max_tokens;
   if ((rc = make_act(m, m->a, TM, d))) return bail(rc);
   if ((rc = make_act(m, m->o, TM, attn_dim))) return bail(rc);
@@ -1285,10 +1313,15 @@ int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int3
   if (K % kGemmBK || (glu ? N % 64 : N % kGemmBM)) return fail(VD_ERR_UNSUPPORTED, "N or K not a multiple of the tile");
   if (epilogue == VD_EPI_RESIDUAL && !residual) return fail(VD_ERR_INVALID_ARG, "residual required");
   if (!aligned16(A) || !aligned16(W) || !aligned16(C)) return fail(VD_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-  CUtensorMap wm, xm;
+  WeightMaps wm;
+  std::array<CUtensorMap, kNumBn> xm;
   int rc;
-  if ((rc = glu ? make_map_glu(&wm, W, N, K) : make_map_2d(&wm, W, N, K, kGemmBM))) return rc;
-  if ((rc = make_map_2d(&xm, A, T, K, std::min<int>(T, kGemmBN)))) return rc;
+  if ((rc = make_weight_maps(&wm, W, glu ? 2 * static_cast<uint64_t>(N) : N, K, glu))) return rc;
+  for (int i = 0; i < kNumBn; ++i)
+    if ((rc = make_map_2d(&xm[i], A, T, K, std::min<int>(T, 16 << i)))) return rc;
+  ActMaps xv;
+  xv.maps = xm.data();
+  xv.rows = T;
   GemmArgs g{};
   g.out = C;
   g.residual = residual;
@@ -1296,9 +1329,16 @@ int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int3
   g.K = K;
   g.ldo = N;
   g.glu_up_row = N;
-  g.b_box_rows = std::min<int>(T, kGemmBN);
   g.status = op_status();
-  return launch_gemm(wm, xm, glu ? N / 64 : N / kGemmBM, g, epilogue, static_cast<cudaStream_t>(stream));
+  return launch_gemm(wm, xv, g, epilogue, static_cast<cudaStream_t>(stream));
+}
+
+int vd_set_gemm_plan(int32_t bm, int32_t bn, int32_t kpo) {
+  GemmPlan p;
+  p.bm = bm;
+  p.bn = bn;
+  p.kpo = kpo;
+  return set_forced_gemm_plan(p);
 }
 
 int vd_op_rmsnorm(const void* x, const void* w, void* y, int32_t rows, int32_t d, float eps, void* stream) {

@@ -1,37 +1,40 @@
 // Batch-invariant bf16 GEMM on 5th-generation tensor cores (tcgen05).
 //
 // acc[t][n] = sum_k X[t][k] * W[n][k], fp32 accumulation in TMEM.  The
-// weight matrix is the MMA's A operand (M = 128 weight rows per tile) and
-// the tokens are its N dimension (N = 256 per tile), so decode batches of
-// up to 256 requests stream each weight tile exactly once.  Every launch,
-// whatever the number of tokens T, uses the same instruction shape
-// (M=128, N=256, K=16), the same K order (stage by stage, 4 MMAs of K=16 per
-// 64-wide stage) and no split-K: column t of D depends only on row t of X and
-// on W, which is the matmul contract of 深入解析 Vosti §六 6.1 (row x of a
-// batched run equals the singleton run bit for bit; zero-initialised
-// accumulator, same iteration order).
+// weight matrix is the MMA's A operand (BM = 128 or 64 weight rows per tile)
+// and the tokens are its N dimension (BN = 16 .. 256 per tile), so a decode
+// batch streams each weight tile once per token tile.  Every output element
+// is one chain of K = 16 MMA steps in ascending K order (4 per 64-wide K
+// block, K blocks in order) into a zero-initialised accumulator, and no launch
+// splits K: column t of D depends only on row t of X and on W, the matmul
+// contract of 深入解析 Vosti §六 6.1 (row x of a batched run equals the singleton
+// run bit for bit).  The tile shape is chosen per launch for speed; it sets
+// the instruction's M and N, and tcgen05.mma computes each element of D the
+// same way whatever M (64, 128) and N (16 .. 256) are, which the GPU tests
+// check bitwise across all shapes.
 //
 // Warp roles (192 threads, one persistent CTA per SM): warp 0 issues TMA
 // loads (one elected lane) and owns the TMEM allocation; warp 1 issues
 // tcgen05.mma (one lane) into one of two TMEM accumulators; warps 2..5 read
-// the other accumulator (warp w reaches lanes 32*(w%4)..+31) and run the
-// fused epilogue.  Every wait is bounded (see vd_device.cuh).
+// the other accumulator (warp w reaches lanes 32*(w%4)..+31; with BM = 64 the
+// tile's rows sit in lanes 0..15 of each group of 32) and run the fused
+// epilogue.  Every wait is bounded (see vd_device.cuh).
 //
-// The activation box is as tall as the launch needs (up to 256 rows): rows of
-// the B tile past it keep stale shared-memory contents, which only feed
+// A pipeline stage holds kpo K blocks: one weight copy of kpo x BM rows x 64
+// (a 3-D or 4-D box, 8 to 64 KB) and kpo activation boxes of up to BN rows.
+// Larger weight copies raise the rate at which one SM pulls a narrow matrix
+// in; the ring (200 KB) holds as many stages as fit.  Rows of a B block past
+// the activation box keep stale shared-memory contents, which only feed
 // columns that are never stored (a column depends on its own row alone).
-//
-// Pipeline depth follows the box: a 192 KB ring holds S stages of A tiles
-// (16 KB each) followed by S B tiles spaced b_stride = box bytes rounded up to
-// 1 KB, S being the most for which the last B tile plus the 32 KB the MMA
-// reads from it still ends inside the ring (4 stages at 256 rows, 9 at <= 16).
-// Short boxes thus keep up to 144 KB of weights in flight per SM, which is
-// what a decode GEMM with few weight tiles needs to approach HBM bandwidth.
-// The depth changes only when copies are issued, never the MMA sequence.
+// The depth and the copy size change when copies are issued, never the MMA
+// sequence.
 #include <limits.h>
 #include <math.h>
 
+#include <cmath>
+
 #include <algorithm>
+#include <atomic>
 
 #include "vd_device.cuh"
 #include "vd_internal.h"
@@ -39,16 +42,15 @@
 namespace vd {
 namespace {
 
-constexpr int kMaxStages = 9;
+constexpr int kMaxStages = 12;
 constexpr int kThreads = 192;
-constexpr int kAStageBytes = kGemmBM * kGemmBK * 2;
-constexpr int kBStageBytes = kGemmBN * kGemmBK * 2;  // what one MMA reads of B
-constexpr int kRingBytes = 4 * (kAStageBytes + kBStageBytes);
+constexpr int kRingBytes = 200 * 1024;
 // Epilogue exchange: the sampling epilogue transposes each warp's 32 x 32
 // block (4 x 32 x 33).
 constexpr int kXchgFloats = 128 * 33;
 constexpr int kSmemBytes = 1024 + kRingBytes + kXchgFloats * 4 + 256;
 static_assert((2 * kMaxStages + 5) * 8 + 8 <= 256, "barrier block");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
 __device__ __forceinline__ float gelu_tanh_f(float g) {
@@ -66,35 +68,43 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Epilogue of one tile: accumulator columns [c*32, c*32+32) are tokens
-// t0.. of the tile; TMEM lane = weight row of the tile.
+// t0.. of the tile.  TMEM lane 32*lg + i holds tile row lg*32 + i (BM = 128)
+// or, for i < 16, tile row lg*16 + i (BM = 64).
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tacc, int tile_t, int tile_n, int lg,
                                               int lane, float* xchg, int ksplit) {
-  const int row = lg * 32 + lane;  // tile row == TMEM lane
+  const int BM = args.bm, BN = args.bn;
+  const int rpw = BM >> 2;            // tile rows per lane group
+  const bool live = lane < rpw;       // lane holds a tile row
+  const int row = lg * rpw + lane;    // that row
   const uint32_t taddr = tacc + (static_cast<uint32_t>(lg * 32) << 16);
-  for (int c = 0; c < kGemmBN / 32; ++c) {
-    const int t0 = tile_t * kGemmBN + c * 32;
+  for (int c = 0; c * 32 < BN; ++c) {
+    const int t0 = tile_t * BN + c * 32;
     if (t0 >= args.T) break;  // uniform over the four epilogue warps
     float v[32];
     tmem_ld32(taddr + c * 32, v);
-    const int nt = min(32, args.T - t0);
+    const int nt = min(min(32, BN - c * 32), args.T - t0);
     if (EPI == EPI_PARTIAL) {
       // fp32 partial of K split `ksplit`: part[ksplit][t][n], n the row of the
       // full output (gate rows then up rows for a GLU matrix)
-      const int n = args.glu ? ((row & 1) ? args.glu_up_row : 0) + tile_n * 64 + (row >> 1)
-                             : tile_n * kGemmBM + row;
+      const int n = args.glu ? ((row & 1) ? args.glu_up_row : 0) + tile_n * (BM >> 1) + (row >> 1)
+                             : tile_n * BM + row;
       float* out = static_cast<float*>(args.out) + (static_cast<size_t>(ksplit) * args.T) * args.ldo + n;
+      if (live) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
+        for (int j = 0; j < 32; ++j)
+          if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
+      }
     } else if (EPI == EPI_F32) {
-      float* out = static_cast<float*>(args.out) + tile_n * kGemmBM + row;
+      float* out = static_cast<float*>(args.out) + tile_n * BM + row;
+      if (live) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
-    } else if (EPI == EPI_F32_SAMPLE) {
+        for (int j = 0; j < 32; ++j)
+          if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
+      }
+    } else if (EPI == EPI_F32_SAMPLE) {  // BM = 128 only
       if (args.out) {
-        float* out = static_cast<float*>(args.out) + tile_n * kGemmBM + row;
+        float* out = static_cast<float*>(args.out) + tile_n * BM + row;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
@@ -110,7 +120,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tac
         const int t = t0 + lane;
         const vd_sampler sp = args.samp[t];
         const bool greedy = !(sp.temperature > 0.f);
-        const int n0 = tile_n * kGemmBM + lg * 32;
+        const int n0 = tile_n * BM + lg * 32;
         float bv = -INFINITY;
         int bi = INT_MAX;
 #pragma unroll
@@ -137,27 +147,32 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tac
       }
       __syncwarp();
     } else if (EPI == EPI_BF16) {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * kGemmBM + row;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * BM + row;
+      if (live) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(v[j]);
+        for (int j = 0; j < 32; ++j)
+          if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(v[j]);
+      }
     } else if (EPI == EPI_RESIDUAL) {
-      const size_t col = static_cast<size_t>(tile_n) * kGemmBM + row;
+      const size_t col = static_cast<size_t>(tile_n) * BM + row;
       const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(args.residual) + col;
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + col;
-      // The residual may alias the output: load the whole chunk first so
-      // the loads are not serialised behind the stores.
-      float r[32];
+      if (live) {
+        // The residual may alias the output: load the whole chunk first so
+        // the loads are not serialised behind the stores.
+        float r[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        r[j] = (j < nt) ? __bfloat162float(res[static_cast<size_t>(t0 + j) * args.ldo]) : 0.f;
+        for (int j = 0; j < 32; ++j)
+          r[j] = (j < nt) ? __bfloat162float(res[static_cast<size_t>(t0 + j) * args.ldo]) : 0.f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < nt)
-          out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fadd_rn(bf16_round(v[j]), r[j]));
-    } else {  // GLU: TMEM lane 2f holds gate, 2f+1 up of feature f (the 3-D weight box interleaves them)
-      const bool gate_lane = (lane & 1) == 0;
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * 64 + lg * 16 + (lane >> 1);
+        for (int j = 0; j < 32; ++j)
+          if (j < nt)
+            out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fadd_rn(bf16_round(v[j]), r[j]));
+      }
+    } else {  // GLU: tile row 2f holds gate, 2f+1 up of feature f (the weight box interleaves them)
+      const bool gate_lane = live && (lane & 1) == 0;
+      __nv_bfloat16* out =
+          static_cast<__nv_bfloat16*>(args.out) + tile_n * (BM >> 1) + lg * (rpw >> 1) + (lane >> 1);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float u = __shfl_xor_sync(0xffffffffu, bf16_round(v[j]), 1);  // the neighbour's up value
@@ -172,17 +187,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tac
 }
 
 // Persistent: CTA b handles tiles b, b + gridDim.x, ...; tile i = (token
-// tile i % n_tok_tiles, weight tile i / n_tok_tiles).  Two TMEM accumulators
-// (2 x 256 columns) let the MMAs of one tile run while the epilogue warps
-// drain the previous one.
+// tile i % n_tok_tiles, weight tile i / n_tok_tiles), so CTAs working on the
+// same weight tile at the same time share its reads through L2.  Two TMEM
+// accumulators (2 x 256 columns) let the MMAs of one tile run while the
+// epilogue warps drain the previous one.
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  const int S = args.stages, b_stride = args.b_stride;
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + S * kAStageBytes;
+  const int S = args.stages;
+  uint8_t* ring = smem;
   float* xchg = reinterpret_cast<float*>(smem + kRingBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(xchg + kXchgFloats);
   uint64_t* empty = full + kMaxStages;
@@ -192,16 +207,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  // a GLU weight tile: gate rows and up rows of the same 64 features, two boxes
+  // a GLU weight tile: gate and up rows of the same BM / 2 features, interleaved
   const bool kGlu = EPI == EPI_SWIGLU || EPI == EPI_GEGLU || (EPI == EPI_PARTIAL && args.glu);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KB = args.K / kGemmBK;
-  const int ntt = (args.T + kGemmBN - 1) / kGemmBN;
+  const int BM = args.bm, BN = args.bn, kpo = args.kpo;
+  const int n_ops = args.K / kGemmBK / kpo;  // stages per tile over the whole K
+  const int ntt = (args.T + BN - 1) / BN;
   const int KS = args.k_splits;  // 1 on the invariant path
   const int ntiles = ntt * args.n_wtiles * KS;
-  // tile -> (K split, token tile, weight tile); a split covers K blocks [kb_lo, kb_hi)
-  auto kb_lo = [&](int tile) { return (tile % KS) * KB / KS; };
-  auto kb_hi = [&](int tile) { return (tile % KS + 1) * KB / KS; };
+  // tile -> (K split, token tile, weight tile); a split covers stages [op_lo, op_hi)
+  auto op_lo = [&](int tile) { return (tile % KS) * n_ops / KS; };
+  auto op_hi = [&](int tile) { return (tile % KS + 1) * n_ops / KS; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -234,26 +250,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   pdl_trigger();
   const uint32_t tmem = *tmem_slot;
+  const int a_sub = BM * 128;            // one K block of A
+  const int a_bytes = kpo * a_sub;       // B blocks follow the A blocks in a stage
+  const int b_sub = args.b_sub;
 
   int issued = 0;  // producer: stages loaded so far (all tiles)
   if (skip) {
     // nothing issued: fall through to the teardown
   } else if (warp == 0) {
     if (lane == 0) {
+      const uint32_t tx = static_cast<uint32_t>(kpo * (a_sub + args.b_box_rows * 128));
       int g = 0, s = 0;  // stage g lives in slot s = g % S, round g / S
       uint32_t ph = 0;     // parity of round g / S
       for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
         const int tile_t = (tile / KS) % ntt, tile_n = (tile / KS) / ntt;
-        for (int kb = kb_lo(tile); kb < kb_hi(tile); ++kb, ++g) {
+        for (int op = op_lo(tile); op < op_hi(tile); ++op, ++g) {
           if (g >= S && !mbar_wait(&empty[s], ph ^ 1u, abort_flag, args.status)) break;
-          mbar_arrive_expect_tx(&full[s], kAStageBytes + args.b_box_rows * 128);
-          uint8_t* a = sA + s * kAStageBytes;
-          if (kGlu) {  // rows (feature, half) of 64 features: gate and up of a feature side by side
-            tma_load_3d(a, &wmap, &full[s], kb * kGemmBK, 0, tile_n * 64);
-          } else {
-            tma_load_2d(a, &wmap, &full[s], kb * kGemmBK, tile_n * kGemmBM);
-          }
-          tma_load_2d(sB + s * b_stride, &xmap, &full[s], kb * kGemmBK, tile_t * kGemmBN);
+          mbar_arrive_expect_tx(&full[s], tx);
+          uint8_t* st = ring + s * args.stage_bytes;
+          const int kb = op * kpo;
+          if (kGlu)
+            tma_load_4d(st, &wmap, &full[s], 0, 0, tile_n * (BM >> 1), kb);
+          else
+            tma_load_3d(st, &wmap, &full[s], 0, tile_n * BM, kb);
+          for (int j = 0; j < kpo; ++j)
+            tma_load_2d(st + a_bytes + j * b_sub, &xmap, &full[s], (kb + j) * kGemmBK, tile_t * BN);
           issued = g + 1;
           if (++s == S) {
             s = 0;
@@ -264,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16(kGemmBM, kGemmBN);
+      const uint32_t idesc = umma_idesc_bf16(BM, BN);
       int i = 0, s = 0;
       uint32_t ph = 0;
       for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x, ++i) {
@@ -272,15 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i >= 2 && !mbar_wait(&acc_empty[b], ((i >> 1) - 1) & 1, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t tacc = tmem + b * kGemmBN;
-        const int kb0 = kb_lo(tile);
-        for (int kb = kb0; kb < kb_hi(tile); ++kb) {
+        const int op0 = op_lo(tile);
+        for (int op = op0; op < op_hi(tile); ++op) {
           if (!mbar_wait(&full[s], ph, abort_flag, args.status)) break;
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + s * kAStageBytes);
-          const uint32_t b0 = smem_u32(sB + s * b_stride);
+          const uint32_t a0 = smem_u32(ring + s * args.stage_bytes);
+          const uint32_t b0 = a0 + a_bytes;
+          for (int j = 0; j < kpo; ++j)
 #pragma unroll
-          for (int kk = 0; kk < kGemmBK / 16; ++kk)
-            umma_bf16(tacc, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (kb - kb0) | kk);
+            for (int kk = 0; kk < kGemmBK / 16; ++kk)
+              umma_bf16(tacc, sw128_desc(a0 + j * a_sub + kk * 32), sw128_desc(b0 + j * b_sub + kk * 32), idesc,
+                        (op - op0) | j | kk);
           umma_commit(&empty[s]);
           if (++s == S) {
             s = 0;
@@ -365,13 +388,114 @@ int launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const GemmArgs&
     VD_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
     configured = true;
   }
-  const int tiles = ((a.T + kGemmBN - 1) / kGemmBN) * a.n_wtiles * a.k_splits;
+  const int tiles = ((a.T + a.bn - 1) / a.bn) * a.n_wtiles * a.k_splits;
   VD_CUDA_TRY(launch_k(gemm_kernel<EPI>, dim3(std::min(tiles, sm_count())), dim3(kThreads), kSmemBytes, s, wmap, xmap,
                        a));
   return VD_OK;
 }
 
+GemmPlan g_forced;
+std::atomic<unsigned> g_plan_epoch{0};
+
+int ilog2(int x) {
+  int l = 0;
+  while ((1 << (l + 1)) <= x) ++l;
+  return l;
+}
+
+// Pipeline layout of a plan: kpo is halved until at least two stages fit.
+void layout(GemmArgs& a, int act_rows) {
+  for (;;) {
+    a.b_box_rows = std::min(a.bn, act_rows);
+    a.b_sub = (a.bn * 128 + 1023) / 1024 * 1024;
+    a.stage_bytes = a.kpo * (a.bm * 128 + a.b_sub);
+    a.stages = std::min(kMaxStages, kRingBytes / a.stage_bytes);
+    if (a.stages >= 2 || a.kpo == 1) break;
+    a.kpo >>= 1;
+  }
+}
+
 }  // namespace
+
+namespace {
+
+// Estimated time (us) of one launch under a plan.  The model only ranks
+// plans; its constants were fitted to the measured times of every plan on the
+// Llama-3.1-8B-shaped matrices (QKV, O, gate/up, down, LM head) at 1 .. 8192
+// tokens, where it picks within 10 % of the fastest plan everywhere.  A
+// pipeline stage costs the longest of: its copies (a fixed issue cost per
+// copy, or the copy's bytes at the per-SM fill rate), its MMAs (an N <= 32
+// instruction takes about 49 cycles, N = 256 about 136), and the latency of a
+// copy-and-MMA round trip shared by the stages in flight.  A launch costs its
+// tiles' stages over the SMs, and at least the weights' bytes at HBM speed.
+double plan_cost(int bm, int bn, int kpo, int T, int rows, int K, int ks) {
+  constexpr double kCopyUs = 0.3, kActCopyUs = 0.05, kFillGBs = 60.0, kLatencyUs = 3.0, kTileUs = 0.5;
+  constexpr double kClockMHz = 2070.0, kHbmGBs = 6800.0;
+  int stage = 0, S = 0;
+  for (;;) {
+    stage = kpo * (bm * 128 + (bn * 128 + 1023) / 1024 * 1024);
+    S = std::min(kMaxStages, kRingBytes / stage);
+    if (S >= 2 || kpo == 1) break;
+    kpo >>= 1;
+  }
+  if (S < 2) return 1e30;
+  int bucket = 1;
+  while (bucket < T) bucket <<= 1;
+  const int brows = std::min(bn, bucket);
+  const double tiles = static_cast<double>(rows / bm) * ((T + bn - 1) / bn) * ks;
+  const double per_sm = std::ceil(tiles / sm_count());
+  const double mma_clk = std::max(49.0, 136.0 * bn / 256);
+  const double t_mma = 4.0 * kpo * mma_clk / kClockMHz;
+  const double t_copy = std::max(kCopyUs, kpo * bm * 128 / kFillGBs / 1e3) +
+                        kpo * std::max(kActCopyUs, brows * 128 / kFillGBs / 1e3);
+  const double t_lat = (kLatencyUs + t_mma) / S;
+  const double t_stage = std::max({t_copy, t_lat, t_mma});
+  const double stages_per_tile = static_cast<double>(K / kGemmBK) / kpo / ks;
+  const double t_hbm = static_cast<double>(rows) * K * 2 / kHbmGBs / 1e3;
+  return std::max(per_sm * (stages_per_tile * t_stage + kTileUs), t_hbm);
+}
+
+}  // namespace
+
+GemmPlan gemm_plan(const WeightMaps& w, int T, int epi, int k_splits) {
+  const int KB = w.K / kGemmBK;
+  const bool bm64_ok = epi != EPI_F32_SAMPLE && w.rows % 64 == 0 && (!w.glu || (w.rows / 2) % 32 == 0);
+  int top = 16;  // no wider token tile than the activation bucket needs
+  while (top < T && top < kGemmBN) top <<= 1;
+  GemmPlan p;
+  double best = 0;
+  for (int bm : {kGemmBM, kGemmBM / 2}) {
+    if (bm != kGemmBM && !bm64_ok) continue;
+    if (w.rows % bm) continue;
+    for (int bn = 16; bn <= top; bn <<= 1)
+      for (int kpo = 1; kpo <= 4; kpo <<= 1) {
+        if (KB % kpo || (k_splits > 1 && kpo > 1)) continue;
+        const double c = plan_cost(bm, bn, kpo, T, w.rows, w.K, k_splits);
+        if (p.bm == 0 || c < best) {
+          best = c;
+          p.bm = bm;
+          p.bn = bn;
+          p.kpo = kpo;
+        }
+      }
+  }
+  const GemmPlan f = g_forced;
+  if (f.bm == 128 || (f.bm == 64 && bm64_ok && w.rows % 64 == 0)) p.bm = f.bm;
+  if (f.bn) p.bn = f.bn;
+  if (f.kpo && k_splits == 1 && KB % f.kpo == 0) p.kpo = f.kpo;
+  return p;
+}
+
+int set_forced_gemm_plan(GemmPlan p) {
+  if ((p.bm != 0 && p.bm != 64 && p.bm != 128) || (p.bn != 0 && (p.bn < 16 || p.bn > kGemmBN || (p.bn & (p.bn - 1)))) ||
+      (p.kpo != 0 && p.kpo != 1 && p.kpo != 2 && p.kpo != 4))
+    return fail(VD_ERR_INVALID_ARG, "GEMM plan: bm in {0, 64, 128}, bn in {0, 16 .. 256} (a power of two), kpo in {0, 1, 2, 4}");
+  g_forced = p;
+  ++g_plan_epoch;
+  return VD_OK;
+}
+
+unsigned gemm_plan_epoch() { return g_plan_epoch.load(); }
 
 int launch_splitk_reduce(const float* part, int k_splits, int T, int N, int epi, void* out, const void* residual,
                          cudaStream_t s) {
@@ -390,30 +514,33 @@ int launch_splitk_reduce(const float* part, int k_splits, int T, int N, int epi,
   return VD_OK;
 }
 
-int launch_gemm(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, const GemmArgs& a0, int epi,
-                cudaStream_t s) {
+int launch_gemm(const WeightMaps& w, const ActMaps& x, const GemmArgs& a0, int epi, cudaStream_t s) {
   if (a0.T <= 0) return VD_OK;
   GemmArgs a = a0;
-  a.n_wtiles = n_tiles;
   if (a.k_splits < 1) a.k_splits = 1;
   if ((a.k_splits > 1) != (epi == EPI_PARTIAL) || a.k_splits > a.K / kGemmBK)
     return fail(VD_ERR_INVALID_ARG, "K splits need the partial epilogue and at most one split per K block");
-  if (a.b_box_rows < 1 || a.b_box_rows > kGemmBN) return fail(VD_ERR_INVALID_ARG, "activation box rows out of range");
-  a.b_stride = std::max(1024, (a.b_box_rows * 128 + 1023) / 1024 * 1024);
-  a.stages = std::min(kMaxStages, (kRingBytes - (kBStageBytes - a.b_stride)) / (kAStageBytes + a.b_stride));
-  // the MMA reads kBStageBytes from the last stage's B tile: keep that in the ring
-  if (a.stages < 2 || a.stages * kAStageBytes + (a.stages - 1) * a.b_stride + kBStageBytes > kRingBytes)
-    return fail(VD_ERR_INVALID_ARG, "GEMM pipeline layout");
+  if (a.K != w.K || x.rows < 1 || !x.maps) return fail(VD_ERR_INVALID_ARG, "GEMM operand shapes");
+  const GemmPlan p = gemm_plan(w, a.T, epi, a.k_splits);
+  a.bm = p.bm;
+  a.bn = p.bn;
+  a.kpo = p.kpo;
+  layout(a, x.rows);
+  if (a.stages < 2 || w.rows % a.bm || (a.K / kGemmBK) % a.kpo || (a.k_splits > 1 && a.kpo != 1))
+    return fail(VD_ERR_INVALID_ARG, "GEMM plan does not fit the matrix");
+  a.n_wtiles = w.rows / a.bm;
+  const CUtensorMap& wm = w.m[a.bm == 64][ilog2(a.kpo)];
+  const CUtensorMap& xm = x.maps[ilog2(a.bn / 16)];
   switch (epi) {
-    case EPI_BF16: return launch_one<EPI_BF16>(wmap, xmap, a, s);
-    case EPI_RESIDUAL: return launch_one<EPI_RESIDUAL>(wmap, xmap, a, s);
-    case EPI_F32: return launch_one<EPI_F32>(wmap, xmap, a, s);
-    case EPI_PARTIAL: return launch_one<EPI_PARTIAL>(wmap, xmap, a, s);
+    case EPI_BF16: return launch_one<EPI_BF16>(wm, xm, a, s);
+    case EPI_RESIDUAL: return launch_one<EPI_RESIDUAL>(wm, xm, a, s);
+    case EPI_F32: return launch_one<EPI_F32>(wm, xm, a, s);
+    case EPI_PARTIAL: return launch_one<EPI_PARTIAL>(wm, xm, a, s);
     case EPI_F32_SAMPLE:
       if (!a.samp || !a.part_v || !a.part_i) return fail(VD_ERR_INVALID_ARG, "sampling epilogue without buffers");
-      return launch_one<EPI_F32_SAMPLE>(wmap, xmap, a, s);
-    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(wmap, xmap, a, s);
-    case EPI_GEGLU: return launch_one<EPI_GEGLU>(wmap, xmap, a, s);
+      return launch_one<EPI_F32_SAMPLE>(wm, xm, a, s);
+    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(wm, xm, a, s);
+    case EPI_GEGLU: return launch_one<EPI_GEGLU>(wm, xm, a, s);
     default: return fail(VD_ERR_INVALID_ARG, "unknown GEMM epilogue");
   }
 }

@@ -50,10 +50,6 @@ cudaError_t launch_k(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
 // 2-D bf16 map over a row-major [rows][cols] matrix; box = box_rows x 64
 // columns (128 bytes), 128-byte swizzle, zero fill outside the matrix.
 int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
-// 3-D bf16 map over a gate/up matrix [2F][cols] (gate rows 0..F-1, up rows
-// F..2F-1) as (cols, half, feature): a box (64, 2, 64) stages 64 features with
-// each gate row next to its up row.
-int make_map_glu(CUtensorMap* map, const void* base, uint64_t F, uint64_t cols);
 // 3-D bf16 map for the KV pool: dims (64, hd/64, rows), box (64, hd/64, 16).
 int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd);
 
@@ -65,9 +61,39 @@ int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd);
 enum Epilogue {
   EPI_BF16 = 0, EPI_RESIDUAL = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_GEGLU = 4, EPI_F32_SAMPLE = 5, EPI_PARTIAL = 6
 };
-constexpr int kGemmBM = 128;  // weight rows per tile (MMA M)
-constexpr int kGemmBN = 256;  // tokens per tile (MMA N), one shape for every T
-constexpr int kGemmBK = 64;   // K per pipeline stage (one 128-byte swizzle row)
+constexpr int kGemmBM = 128;  // weight rows per tile (MMA M), or kGemmBM / 2
+constexpr int kGemmBN = 256;  // most tokens per tile (MMA N)
+constexpr int kGemmBK = 64;   // K per block (one 128-byte swizzle row)
+constexpr int kNumKpo = 3;    // K blocks per weight copy: 1, 2 or 4
+constexpr int kNumBn = 5;     // token tile widths 16, 32, 64, 128, 256
+
+// Launch shape of one GEMM: weight rows per tile (128 or 64), tokens per tile
+// (16 .. 256, a power of two) and K blocks per weight copy (1, 2, 4).  None
+// of them changes the arithmetic of an output element: every element is the
+// same chain of K = 16 MMA steps in ascending K order into a zeroed fp32
+// accumulator, whatever the instruction's M and N.
+struct GemmPlan {
+  int bm = 0, bn = 0, kpo = 0;
+};
+
+// A weight matrix with one TMA map per (tile height, K blocks per copy):
+// plain [rows][K] as (64, row, K block); gate/up [2F][K] as
+// (64, half, feature, K block), so a tile stages each gate row next to its up
+// row (tile rows 2f, 2f + 1).
+struct WeightMaps {
+  CUtensorMap m[2][kNumKpo];  // [bm == 64][log2 kpo]
+  int rows = 0;               // output rows (2F for gate/up)
+  int K = 0;
+  bool glu = false;
+};
+int make_weight_maps(WeightMaps* w, const void* base, uint64_t rows, uint64_t K, bool glu);
+
+// Activation rows [rows][cols] with one map per token tile width: map i has a
+// box of min(16 << i, rows) rows.
+struct ActMaps {
+  const CUtensorMap* maps = nullptr;  // [kNumBn]
+  int rows = 0;
+};
 
 struct GemmArgs {
   void* out;             // [T][ldo] bf16 (or fp32 for EPI_F32)
@@ -76,7 +102,6 @@ struct GemmArgs {
   int K;                 // reduction length
   int ldo;               // output row stride (elements)
   int glu_up_row;        // GLU: first row of the up half in the weight matrix (= F)
-  int b_box_rows;        // rows of the activation TMA box (1..kGemmBN)
   int n_wtiles;          // weight tiles (set by launch_gemm)
   const vd_sampler* samp;  // EPI_F32_SAMPLE: per-token sampler state [T]
   float* part_v;           // EPI_F32_SAMPLE: [T][part_stride] group winners' scores
@@ -84,8 +109,12 @@ struct GemmArgs {
   int part_stride;         //                 = vocab / 32
   int k_splits;          // K splits (1: the invariant path; > 1 only with EPI_PARTIAL)
   int glu;               // EPI_PARTIAL over a GLU weight matrix (gate/up tile layout)
-  int stages;            // pipeline depth (set by launch_gemm from b_box_rows)
-  int b_stride;          // bytes between the B tiles of two stages (set by launch_gemm)
+  // set by launch_gemm:
+  int bm, bn, kpo;       // the plan
+  int b_box_rows;        // rows of the activation TMA box (min(bn, activation rows))
+  int b_sub;             // bytes of one K block of B in a stage (>= bn * 128, 1 KB multiple)
+  int stage_bytes;       // kpo * (bm * 128 + b_sub)
+  int stages;            // pipeline depth
   int* status;           // device status word
 };
 // Fast path: out = epilogue(sum over ks of part[ks][t][n]) for the T x N
@@ -93,9 +122,14 @@ struct GemmArgs {
 // split order.  epi: EPI_BF16, EPI_RESIDUAL, EPI_SWIGLU or EPI_GEGLU.
 int launch_splitk_reduce(const float* part, int k_splits, int T, int N, int epi, void* out, const void* residual,
                          cudaStream_t s);
-// A = weight map (box 128 rows, or 64 for GLU), B = activation map (box kGemmBN rows).
-int launch_gemm(const CUtensorMap& wmap, const CUtensorMap& xmap, int n_tiles, const GemmArgs& a, int epi,
-                cudaStream_t s);
+// The plan launch_gemm takes for T tokens against this matrix (the forced
+// plan where one is set, else the estimated fastest).
+GemmPlan gemm_plan(const WeightMaps& w, int T, int epi, int k_splits);
+// Forced plan for every later launch (fields 0: chosen per launch); returns
+// a counter that changes with every call.
+int set_forced_gemm_plan(GemmPlan p);
+unsigned gemm_plan_epoch();
+int launch_gemm(const WeightMaps& w, const ActMaps& x, const GemmArgs& a, int epi, cudaStream_t s);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {

@@ -115,6 +115,7 @@ _SIGS = {
     "vd_version": (ctypes.c_char_p, []),
     "vd_op_gemm": (ctypes.c_int, [_VP, _VP, _VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                   _VP, _VP]),
+    "vd_set_gemm_plan": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     "vd_op_rmsnorm": (ctypes.c_int, [_VP, _VP, _VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _VP]),
     "vd_op_attention": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
     "vd_op_rope_kv": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
@@ -410,6 +411,11 @@ def gemm(A, W, C, epilogue=EPI_BF16, residual=None, stream=None):
     T, K = A.shape
     N = C.shape[1]
     check(lib().vd_op_gemm(_ptr(A), _ptr(W), _ptr(C), T, N, K, epilogue, _ptr(residual), _stream(stream)))
+
+
+def set_gemm_plan(bm=0, bn=0, kpo=0):
+    """Process-wide GEMM launch shape override (0: chosen per launch); changes speed only."""
+    check(lib().vd_set_gemm_plan(bm, bn, kpo))
 
 
 def rmsnorm(x, w, y, eps, stream=None):
