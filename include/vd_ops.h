@@ -55,6 +55,13 @@ int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int3
  * Errors: VD_ERR_INVALID_ARG for values outside those sets. */
 int vd_set_gemm_plan(int32_t bm, int32_t bn, int32_t kpo);
 
+/* The plan a GEMM launch over T tokens against an N x K weight matrix (GLU:
+ * 2N rows, N = F) with this epilogue takes, including a forced plan:
+ * out[0] = bm, out[1] = bn, out[2] = kpo (host array).  epilogue: a VD_EPI_*
+ * value, or 5 for the LM head with the fused token choice.  Needs no GPU
+ * work (it reads the device's SM count).  Errors: VD_ERR_INVALID_ARG. */
+int vd_gemm_plan_query(int32_t T, int32_t N, int32_t K, int32_t epilogue, int32_t out[3]);
+
 /* Batch-invariant RMSNorm [T technical: batch-invariant RMSNorm]:
  * y[r] = bf16(x[r] / sqrt(mean(x[r]^2) + eps) * w), one warp per row, fixed
  * lane-strided sum of squares and fixed butterfly.  x, y: dev bf16 [rows][d],

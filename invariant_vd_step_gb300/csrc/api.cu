@@ -1333,6 +1333,22 @@ int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int3
   return launch_gemm(wm, xv, g, epilogue, static_cast<cudaStream_t>(stream));
 }
 
+int vd_gemm_plan_query(int32_t T, int32_t N, int32_t K, int32_t epilogue, int32_t out[3]) {
+  if (!out) return fail(VD_ERR_INVALID_ARG, "null pointer");
+  if (T < 1 || N < 1 || K < 1 || K % kGemmBK) return fail(VD_ERR_INVALID_ARG, "sizes");
+  if (epilogue < 0 || epilogue > EPI_F32_SAMPLE) return fail(VD_ERR_INVALID_ARG, "unknown epilogue");
+  const bool glu = epilogue == EPI_SWIGLU || epilogue == EPI_GEGLU;
+  WeightMaps w;  // shapes only: no map is encoded
+  w.rows = glu ? 2 * N : N;
+  w.K = K;
+  w.glu = glu;
+  const GemmPlan p = gemm_plan(w, T, epilogue, 1);
+  out[0] = p.bm;
+  out[1] = p.bn;
+  out[2] = p.kpo;
+  return VD_OK;
+}
+
 int vd_set_gemm_plan(int32_t bm, int32_t bn, int32_t kpo) {
   GemmPlan p;
   p.bm = bm;

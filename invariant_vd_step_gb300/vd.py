@@ -116,6 +116,8 @@ _SIGS = {
     "vd_op_gemm": (ctypes.c_int, [_VP, _VP, _VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                   _VP, _VP]),
     "vd_set_gemm_plan": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    "vd_gemm_plan_query": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.POINTER(ctypes.c_int32)]),
     "vd_op_rmsnorm": (ctypes.c_int, [_VP, _VP, _VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _VP]),
     "vd_op_attention": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
     "vd_op_rope_kv": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
@@ -416,6 +418,13 @@ def gemm(A, W, C, epilogue=EPI_BF16, residual=None, stream=None):
 def set_gemm_plan(bm=0, bn=0, kpo=0):
     """Process-wide GEMM launch shape override (0: chosen per launch); changes speed only."""
     check(lib().vd_set_gemm_plan(bm, bn, kpo))
+
+
+def gemm_plan(T, N, K, epilogue=EPI_BF16):
+    """(bm, bn, kpo) that a GEMM launch over T tokens takes (epilogue 5: LM head with token choice)."""
+    out = (ctypes.c_int32 * 3)()
+    check(lib().vd_gemm_plan_query(T, N, K, epilogue, out))
+    return tuple(out)
 
 
 def rmsnorm(x, w, y, eps, stream=None):
