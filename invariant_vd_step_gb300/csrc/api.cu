@@ -83,10 +83,11 @@ int make_weight_maps(WeightMaps* w, const void* base, uint64_t rows, uint64_t K,
   w->K = static_cast<int>(K);
   w->glu = glu;
   const uint64_t KB = K / kGemmBK, F = rows / 2;
-  for (int bi = 0; bi < 2; ++bi)
+  for (int bi = 0; bi < 3; ++bi)
     for (int ki = 0; ki < kNumKpo; ++ki) {
-      const uint32_t bm = bi ? kGemmBM / 2 : kGemmBM, kpo = 1u << ki;
+      const uint32_t bm = bi == 0 ? kGemmBM : bi == 1 ? kGemmBM / 2 : 2 * kGemmBM, kpo = 1u << ki;
       if (KB % kpo) continue;  // never used: a plan's kpo divides the K blocks
+      if (bi == 2 && (kpo > 1 || rows % bm)) continue;  // 256-row tiles: one K block per copy
       CUresult r;
       if (!glu) {  // (64, row, K block)
         cuuint64_t dims[3] = {64, rows, KB};

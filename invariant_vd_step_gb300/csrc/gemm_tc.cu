@@ -69,128 +69,134 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // Epilogue of one tile: accumulator columns [c*32, c*32+32) are tokens
 // t0.. of the tile.  TMEM lane 32*lg + i holds tile row lg*32 + i (BM = 128)
-// or, for i < 16, tile row lg*16 + i (BM = 64).
+// or, for i < 16, tile row lg*16 + i (BM = 64).  A 256-row tile is two
+// 128-row halves, the second one's accumulator BN columns further on.
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tacc, int tile_t, int tile_n, int lg,
                                               int lane, float* xchg, int ksplit) {
   const int BM = args.bm, BN = args.bn;
-  const int rpw = BM >> 2;            // tile rows per lane group
+  const int HM = BM > kGemmBM ? kGemmBM : BM;  // rows of one MMA half
+  const int rpw = HM >> 2;            // tile rows per lane group and half
   const bool live = lane < rpw;       // lane holds a tile row
-  const int row = lg * rpw + lane;    // that row
-  const uint32_t taddr = tacc + (static_cast<uint32_t>(lg * 32) << 16);
-  for (int c = 0; c * 32 < BN; ++c) {
-    const int t0 = tile_t * BN + c * 32;
-    if (t0 >= args.T) break;  // uniform over the four epilogue warps
-    float v[32];
-    tmem_ld32(taddr + c * 32, v);
-    const int nt = min(min(32, BN - c * 32), args.T - t0);
-    if (EPI == EPI_PARTIAL) {
-      // fp32 partial of K split `ksplit`: part[ksplit][t][n], n the row of the
-      // full output (gate rows then up rows for a GLU matrix)
-      const int n = args.glu ? ((row & 1) ? args.glu_up_row : 0) + tile_n * (BM >> 1) + (row >> 1)
-                             : tile_n * BM + row;
-      float* out = static_cast<float*>(args.out) + (static_cast<size_t>(ksplit) * args.T) * args.ldo + n;
-      if (live) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
-      }
-    } else if (EPI == EPI_F32) {
-      float* out = static_cast<float*>(args.out) + tile_n * BM + row;
-      if (live) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
-      }
-    } else if (EPI == EPI_F32_SAMPLE) {  // BM = 128 only
-      if (args.out) {
-        float* out = static_cast<float*>(args.out) + tile_n * BM + row;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
-      }
-      // Transpose the warp's block (lane = vocabulary row, j = token) so that
-      // lane j scans token t0 + j over the warp's 32 consecutive rows, one
-      // Philox block per 4 rows, exactly as the standalone sampler does.
-      float* xs = xchg + lg * 32 * 33;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) xs[lane * 33 + j] = v[j];
-      __syncwarp();
-      if (lane < nt) {
-        const int t = t0 + lane;
-        const vd_sampler sp = args.samp[t];
-        const bool greedy = !(sp.temperature > 0.f);
-        const int n0 = tile_n * BM + lg * 32;
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-#pragma unroll
-        for (int r4 = 0; r4 < 32; r4 += 4) {
-          float sc[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) sc[q] = xs[(r4 + q) * 33 + lane];
-          if (!greedy) {
-            const uint4 w = philox_block(sp.seed, sp.step, static_cast<uint32_t>((n0 + r4) >> 2));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) sc[q] = gumbel_score(sc[q], ws[q], sp.temperature);
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (better(sc[q], n0 + r4 + q, bv, bi)) {
-              bv = sc[q];
-              bi = n0 + r4 + q;
-            }
+  for (int h = 0; h * HM < BM; ++h) {
+    const int row = h * HM + lg * rpw + lane;  // tile row of this lane
+    const uint32_t taddr = tacc + h * BN + (static_cast<uint32_t>(lg * 32) << 16);
+    for (int c = 0; c * 32 < BN; ++c) {
+      const int t0 = tile_t * BN + c * 32;
+      if (t0 >= args.T) break;  // uniform over the four epilogue warps
+      float v[32];
+      tmem_ld32(taddr + c * 32, v);
+      const int nt = min(min(32, BN - c * 32), args.T - t0);
+      if (EPI == EPI_PARTIAL) {
+        // fp32 partial of K split `ksplit`: part[ksplit][t][n], n the row of the
+        // full output (gate rows then up rows for a GLU matrix)
+        const int n = args.glu ? ((row & 1) ? args.glu_up_row : 0) + tile_n * (BM >> 1) + (row >> 1)
+                               : tile_n * BM + row;
+        float* out = static_cast<float*>(args.out) + (static_cast<size_t>(ksplit) * args.T) * args.ldo + n;
+        if (live) {
+  #pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
         }
-        const size_t pi = static_cast<size_t>(t) * args.part_stride + tile_n * 4 + lg;
-        args.part_v[pi] = bv;
-        args.part_i[pi] = bi;
-      }
-      __syncwarp();
-    } else if (EPI == EPI_BF16) {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * BM + row;
-      if (live) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(v[j]);
-      }
-    } else if (EPI == EPI_RESIDUAL) {
-      const size_t col = static_cast<size_t>(tile_n) * BM + row;
-      const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(args.residual) + col;
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + col;
-      if (live) {
-        // The residual may alias the output: load the whole chunk first so
-        // the loads are not serialised behind the stores.
-        float r[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          r[j] = (j < nt) ? __bfloat162float(res[static_cast<size_t>(t0 + j) * args.ldo]) : 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nt)
-            out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fadd_rn(bf16_round(v[j]), r[j]));
-      }
-    } else {  // GLU: tile row 2f holds gate, 2f+1 up of feature f (the weight box interleaves them)
-      const bool gate_lane = live && (lane & 1) == 0;
-      __nv_bfloat16* out =
-          static_cast<__nv_bfloat16*>(args.out) + tile_n * (BM >> 1) + lg * (rpw >> 1) + (lane >> 1);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float u = __shfl_xor_sync(0xffffffffu, bf16_round(v[j]), 1);  // the neighbour's up value
-        if (gate_lane && j < nt) {
-          const float g = bf16_round(v[j]);
-          const float a = (EPI == EPI_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
-          out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fmul_rn(a, u));
+      } else if (EPI == EPI_F32) {
+        float* out = static_cast<float*>(args.out) + tile_n * BM + row;
+        if (live) {
+  #pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
+        }
+      } else if (EPI == EPI_F32_SAMPLE) {  // BM = 128 only
+        if (args.out) {
+          float* out = static_cast<float*>(args.out) + tile_n * BM + row;
+  #pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = v[j];
+        }
+        // Transpose the warp's block (lane = vocabulary row, j = token) so that
+        // lane j scans token t0 + j over the warp's 32 consecutive rows, one
+        // Philox block per 4 rows, exactly as the standalone sampler does.
+        float* xs = xchg + lg * 32 * 33;
+  #pragma unroll
+        for (int j = 0; j < 32; ++j) xs[lane * 33 + j] = v[j];
+        __syncwarp();
+        if (lane < nt) {
+          const int t = t0 + lane;
+          const vd_sampler sp = args.samp[t];
+          const bool greedy = !(sp.temperature > 0.f);
+          const int n0 = tile_n * BM + h * HM + lg * 32;
+          float bv = -INFINITY;
+          int bi = INT_MAX;
+  #pragma unroll
+          for (int r4 = 0; r4 < 32; r4 += 4) {
+            float sc[4];
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) sc[q] = xs[(r4 + q) * 33 + lane];
+            if (!greedy) {
+              const uint4 w = philox_block(sp.seed, sp.step, static_cast<uint32_t>((n0 + r4) >> 2));
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  #pragma unroll
+              for (int q = 0; q < 4; ++q) sc[q] = gumbel_score(sc[q], ws[q], sp.temperature);
+            }
+  #pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (better(sc[q], n0 + r4 + q, bv, bi)) {
+                bv = sc[q];
+                bi = n0 + r4 + q;
+              }
+          }
+          const size_t pi = static_cast<size_t>(t) * args.part_stride + tile_n * (BM / 32) + h * 4 + lg;
+          args.part_v[pi] = bv;
+          args.part_i[pi] = bi;
+        }
+        __syncwarp();
+      } else if (EPI == EPI_BF16) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * BM + row;
+        if (live) {
+  #pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(v[j]);
+        }
+      } else if (EPI == EPI_RESIDUAL) {
+        const size_t col = static_cast<size_t>(tile_n) * BM + row;
+        const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(args.residual) + col;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + col;
+        if (live) {
+          // The residual may alias the output: load the whole chunk first so
+          // the loads are not serialised behind the stores.
+          float r[32];
+  #pragma unroll
+          for (int j = 0; j < 32; ++j)
+            r[j] = (j < nt) ? __bfloat162float(res[static_cast<size_t>(t0 + j) * args.ldo]) : 0.f;
+  #pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nt)
+              out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fadd_rn(bf16_round(v[j]), r[j]));
+        }
+      } else {  // GLU: tile row 2f holds gate, 2f+1 up of feature f (the weight box interleaves them)
+        const bool gate_lane = live && (lane & 1) == 0;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * (BM >> 1) + h * (HM >> 1) +
+                             lg * (rpw >> 1) + (lane >> 1);
+  #pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float u = __shfl_xor_sync(0xffffffffu, bf16_round(v[j]), 1);  // the neighbour's up value
+          if (gate_lane && j < nt) {
+            const float g = bf16_round(v[j]);
+            const float a = (EPI == EPI_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
+            out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fmul_rn(a, u));
+          }
         }
       }
     }
-  }
+  }  // halves
 }
 
 // Persistent: CTA b handles tiles b, b + gridDim.x, ...; tile i = (token
 // tile i % n_tok_tiles, weight tile i / n_tok_tiles), so CTAs working on the
 // same weight tile at the same time share its reads through L2.  Two TMEM
 // accumulators (2 x 256 columns) let the MMAs of one tile run while the
-// epilogue warps drain the previous one.
+// epilogue warps drain the previous one; a tile that needs more than 256
+// accumulator columns (256 rows x more than 128 tokens) has all 512 and the
+// two overlap no longer.
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, GemmArgs args) {
@@ -211,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool kGlu = EPI == EPI_SWIGLU || EPI == EPI_GEGLU || (EPI == EPI_PARTIAL && args.glu);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BM = args.bm, BN = args.bn, kpo = args.kpo;
+  const int nbuf = ((BM > kGemmBM ? 2 : 1) * BN <= kGemmBN) ? 2 : 1;  // accumulators that fit in TMEM
   const int n_ops = args.K / kGemmBK / kpo;  // stages per tile over the whole K
   const int ntt = (args.T + BN - 1) / BN;
   const int KS = args.k_splits;  // 1 on the invariant path
@@ -285,25 +292,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16(BM, BN);
+      const int HM = BM > kGemmBM ? kGemmBM : BM;  // rows per MMA (a 256-row tile issues two)
+      const uint32_t idesc = umma_idesc_bf16(HM, BN);
       int i = 0, s = 0;
       uint32_t ph = 0;
       for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x, ++i) {
-        const int b = i & 1;
-        if (i >= 2 && !mbar_wait(&acc_empty[b], ((i >> 1) - 1) & 1, abort_flag, args.status)) break;
+        const int b = i % nbuf;
+        if (i >= nbuf && !mbar_wait(&acc_empty[b], ((i / nbuf) - 1) & 1, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t tacc = tmem + b * kGemmBN;
         const int op0 = op_lo(tile);
         for (int op = op0; op < op_hi(tile); ++op) {
           if (!mbar_wait(&full[s], ph, abort_flag, args.status)) break;
           tc_fence_after();
+          // One descriptor per operand and stage; a K step of 16 elements is 32
+          // bytes, i.e. 2 in the descriptor's address field (16-byte units).
+          // This thread issues every MMA, so its loop is kept short.
           const uint32_t a0 = smem_u32(ring + s * args.stage_bytes);
-          const uint32_t b0 = a0 + a_bytes;
-          for (int j = 0; j < kpo; ++j)
+          const uint64_t ad = sw128_desc(a0), bd = sw128_desc(a0 + a_bytes);
+          if (BM <= kGemmBM) {
+            for (int j = 0; j < kpo; ++j)
 #pragma unroll
-            for (int kk = 0; kk < kGemmBK / 16; ++kk)
-              umma_bf16(tacc, sw128_desc(a0 + j * a_sub + kk * 32), sw128_desc(b0 + j * b_sub + kk * 32), idesc,
-                        (op - op0) | j | kk);
+              for (int kk = 0; kk < kGemmBK / 16; ++kk)
+                umma_bf16(tacc, ad + j * (a_sub >> 4) + 2 * kk, bd + j * (b_sub >> 4) + 2 * kk, idesc,
+                          (op - op0) | j | kk);
+          } else {  // rows 128..255 of the tile: A rows 16 KB on, accumulator BN columns on
+#pragma unroll
+            for (int kk = 0; kk < kGemmBK / 16; ++kk) {
+              umma_bf16(tacc, ad + 2 * kk, bd + 2 * kk, idesc, (op - op0) | kk);
+              umma_bf16(tacc + BN, ad + ((kGemmBM * 128) >> 4) + 2 * kk, bd + 2 * kk, idesc, (op - op0) | kk);
+            }
+          }
           umma_commit(&empty[s]);
           if (++s == S) {
             s = 0;
@@ -318,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lg = warp & 3;  // TMEM lane group reachable by this warp
     int i = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
-      const int b = i & 1;
-      if (!mbar_wait(&acc_full[b], (i >> 1) & 1, abort_flag, args.status)) break;
+      const int b = i % nbuf;
+      if (!mbar_wait(&acc_full[b], (i / nbuf) & 1, abort_flag, args.status)) break;
       tc_fence_after();
       epilogue_tile<EPI>(args, tmem + b * kGemmBN, (tile / KS) % ntt, (tile / KS) / ntt, lg, lane, xchg, tile % KS);
       tc_fence_before();
@@ -430,6 +449,7 @@ namespace {
 // tiles' stages over the SMs, and at least the weights' bytes at HBM speed.
 double plan_cost(int bm, int bn, int kpo, int T, int rows, int K, int ks) {
   constexpr double kCopyUs = 0.3, kActCopyUs = 0.05, kFillGBs = 60.0, kLatencyUs = 3.0, kTileUs = 0.5;
+  constexpr double kExposedEpilogueUs = 2.0;  // per tile, when one accumulator fills TMEM
   constexpr double kClockMHz = 2070.0, kHbmGBs = 6800.0;
   int stage = 0, S = 0;
   for (;;) {
@@ -444,7 +464,7 @@ double plan_cost(int bm, int bn, int kpo, int T, int rows, int K, int ks) {
   const int brows = std::min(bn, bucket);
   const double tiles = static_cast<double>(rows / bm) * ((T + bn - 1) / bn) * ks;
   const double per_sm = std::ceil(tiles / sm_count());
-  const double mma_clk = std::max(49.0, 136.0 * bn / 256);
+  const double mma_clk = std::max(49.0, 136.0 * bn / 256) * (bm > kGemmBM ? 2 : 1);
   const double t_mma = 4.0 * kpo * mma_clk / kClockMHz;
   const double t_copy = std::max(kCopyUs, kpo * bm * 128 / kFillGBs / 1e3) +
                         kpo * std::max(kActCopyUs, brows * 128 / kFillGBs / 1e3);
@@ -452,7 +472,8 @@ double plan_cost(int bm, int bn, int kpo, int T, int rows, int K, int ks) {
   const double t_stage = std::max({t_copy, t_lat, t_mma});
   const double stages_per_tile = static_cast<double>(K / kGemmBK) / kpo / ks;
   const double t_hbm = static_cast<double>(rows) * K * 2 / kHbmGBs / 1e3;
-  return std::max(per_sm * (stages_per_tile * t_stage + kTileUs), t_hbm);
+  const bool one_acc = (bm > kGemmBM ? 2 : 1) * bn > kGemmBN;
+  return std::max(per_sm * (stages_per_tile * t_stage + kTileUs + (one_acc ? kExposedEpilogueUs : 0)), t_hbm);
 }
 
 }  // namespace
@@ -462,14 +483,20 @@ GemmPlan gemm_plan(const WeightMaps& w, int T, int epi, int k_splits) {
   const bool bm64_ok = epi != EPI_F32_SAMPLE && w.rows % 64 == 0 && (!w.glu || (w.rows / 2) % 32 == 0);
   int top = 16;  // no wider token tile than the activation bucket needs
   while (top < T && top < kGemmBN) top <<= 1;
+  // 256-row tiles fill TMEM with one accumulator, so the epilogue no longer
+  // overlaps the next tile's MMAs; measured, they pay off only for the LM
+  // head's light fp32 epilogue at 512 tokens and more (about 16 % faster
+  // there), and are chosen only then (a forced plan may take them anywhere).
+  const bool bm256_ok = k_splits == 1 && w.rows % 256 == 0;
+  const bool bm256_auto = bm256_ok && T >= 512 && (epi == EPI_F32 || epi == EPI_F32_SAMPLE);
   GemmPlan p;
   double best = 0;
-  for (int bm : {kGemmBM, kGemmBM / 2}) {
-    if (bm != kGemmBM && !bm64_ok) continue;
+  for (int bm : {kGemmBM, kGemmBM / 2, 2 * kGemmBM}) {
+    if ((bm == kGemmBM / 2 && !bm64_ok) || (bm == 2 * kGemmBM && !bm256_auto)) continue;
     if (w.rows % bm) continue;
     for (int bn = 16; bn <= top; bn <<= 1)
       for (int kpo = 1; kpo <= 4; kpo <<= 1) {
-        if (KB % kpo || (k_splits > 1 && kpo > 1)) continue;
+        if (KB % kpo || (k_splits > 1 && kpo > 1) || (bm > kGemmBM && kpo > 1)) continue;
         const double c = plan_cost(bm, bn, kpo, T, w.rows, w.K, k_splits);
         if (p.bm == 0 || c < best) {
           best = c;
@@ -480,16 +507,18 @@ GemmPlan gemm_plan(const WeightMaps& w, int T, int epi, int k_splits) {
       }
   }
   const GemmPlan f = g_forced;
-  if (f.bm == 128 || (f.bm == 64 && bm64_ok && w.rows % 64 == 0)) p.bm = f.bm;
+  if (f.bm == 128 || (f.bm == 64 && bm64_ok) || (f.bm == 256 && bm256_ok)) p.bm = f.bm;
   if (f.bn) p.bn = f.bn;
   if (f.kpo && k_splits == 1 && KB % f.kpo == 0) p.kpo = f.kpo;
+  if (p.bm > kGemmBM) p.kpo = 1;  // 256-row tiles copy one K block at a time
   return p;
 }
 
 int set_forced_gemm_plan(GemmPlan p) {
-  if ((p.bm != 0 && p.bm != 64 && p.bm != 128) || (p.bn != 0 && (p.bn < 16 || p.bn > kGemmBN || (p.bn & (p.bn - 1)))) ||
+  if ((p.bm != 0 && p.bm != 64 && p.bm != 128 && p.bm != 256) || (p.bn != 0 && (p.bn < 16 || p.bn > kGemmBN || (p.bn & (p.bn - 1)))) ||
       (p.kpo != 0 && p.kpo != 1 && p.kpo != 2 && p.kpo != 4))
-    return fail(VD_ERR_INVALID_ARG, "GEMM plan: bm in {0, 64, 128}, bn in {0, 16 .. 256} (a power of two), kpo in {0, 1, 2, 4}");
+    return fail(VD_ERR_INVALID_ARG,
+                "GEMM plan: bm in {0, 64, 128, 256}, bn in {0, 16 .. 256} (a power of two), kpo in {0, 1, 2, 4}");
   g_forced = p;
   ++g_plan_epoch;
   return VD_OK;
@@ -529,7 +558,7 @@ int launch_gemm(const WeightMaps& w, const ActMaps& x, const GemmArgs& a0, int e
   if (a.stages < 2 || w.rows % a.bm || (a.K / kGemmBK) % a.kpo || (a.k_splits > 1 && a.kpo != 1))
     return fail(VD_ERR_INVALID_ARG, "GEMM plan does not fit the matrix");
   a.n_wtiles = w.rows / a.bm;
-  const CUtensorMap& wm = w.m[a.bm == 64][ilog2(a.kpo)];
+  const CUtensorMap& wm = w.m[a.bm == 64 ? 1 : a.bm == 256 ? 2 : 0][ilog2(a.kpo)];
   const CUtensorMap& xm = x.maps[ilog2(a.bn / 16)];
   switch (epi) {
     case EPI_BF16: return launch_one<EPI_BF16>(wm, xm, a, s);

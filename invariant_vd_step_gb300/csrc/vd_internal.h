@@ -61,13 +61,14 @@ int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd);
 enum Epilogue {
   EPI_BF16 = 0, EPI_RESIDUAL = 1, EPI_F32 = 2, EPI_SWIGLU = 3, EPI_GEGLU = 4, EPI_F32_SAMPLE = 5, EPI_PARTIAL = 6
 };
-constexpr int kGemmBM = 128;  // weight rows per tile (MMA M), or kGemmBM / 2
+constexpr int kGemmBM = 128;  // weight rows per tile (MMA M); tiles of 64 and 256 rows too
 constexpr int kGemmBN = 256;  // most tokens per tile (MMA N)
 constexpr int kGemmBK = 64;   // K per block (one 128-byte swizzle row)
 constexpr int kNumKpo = 3;    // K blocks per weight copy: 1, 2 or 4
 constexpr int kNumBn = 5;     // token tile widths 16, 32, 64, 128, 256
 
-// Launch shape of one GEMM: weight rows per tile (128 or 64), tokens per tile
+// Launch shape of one GEMM: weight rows per tile (64, 128, or 256 = two
+// M = 128 instructions sharing each activation block), tokens per tile
 // (16 .. 256, a power of two) and K blocks per weight copy (1, 2, 4).  None
 // of them changes the arithmetic of an output element: every element is the
 // same chain of K = 16 MMA steps in ascending K order into a zeroed fp32
@@ -81,7 +82,7 @@ struct GemmPlan {
 // (64, half, feature, K block), so a tile stages each gate row next to its up
 // row (tile rows 2f, 2f + 1).
 struct WeightMaps {
-  CUtensorMap m[2][kNumKpo];  // [bm == 64][log2 kpo]
+  CUtensorMap m[3][kNumKpo];  // [0: 128 rows, 1: 64 rows, 2: 256 rows (kpo 1 only)][log2 kpo]
   int rows = 0;               // output rows (2F for gate/up)
   int K = 0;
   bool glu = false;

@@ -69,8 +69,8 @@ def test_step_batch_from_arrays_matches_per_request_builder():
 
 def test_gemm_plan_query_and_override_host_logic(L):
     """The per-launch GEMM shape is host logic: it comes from the documented
-    sets, never splits a K block between copies, keeps 128-row tiles for the
-    fused token choice, and a forced shape applies where a launch can take
+    sets, never splits a K block between copies, keeps 64-row tiles away from
+    the fused token choice, and a forced shape applies where a launch can take
     it (no GPU work; the SM count falls back to a default without a GPU)."""
     shapes = [(6144, 4096, vd.EPI_BF16), (4096, 14336, vd.EPI_RESIDUAL), (14336, 4096, vd.EPI_SWIGLU),
               (128256, 4096, 5), (512, 256, vd.EPI_BF16), (768, 256, vd.EPI_GEGLU)]
@@ -78,14 +78,17 @@ def test_gemm_plan_query_and_override_host_logic(L):
         for N, K, epi in shapes:
             for T in (1, 5, 16, 64, 100, 256, 300, 2048, 8192):
                 bm, bn, kpo = vd.gemm_plan(T, N, K, epi)
-                assert bm in (64, 128) and bn in (16, 32, 64, 128, 256) and kpo in (1, 2, 4), (N, K, T)
+                assert bm in (64, 128, 256) and bn in (16, 32, 64, 128, 256) and kpo in (1, 2, 4), (N, K, T)
                 assert (K // 64) % kpo == 0
                 assert bn <= max(16, 1 << (T - 1).bit_length())
                 if epi == 5:
-                    assert bm == 128
+                    assert bm != 64          # the token choice scores 32-row groups per warp
+                if bm == 256:
+                    assert kpo == 1 and N * (2 if epi in (vd.EPI_SWIGLU, vd.EPI_GEGLU) else 1) % 256 == 0
         vd.set_gemm_plan(64, 32, 4)
         assert vd.gemm_plan(7, 4096, 4096, vd.EPI_BF16) == (64, 32, 4)
-        assert vd.gemm_plan(7, 128256, 4096, 5) == (128, 32, 4)   # bm 64 is not taken by the token choice
+        bm, bn, _ = vd.gemm_plan(7, 128256, 4096, 5)              # bm 64 is not taken by the token choice
+        assert bm != 64 and bn == 32
         assert vd.gemm_plan(7, 512, 192, vd.EPI_BF16)[2] == 1      # 3 K blocks: kpo 4 does not divide them
         vd.set_gemm_plan(0, 256, 0)
         assert vd.gemm_plan(7, 4096, 4096, vd.EPI_BF16)[1] == 256

@@ -1,6 +1,7 @@
 """GEMM launch shapes change speed, never bits.
 
-The tile of a GEMM launch -- weight rows per tile (64 or 128, the MMA's M),
+The tile of a GEMM launch -- weight rows per tile (64 or 128, the MMA's M,
+or 256 as two M = 128 instructions sharing each activation block),
 tokens per tile (16 .. 256, the MMA's N) and 64-wide K blocks per weight copy
 (1, 2, 4) -- is chosen per launch.  Every output element stays one chain of
 K = 16 MMA steps in ascending K order into a zeroed accumulator, so the
@@ -22,7 +23,7 @@ from invariant_vd_step_gb300 import synth, vd
 
 pytestmark = pytest.mark.gpu
 
-PLANS = [(bm, bn, kpo) for bm in (128, 64) for bn in (16, 32, 64, 128, 256) for kpo in (1, 2, 4)]
+PLANS = [(bm, bn, kpo) for bm in (128, 64, 256) for bn in (16, 32, 64, 128, 256) for kpo in (1, 2, 4)]
 
 
 @pytest.fixture(autouse=True)
@@ -65,7 +66,7 @@ def test_row_equals_singleton_under_small_token_tiles():
     W = synth.make_normal_bf16((N, K), seed=61, std=0.05).cuda()
     vd.set_gemm_plan(0, 0, 0)
     single = {x: bits(_run(A[x:x + 1].contiguous(), W, N, vd.EPI_BF16))[0] for x in (0, 15, 16, 150, 299)}
-    for plan in [(64, 16, 4), (128, 16, 2), (64, 64, 1), (128, 256, 4)]:
+    for plan in [(64, 16, 4), (128, 16, 2), (64, 64, 1), (128, 256, 4), (256, 256, 1), (256, 32, 1)]:
         vd.set_gemm_plan(*plan)
         C = bits(_run(A, W, N, vd.EPI_BF16))
         for x, row in single.items():
@@ -89,7 +90,7 @@ GEMMA_TINY = synth.ModelSpec("gemma-tiny", 3, 256, 2, 1, 256, 512, 512, act="geg
 def test_step_logits_do_not_move_under_any_forced_plan(spec, sample):
     """A mixed step (one prefill chunk, decode rows, a short chunk) and a
     pure decode step, with and without the fused token choice in the LM head
-    (which keeps 128-row weight tiles), under forced shapes."""
+    (which takes no 64-row weight tiles), under forced shapes."""
     ready()
     W = {k: v.cuda() for k, v in synth.make_weights(spec, seed=4, gain_std=0.1).items()}
     m = vd.Model(spec, W, max_tokens=320, max_seqs=16, max_logit_rows=64, max_context=512)
@@ -121,7 +122,8 @@ def test_step_logits_do_not_move_under_any_forced_plan(spec, sample):
 
     vd.set_gemm_plan(0, 0, 0)
     ref = steps()
-    for plan in [(64, 16, 4), (128, 16, 1), (64, 32, 2), (128, 64, 4), (64, 128, 1), (128, 256, 2)]:
+    for plan in [(64, 16, 4), (128, 16, 1), (64, 32, 2), (128, 64, 4), (64, 128, 1), (128, 256, 2),
+                 (256, 256, 1), (256, 64, 1)]:
         vd.set_gemm_plan(*plan)
         got = steps()
         for i, ((lb, tb), (rb, rt)) in enumerate(zip(got, ref)):
