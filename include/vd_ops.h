@@ -44,11 +44,14 @@ int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int3
 
 /* GEMM launch shape override, process-wide, for every later GEMM launch
  * (vd_op_gemm and the GEMMs of vd_step / vd_step_sample): bm = weight rows
- * per tile (64 or 128), bn = tokens per tile (16, 32, 64, 128 or 256), kpo =
- * 64-wide K blocks per weight copy (1, 2 or 4); 0 leaves a field to the
- * per-launch choice.  A field a launch cannot take is left to that choice
- * too (bm 64 for the fused token choice of the LM head; a kpo that does not
- * divide K / 64; kpo is halved while two pipeline stages do not fit).  The
+ * per tile (64, 128, or 256 = two M = 128 MMAs sharing each activation
+ * block), bn = tokens per tile (16, 32, 64, 128 or 256), kpo = 64-wide K
+ * blocks per weight copy (1, 2 or 4); 0 leaves a field to the per-launch
+ * choice.  A field a launch cannot take is left to that choice too (bm 64
+ * for the fused token choice of the LM head; bm 256 when the matrix's rows
+ * are not a multiple of 256 or K is split; a kpo that does not divide
+ * K / 64; kpo is 1 with bm 256 and is halved while two pipeline stages do
+ * not fit).  The
  * plan changes speed only, never a bit of the result: it exists to test that
  * and to measure each shape.  Step graphs captured under another override are
  * not replayed.  (An engineering addition; the pages have no counterpart.)
