@@ -413,8 +413,19 @@ int launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const GemmArgs&
   return VD_OK;
 }
 
-GemmPlan g_forced;
+// The forced plan as one word (bm | bn << 9 | kpo << 18), so that a host
+// thread setting it never races a launching thread reading it.
+std::atomic<uint32_t> g_forced{0};
 std::atomic<unsigned> g_plan_epoch{0};
+
+GemmPlan forced_plan() {
+  const uint32_t v = g_forced.load();
+  GemmPlan p;
+  p.bm = static_cast<int>(v & 511u);
+  p.bn = static_cast<int>((v >> 9) & 511u);
+  p.kpo = static_cast<int>((v >> 18) & 7u);
+  return p;
+}
 
 int ilog2(int x) {
   int l = 0;
@@ -506,7 +517,7 @@ GemmPlan gemm_plan(const WeightMaps& w, int T, int epi, int k_splits) {
         }
       }
   }
-  const GemmPlan f = g_forced;
+  const GemmPlan f = forced_plan();
   if (f.bm == 128 || (f.bm == 64 && bm64_ok) || (f.bm == 256 && bm256_ok)) p.bm = f.bm;
   if (f.bn) p.bn = f.bn;
   if (f.kpo && k_splits == 1 && KB % f.kpo == 0) p.kpo = f.kpo;
@@ -519,8 +530,9 @@ int set_forced_gemm_plan(GemmPlan p) {
       (p.kpo != 0 && p.kpo != 1 && p.kpo != 2 && p.kpo != 4))
     return fail(VD_ERR_INVALID_ARG,
                 "GEMM plan: bm in {0, 64, 128, 256}, bn in {0, 16 .. 256} (a power of two), kpo in {0, 1, 2, 4}");
-  g_forced = p;
-  ++g_plan_epoch;
+  const uint32_t v = static_cast<uint32_t>(p.bm) | static_cast<uint32_t>(p.bn) << 9 |
+                     static_cast<uint32_t>(p.kpo) << 18;
+  if (g_forced.exchange(v) != v) ++g_plan_epoch;  // captured step graphs stay valid for an unchanged plan
   return VD_OK;
 }
 

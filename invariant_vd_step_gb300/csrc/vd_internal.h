@@ -126,8 +126,8 @@ int launch_splitk_reduce(const float* part, int k_splits, int T, int N, int epi,
 // The plan launch_gemm takes for T tokens against this matrix (the forced
 // plan where one is set, else the estimated fastest).
 GemmPlan gemm_plan(const WeightMaps& w, int T, int epi, int k_splits);
-// Forced plan for every later launch (fields 0: chosen per launch); returns
-// a counter that changes with every call.
+// Forced plan for every later launch (fields 0: chosen per launch).
+// gemm_plan_epoch() changes whenever the forced plan does.
 int set_forced_gemm_plan(GemmPlan p);
 unsigned gemm_plan_epoch();
 int launch_gemm(const WeightMaps& w, const ActMaps& x, const GemmArgs& a, int epi, cudaStream_t s);

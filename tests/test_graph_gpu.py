@@ -96,3 +96,39 @@ def test_graph_mode_rejects_negative():
     m = vd.Model(spec, W, max_tokens=64, max_seqs=4, max_logit_rows=64, max_context=256)
     with pytest.raises(vd.VDError):
         m.set_graph_mode(-1)
+
+
+def test_a_new_gemm_plan_is_captured_not_replayed_stale():
+    """A captured step graph holds its GEMM launches with the tile shapes of
+    its capture; after vd_set_gemm_plan the same step key is seen afresh
+    (captured again on its second sighting), and its logits stay bitwise
+    those of the eager step either way."""
+    ready()
+    spec = synth.TINY
+    W = {k: v.cuda() for k, v in synth.make_weights(spec, seed=3, gain_std=0.1).items()}
+    m = vd.Model(spec, W, max_tokens=64, max_seqs=4, max_logit_rows=8, max_context=256)
+    e = vd.Model(spec, W, max_tokens=64, max_seqs=4, max_logit_rows=8, max_context=256)
+    m.set_graph_mode(8)
+    pm, pe = vd.KVPool(m, 32), vd.KVPool(e, 32)
+    toks = synth.make_tokens(40, spec.vocab, seed=9)
+    pages = np.arange(8, dtype=np.int32)
+    lm, le = torch.empty(1, spec.vocab, device="cuda"), torch.empty(1, spec.vocab, device="cuda")
+    pre = vd.StepBatch([(toks[:30], 0, pages)], logit_rows=[29])
+    m.step(pm, pre, lm)
+    e.step(pe, pre, le)
+    try:
+        for i, plan in enumerate([(0, 0, 0), (0, 0, 0), (0, 0, 0), (64, 16, 4), (64, 16, 4), (64, 16, 4)]):
+            vd.set_gemm_plan(*plan)
+            b = vd.StepBatch([(toks[30:31], 30, pages)], logit_rows=[0])  # the same step each time
+            m.step(pm, b, lm)
+            e.step(pe, b, le)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(bits(lm), bits(le), err_msg=f"step {i} plan {plan}")
+            st = m.graph_stats()
+            if i == 2:
+                assert (st["captures"], st["replays"]) == (1, 1), st
+        st = m.graph_stats()
+        assert (st["captures"], st["replays"]) == (2, 2), st  # one capture and one replay per plan
+    finally:
+        vd.set_gemm_plan(0, 0, 0)
+    assert m.device_status() == 0
