@@ -131,16 +131,19 @@ def _is_gain(name: str) -> bool:
 
 
 def make_weights(spec: ModelSpec, seed: int = 0, device="cpu", std: float = 0.02,
-                 gain_std: float = 0.0, zero: bool = False) -> dict:
+                 gain_std: float = 0.0, zero: bool = False, exclude=()) -> dict:
     """Random-init bf16 weights, one independent generator stream per tensor.
 
     Matrices ~ N(0, std) rounded to bf16; norm gains are 1 + N(0, gain_std)
     (exactly 1.0 for gain_std == 0).  With ``spec.norm_offset`` the stored
     weight w is the gain minus one, N(0, gain_std).  ``zero=True`` gives the
-    all-zero model.
+    all-zero model.  Tensors named in ``exclude`` are left out (the others
+    are unchanged: each tensor has its own stream).
     """
     out = {}
     for name, shape in weight_shapes(spec).items():
+        if name in exclude:
+            continue
         if zero:
             out[name] = torch.zeros(shape, dtype=torch.bfloat16, device=device)
             continue
