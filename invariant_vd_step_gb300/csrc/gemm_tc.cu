@@ -1,7 +1,8 @@
 // Batch-invariant bf16 GEMM on 5th-generation tensor cores (tcgen05).
 //
 // acc[t][n] = sum_k X[t][k] * W[n][k], fp32 accumulation in TMEM.  The
-// weight matrix is the MMA's A operand (BM = 128 or 64 weight rows per tile)
+// weight matrix is the MMA's A operand (BM = 64, 128 or 256 weight rows per
+// tile, the last as two M = 128 instructions sharing each activation block)
 // and the tokens are its N dimension (BN = 16 .. 256 per tile), so a decode
 // batch streams each weight tile once per token tile.  Every output element
 // is one chain of K = 16 MMA steps in ascending K order (4 per 64-wide K
@@ -21,7 +22,8 @@
 // epilogue.  Every wait is bounded (see vd_device.cuh).
 //
 // A pipeline stage holds kpo K blocks: one weight copy of kpo x BM rows x 64
-// (a 3-D or 4-D box, 8 to 64 KB) and kpo activation boxes of up to BN rows.
+// (a 3-D or 4-D box, 8 to 64 KB; kpo = 1 for 256-row tiles) and kpo
+// activation boxes of up to BN rows.
 // Larger weight copies raise the rate at which one SM pulls a narrow matrix
 // in; the ring (200 KB) holds as many stages as fit.  Rows of a B block past
 // the activation box keep stale shared-memory contents, which only feed
