@@ -711,6 +711,25 @@ def cache_from_pages(spec, pages_u16, c):
     return cache
 
 
+def cpu_model() -> str:
+    """The host CPU's name from /proc/cpuinfo (x86 "model name"; on Arm the
+    implementer/part codes), else the machine type."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if fields.get("model name"):
+        return fields["model name"]
+    if fields.get("CPU implementer"):
+        return f"{platform.machine()} implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline(spec, weights, ctx, tables, mem, n_req):
     """Times the oracle (as it stands) on this host for a bounded sample."""
     from invariant_vd_step_gb300 import synth
@@ -728,7 +747,7 @@ def cpu_baseline(spec, weights, ctx, tables, mem, n_req):
     t0 = time.perf_counter()
     oracle_decode_sample(spec, w_np, caches, toks)
     dt = time.perf_counter() - t0
-    return {"value": round(n_req / dt, 4), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": round(n_req / dt, 4), "unit": UNIT, "cores": os.cpu_count(), "cpu": cpu_model(), "kind": "oracle",
             "sample": f"{n_req} decode rows of the same workload (1 layer + LM head, float64 numpy), "
                       f"{dt:.1f} s"}
 
@@ -765,7 +784,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "llama3.1-8b-shape 1 decoder layer + LM head, pure decode", "batch": B,
                    "ctx": f"U[{CTX_LO},{CTX_HI}]", "page_size": 16},
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "cpu": cpu_model(), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
