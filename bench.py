@@ -166,6 +166,22 @@ def algorithmic_bytes(spec, ctx_lens, B):
     return total, kernels
 
 
+def gemm_plans(spec, T, R):
+    """The tile shape (weight rows, tokens, K blocks per weight copy) each GEMM
+    of a step over T tokens with R logit rows takes (LM head with the fused
+    token choice)."""
+    from invariant_vd_step_gb300 import vd
+    d, F = spec.d_model, spec.ffn_dim
+    glu = vd.EPI_GEGLU if spec.act == "geglu" else vd.EPI_SWIGLU
+    return {
+        "gemm_qkv": list(vd.gemm_plan(T, spec.qkv_dim, d, vd.EPI_BF16)),
+        "gemm_o": list(vd.gemm_plan(T, d, spec.attn_dim, vd.EPI_RESIDUAL)),
+        "gemm_gate_up": list(vd.gemm_plan(T, F, d, glu)),
+        "gemm_down": list(vd.gemm_plan(T, d, F, vd.EPI_RESIDUAL)),
+        "gemm_lm_head": list(vd.gemm_plan(R, spec.vocab, d, 5)),
+    }
+
+
 def decode_sweep_point(spec, weights, B, K, Wm, graphs, dev, hbm):
     """One point of the decode batch sweep: the bench workload at batch B
     (contexts U[512, 8192], permuted pages, random cached K/V), K timed steps
@@ -354,6 +370,7 @@ def run_gpu(args):
         return
     hbm, tf, peak_kind = load_peaks()
     total_bytes, kbytes = algorithmic_bytes(spec, ctx, B)
+    plans = gemm_plans(spec, B, B)
     step_ms = ms_max / K
     kernels = {}
     for name, (n, nk, tot) in prof.items():
@@ -363,6 +380,8 @@ def run_gpu(args):
         if name in kbytes:
             gbs = kbytes[name] / (per_step * 1e-3) / 1e9
             e.update({"algorithmic_bytes": kbytes[name], "GB_s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)})
+        if name in plans:
+            e["plan_bm_bn_kpo"] = plans[name]
         kernels[name] = e
     dom = max((k for k in kernels if k in kbytes), key=lambda k: kernels[k]["ms_per_step"])
     dk = kernels[dom]
