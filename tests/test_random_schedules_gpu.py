@@ -9,9 +9,10 @@ at random per seed instead: request counts and prompt lengths (1..120
 tokens, some sharing prefixes of any length), greedy and sampled requests,
 the engine's batch cap, chunk budget, prefix reuse and page placement, a
 pool small enough to force eviction, recomputation and preemption in some
-runs, step-graph replay on or off, and a forced GEMM tile shape.  The
-canonical execution runs one request at a time with a large budget, no
-reuse, sequential pages and a roomy pool.
+runs, step-graph replay on or off, and a forced GEMM tile shape, for a
+Llama-style and a Gemma-style block (sliding windows, QK-norm, GeGLU,
+sandwich norms).  The canonical execution runs one request at a time with a
+large budget, no reuse, sequential pages and a roomy pool.
 """
 
 import numpy as np
@@ -59,9 +60,13 @@ def _execute(model, pool, reqs, max_batch, budget, reuse, placement, num_pages):
     return views, stats
 
 
-def _one_seed(seed, totals):
+GEMMA_TINY = synth.ModelSpec("gemma-tiny", 3, 256, 2, 1, 256, 512, 512, act="geglu", qk_norm=True,
+                             rope_theta=1e6, rope_theta_local=1e4, sliding_window=24, local_global_period=2,
+                             rms_eps=1e-6, embed_scale=True, norm_offset=True, sandwich_norm=True)
+
+
+def _one_seed(spec, seed, totals):
     rng = np.random.default_rng(1000 + seed)
-    spec = synth.TINY
     W = {k: v.cuda() for k, v in synth.make_weights(spec, seed=seed, gain_std=0.1).items()}
     reqs = _workload(rng, spec.vocab)
     longest = max(len(p) + m for p, m, _, _ in reqs)
@@ -99,10 +104,11 @@ def _one_seed(seed, totals):
         model.close()
 
 
-def test_random_schedules_match_the_canonical_execution():
+@pytest.mark.parametrize("spec,seeds", [(synth.TINY, 24), (GEMMA_TINY, 8)], ids=["tiny-llama", "gemma-tiny"])
+def test_random_schedules_match_the_canonical_execution(spec, seeds):
     ready()
     totals = {"evicted": 0, "preempted": 0, "prefix_hit_pages": 0, "runs": 0}
-    for seed in range(24):
-        _one_seed(seed, totals)
+    for seed in range(seeds):
+        _one_seed(spec, seed, totals)
     # the draws did reach the behaviours they are meant to exercise
-    assert totals["runs"] == 96 and totals["evicted"] > 0 and totals["prefix_hit_pages"] > 0, totals
+    assert totals["runs"] == 4 * seeds and totals["evicted"] > 0 and totals["prefix_hit_pages"] > 0, totals
