@@ -47,6 +47,22 @@ def _bits(t: torch.Tensor) -> torch.Tensor:
     return t.contiguous().view(torch.int32)
 
 
+def _row_bits(x) -> bytes:
+    if isinstance(x, torch.Tensor):
+        return x.detach().contiguous().view(torch.int32).cpu().numpy().tobytes()
+    return np.ascontiguousarray(x, dtype=np.float32).view(np.int32).tobytes()
+
+
+def prefix_comparable(view_a, view_b) -> bool:
+    """Definition 2.1 (深入解析 Vosti §二): two views of one request are
+    prefix-comparable iff the shorter is a prefix of the longer.  A view is a
+    list of (logits, token) rows; logits compare by their float32 bits."""
+    for (la, ta), (lb, tb) in zip(view_a, view_b):
+        if int(ta) != int(tb) or _row_bits(la) != _row_bits(lb):
+            return False
+    return True
+
+
 def tiny_workload(seed: int = 1):
     spec = synth.TINY
     prompts = synth.make_prompts(8, 17, 64, spec.vocab, seed=seed, shared_prefix=32, n_sharing=4)

@@ -78,12 +78,22 @@ def test_step_logits_vs_oracle(spec):
 
 
 def test_zero_model_gives_zero_logits_bitwise():
+    """The all-zero model returns the golden outputs (tests/golden/zero_model_outputs.txt):
+    every logit +0.0 bit for bit, and greedy token id 0."""
     ready()
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "zero_model_outputs.txt")) as f:
+        kv = dict(line.split() for line in f if line.strip() and not line.startswith("#"))
+    want_bits, want_token = int(kv["logit_float32_bits"], 16), int(kv["greedy_token"])
     run = Runner(synth.TINY, zero=True)
     hist = synth.make_prompts(2, 10, 40, synth.TINY.vocab, seed=4)
     res = run.execute(hist, [[(0, len(hist[0])), (1, len(hist[1]))]])
-    for row in res.values():
-        assert torch.all(row == 0)
+    rows = torch.stack(list(res.values()))
+    assert torch.all(rows.contiguous().view(torch.int32) == want_bits)
+    tok = torch.empty(rows.shape[0], dtype=torch.int32, device="cuda")
+    run.model.sample(rows, [(1, i, 0.0) for i in range(rows.shape[0])], tok)
+    torch.cuda.synchronize()
+    assert torch.all(tok == want_token)
 
 
 def test_invariance_across_batching_chunking_and_pages():
