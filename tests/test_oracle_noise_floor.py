@@ -69,10 +69,12 @@ def test_bf16_flip_cascade_reaches_the_stated_tolerance(layer, monkeypatch):
 def test_gemma_block_flip_cascade_is_wider(monkeypatch):
     """The same measurement on the Gemma-3-4B-shaped block (2 layers, one
     local window-1024 and one global; embedding scale, (1 + w) gains,
-    sandwich norms, vocab 262144).  One 1e-5 disagreement already puts about
-    one logit in ten thousand beyond the stated tolerance (30 of 262144 here),
-    more than the 8B check's 99.99 % allows, which is why the full-size Gemma
-    check asks for 99.9 % (and twice the tolerance everywhere)."""
+    sandwich norms, vocab 262144).  A single 1e-5 disagreement already puts
+    logits beyond the stated tolerance (17 of 262144 here, against 3 of
+    128256 for the 8B-shaped layer): the same order as all that a 99.99 %
+    criterion allows (26), while the GPU differs from the oracle in many
+    roundings, not one.  That is why the full-size Gemma check asks for
+    99.9 % (and twice the tolerance everywhere)."""
     spec = synth.GEMMA3_4B.with_(name="gemma3-4b-shape-2layer", n_layers=2, local_global_period=2)
     dec = od.OracleDecoder(spec, _weights(spec, gain_std=0.1))
     rng = np.random.default_rng(4)
