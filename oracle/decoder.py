@@ -72,6 +72,40 @@ def rope(x, positions, theta):
     return round_bf16(np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1))
 
 
+def layer_is_local(layer: int, window: int, period: int) -> bool:
+    """Layer ``layer`` is a local (sliding-window) layer unless the model has
+    no window, or no local:global period, or (layer + 1) % period == 0.
+
+    With period 6 this is the 5:1 interleave of the Gemma-3-4B configuration:
+    five local layers, then one global layer.
+    """
+    return window > 0 and period > 0 and (layer + 1) % period != 0
+
+
+def _visible(p: int, window: int) -> int:
+    """First key a row at position p sees (深入解析 Vosti §六 6.2 traversal range)."""
+    return max(0, p - window + 1) if window > 0 else 0
+
+
+def _softmax_row(q_h, Kg, lo, p, hd):
+    s = (Kg[lo:p + 1] @ q_h) * (1.0 / math.sqrt(hd))
+    e = np.exp(s - s.max())
+    return e / e.sum()
+
+
+def attention_weights(q, K, positions, window):
+    """The softmax weights [n, Hq, P] of ``attention`` (0 off the visible range)."""
+    n, Hq, hd = q.shape
+    rep = Hq // K.shape[1]
+    w = np.zeros((n, Hq, K.shape[0]))
+    for t in range(n):
+        p = int(positions[t])
+        lo = _visible(p, window)
+        for h in range(Hq):
+            w[t, h, lo:p + 1] = _softmax_row(q[t, h], K[:, h // rep, :], lo, p, hd)
+    return w
+
+
 def attention(q, K, V, positions, window):
     """Causal (optionally windowed) GQA softmax attention, rounded to bf16.
 
@@ -81,16 +115,13 @@ def attention(q, K, V, positions, window):
     n, Hq, hd = q.shape
     Hkv = K.shape[1]
     rep = Hq // Hkv
-    scale = 1.0 / math.sqrt(hd)
     out = np.empty((n, Hq, hd), dtype=np.float64)
     for t in range(n):
         p = int(positions[t])
-        lo = max(0, p - window + 1) if window > 0 else 0
+        lo = _visible(p, window)
         for h in range(Hq):
             g = h // rep
-            s = (K[lo:p + 1, g, :] @ q[t, h]) * scale
-            e = np.exp(s - s.max())
-            out[t, h] = (e / e.sum()) @ V[lo:p + 1, g, :]
+            out[t, h] = _softmax_row(q[t, h], K[:, g, :], lo, p, hd) @ V[lo:p + 1, g, :]
     return round_bf16(out)
 
 
@@ -105,8 +136,11 @@ def gelu_tanh(g):
 class OracleDecoder:
     """float64 decoder over bf16 weights given as raw uint16 bit arrays.
 
-    ``spec`` is any object with the attributes of
-    ``invariant_vd_step_gb300.synth.ModelSpec`` (read, never imported).
+    ``spec`` is any object with the plain shape fields of a model
+    (n_layers, d_model, heads, head_dim, ffn_dim, vocab, rms_eps, act,
+    qk_norm, rope_theta, rope_theta_local, sliding_window,
+    local_global_period and the Gemma-3 block flags); which layers are
+    local is this module's own ``layer_is_local``, not a method of spec.
     """
 
     def __init__(self, spec, weights_u16: dict, chunk_rows: int = 8192):
@@ -171,13 +205,15 @@ class OracleDecoder:
             if s.qk_norm:
                 q = self.rms(q, p + "q_norm")
                 k = self.rms(k, p + "k_norm")
-            theta = s.layer_theta(i)
+            local = layer_is_local(i, getattr(s, "sliding_window", 0), getattr(s, "local_global_period", 0))
+            theta = s.rope_theta_local if local else s.rope_theta
+            window = s.sliding_window if local else 0
             q = rope(q, positions, theta)
             k = rope(k, positions, theta)
             K = np.concatenate([cache[i][0], k], axis=0)
             V = np.concatenate([cache[i][1], v], axis=0)
             new_cache.append((K, V))
-            o = attention(q, K, V, positions, s.layer_window(i)).reshape(n, Hq * hd)
+            o = attention(q, K, V, positions, window).reshape(n, Hq * hd)
             h = round_bf16(self.linear(p + "wo", o))
             if self.sandwich:
                 h = self.rms(h, p + "post_attn_norm")

@@ -12,6 +12,7 @@ import numpy as np
 
 from invariant_vd_step_gb300 import invariance, synth
 from oracle import decoder as od
+from oracle import fp32 as oc
 from oracle import sampler
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -25,8 +26,10 @@ def _rows(name):
 def test_zero_model_outputs_match_the_golden_values():
     kv = dict(_rows("zero_model_outputs.txt"))
     want_bits, want_token = int(kv["logit_float32_bits"], 16), int(kv["greedy_token"])
-    for spec in (synth.TINY, synth.TINY.with_(name="tiny-window", sliding_window=8, local_global_period=2)):
-        dec = od.OracleDecoder(spec, synth.weights_to_numpy(synth.make_weights(spec, zero=True)))
+    for spec, Oracle in ((s, o) for s in (synth.TINY, synth.TINY.with_(name="tiny-window", sliding_window=8,
+                                                                           local_global_period=2))
+                         for o in (od.OracleDecoder, oc.Fp32Decoder)):
+        dec = Oracle(spec, synth.weights_to_numpy(synth.make_weights(spec, zero=True)))
         for seed, n in ((3, 1), (4, 17), (5, 40)):
             logits = dec.forward(synth.make_tokens(n, spec.vocab, seed=seed))
             bits = np.asarray(logits, dtype=np.float32).view(np.uint32)

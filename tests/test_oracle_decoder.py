@@ -247,7 +247,7 @@ def test_incremental_equals_cold_forward_bitwise():
 
 def test_sliding_window_one_layer_ignores_tokens_before_window():
     spec, W, dec = _tiny(seed=4, n_layers=1, sliding_window=4, local_global_period=1000)
-    assert spec.layer_window(0) == 4
+    assert od.layer_is_local(0, spec.sliding_window, spec.local_global_period)
     h = synth.make_tokens(12, spec.vocab, seed=13)
     h2 = h.copy(); h2[:8] = (h2[:8] + 5) % spec.vocab   # row 11 sees 8..11
     np.testing.assert_array_equal(dec.forward(h2), dec.forward(h))
@@ -358,3 +358,128 @@ def test_gemma_block_incremental_equals_cold_forward_bitwise():
         lg, cache = dec.step(h[a:b], cache, logit_rows=range(b - a))
         parts.append(lg)
     np.testing.assert_array_equal(np.concatenate(parts), cold)
+
+
+# ---------------------------------------------------------------- pins added for the layer rule,
+# the softmax weights and QK-norm
+def test_layer_rule_is_five_local_to_one_global():
+    # Config C4 (Gemma-3-4B shape): a 5:1 interleave of window-1024 local layers and
+    # global layers over 34 layers; the oracle's own rule, not the product's.
+    pattern = [od.layer_is_local(i, 1024, 6) for i in range(34)]
+    assert pattern == ([True] * 5 + [False]) * 5 + [True] * 4
+    assert [i for i, loc in enumerate(pattern) if not loc] == [5, 11, 17, 23, 29]
+    # no window or no period: every layer global
+    assert not any(od.layer_is_local(i, 0, 6) for i in range(12))
+    assert not any(od.layer_is_local(i, 1024, 0) for i in range(12))
+
+
+def test_softmax_weights_sum_to_one_and_match_attention():
+    rng = np.random.default_rng(21)
+    P, Hq, Hkv, hd = 40, 4, 2, 16
+    K = round_bf16(rng.standard_normal((P, Hkv, hd)) * 3)
+    V = round_bf16(rng.standard_normal((P, Hkv, hd)))
+    q = round_bf16(rng.standard_normal((5, Hq, hd)) * 3)
+    pos = np.array([0, 7, 20, 33, 39])
+    for window in (0, 6):
+        w = od.attention_weights(q, K, pos, window)
+        np.testing.assert_allclose(w.sum(-1), 1.0, rtol=0, atol=1e-12)
+        assert np.all(w >= 0)
+        for t, p in enumerate(pos):
+            lo = max(0, p - window + 1) if window else 0
+            assert np.all(w[t, :, :lo] == 0) and np.all(w[t, :, p + 1:] == 0)
+        rep = Hq // Hkv
+        want = np.stack([np.stack([w[t, h] @ V[:, h // rep] for h in range(Hq)]) for t in range(5)])
+        np.testing.assert_array_equal(od.attention(q, K, V, pos, window), round_bf16(want))
+
+
+def test_qk_norm_constant_head_closed_form():
+    # QK-norm normalises each head over its own hd elements: a head holding
+    # the constant c_h maps to c_h / sqrt(c_h^2 + eps) * gain, whatever the
+    # other heads hold (a norm over the wrong axis mixes them).
+    c = np.array([0.5, -3.0, 40.0])
+    x = np.repeat(c[None, :, None], 16, axis=2)  # [1 token, 3 heads, hd 16]
+    gain = np.linspace(0.5, 1.5, 16)
+    got = od.rmsnorm(x, gain, 1e-6)
+    want = round_bf16((c / np.sqrt(c * c + 1e-6))[None, :, None] * gain[None, None, :])
+    np.testing.assert_array_equal(got, want)
+
+
+def _qk_reference(spec, W, toks, variant="right", theta=None):
+    """Two-token, one-layer forward with QK-norm written from the definition
+    with torch float64 ops: per-head RMSNorm of q and k with their gains,
+    then RoPE, then a 2-way softmax for row 1.  ``variant`` plants the
+    plausible mistakes the pin must tell apart."""
+    T = {k: v.to(torch.float64) for k, v in W.items()}
+    bf = lambda t: t.to(torch.bfloat16).to(torch.float64)
+    Hq, Hkv, hd, F, eps = spec.n_heads, spec.n_kv_heads, spec.head_dim, spec.ffn_dim, spec.rms_eps
+    off = 1.0 if spec.norm_offset else 0.0
+    def rms(x, w):
+        return bf(x * torch.rsqrt((x * x).mean(-1, keepdim=True) + eps) * (w + off))
+    def rope(x, p):  # x [H, hd] at position p, rotate-half
+        half = hd // 2
+        inv = (theta or spec.rope_theta) ** (-(2.0 * torch.arange(half, dtype=torch.float64)) / hd)
+        c, s = torch.cos(p * inv), torch.sin(p * inv)
+        return bf(torch.cat([x[:, :half] * c - x[:, half:] * s, x[:, half:] * c + x[:, :half] * s], -1))
+    x = T["embed"][torch.from_numpy(np.asarray(toks))]
+    a = rms(x, T["layers.0.attn_norm"])
+    qkv = bf(a @ T["layers.0.wqkv"].T)
+    q = qkv[:, :Hq * hd].reshape(2, Hq, hd)
+    k = qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(2, Hkv, hd)
+    v = qkv[:, (Hq + Hkv) * hd:].reshape(2, Hkv, hd)
+    qn, kn = (T["layers.0.q_norm"], T["layers.0.k_norm"]) if spec.qk_norm else (None, None)
+    if not spec.qk_norm:
+        q1 = rope(q[1], 1)
+        kr = torch.stack([rope(k[0], 0), rope(k[1], 1)])
+    elif variant == "right":
+        q1 = rope(rms(q[1], qn), 1)
+        kr = torch.stack([rope(rms(k[0], kn), 0), rope(rms(k[1], kn), 1)])
+    elif variant == "after_rope":
+        q1 = rms(rope(q[1], 1), qn)
+        kr = torch.stack([rms(rope(k[0], 0), kn), rms(rope(k[1], 1), kn)])
+    elif variant == "no_gain":
+        one = torch.ones(hd, dtype=torch.float64) - off
+        q1 = rope(rms(q[1], one), 1)
+        kr = torch.stack([rope(rms(k[0], one), 0), rope(rms(k[1], one), 1)])
+    elif variant == "whole_row":  # one norm over all heads of the row
+        q1 = rope(rms(q[1].reshape(-1), qn.repeat(Hq)).reshape(Hq, hd), 1)
+        kr = torch.stack([rope(rms(k[j].reshape(-1), kn.repeat(Hkv)).reshape(Hkv, hd), j) for j in (0, 1)])
+    o = []
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        s = kr[:, g, :] @ q1[h] / math.sqrt(hd)
+        o.append(torch.softmax(s, 0) @ v[:, g, :])
+    o = bf(torch.cat(o))
+    x1 = bf(x[1] + bf(T["layers.0.wo"] @ o))
+    a = rms(x1, T["layers.0.ffn_norm"])
+    g = bf(T["layers.0.w_gate_up"][:F] @ a)
+    u = bf(T["layers.0.w_gate_up"][F:] @ a)
+    act = torch.nn.functional.gelu(g, approximate="tanh") if spec.act == "geglu" else torch.nn.functional.silu(g)
+    x2 = bf(x1 + bf(T["layers.0.w_down"] @ bf(act * u)))
+    return (T["lm_head"] @ rms(x2, T["final_norm"])).numpy()
+
+
+QK_SPEC = dict(n_layers=1, qk_norm=True)
+
+
+def test_qk_norm_two_token_wiring():
+    # Row 1 attends to keys 0 and 1, so its logits depend on q and k: the
+    # norm must come before RoPE, over each head, with the q_norm / k_norm gains.
+    spec, W, dec = _tiny(seed=9, gain_std=0.5, **QK_SPEC)
+    toks = np.array([11, 1500])
+    want = _qk_reference(spec, W, toks)
+    np.testing.assert_allclose(dec.forward(toks), want, rtol=0, atol=1e-9)
+    for wrong in ("after_rope", "no_gain", "whole_row"):
+        assert np.abs(_qk_reference(spec, W, toks, wrong) - want).max() > 0.05, wrong
+
+
+LOCAL_THETA = dict(n_layers=1, qk_norm=True, sliding_window=4, local_global_period=1000, rope_theta=1e6, rope_theta_local=50.0)
+
+
+def test_local_layer_uses_its_own_rope_theta():
+    # Layer 0 of a model with a window and period 1000 is local: RoPE there
+    # uses rope_theta_local.  Two tokens sit inside the window of 4 keys.
+    spec, W, dec = _tiny(seed=10, gain_std=0.5, **LOCAL_THETA)
+    toks = np.array([7, 1999])
+    want = _qk_reference(spec, W, toks, theta=spec.rope_theta_local)
+    np.testing.assert_allclose(dec.forward(toks), want, rtol=0, atol=1e-9)
+    assert np.abs(_qk_reference(spec, W, toks, theta=spec.rope_theta) - want).max() > 0.05
