@@ -106,11 +106,13 @@ def attention_weights(q, K, positions, window):
     return w
 
 
-def attention(q, K, V, positions, window):
+def attention(q, K, V, positions, window, perturb=None):
     """Causal (optionally windowed) GQA softmax attention, rounded to bf16.
 
     q: [n, Hq, hd] rows at absolute ``positions``; K, V: [P, Hkv, hd] for
-    absolute positions 0..P-1 (P > max(positions)).
+    absolute positions 0..P-1 (P > max(positions)).  ``perturb`` (a test
+    hook for measuring the noise floor, off by default): a function applied
+    to the exact output before its rounding.
     """
     n, Hq, hd = q.shape
     Hkv = K.shape[1]
@@ -122,7 +124,7 @@ def attention(q, K, V, positions, window):
         for h in range(Hq):
             g = h // rep
             out[t, h] = _softmax_row(q[t, h], K[:, g, :], lo, p, hd) @ V[lo:p + 1, g, :]
-    return round_bf16(out)
+    return round_bf16(out if perturb is None else perturb(out))
 
 
 def silu(g):
@@ -143,8 +145,19 @@ class OracleDecoder:
     local is this module's own ``layer_is_local``, not a method of spec.
     """
 
-    def __init__(self, spec, weights_u16: dict, chunk_rows: int = 8192):
+    def __init__(self, spec, weights_u16: dict, chunk_rows: int = 8192, attention_perturbation=None):
+        """``attention_perturbation`` = (rel, seed) is a test hook, off by
+        default: every attention output is multiplied by 1 + rel * N(0, 1)
+        (a seeded stream) before its bf16 rounding.  With rel = 1e-6 it
+        stands for one evaluation of the same definition whose float
+        operations round differently at that single site; the spread of the
+        logits it causes is the noise floor of a model shape."""
         self.spec = spec
+        self._perturb = None
+        if attention_perturbation is not None:
+            rel, seed = attention_perturbation
+            rng = np.random.default_rng(seed)
+            self._perturb = lambda o: o * (1.0 + rel * rng.standard_normal(o.shape))
         self.w = weights_u16
         self.chunk_rows = chunk_rows
         self._vec = {}
@@ -213,7 +226,7 @@ class OracleDecoder:
             K = np.concatenate([cache[i][0], k], axis=0)
             V = np.concatenate([cache[i][1], v], axis=0)
             new_cache.append((K, V))
-            o = attention(q, K, V, positions, window).reshape(n, Hq * hd)
+            o = attention(q, K, V, positions, window, self._perturb).reshape(n, Hq * hd)
             h = round_bf16(self.linear(p + "wo", o))
             if self.sandwich:
                 h = self.rms(h, p + "post_attn_norm")

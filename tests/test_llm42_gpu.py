@@ -13,7 +13,7 @@ import torch
 
 from gpu_util import assert_logits_close, bits, f64, ready
 from invariant_vd_step_gb300 import llm42, synth, vd
-from oracle.decoder import OracleDecoder
+from oracle.fp32 import Fp32Decoder
 
 pytestmark = pytest.mark.gpu
 
@@ -39,7 +39,7 @@ def test_fast_path_logits_meet_the_oracle_tolerance(spec):
     for p in range(30, 40):  # decode steps on the fast path
         m.step(pool, vd.StepBatch([(h[p:p + 1], p, pt)], logit_rows=[0]), lg[p:p + 1])
     torch.cuda.synchronize()
-    ref = OracleDecoder(spec, synth.weights_to_numpy(Wc)).forward_all(h)
+    ref = Fp32Decoder(spec, synth.weights_to_numpy(Wc)).forward_all(h)
     assert_logits_close(f64(lg), ref)
     assert m.device_status() == 0
 

@@ -1,16 +1,18 @@
-"""How far two exact evaluations of the 8B-shaped layer drift apart when they
-disagree by one part in 1e5 at a single point before a bf16 rounding.
+"""How far two exact evaluations of the same definition drift apart at the
+full-size shapes (the noise floor of a shape), measured on the oracles alone.
 
-Every module output is rounded to bf16, so a tiny disagreement flips a few
-roundings; the flips feed the next roundings and the logits of the
-Llama-3.1-8B-shaped layer + LM head (random init, 4000 random cached keys)
-move by up to ~2e-2.  That is the stated GPU-vs-oracle tolerance itself, so
-the full-size GPU check cannot ask more than "within it almost everywhere,
-within twice it everywhere".  This test measures the floor on the oracle
-alone (no GPU) and pins that it is of that size.
+Every module output is rounded to bf16, so a disagreement before one
+rounding flips a few bf16 values, and each flip is fed to the next
+roundings.  At the Llama-3.1-8B-shaped layer + LM head (random init, 4000
+random cached keys) the attention output is the sensitive site: a
+disagreement of one part in 1e6 there (the float64 oracle's test hook),
+already moves the logits by ~4e-3 on average and ~2e-2 at most, the same
+spread that the float32 oracle shows against the float64 one.  A single
+flip at that site fans out into a cascade whose size no longer depends on
+how many flips started it.  The full-size GPU checks use this measured
+floor (tests/test_fullsize_gpu.py); the tests here pin that it is of that
+size.
 """
-
-import math
 
 import numpy as np
 import pytest
@@ -18,6 +20,7 @@ import pytest
 from invariant_vd_step_gb300 import synth
 from oracle import decoder as od
 from oracle.bf16 import round_bf16
+from oracle.fp32 import Fp32Decoder
 
 
 def _weights(spec, **kw):
@@ -30,80 +33,59 @@ def _weights(spec, **kw):
     return synth.weights_to_numpy(W)
 
 
-@pytest.fixture(scope="module")
-def layer():
-    spec = synth.LLAMA8B_1L
-    return spec, od.OracleDecoder(spec, _weights(spec))
+def _cache(spec, c=4000, seed=4):
+    rng = np.random.default_rng(seed)
+    return [(round_bf16(rng.standard_normal((c, spec.n_kv_heads, spec.head_dim))),
+             round_bf16(rng.standard_normal((c, spec.n_kv_heads, spec.head_dim)))) for _ in range(spec.n_layers)]
 
 
-def test_bf16_flip_cascade_reaches_the_stated_tolerance(layer, monkeypatch):
-    spec, dec = layer
-    rng = np.random.default_rng(4)
-    c = 4000
-    K = round_bf16(rng.standard_normal((c, spec.n_kv_heads, spec.head_dim)))
-    V = round_bf16(rng.standard_normal((c, spec.n_kv_heads, spec.head_dim)))
-    ref, _ = dec.step(np.array([1234]), [(K, V)])
-    exact_attention = od.attention
-
-    def perturbed(q, Kf, Vf, positions, window):
-        # the exact attention output, off by 1e-5 relative before its rounding
-        n, Hq, hd = q.shape
-        rep = Hq // Kf.shape[1]
-        out = np.empty((n, Hq, hd))
-        for t in range(n):
-            p = int(positions[t])
-            for h in range(Hq):
-                s = (Kf[:p + 1, h // rep] @ q[t, h]) / math.sqrt(hd)
-                e = np.exp(s - s.max())
-                out[t, h] = (e / e.sum()) @ Vf[:p + 1, h // rep]
-        out *= 1 + 1e-5 * np.random.default_rng(99).standard_normal(out.shape)
-        return round_bf16(out)
-
-    monkeypatch.setattr(od, "attention", perturbed)
-    alt, _ = dec.step(np.array([1234]), [(K, V)])
-    monkeypatch.setattr(od, "attention", exact_attention)
-    d = np.abs(alt - ref)
-    assert 5e-3 < d.max() < 5e-2, d.max()
-
-
-def test_gemma_block_flip_cascade_is_wider(monkeypatch):
-    """The same measurement on the Gemma-3-4B-shaped block (2 layers, one
-    local window-1024 and one global; embedding scale, (1 + w) gains,
-    sandwich norms, vocab 262144).  A single 1e-5 disagreement already puts
-    logits beyond the stated tolerance (17 of 262144 here, against 3 of
-    128256 for the 8B-shaped layer): the same order as all that a 99.99 %
-    criterion allows (26), while the GPU differs from the oracle in many
-    roundings, not one.  That is why the full-size Gemma check asks for
-    99.9 % (and twice the tolerance everywhere)."""
-    spec = synth.GEMMA3_4B.with_(name="gemma3-4b-shape-2layer", n_layers=2, local_global_period=2)
-    dec = od.OracleDecoder(spec, _weights(spec, gain_std=0.1))
-    rng = np.random.default_rng(4)
-    c = 4000
-    cache = [(round_bf16(rng.standard_normal((c, spec.n_kv_heads, spec.head_dim))),
-              round_bf16(rng.standard_normal((c, spec.n_kv_heads, spec.head_dim)))) for _ in range(2)]
-    ref, _ = dec.step(np.array([1234]), cache)
-    exact_attention = od.attention
-
-    def perturbed(q, Kf, Vf, positions, window):
-        n, Hq, hd = q.shape
-        rep = Hq // Kf.shape[1]
-        out = np.empty((n, Hq, hd))
-        for t in range(n):
-            p = int(positions[t])
-            lo = max(0, p - window + 1) if window > 0 else 0
-            for h in range(Hq):
-                s = (Kf[lo:p + 1, h // rep] @ q[t, h]) / math.sqrt(hd)
-                e = np.exp(s - s.max())
-                out[t, h] = (e / e.sum()) @ Vf[lo:p + 1, h // rep]
-        out *= 1 + 1e-5 * np.random.default_rng(99).standard_normal(out.shape)
-        return round_bf16(out)
-
-    monkeypatch.setattr(od, "attention", perturbed)
-    alt, _ = dec.step(np.array([1234]), cache)
-    monkeypatch.setattr(od, "attention", exact_attention)
+def _stats(alt, ref):
     d = np.abs(alt - ref)[0]
     tol = 2e-2 + 1e-2 * np.abs(ref[0])
-    beyond = int((d > tol).sum())
-    assert 1e-2 < d.max() < 5e-2, d.max()
-    assert 0.5e-4 * d.size < beyond < 1e-3 * d.size, beyond
-    assert np.all(d <= 2 * tol)
+    return d.mean(), d.max(), int((d > tol).sum()), bool(np.all(d <= 2 * tol))
+
+
+@pytest.fixture(scope="module")
+def llama_layer():
+    spec = synth.LLAMA8B_1L
+    W = _weights(spec)
+    cache = _cache(spec)
+    ref, _ = od.OracleDecoder(spec, W).step(np.array([1234]), cache)
+    return spec, W, cache, ref
+
+
+def test_one_part_in_1e6_at_the_attention_output_saturates_the_cascade(llama_layer):
+    spec, W, cache, ref = llama_layer
+    alt, _ = od.OracleDecoder(spec, W, attention_perturbation=(1e-6, 99)).step(np.array([1234]), cache)
+    mean, mx, beyond, within2 = _stats(alt, ref)
+    assert 2e-3 < mean < 8e-3, mean
+    assert 5e-3 < mx < 5e-2, mx
+    assert within2
+    # ten times the disagreement does not make a ten times larger cascade
+    alt10, _ = od.OracleDecoder(spec, W, attention_perturbation=(1e-5, 99)).step(np.array([1234]), cache)
+    mean10 = _stats(alt10, ref)[0]
+    assert mean10 < 2.5 * mean, (mean10, mean)
+
+
+def test_the_float32_oracle_sits_on_the_same_floor(llama_layer):
+    spec, W, cache, ref = llama_layer
+    f32, _ = Fp32Decoder(spec, W).step(np.array([1234]), cache)
+    alt, _ = od.OracleDecoder(spec, W, attention_perturbation=(1e-6, 99)).step(np.array([1234]), cache)
+    m32, mp = _stats(f32, ref)[0], _stats(alt, ref)[0]
+    assert 0.5 < m32 / mp < 2.0, (m32, mp)
+
+
+def test_gemma_block_flip_cascade_is_wider():
+    """The same measurement on the Gemma-3-4B-shaped block (2 layers, one
+    local window-1024 and one global; embedding scale, (1 + w) gains,
+    sandwich norms, vocab 262144): a single-site disagreement already puts
+    ~1e-4 of the logits beyond the stated tolerance, all within twice it."""
+    spec = synth.GEMMA3_4B.with_(name="gemma3-4b-shape-2layer", n_layers=2, local_global_period=2)
+    W = _weights(spec, gain_std=0.1)
+    cache = _cache(spec)
+    ref, _ = od.OracleDecoder(spec, W).step(np.array([1234]), cache)
+    alt, _ = od.OracleDecoder(spec, W, attention_perturbation=(1e-5, 99)).step(np.array([1234]), cache)
+    mean, mx, beyond, within2 = _stats(alt, ref)
+    assert 1e-2 < mx < 5e-2, mx
+    assert 0.5e-4 * ref.size < beyond < 1e-3 * ref.size, beyond
+    assert within2

@@ -6,7 +6,7 @@ import torch
 
 from gpu_util import assert_logits_close, bits, f64, ready
 from invariant_vd_step_gb300 import synth, vd
-from oracle.decoder import OracleDecoder
+from oracle.fp32 import Fp32Decoder
 
 pytestmark = pytest.mark.gpu
 
@@ -20,14 +20,22 @@ LLAMA_TINY128 = synth.ModelSpec("llama-tiny-128", 2, 512, 8, 2, 128, 1024, 1024,
 class Runner:
     """Runs teacher-forced schedules of chunks; pages handed out from a permutation."""
 
-    def __init__(self, spec, seed=0, gain_std=0.1, num_pages=256, zero=False, max_tokens=512):
+    def __init__(self, spec, seed=0, gain_std=0.1, num_pages=256, zero=False, max_tokens=512, max_context=1024,
+                 mode="eager"):
         self.spec = spec
         self.Wc = synth.make_weights(spec, seed=seed, gain_std=gain_std, zero=zero)
         self.W = {k: v.cuda() for k, v in self.Wc.items()}
         self.model = vd.Model(spec, self.W, max_tokens=max_tokens, max_seqs=32, max_logit_rows=max_tokens,
-                              max_context=1024)
+                              max_context=max_context)
+        # launch modes that must not change a bit: graph replay of steps,
+        # and decode attention folding all of a row's KV splits in one CTA
+        if "graph" in mode:
+            self.model.set_graph_mode(16)
+        if "fold" in mode:
+            self.model.set_attention_fold(1)
         self.pool = vd.KVPool(self.model, num_pages)
         self.num_pages = num_pages
+        self.logits = torch.empty((max_tokens, spec.vocab), device="cuda")
 
     def execute(self, histories, steps, perm_seed=None):
         """steps: list of lists of (request, n_new_tokens).  Returns {(r, pos): logits bits row}."""
@@ -49,7 +57,9 @@ class Runner:
                 keys += [(r, c + i) for i in range(n)]
                 done[r] = c + n
             T = len(keys)
-            logits = torch.full((T, self.spec.vocab), float("nan"), device="cuda")
+            # one logits buffer for every step: graph replay keys a step on its output address
+            logits = self.logits[:T]
+            logits.fill_(float("nan"))
             self.model.step(self.pool, vd.StepBatch(seqs, logit_rows=range(T)), logits)
             torch.cuda.synchronize()
             for i, k in enumerate(keys):
@@ -58,23 +68,60 @@ class Runner:
         return out
 
     def oracle_all(self, history):
-        return OracleDecoder(self.spec, synth.weights_to_numpy(self.Wc)).forward_all(history)
+        return Fp32Decoder(self.spec, synth.weights_to_numpy(self.Wc)).forward_all(history)
 
 
+MODES = ["eager", "graph", "fold", "graph+fold"]
+
+
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("spec", [synth.TINY, GEMMA_TINY, LLAMA_TINY128], ids=lambda s: s.name)
-def test_step_logits_vs_oracle(spec):
+def test_step_logits_vs_oracle(spec, mode):
     ready()
-    run = Runner(spec, seed=1)
+    run = Runner(spec, seed=1, mode=mode)
     hist = synth.make_prompts(3, 20, 70, spec.vocab, seed=2)
     hist = [np.concatenate([h, synth.make_tokens(5, spec.vocab, seed=10 + i)]) for i, h in enumerate(hist)]
     L = [len(h) for h in hist]
     steps = [[(0, L[0] - 5), (1, 16)], [(1, L[1] - 21), (2, L[2] - 5)]]
     steps += [[(0, 1), (1, 1), (2, 1)] for _ in range(5)]
     res = run.execute(hist, steps, perm_seed=3)
+    if "graph" in mode:
+        assert run.model.graph_stats()["replays"] >= 2
     for r, h in enumerate(hist):
         ref = run.oracle_all(h)
         got = np.stack([f64(res[(r, p)]) for p in range(len(h))])
         assert_logits_close(got, ref)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("spec", [synth.TINY, LLAMA_TINY128, GEMMA_TINY], ids=lambda s: s.name)
+def test_long_context_decode_vs_oracle(spec, mode):
+    """Contexts past one and two 512-key splits (decode rows of several
+    splits, merged in split order or folded in one CTA), prefilled in chunks
+    of up to 512 tokens, then decode steps: every row against the oracle."""
+    ready()
+    run = Runner(spec, seed=2, mode=mode, num_pages=400, max_tokens=1024, max_context=2048)
+    hist = synth.make_prompts(3, 500, 1100, spec.vocab, seed=4)
+    hist = [np.concatenate([h, synth.make_tokens(6, spec.vocab, seed=20 + i)]) for i, h in enumerate(hist)]
+    L = [len(h) for h in hist]
+    steps, done = [], [0, 0, 0]
+    while any(done[r] < L[r] - 6 for r in range(3)):
+        step = []
+        for r in range(3):
+            n = min(L[r] - 6 - done[r], (300, 512, 170)[r])
+            if n > 0:
+                step.append((r, n))
+                done[r] += n
+        steps.append(step)
+    steps += [[(0, 1), (1, 1), (2, 1)] for _ in range(6)]
+    res = run.execute(hist, steps, perm_seed=5)
+    if "graph" in mode:
+        assert run.model.graph_stats()["replays"] >= 1
+    for r, h in enumerate(hist):
+        ref = run.oracle_all(h)
+        tail = range(len(h) - 8, len(h))  # the prompt's last rows and every decode row
+        got = np.stack([f64(res[(r, p)]) for p in tail])
+        assert_logits_close(got, ref[list(tail)])
 
 
 def test_zero_model_gives_zero_logits_bitwise():
