@@ -104,9 +104,14 @@ int vd_op_attention(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b
  *    or models) race on it and must be ordered by the caller;
  *  - nothing in it needs to start at zero (each call writes every partial
  *    it reads), so it is never cleared;
- *  - the first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *  - every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress, a host-side lookup that allocates nothing), so
+ *    a context re-created on the same device (after cudaDeviceReset) gets
+ *    the new address; make the first call on a device before any stream
+ *    capture, as that one also loads the library's module on the device;
+ *  - arguments are validated exactly as vd_op_attention validates them
+ *    (the same error codes for the same batch) before the scratch size is
+ *    checked.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
 #define VD_ATTN_STATIC_SCRATCH_BYTES (16u << 20)
 int vd_op_attention_static(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, const void* q,
@@ -122,6 +127,21 @@ int vd_op_rope_kv(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, 
 /* The sampler's Philox4x32-10 stream: out[i] = word used for vocabulary index
  * i at (seed, step); dev uint32 [n]. */
 int vd_op_philox(uint64_t seed, uint64_t step, int32_t n, uint32_t* out, void* stream);
+
+/* Test of the failure path of every on-device wait (the bounded waits of
+ * the pipelined GEMM and attention kernels; no counterpart in the paper, it
+ * exercises this library's own failure detection).  Launches one CTA whose
+ * two waiting threads wait, with the limit limit_us, on an mbarrier that
+ * nothing completes; nothing else is in flight and no memory but the
+ * model's status word and `out` is touched.  The wait gives up, records
+ * VD_ERR_TIMEOUT in the model's device status word (read and cleared by
+ * vd_device_status) and the kernel returns, so the context stays usable.
+ * While the status word holds the timeout, the step kernels of this model
+ * skip their work (a failed step's outputs are not written); reading the
+ * status clears it.  out (nullable): dev int32 [3], set to 1 for each wait
+ * that gave up (warp 0's, warp 1's, the teardown wait).  limit_us in
+ * [1, 2000000]; errors: VD_ERR_INVALID_ARG. */
+int vd_op_wait_probe(vd_model* m, int32_t limit_us, int32_t* out, void* stream);
 
 #ifdef __cplusplus
 }

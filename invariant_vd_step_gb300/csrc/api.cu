@@ -1378,17 +1378,19 @@ int vd_op_attention(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b
 
 int vd_op_attention_static(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, const void* q,
                            void* out, void* stream) {
-  if (check_model(m) || !p || p->m != m || !q || !out || !b) return fail(VD_ERR_INVALID_ARG, "null argument");
+  if (check_model(m) || !p || p->m != m || !q || !out) return fail(VD_ERR_INVALID_ARG, "null argument");
   if (layer < 0 || layer >= m->cfg.n_layers) return fail(VD_ERR_OUT_OF_RANGE, "layer out of range");
-  if (b->num_tokens < 0 || b->num_seqs < 0 || b->num_tokens > m->cfg.max_tokens || b->num_seqs > m->cfg.max_seqs)
-    return fail(VD_ERR_CAPACITY, "step exceeds max_tokens / max_seqs");
-  if (b->num_tokens == 0) return VD_OK;
-  if (!b->cu_q || !b->cached_len) return fail(VD_ERR_INVALID_ARG, "missing descriptor array");
+  // The descriptor is validated (and uploaded) exactly as vd_op_attention
+  // does it, so both entries give the same error for the same batch; only
+  // then is the scratch the call needs checked against the array.
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Desc d;
+  int rc = upload_desc(m, p, b, false, d, s);
+  if (rc || d.T == 0) return rc;
   // Splits per row stride: the largest split count of any request of the call.
   int splits = 1;
   for (int i = 0; i < b->num_seqs; ++i) {
     const long long kv = static_cast<long long>(b->cached_len[i]) + b->cu_q[i + 1] - b->cu_q[i];
-    if (kv < 1 || kv > m->cfg.max_context) return fail(VD_ERR_INVALID_ARG, "request length out of range");
     splits = std::max(splits, static_cast<int>((kv - 1) / m->split + 1));
   }
   const size_t rows = static_cast<size_t>(b->num_tokens) * m->cfg.n_heads * splits;
@@ -1397,11 +1399,7 @@ int vd_op_attention_static(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_b
     return fail(VD_ERR_CAPACITY, "call needs " + std::to_string(need) + " bytes of split scratch; the static buffer holds " +
                                      std::to_string(kAttnStaticScratchBytes) + " (fewer tokens or shorter contexts per call)");
   void* scratch = nullptr;
-  int rc = attn_static_scratch(&scratch);
-  if (rc) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  Desc d;
-  if ((rc = upload_desc(m, p, b, false, d, s)) || d.T == 0) return rc;
+  if ((rc = attn_static_scratch(&scratch))) return rc;
   float* part_o = static_cast<float*>(scratch);
   float* part_ml = part_o + rows * m->cfg.head_dim;
   return run_attention_static(m, p, layer, d, static_cast<const __nv_bfloat16*>(q),
@@ -1417,6 +1415,13 @@ int vd_op_rope_kv(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, 
   int rc = upload_desc(m, p, b, false, d, s);
   if (rc || d.T == 0) return rc;
   return run_rope(m, p, layer, d, static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(q_out), s);
+}
+
+int vd_op_wait_probe(vd_model* m, int32_t limit_us, int32_t* out, void* stream) {
+  if (check_model(m)) return fail(VD_ERR_INVALID_ARG, "null model");
+  if (limit_us < 1 || limit_us > 2000000) return fail(VD_ERR_INVALID_ARG, "limit_us must be in [1, 2000000]");
+  if (out && !aligned16(out)) return fail(VD_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  return launch_wait_probe(m->status, static_cast<uint64_t>(limit_us) * 1000u, out, static_cast<cudaStream_t>(stream));
 }
 
 int vd_op_philox(uint64_t seed, uint64_t step, int32_t n, uint32_t* out, void* stream) {

@@ -31,8 +31,6 @@
 // sum), every other float operation an explicitly rounded intrinsic.
 #include <math.h>
 
-#include <mutex>
-
 #include "vd_device.cuh"
 #include "vd_internal.h"
 
@@ -159,12 +157,6 @@ __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)
       mma_bf16_16816(st.o[2 * np + 1], pl[ks], b + 2);
     }
   }
-}
-
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > kWaitLimitNs) return;
 }
 
 // NW warps per CTA; groups of DS warps own the same 16 rows and split the
@@ -492,24 +484,15 @@ int launch_attn_t(const CUtensorMap& kvmap, const AttnArgs& a0, int n_items, cud
 static __device__ __align__(256) float g_attn_static_scratch[kAttnStaticScratchBytes / sizeof(float)];
 
 int attn_static_scratch(void** ptr) {
-  // Device address of the array on the current device, looked up once per
-  // device (host code cannot take the address of a __device__ symbol).
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
-  int dev = 0;
-  VD_CUDA_TRY(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) return fail(VD_ERR_UNSUPPORTED, "device ordinal too large");
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
-    if (e != cudaSuccess)
-      return fail(VD_ERR_CUDA, std::string("cudaGetSymbolAddress(static attention scratch): ") +
-                                   cudaGetErrorString(e));
-    addr[dev] = p;
-  }
-  *ptr = addr[dev];
+  // Device address of the array on the current device.  Host code cannot
+  // take the address of a __device__ symbol; the lookup allocates nothing
+  // and is made on every call, so a context re-created on the same device
+  // never gets an address cached from the old one.
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+  if (e != cudaSuccess)
+    return fail(VD_ERR_CUDA, std::string("cudaGetSymbolAddress(static attention scratch): ") + cudaGetErrorString(e));
+  *ptr = p;
   return VD_OK;
 }
 

@@ -355,4 +355,42 @@ int launch_rope_kv(const RopeArgs& a, cudaStream_t s) {
   return VD_OK;
 }
 
+
+// ---------------------------------------------------------------- failure path
+// Drives the bounded waits every pipelined kernel uses to their limit, with
+// nothing in flight: thread 0 of warp 0 and thread 0 of warp 1 wait on an
+// mbarrier that no thread ever arrives at.  The first to reach the limit
+// records VD_ERR_TIMEOUT in the status word and raises the CTA's abort flag,
+// which ends the other wait; then the teardown wait, which ignores the
+// flag, gives up after the limit too, and the kernel returns.  out[0] = 1 if
+// warp 0's wait gave up, out[1] = 1 if warp 1's did, out[2] = 1 if the
+// teardown wait gave up.
+namespace {
+__global__ void wait_probe_kernel(int* status, uint64_t limit_ns, int* out) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    const bool ok = mbar_wait(&bar, 0, &abort_flag, status, limit_ns);
+    if (out) out[warp] = ok ? 0 : 1;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool drained = drain_wait(&bar, 0, limit_ns);
+    if (out) out[2] = drained ? 0 : 1;
+  }
+}
+}  // namespace
+
+int launch_wait_probe(int* status, uint64_t limit_ns, int* out, cudaStream_t s) {
+  VD_CUDA_TRY(launch_k(wait_probe_kernel, dim3(1), dim3(64), 0, s, status, limit_ns, out));
+  return VD_OK;
+}
+
 }  // namespace vd

@@ -61,14 +61,6 @@ __device__ __forceinline__ float gelu_tanh_f(float g) {
   return __fmul_rn(__fmul_rn(0.5f, g), __fadd_rn(1.0f, tanhf(inner)));
 }
 
-// Waits without looking at the abort flag (used only on the teardown path to
-// let copies and MMAs already in flight finish before the CTA exits).
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > kWaitLimitNs) return;
-}
-
 // Epilogue of one tile: accumulator columns [c*32, c*32+32) are tokens
 // t0.. of the tile.  TMEM lane 32*lg + i holds tile row lg*32 + i (BM = 128)
 // or, for i < 16, tile row lg*16 + i (BM = 64).  A 256-row tile is two

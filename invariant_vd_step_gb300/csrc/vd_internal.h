@@ -212,5 +212,6 @@ int launch_sample(const float* logits, int R, int V, const vd_sampler* dev_param
 // Second pass alone: per row, the best of nchunk (score, index) partials.
 int launch_sample_final(const float* part_v, const int* part_i, int R, int nchunk, int* out, cudaStream_t s);
 int launch_philox(uint64_t seed, uint64_t step, int n, uint32_t* out, cudaStream_t s);
+int launch_wait_probe(int* status, uint64_t limit_ns, int* out, cudaStream_t s);
 
 }  // namespace vd

@@ -123,6 +123,7 @@ _SIGS = {
     "vd_op_rope_kv": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
     "vd_op_attention_static": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
     "vd_op_philox": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int32, _VP, _VP]),
+    "vd_op_wait_probe": (ctypes.c_int, [_VP, ctypes.c_int32, _VP, _VP]),
     "vd_engine_create": (ctypes.c_int, [ctypes.POINTER(EngineConfig), ctypes.POINTER(_VP)]),
     "vd_engine_destroy": (None, [_VP]),
     "vd_engine_add_request": (ctypes.c_int, [_VP, _I32P, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64,
@@ -341,6 +342,10 @@ class Model:
     def rope_kv(self, pool, layer, batch: StepBatch, qkv, q_out, stream=None):
         check(lib().vd_op_rope_kv(self.h, pool.h, layer, ctypes.byref(batch.c), _ptr(qkv), _ptr(q_out),
                                   _stream(stream)))
+
+    def wait_probe(self, limit_us: int, out=None, stream=None):
+        """vd_op_wait_probe: one bounded wait that nothing completes (records VD_ERR_TIMEOUT)."""
+        check(lib().vd_op_wait_probe(self.h, int(limit_us), _ptr(out), _stream(stream)))
 
     def device_status(self) -> int:
         return int(lib().vd_device_status(self.h))
