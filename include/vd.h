@@ -233,9 +233,17 @@ int vd_set_graph_mode(vd_model* m, int32_t max_graphs);
  * new (a key is captured the second time it is seen) (host int64 [4]). */
 int vd_graph_stats(const vd_model* m, int64_t* out4);
 
-/* Token choice for R rows of dev float32 logits [R][V] (16-byte aligned) -> dev int32 [R]:
- * greedy argmax (lowest index on ties) or Gumbel-max with Philox4x32-10
- * (per-row state in host array per_row[R]). */
+/* Token choice for R rows of dev float32 logits [R][V] (16-byte aligned) ->
+ * dev int32 [R]: the sampler of the engine-step outputs, whose state is
+ * part of a request's configuration [B §二 Definition 2.1: sampler_0 and the
+ * per-request view (logits, token)], and whose choice is a fixed-order
+ * function of the logits row and that state [B §六 6.3: argmax / sampling
+ * take finite logits].  Temperature 0: greedy argmax, lowest index on ties.
+ * Temperature T > 0: Gumbel-max argmax_i(l_i / T - log(-log(u_i))) with u_i
+ * from Philox4x32-10 (Salmon et al., SC'11) keyed by the row's (seed, step)
+ * (host array per_row[R]; the generator is this library's choice).  The
+ * result depends on the row and its state only, never on R or the other
+ * rows.  Errors: VD_ERR_INVALID_ARG (null or misaligned pointers, R < 0). */
 int vd_sample(vd_model* m, const float* logits, int32_t R, const vd_sampler* per_row,
               int32_t* tokens_out, void* stream);
 
