@@ -18,8 +18,14 @@ token per request.
             feeds the previous step's sampled tokens back, uploads the host
             descriptor and reads the sampled tokens back to the host.
 
+The line also carries: the same step at B = 1 and 64 (``decode_points``),
+an 8192-token prefill step with each GEMM's TFLOP/s (``prefill``), repeated
+K-step windows (``stability``), the 3,200-pair invariance matrix, and the
+C++ oracle timed on the host cores for a sample of one step's rows
+(``cpu_baseline``, with the GPU's parity on those rows).
+
 Usage: python bench.py [--gpus N --steps K --warmup W --batch B]
-       python bench.py --impl reference ...   (the CPU oracle, bounded sample)
+       python bench.py --impl reference ...   (the C++ oracle, bounded sample)
 """
 
 from __future__ import annotations
@@ -288,14 +294,26 @@ def run_gpu(args):
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    windows = []
     with Clocks(local) as clk:
         ev0.record(stream)
         for s in range(Wm, Wm + K):
             one(s)
         ev1.record(stream)
         torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
+        if ws > 1:
+            dist.barrier()
+        # the same K steps again, window after window (each step rewrites its
+        # token's K/V slot with the same value), so that the clock record and
+        # the spread of the step time cover at least 200 steps
+        for _ in range(max(0, -(-200 // K) - 1)):
+            w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w0.record(stream)
+            for s in range(Wm, Wm + K):
+                one(s)
+            w1.record(stream)
+            torch.cuda.synchronize()
+            windows.append(w0.elapsed_time(w1) / K)
     ms = ev0.elapsed_time(ev1)
     graph_stats = model.graph_stats()
     # Per-kernel times: the same K steps again, eager, with events around
@@ -361,6 +379,13 @@ def run_gpu(args):
     e2e_s = time.perf_counter() - t0
     h2d = h2d_bytes(base + E - 1)
     assert len(emitted) == E and model.device_status() == 0
+    # one more decode step, with every row's logits stored, for the CPU
+    # baseline to recompute a sample of its rows (outside the timed region)
+    check_step = base + E
+    check_toks = toks[check_step % len(toks)]
+    model.step(pool, batch_at(check_step, check_toks), logits, stream)
+    torch.cuda.synchronize()
+    check_logits = logits.cpu().numpy()
 
     ms_max, e2e_max, e2e_sync_max = max_over_ranks([ms, e2e_s, e2e_sync_s], ws,
                                                    dev if ws > 1 and dist.get_backend() == "nccl" else "cpu")
@@ -420,8 +445,20 @@ def run_gpu(args):
         line["invariance"] = {"pairs": r.pairs, "bitwise_equal": r.equal, "pass_pct": round(r.pass_pct, 3),
                               "categories": r.categories, "runs": r.runs,
                               "workload": "tiny llama-style decoder, 8 requests, 16 greedy decode steps"}
+    if windows:
+        line["stability"] = {"windows": len(windows) + 1, "steps_per_window": K,
+                             "ms_per_step_median": round(statistics.median([step_ms] + windows), 4),
+                             "ms_per_step_min": round(min([step_ms] + windows), 4),
+                             "ms_per_step_max": round(max([step_ms] + windows), 4),
+                             "note": "value is the first window; the clock record covers all windows"}
+    if not args.no_points:
+        # decode at B = 1 and 64 (same workload, graph replay) and the 8192-token prefill step
+        line["decode_points"] = {str(b): decode_sweep_point(spec, weights, b, K, Wm, args.graphs, dev, hbm)
+                                 for b in (1, 64)}
+        line["prefill"] = prefill_result(dev, 8192, 4, max(5, min(K, 20)), Wm)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(spec, weights, ctx, tables, mem, args.cpu_sample)
+        line["cpu_baseline"] = cpu_baseline(spec, weights, ctx + check_step, tables, mem, check_toks, check_logits,
+                                            args.cpu_sample)
     if args.sweep:
         line["sweep"] = [decode_sweep_point(spec, weights, b, 10, 3, args.graphs, dev, hbm)
                          for b in (1, 2, 4, 8, 16, 32, 64, 128, 256)]
@@ -430,21 +467,14 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def run_prefill(args):
-    """Prefill mode: one step of T new tokens (several requests from an empty
-    cache) through the same layer + LM head; reports prefill tok/s and the
-    GEMMs' TFLOP/s against the measured bf16 tensor peak."""
+def prefill_result(dev, T, nreq, K, Wm):
+    """One prefill step of T new tokens (nreq requests of T / nreq tokens
+    from an empty cache) through the layer + LM head: prefill tok/s and each
+    GEMM's TFLOP/s against the measured bf16 tensor peak (sustained)."""
     import torch
-    import __graft_entry__
-    __graft_entry__.build()
     from invariant_vd_step_gb300 import synth, vd
-    ws, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
     spec = synth.LLAMA8B_1L
-    T, nreq = args.tokens, args.prefill_requests
     per = T // nreq
-    K, Wm = args.steps, args.warmup
     weights = synth.make_weights(spec, seed=0, device=dev)
     model = vd.Model(spec, weights, max_tokens=T, max_seqs=nreq, max_logit_rows=nreq, max_context=per + 16)
     npg = (per + 15) // 16
@@ -458,18 +488,25 @@ def run_prefill(args):
     for _ in range(Wm):
         model.step(pool, b, logits, stream)
     torch.cuda.synchronize()
-    model.profile_collect()
-    model.profile(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
+    with Clocks(dev.index or 0) as clk:
         ev0.record(stream)
         for _ in range(K):
             model.step(pool, b, logits, stream)
         ev1.record(stream)
         torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    # per-kernel times: the same K steps again with events around every kernel class
+    model.profile_collect()
+    model.profile(True)
+    for _ in range(K):
+        model.step(pool, b, logits, stream)
+    torch.cuda.synchronize()
     model.profile(False)
     prof = model.profile_collect()
-    ms = ev0.elapsed_time(ev1)
+    assert model.device_status() == 0
+    pool.close()
+    model.close()
     hbm, tf_burst, peak_kind = load_peaks()
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -481,6 +518,8 @@ def run_prefill(args):
     flops = {"gemm_qkv": 2 * Tt * spec.qkv_dim * d, "gemm_o": 2 * Tt * d * spec.attn_dim,
              "gemm_gate_up": 2 * Tt * 2 * F * d, "gemm_down": 2 * Tt * d * F,
              "gemm_lm_head": 2 * nreq * spec.vocab * d}
+    # causal attention: 4 * Hq * hd flops per visible key (QK^T and PV)
+    flops_attn = 4 * spec.n_heads * spec.head_dim * nreq * per * (per + 1) // 2
     kernels = {}
     for name, (n, nk, tot) in prof.items():
         per_step = tot / K
@@ -488,22 +527,41 @@ def run_prefill(args):
         if name in flops:
             tfs = flops[name] / (per_step * 1e-3) / 1e12
             e.update({"TFLOP_s": round(tfs, 1), "tensor_frac": round(tfs / tf_sust, 4)})
+        if name == "attention":
+            e["TFLOP_s"] = round(flops_attn / (per_step * 1e-3) / 1e12, 1)
         kernels[name] = e
     dom = max((k for k in kernels if k in flops), key=lambda k: kernels[k]["ms_per_step"])
     gemm_ms = sum(kernels[k]["ms_per_step"] for k in kernels if k in flops)
     gemm_tf = sum(flops.values()) / (gemm_ms * 1e-3) / 1e12
-    print(json.dumps({
-        "metric": "prefill tok/s (Llama-8B shape, 1 GB300)", "value": round(Tt * K / (ms * 1e-3), 1),
-        "unit": "tok/s", "n_gpus": 1, "steps": K, "warmup": Wm, "ms_per_step": round(ms / K, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "llama3.1-8b-shape 1 decoder layer + LM head, prefill from an empty cache",
-                   "tokens_per_step": Tt, "requests": nreq, "page_size": 16, "pages": "randomly permuted"},
+    return {
+        "value": round(Tt * K / (ms * 1e-3), 1), "unit": "tok/s", "ms_per_step": round(ms / K, 4), "steps": K,
+        "warmup": Wm, "tokens_per_step": Tt, "requests": nreq,
+        "workload": "llama3.1-8b-shape 1 decoder layer + LM head, prefill from an empty cache",
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": kernels[dom]["TFLOP_s"], "peak": tf_sust,
                      "unit": "TFLOP/s", "frac": kernels[dom]["tensor_frac"], "traffic": None,
                      "peak_source": peak_kind + " (sustained)"},
         "gemms": {"TFLOP_s": round(gemm_tf, 1), "frac_of_sustained": round(gemm_tf / tf_sust, 4),
                   "frac_of_burst": round(gemm_tf / tf_burst, 4)},
-        "kernels": kernels, "clocks": clk.summary()}))
+        "kernels": kernels, "clocks": clk.summary()}
+
+
+def run_prefill(args):
+    """Prefill mode: one step of --tokens new tokens (--prefill-requests
+    requests from an empty cache) through the same layer + LM head."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    r = prefill_result(dev, args.tokens, args.prefill_requests, args.steps, args.warmup)
+    print(json.dumps({
+        "metric": "prefill tok/s (Llama-8B shape, 1 GB300)", "value": r["value"], "unit": "tok/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": r["workload"], "tokens_per_step": r["tokens_per_step"], "requests": r["requests"],
+                   "page_size": 16, "pages": "randomly permuted"},
+        "roofline": r["roofline"], "gemms": r["gemms"], "kernels": r["kernels"], "clocks": r["clocks"]}))
 
 
 def step_roofline_s(spec, seqs, R, hbm_gbs, tf_peak):
@@ -711,23 +769,35 @@ def run_llm42(args):
     }))
 
 
-def oracle_decode_sample(spec, weights_np, caches, toks):
-    """The oracle's decode step for each request over its cached K/V."""
-    from oracle.decoder import OracleDecoder
-    dec = OracleDecoder(spec, weights_np)
+def oracle_decode_rows(spec, weights_np, caches, toks, threads):
+    """The C++ oracle's decode step for each request over its cached K/V."""
+    from oracle.fp32 import Fp32Decoder
+    dec = Fp32Decoder(spec, weights_np, threads=threads)
     return [dec.step(np.array([toks[r]]), cache)[0][0] for r, cache in enumerate(caches)]
 
 
 def cache_from_pages(spec, pages_u16, c):
-    """pages_u16: [layers][n_pages][2][Hkv][16][hd] uint16 -> per-layer (K, V) float64 [c][Hkv][hd]."""
-    from oracle.bf16 import bits_to_f64
-    cache = []
+    """pages_u16: [layers][n_pages][2][Hkv][16][hd] -> the oracle's cache of positions [0, c)."""
+    from oracle.fp32 import KVCache
+    kv = []
     for layer in range(spec.n_layers):
-        kv = pages_u16[layer]
-        k = kv[:, 0].transpose(0, 2, 1, 3).reshape(-1, spec.n_kv_heads, spec.head_dim)[:c]
-        v = kv[:, 1].transpose(0, 2, 1, 3).reshape(-1, spec.n_kv_heads, spec.head_dim)[:c]
-        cache.append((bits_to_f64(k), bits_to_f64(v)))
-    return cache
+        p = pages_u16[layer]
+        k = p[:, 0].transpose(0, 2, 1, 3).reshape(-1, spec.n_kv_heads, spec.head_dim)[:c]
+        v = p[:, 1].transpose(0, 2, 1, 3).reshape(-1, spec.n_kv_heads, spec.head_dim)[:c]
+        kv.append((k, v))
+    return KVCache.from_bits(kv)
+
+
+def literal_stats(got, ref):
+    """The stated tolerance read literally (max-abs 2e-2 and max-rel 1e-2,
+    each on its own) and combined as allclose combines them."""
+    d, a = np.abs(got - ref), np.abs(ref)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        rel = np.where(a > 0, d / a, np.where(d > 0, np.inf, 0.0))
+    return {"logits": int(d.size), "max_abs": float(d.max()), "max_rel": float(rel.max()),
+            "beyond_abs": int((d > 2e-2).sum()), "beyond_rel": int((d > 1e-2 * a).sum()),
+            "beyond_combined": int((d > 2e-2 + 1e-2 * a).sum()),
+            "beyond_twice_combined": int((d > 2 * (2e-2 + 1e-2 * a)).sum()), "mean_abs": float(d.mean())}
 
 
 def cpu_model() -> str:
@@ -749,26 +819,40 @@ def cpu_model() -> str:
     return platform.machine() or "unknown"
 
 
-def cpu_baseline(spec, weights, ctx, tables, mem, n_req):
-    """Times the oracle (as it stands) on this host for a bounded sample."""
+def cpu_baseline(spec, weights, ctx_now, tables, mem, toks, gpu_logits, n_req):
+    """Times the C++ oracle (as it stands) on this host's cores for a bounded
+    sample of one decode step of the same workload: n_req rows spread over
+    the context range on all cores, and 2 of them on one core.  The rows are
+    the ones the GPU computed in its last (untimed) step, so the oracle's
+    logits also give that step's parity against the stated tolerance."""
     from invariant_vd_step_gb300 import synth
     import torch
     w_np = synth.weights_to_numpy(weights)
     pool = mem.view(torch.int16)[: spec.n_layers * (mem.numel() // 2 // spec.n_layers)]
     pool = pool.view(spec.n_layers, -1, 2, spec.n_kv_heads, 16, spec.head_dim)
+    order = np.argsort(ctx_now, kind="stable")
+    rows = sorted({int(order[int(round(x))]) for x in np.linspace(0, len(ctx_now) - 1, n_req)})
     caches = []
-    for r in range(n_req):
-        c = int(ctx[r])
+    for r in rows:
+        c = int(ctx_now[r])
         idx = torch.as_tensor(tables[r][:(c + 15) // 16], dtype=torch.long, device=mem.device)
-        pages = pool[:, idx].cpu().numpy().view(np.uint16)
-        caches.append(cache_from_pages(spec, pages, c))
-    toks = synth.make_tokens(n_req, spec.vocab, seed=9)
+        caches.append(cache_from_pages(spec, pool[:, idx].cpu().numpy().view(np.uint16), c))
+    cores = os.cpu_count() or 1
+    sel = [toks[r] for r in rows]
     t0 = time.perf_counter()
-    oracle_decode_sample(spec, w_np, caches, toks)
-    dt = time.perf_counter() - t0
-    return {"value": round(n_req / dt, 4), "unit": UNIT, "cores": os.cpu_count(), "cpu": cpu_model(), "kind": "oracle",
-            "sample": f"{n_req} decode rows of the same workload (1 layer + LM head, float64 numpy), "
-                      f"{dt:.1f} s"}
+    refs = oracle_decode_rows(spec, w_np, caches, sel, cores)
+    dt_all = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle_decode_rows(spec, w_np, caches[:2], sel[:2], 1)
+    dt_one = time.perf_counter() - t0
+    par = literal_stats(np.stack([gpu_logits[r].astype(np.float64) for r in rows]), np.stack(refs))
+    return {"value": round(len(rows) / dt_all, 4), "unit": UNIT, "cores": cores, "cpu": cpu_model(), "kind": "oracle",
+            "single_thread": {"value": round(2 / dt_one, 4), "unit": UNIT, "cores": 1},
+            "sample": f"{len(rows)} decode rows of the same workload (1 layer + LM head, C++ float32 oracle) on "
+                      f"{cores} threads in {dt_all:.1f} s; 2 of them on 1 thread in {dt_one:.1f} s",
+            "parity_vs_gpu": dict(par, rows=len(rows),
+                                  note="the GPU's logits of these rows against the oracle's, at the stated "
+                                       "tolerance (max-abs 2e-2, max-rel 1e-2)")}
 
 
 def run_reference(args):
@@ -776,7 +860,6 @@ def run_reference(args):
     if rank != 0:
         return
     from invariant_vd_step_gb300 import synth
-    from oracle.bf16 import f64_to_bits
     B = args.batch
     spec, ctx, tables, num_pages = make_workload(B, 4)
     weights = synth.make_weights(spec, seed=0)
@@ -787,23 +870,26 @@ def run_reference(args):
     for r in range(n_req):  # seeded N(0,1) bf16 cached K/V of the sampled requests
         c = int(ctx[r])
         shape = (spec.n_layers, (c + 15) // 16, 2, spec.n_kv_heads, 16, spec.head_dim)
-        caches.append(cache_from_pages(spec, f64_to_bits(rng.standard_normal(shape)), c))
+        import torch
+        vals = torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.bfloat16)
+        caches.append(cache_from_pages(spec, synth.bf16_to_u16(vals), c))
     toks = synth.make_tokens(n_req, spec.vocab, seed=9)
+    cores = os.cpu_count() or 1
     for _ in range(args.warmup):
-        oracle_decode_sample(spec, w_np, caches[:1], toks)
+        oracle_decode_rows(spec, w_np, caches[:1], toks, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_decode_sample(spec, w_np, caches, toks)
+        oracle_decode_rows(spec, w_np, caches, toks, cores)
     dt = time.perf_counter() - t0
     v = round(n_req * args.steps / dt, 4)
-    sample = f"{n_req} of the {B} decode rows per step (1 layer + LM head, float64 numpy)"
+    sample = f"{n_req} of the {B} decode rows per step (1 layer + LM head, C++ float32 oracle, {cores} threads)"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "llama3.1-8b-shape 1 decoder layer + LM head, pure decode", "batch": B,
                    "ctx": f"U[{CTX_LO},{CTX_HI}]", "page_size": 16},
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "cpu": cpu_model(), "kind": "oracle",
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "cpu": cpu_model(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -818,7 +904,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--graphs", type=int, default=64,
                     help="decode: keep up to N captured step graphs (0 = eager launches)")
-    ap.add_argument("--cpu-sample", type=int, default=6)
+    ap.add_argument("--cpu-sample", type=int, default=8)
+    ap.add_argument("--no-points", action="store_true", help="decode: leave out the B = 1 / 64 points and the prefill step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-invariance", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="decode: add the batch sweep 1..256 to the line")
@@ -843,7 +930,6 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
-        args.cpu_sample = min(args.cpu_sample, 2)
         run_reference(args)
     elif args.mode == "prefill":
         run_prefill(args)
