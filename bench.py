@@ -564,6 +564,106 @@ def run_prefill(args):
         "roofline": r["roofline"], "gemms": r["gemms"], "kernels": r["kernels"], "clocks": r["clocks"]}))
 
 
+def run_ceiling(args):
+    """Ceiling mode: for each GEMM of the decode step (the Llama-3.1-8B-shaped
+    layer + LM head) at B tokens, the time of one launch, replayed from a CUDA
+    graph over copies of the weight matrix that together exceed L2, of
+    (a) the plan's weight copies alone (vd_op_tma_stream), (b) the plan's
+    weight and activation copies, (c) the same weight bytes over every SM
+    (K cut into parts), and (d) the GEMM itself with that plan; each as
+    weight GB/s and a fraction of the measured HBM peak."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from invariant_vd_step_gb300 import synth, vd
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm, _, peak_kind = load_peaks()
+    spec = synth.LLAMA8B_1L
+    d, F = spec.d_model, spec.ffn_dim
+    glu = vd.EPI_SWIGLU
+    gemms = [("gemm_qkv", spec.qkv_dim, d, vd.EPI_BF16), ("gemm_o", d, spec.attn_dim, vd.EPI_RESIDUAL),
+             ("gemm_gate_up", F, d, glu), ("gemm_down", d, F, vd.EPI_RESIDUAL),
+             ("gemm_lm_head", spec.vocab, d, vd.EPI_F32)]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rows_out = []
+
+    def timed(fn, n):
+        for i in range(n):  # warm-up (first launches set attributes; nothing is captured yet)
+            fn(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream()
+        with torch.cuda.graph(g, stream=cs):
+            for i in range(n):
+                fn(i)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (3 * n)
+
+    for T in [int(t) for t in args.ceiling_batches.split(",")]:
+        for name, N, K, epi in gemms:
+            rows = 2 * N if epi == glu else N
+            wbytes = rows * K * 2
+            copies = max(1, -(-400_000_000 // wbytes))  # together past L2 (129 MB)
+            Ws = [synth.make_normal_bf16((rows, K), seed=10 + i, std=0.02).to(dev) for i in range(copies)]
+            bucket = 1
+            while bucket < T:
+                bucket <<= 1
+            X = synth.make_normal_bf16((bucket, K), seed=3).to(dev)
+            bm, bn, kpo = vd.gemm_plan(T, N, K, epi)
+            xrows = min(bn, bucket)
+            out_dt = torch.float32 if epi == vd.EPI_F32 else torch.bfloat16
+            C = torch.empty((T, N), dtype=out_dt, device=dev)
+            Xt = X[:T].contiguous()
+            R = torch.zeros((T, N), dtype=torch.bfloat16, device=dev) if epi == vd.EPI_RESIDUAL else None
+            kparts = 1
+            while (rows // bm) * kparts * 2 <= sms and (K // 64) % (kpo * kparts * 2) == 0:
+                kparts *= 2
+            n = max(4, copies)
+            t_w = timed(lambda i: vd.tma_stream(Ws[i % copies], bm, kpo), n)
+            t_wx = timed(lambda i: vd.tma_stream(Ws[i % copies], bm, kpo, X, xrows), n)
+            t_all = timed(lambda i: vd.tma_stream(Ws[i % copies], bm, kpo, k_parts=kparts), n)
+            t_g = timed(lambda i: vd.gemm(Xt, Ws[i % copies], C, epi, R), n)
+            row = {"gemm": name, "tokens": T, "weight_MB": round(wbytes / 1e6, 1), "plan_bm_bn_kpo": [bm, bn, kpo],
+                   "row_tiles": rows // bm}
+            if args.ceiling_sweep:  # the GEMM under every forced plan the matrix allows
+                sweep = {}
+                for fbm in (64, 128, 256):
+                    for fbn in (16, 32, 64, 128, 256):
+                        for fk in (1, 2, 4):
+                            if rows % fbm or (K // 64) % fk or (fbm == 256 and fk > 1) or fbn > max(16, bucket):
+                                continue
+                            vd.set_gemm_plan(fbm, fbn, fk)
+                            try:
+                                if tuple(vd.gemm_plan(T, N, K, epi)) != (fbm, fbn, fk):
+                                    continue
+                                sweep[f"{fbm}x{fbn}x{fk}"] = round(timed(lambda i: vd.gemm(Xt, Ws[i % copies], C, epi, R), n) * 1e3, 2)
+                            finally:
+                                vd.set_gemm_plan(0, 0, 0)
+                best = min(sweep, key=sweep.get)
+                row["plan_sweep_us"] = sweep
+                row["best_plan"] = {"plan": best, "us": sweep[best]}
+            for tag, t in (("stream_plan", t_w), ("stream_plan_with_activations", t_wx),
+                           (f"stream_all_sms_k{kparts}", t_all), ("gemm_launch", t_g)):
+                gbs = wbytes / (t * 1e-3) / 1e9
+                row[tag] = {"us": round(t * 1e3, 2), "GB_s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
+            rows_out.append(row)
+            del Ws, X, C, Xt, R
+            torch.cuda.empty_cache()
+    print(json.dumps({"metric": "decode GEMM weight-stream ceilings (Llama-8B shape, 1 GB300)", "unit": "GB/s",
+                      "peak": hbm, "peak_source": peak_kind, "launch": "one launch per graph node, replayed",
+                      "l2": "weight copies rotated, together > 400 MB", "rows": rows_out}))
+
+
 def step_roofline_s(spec, seqs, R, hbm_gbs, tf_peak):
     """Roofline time of one engine step: max(algorithmic bytes / HBM, flops / tensor peak).
 
@@ -913,7 +1013,9 @@ def main():
     ap.add_argument("--attention-fold", type=int, default=0, choices=[0, 1, 2],
                     help="decode attention mapping: 0 default (one CTA per split), 1 fold splits in one CTA, 2 split")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "serve", "llm42"])
+    ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "serve", "llm42", "ceiling"])
+    ap.add_argument("--ceiling-batches", default="1,256", help="ceiling mode: token counts")
+    ap.add_argument("--ceiling-sweep", action="store_true", help="ceiling mode: also time every forced GEMM plan")
     ap.add_argument("--window", type=int, default=8, help="llm42 mode: verification window")
     ap.add_argument("--new-tokens", type=int, default=64, help="llm42 mode: tokens per request")
     ap.add_argument("--workload", default="c3", choices=["c3", "c5"], help="serve mode workload")
@@ -937,6 +1039,8 @@ def main():
         run_serve(args)
     elif args.mode == "llm42":
         run_llm42(args)
+    elif args.mode == "ceiling":
+        run_ceiling(args)
     else:
         run_gpu(args)
 

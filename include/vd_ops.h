@@ -128,6 +128,22 @@ int vd_op_rope_kv(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, 
  * i at (seed, step); dev uint32 [n]. */
 int vd_op_philox(uint64_t seed, uint64_t step, int32_t n, uint32_t* out, void* stream);
 
+/* Measurement op (no counterpart in the paper; the yardstick of the decode
+ * GEMMs): streams the dev bf16 matrix w [rows][K] from HBM through shared
+ * memory with exactly the weight copies a GEMM launch with plan (box_rows,
+ * kpo) issues -- 3-D TMA boxes of box_rows rows x kpo K blocks of 64, into
+ * the GEMM's 200 KB ring, in its tile order -- and, if x_box_rows > 0, its
+ * activation copies of x_box_rows rows of the dev bf16 x [x_rows][K] per K
+ * block.  Nothing is computed or written; one launch's time is the rate a
+ * weight stream of that size and copy shape reaches in one launch.
+ * k_parts > 1 cuts each row block's K into that many tiles (the same bytes
+ * over more CTAs than a GEMM's row tiles allow).
+ * box_rows in {64, 128, 256} dividing rows; kpo in {1, 2, 4} dividing K/64
+ * (1 for 256-row boxes); ctas = 0: one CTA per SM.  Every on-device wait
+ * is bounded.  Errors: VD_ERR_INVALID_ARG. */
+int vd_op_tma_stream(const void* w, int64_t rows, int64_t K, const void* x, int64_t x_rows, int32_t box_rows,
+                     int32_t kpo, int32_t x_box_rows, int32_t k_parts, int32_t ctas, void* stream);
+
 /* Test of the failure path of every on-device wait (the bounded waits of
  * the pipelined GEMM and attention kernels; no counterpart in the paper, it
  * exercises this library's own failure detection).  Launches one CTA whose

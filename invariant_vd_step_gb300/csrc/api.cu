@@ -1417,6 +1417,32 @@ int vd_op_rope_kv(vd_model* m, vd_kv_pool* p, int32_t layer, const vd_batch* b, 
   return run_rope(m, p, layer, d, static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(q_out), s);
 }
 
+int vd_op_tma_stream(const void* w, int64_t rows, int64_t K, const void* x, int64_t x_rows, int32_t box_rows,
+                     int32_t kpo, int32_t x_box_rows, int32_t k_parts, int32_t ctas, void* stream) {
+  if (!w || (x_box_rows > 0 && !x)) return fail(VD_ERR_INVALID_ARG, "null pointer");
+  if (rows < 1 || K < kGemmBK || K % kGemmBK || rows > (1ll << 31) || K > (1ll << 31))
+    return fail(VD_ERR_INVALID_ARG, "rows >= 1, K a positive multiple of 64");
+  if ((box_rows != 64 && box_rows != 128 && box_rows != 256) || rows % box_rows)
+    return fail(VD_ERR_INVALID_ARG, "box_rows in {64, 128, 256}, dividing rows");
+  if ((kpo != 1 && kpo != 2 && kpo != 4) || (K / kGemmBK) % kpo || (box_rows == 256 && kpo != 1))
+    return fail(VD_ERR_INVALID_ARG, "kpo in {1, 2, 4} dividing the K blocks (1 for 256-row boxes)");
+  if (x_box_rows < 0 || x_box_rows > kGemmBN || (x_box_rows > 0 && (x_rows < x_box_rows)))
+    return fail(VD_ERR_INVALID_ARG, "x_box_rows in [0, 256] and at most x_rows");
+  if (ctas < 0) return fail(VD_ERR_INVALID_ARG, "ctas >= 0");
+  if (k_parts < 1 || (K / kGemmBK) % (static_cast<int64_t>(kpo) * k_parts))
+    return fail(VD_ERR_INVALID_ARG, "k_parts >= 1 with kpo * k_parts dividing the K blocks");
+  if (!aligned16(w) || (x_box_rows > 0 && !aligned16(x))) return fail(VD_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  WeightMaps wm;
+  int rc;
+  if ((rc = make_weight_maps(&wm, w, static_cast<uint64_t>(rows), static_cast<uint64_t>(K), false))) return rc;
+  CUtensorMap xm{};
+  if (x_box_rows > 0 && (rc = make_map_2d(&xm, x, x_rows, K, x_box_rows))) return rc;
+  const int ki = kpo == 1 ? 0 : kpo == 2 ? 1 : 2;
+  const CUtensorMap& m = wm.m[box_rows == 128 ? 0 : box_rows == 64 ? 1 : 2][ki];
+  return launch_tma_stream(m, xm, static_cast<int>(rows), static_cast<int>(K), box_rows, kpo, x_box_rows, k_parts,
+                           ctas, op_status(), static_cast<cudaStream_t>(stream));
+}
+
 int vd_op_wait_probe(vd_model* m, int32_t limit_us, int32_t* out, void* stream) {
   if (check_model(m)) return fail(VD_ERR_INVALID_ARG, "null model");
   if (limit_us < 1 || limit_us > 2000000) return fail(VD_ERR_INVALID_ARG, "limit_us must be in [1, 2000000]");

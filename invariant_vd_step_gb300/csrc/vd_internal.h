@@ -213,5 +213,10 @@ int launch_sample(const float* logits, int R, int V, const vd_sampler* dev_param
 int launch_sample_final(const float* part_v, const int* part_i, int R, int nchunk, int* out, cudaStream_t s);
 int launch_philox(uint64_t seed, uint64_t step, int n, uint32_t* out, cudaStream_t s);
 int launch_wait_probe(int* status, uint64_t limit_ns, int* out, cudaStream_t s);
+// Streams a [rows][K] bf16 weight matrix through shared memory with a GEMM
+// plan's weight copies (and, if x_box_rows > 0, its activation copies); no
+// arithmetic.  ctas = 0: one CTA per SM (at most one per tile).
+int launch_tma_stream(const CUtensorMap& wmap, const CUtensorMap& xmap, int rows, int K, int box_rows, int kpo,
+                      int x_box_rows, int k_parts, int ctas, int* status, cudaStream_t s);
 
 }  // namespace vd

@@ -124,6 +124,8 @@ _SIGS = {
     "vd_op_attention_static": (ctypes.c_int, [_VP, _VP, ctypes.c_int32, ctypes.POINTER(Batch), _VP, _VP, _VP]),
     "vd_op_philox": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int32, _VP, _VP]),
     "vd_op_wait_probe": (ctypes.c_int, [_VP, ctypes.c_int32, _VP, _VP]),
+    "vd_op_tma_stream": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_int64, _VP, ctypes.c_int64, ctypes.c_int32,
+                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _VP]),
     "vd_engine_create": (ctypes.c_int, [ctypes.POINTER(EngineConfig), ctypes.POINTER(_VP)]),
     "vd_engine_destroy": (None, [_VP]),
     "vd_engine_add_request": (ctypes.c_int, [_VP, _I32P, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64,
@@ -430,6 +432,14 @@ def gemm_plan(T, N, K, epilogue=EPI_BF16):
     out = (ctypes.c_int32 * 3)()
     check(lib().vd_gemm_plan_query(T, N, K, epilogue, out))
     return tuple(out)
+
+
+def tma_stream(w, box_rows, kpo, x=None, x_box_rows=0, k_parts=1, ctas=0, stream=None):
+    """vd_op_tma_stream: stream the bf16 matrix w [rows][K] through shared memory with a GEMM plan's copies."""
+    rows, K = w.shape
+    x_rows = x.shape[0] if x is not None else 0
+    check(lib().vd_op_tma_stream(_ptr(w), rows, K, _ptr(x), x_rows, box_rows, kpo, x_box_rows, k_parts, ctas,
+                                 _stream(stream)))
 
 
 def rmsnorm(x, w, y, eps, stream=None):

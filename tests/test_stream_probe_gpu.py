@@ -1,0 +1,36 @@
+"""The weight-stream measurement op (vd_op_tma_stream): it runs every copy
+shape the GEMM plans use, with and without activation copies and K parts,
+leaves the device status clean, and rejects shapes the GEMM cannot take."""
+
+import pytest
+import torch
+
+from gpu_util import ready
+from invariant_vd_step_gb300 import synth, vd
+
+pytestmark = pytest.mark.gpu
+
+
+def test_stream_runs_every_plan_copy_shape():
+    ready()
+    W = synth.make_normal_bf16((512, 1024), seed=1).cuda()
+    X = synth.make_normal_bf16((256, 1024), seed=2).cuda()
+    for bm, kpo in ((64, 1), (64, 4), (128, 2), (128, 4), (256, 1)):
+        for xr in (0, 1, 16, 256):
+            for kp in (1, 2):
+                vd.tma_stream(W, bm, kpo, X if xr else None, xr, k_parts=kp)
+    torch.cuda.synchronize()
+    # the ops' status word is checked through a GEMM that must still run in full
+    C = torch.full((3, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vd.gemm(X[:3].contiguous(), W[:128].contiguous(), C)
+    torch.cuda.synchronize()
+    assert not torch.isnan(C.float()).any()
+
+
+def test_stream_rejects_shapes_no_plan_has():
+    ready()
+    W = synth.make_normal_bf16((192, 1024), seed=1).cuda()
+    for bm, kpo, kp in ((128, 2, 1), (96, 1, 1), (64, 3, 1), (256, 2, 1), (64, 4, 5)):
+        with pytest.raises(vd.VDError) as e:
+            vd.tma_stream(W, bm, kpo, k_parts=kp)
+        assert e.value.code == vd.VD_ERR_INVALID_ARG
