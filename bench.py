@@ -609,8 +609,11 @@ def run_ceiling(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / (3 * n)
 
+    only = set(args.ceiling_gemms.split(",")) if args.ceiling_gemms else None
     for T in [int(t) for t in args.ceiling_batches.split(",")]:
         for name, N, K, epi in gemms:
+            if only and name not in only:
+                continue
             rows = 2 * N if epi == glu else N
             wbytes = rows * K * 2
             copies = max(1, -(-400_000_000 // wbytes))  # together past L2 (129 MB)
@@ -1016,6 +1019,7 @@ def main():
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "serve", "llm42", "ceiling"])
     ap.add_argument("--ceiling-batches", default="1,256", help="ceiling mode: token counts")
     ap.add_argument("--ceiling-sweep", action="store_true", help="ceiling mode: also time every forced GEMM plan")
+    ap.add_argument("--ceiling-gemms", default="", help="ceiling mode: only these GEMMs (comma-separated names)")
     ap.add_argument("--window", type=int, default=8, help="llm42 mode: verification window")
     ap.add_argument("--new-tokens", type=int, default=64, help="llm42 mode: tokens per request")
     ap.add_argument("--workload", default="c3", choices=["c3", "c5"], help="serve mode workload")
