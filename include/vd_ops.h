@@ -65,6 +65,19 @@ int vd_set_gemm_plan(int32_t bm, int32_t bn, int32_t kpo);
  * work (it reads the device's SM count).  Errors: VD_ERR_INVALID_ARG. */
 int vd_gemm_plan_query(int32_t T, int32_t N, int32_t K, int32_t epilogue, int32_t out[3]);
 
+/* The GEMM's tile shape (weight rows and tokens per tile) is chosen per
+ * launch because the tensor cores compute each output element the same way
+ * whatever the MMA instruction's M and N -- a property of the hardware that
+ * was measured, not documented [B §六 6.1 asks for one reduction order per
+ * element, which the K order alone fixes].  vd_create_model therefore runs,
+ * once per device, every tile shape on seeded operands and compares the raw
+ * fp32 results bit for bit.  Returns 1 if they all agreed (shapes stay
+ * chosen per launch), 0 if any bit differed (every later launch takes one
+ * fixed shape, 128 rows x 256 tokens x 1 K block per copy), -1 if the check
+ * could not run.  Runs the check on the current device if no model did yet
+ * (launches kernels and synchronises the device). */
+int vd_gemm_shape_check(void);
+
 /* Batch-invariant RMSNorm [T technical: batch-invariant RMSNorm]:
  * y[r] = bf16(x[r] / sqrt(mean(x[r]^2) + eps) * w), one warp per row, fixed
  * lane-strided sum of squares and fixed butterfly.  x, y: dev bf16 [rows][d],

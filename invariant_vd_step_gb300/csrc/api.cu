@@ -1020,6 +1020,8 @@ int vd_create_model(const vd_model_config* cfg, const vd_weight_ptrs* w, vd_mode
       cudaEventCreateWithFlags(&m->samp_ev, cudaEventDisableTiming) != cudaSuccess)
     return bail(fail(VD_ERR_CUDA, "pinned sampler buffer"));
   VD_CUDA_TRY(cudaDeviceSynchronize());
+  int shapes_ok = 0;
+  if ((rc = gemm_shapes_self_check(&shapes_ok))) return bail(rc);
   *out = m;
   return VD_OK;
 }
@@ -1332,6 +1334,13 @@ int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int3
   g.glu_up_row = N;
   g.status = op_status();
   return launch_gemm(wm, xv, g, epilogue, static_cast<cudaStream_t>(stream));
+}
+
+int vd_gemm_shape_check(void) {
+  int dev = 0, r = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (gemm_shapes_self_check(&r) != VD_OK) return -1;
+  return r;
 }
 
 int vd_gemm_plan_query(int32_t T, int32_t N, int32_t K, int32_t epilogue, int32_t out[3]) {

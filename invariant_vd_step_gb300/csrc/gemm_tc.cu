@@ -37,6 +37,9 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "vd_device.cuh"
 #include "vd_internal.h"
@@ -483,7 +486,15 @@ double plan_cost(int bm, int bn, int kpo, int T, int rows, int K, int ks) {
 
 }  // namespace
 
+namespace {
+// Set when the shape self-check saw two tile shapes give different bits:
+// every later launch then takes the one fixed shape below.
+std::atomic<bool> g_shapes_pinned{false};
+constexpr GemmPlan kPinnedPlan{128, 256, 1};
+}  // namespace
+
 GemmPlan gemm_plan(const WeightMaps& w, int T, int epi, int k_splits) {
+  if (g_shapes_pinned.load() && k_splits == 1) return kPinnedPlan;
   const int KB = w.K / kGemmBK;
   const bool bm64_ok = epi != EPI_F32_SAMPLE && w.rows % 64 == 0 && (!w.glu || (w.rows / 2) % 32 == 0);
   int top = 16;  // no wider token tile than the activation bucket needs
@@ -549,14 +560,16 @@ int launch_splitk_reduce(const float* part, int k_splits, int T, int N, int epi,
   return VD_OK;
 }
 
-int launch_gemm(const WeightMaps& w, const ActMaps& x, const GemmArgs& a0, int epi, cudaStream_t s) {
+namespace {
+int launch_gemm_plan(const WeightMaps& w, const ActMaps& x, const GemmArgs& a0, int epi, const GemmPlan* plan,
+                     cudaStream_t s) {
   if (a0.T <= 0) return VD_OK;
   GemmArgs a = a0;
   if (a.k_splits < 1) a.k_splits = 1;
   if ((a.k_splits > 1) != (epi == EPI_PARTIAL) || a.k_splits > a.K / kGemmBK)
     return fail(VD_ERR_INVALID_ARG, "K splits need the partial epilogue and at most one split per K block");
   if (a.K != w.K || x.rows < 1 || !x.maps) return fail(VD_ERR_INVALID_ARG, "GEMM operand shapes");
-  const GemmPlan p = gemm_plan(w, a.T, epi, a.k_splits);
+  const GemmPlan p = plan ? *plan : gemm_plan(w, a.T, epi, a.k_splits);
   a.bm = p.bm;
   a.bn = p.bn;
   a.kpo = p.kpo;
@@ -578,6 +591,100 @@ int launch_gemm(const WeightMaps& w, const ActMaps& x, const GemmArgs& a0, int e
     case EPI_GEGLU: return launch_one<EPI_GEGLU>(wm, xm, a, s);
     default: return fail(VD_ERR_INVALID_ARG, "unknown GEMM epilogue");
   }
+}
+
+// Seeded bf16 test operands in [-2, 2): a 32-bit integer hash of the index.
+__global__ void fill_probe_kernel(__nv_bfloat16* p, int n, uint32_t seed) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  uint32_t h = static_cast<uint32_t>(i) * 0x9E3779B1u ^ seed;
+  h ^= h >> 15;
+  h *= 0x2C1B3C6Du;
+  h ^= h >> 12;
+  h *= 0x297A2D39u;
+  h ^= h >> 15;
+  p[i] = __float2bfloat16_rn(static_cast<float>(static_cast<int>(h >> 8) - (1 << 23)) * (2.0f / (1 << 23)));
+}
+}  // namespace
+
+int launch_gemm(const WeightMaps& w, const ActMaps& x, const GemmArgs& a0, int epi, cudaStream_t s) {
+  return launch_gemm_plan(w, x, a0, epi, nullptr, s);
+}
+
+int gemm_shapes_self_check(int* result) {
+  // The tile shape is chosen per launch because tcgen05.mma computes an
+  // element of D the same way whatever the instruction's M and N: a
+  // property of the hardware, measured, not documented.  Once per device,
+  // before any step runs, compare the raw fp32 accumulators of every tile
+  // shape on seeded operands (40 tokens, 256 rows, K = 512: several token
+  // tiles at every width, a ragged last one); if any bit differs, pin every
+  // later launch to one fixed shape.
+  constexpr int kMaxDev = 64, T = 40, N = 256, K = 512;
+  static std::mutex mu;
+  static int state[kMaxDev];
+  static bool init = false;
+  int dev = 0;
+  VD_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDev) return fail(VD_ERR_UNSUPPORTED, "device ordinal too large");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (int& v : state) v = -1;
+    init = true;
+  }
+  if (state[dev] >= 0) {
+    *result = state[dev];
+    return VD_OK;
+  }
+  const GemmPlan plans[] = {{128, 256, 1}, {64, 16, 4}, {64, 64, 2}, {128, 16, 1}, {128, 32, 4},
+                            {128, 64, 2},  {128, 128, 1}, {256, 64, 1}, {256, 256, 1}};
+  constexpr int kPlans = sizeof(plans) / sizeof(plans[0]);
+  __nv_bfloat16 *A = nullptr, *W = nullptr;
+  float* C = nullptr;
+  int rc = VD_OK;
+  auto cleanup = [&] {
+    cudaFree(A);
+    cudaFree(W);
+    cudaFree(C);
+  };
+  if (cudaMalloc(&A, sizeof(__nv_bfloat16) * T * K) != cudaSuccess ||
+      cudaMalloc(&W, sizeof(__nv_bfloat16) * N * K) != cudaSuccess ||
+      cudaMalloc(&C, sizeof(float) * kPlans * T * N) != cudaSuccess) {
+    cleanup();
+    return fail(VD_ERR_CUDA, "GEMM shape self-check: allocation failed");
+  }
+  fill_probe_kernel<<<(T * K + 255) / 256, 256>>>(A, T * K, 0x1234567u);
+  fill_probe_kernel<<<(N * K + 255) / 256, 256>>>(W, N * K, 0x89ABCDEu);
+  WeightMaps wm;
+  CUtensorMap xm[kNumBn];
+  if ((rc = make_weight_maps(&wm, W, N, K, false))) {
+    cleanup();
+    return rc;
+  }
+  for (int i = 0; i < kNumBn && !rc; ++i) rc = make_map_2d(&xm[i], A, T, K, std::min(T, 16 << i));
+  ActMaps xv;
+  xv.maps = xm;
+  xv.rows = T;
+  for (int p = 0; p < kPlans && !rc; ++p) {
+    GemmArgs g{};
+    g.out = C + static_cast<size_t>(p) * T * N;
+    g.T = T;
+    g.K = K;
+    g.ldo = N;
+    g.glu_up_row = N;
+    rc = launch_gemm_plan(wm, xv, g, EPI_F32, &plans[p], nullptr);
+  }
+  std::vector<float> h(static_cast<size_t>(kPlans) * T * N);
+  if (!rc && cudaMemcpy(h.data(), C, sizeof(float) * h.size(), cudaMemcpyDeviceToHost) != cudaSuccess)
+    rc = fail(VD_ERR_CUDA, "GEMM shape self-check: copy failed");
+  cleanup();
+  if (rc) return rc;
+  bool same = true;
+  for (int p = 1; p < kPlans && same; ++p)
+    same = std::memcmp(h.data(), h.data() + static_cast<size_t>(p) * T * N, sizeof(float) * T * N) == 0;
+  state[dev] = same ? 1 : 0;
+  if (!same && !g_shapes_pinned.exchange(true)) ++g_plan_epoch;
+  *result = state[dev];
+  return VD_OK;
 }
 
 }  // namespace vd

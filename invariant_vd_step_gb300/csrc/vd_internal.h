@@ -131,6 +131,10 @@ GemmPlan gemm_plan(const WeightMaps& w, int T, int epi, int k_splits);
 int set_forced_gemm_plan(GemmPlan p);
 unsigned gemm_plan_epoch();
 int launch_gemm(const WeightMaps& w, const ActMaps& x, const GemmArgs& a, int epi, cudaStream_t s);
+// Once per device: every tile shape on seeded operands, raw fp32 results
+// compared bit for bit; *result = 1 if all agree (shapes stay per launch),
+// 0 if not (every later launch takes one fixed shape).
+int gemm_shapes_self_check(int* result);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {

@@ -116,6 +116,7 @@ _SIGS = {
     "vd_op_gemm": (ctypes.c_int, [_VP, _VP, _VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                   _VP, _VP]),
     "vd_set_gemm_plan": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    "vd_gemm_shape_check": (ctypes.c_int, []),
     "vd_gemm_plan_query": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.POINTER(ctypes.c_int32)]),
     "vd_op_rmsnorm": (ctypes.c_int, [_VP, _VP, _VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _VP]),
@@ -420,6 +421,11 @@ def gemm(A, W, C, epilogue=EPI_BF16, residual=None, stream=None):
     T, K = A.shape
     N = C.shape[1]
     check(lib().vd_op_gemm(_ptr(A), _ptr(W), _ptr(C), T, N, K, epilogue, _ptr(residual), _stream(stream)))
+
+
+def gemm_shape_check() -> int:
+    """vd_gemm_shape_check: 1 if every GEMM tile shape gave the same bits on this device, 0 if shapes are pinned."""
+    return int(lib().vd_gemm_shape_check())
 
 
 def set_gemm_plan(bm=0, bn=0, kpo=0):

@@ -131,3 +131,16 @@ def test_step_logits_do_not_move_under_any_forced_plan(spec, sample):
             if sample:
                 np.testing.assert_array_equal(tb, rt, err_msg=f"plan={plan} step={i} tokens")
     assert m.device_status() == 0
+
+
+def test_model_creation_checks_the_tile_shapes():
+    """vd_create_model compares every GEMM tile shape bit for bit on seeded
+    operands once per device; on this GPU they agree, so shapes stay chosen
+    per launch (the check would otherwise pin one fixed shape)."""
+    ready()
+    spec = synth.TINY
+    W = {k: v.cuda() for k, v in synth.make_weights(spec, seed=1).items()}
+    model = vd.Model(spec, W, max_tokens=32, max_seqs=2, max_logit_rows=2, max_context=64)
+    assert vd.gemm_shape_check() == 1
+    assert vd.gemm_plan(1, 4096, 4096) != vd.gemm_plan(256, 4096, 4096)  # still chosen per launch
+    model.close()
