@@ -958,6 +958,62 @@ def cpu_baseline(spec, weights, ctx_now, tables, mem, toks, gpu_logits, n_req):
                                        "tolerance (max-abs 2e-2, max-rel 1e-2)")}
 
 
+def run_cpu_baseline(args):
+    """CPU-baseline mode (no GPU): the C++ oracle on the host cores, as it
+    stands, on (a) the tiny-model workload end to end -- 8 requests with
+    prompts of 17..64 tokens, 4 sharing a 32-token prefix, 16 greedy decode
+    tokens each (cold prefill, then one decode step per token) -- and (b) one
+    decode step of the Llama-3.1-8B-shaped layer + LM head at B = 1, 8 and
+    32 over seeded N(0, 1) caches of U[512, 8192] tokens; each on one thread
+    and on every core (threads split output features, so the results are
+    the same bits)."""
+    import torch
+    from invariant_vd_step_gb300 import synth
+    from oracle import sampler
+    from oracle.fp32 import Fp32Decoder
+    cores = os.cpu_count() or 1
+    out = {"metric": "C++ oracle throughput on the host cores", "cpu": cpu_model(), "cores": cores, "kind": "oracle"}
+    spec = synth.TINY
+    W = synth.weights_to_numpy(synth.make_weights(spec, seed=0))
+    prompts = synth.make_prompts(8, 17, 64, spec.vocab, seed=1, shared_prefix=32, n_sharing=4)
+    tiny = {}
+    for threads in (1, cores):
+        dec = Fp32Decoder(spec, W, threads=threads)
+        t0 = time.perf_counter()
+        gen = 0
+        for p in prompts:
+            logits, cache = dec.step(p, dec.empty_cache())
+            for _ in range(16):
+                tok = sampler.argmax_lowest(logits[-1])
+                gen += 1
+                logits, cache = dec.step(np.array([tok]), cache)
+        dt = time.perf_counter() - t0
+        tiny[f"threads_{threads}"] = {"generated_tok_s": round(gen / dt, 1), "seconds": round(dt, 3)}
+    out["tiny_end_to_end"] = dict(tiny, workload="tiny llama-style decoder, 8 requests (4 share a 32-token "
+                                                  "prefix), prompts 17..64, 16 greedy tokens each")
+    spec = synth.LLAMA8B_1L
+    W = synth.weights_to_numpy(synth.make_weights(spec, seed=0))
+    rng = np.random.default_rng(4)
+    ctx = synth.make_context_lengths(32, CTX_LO, CTX_HI, seed=3)
+    toks = synth.make_tokens(32, spec.vocab, seed=9)
+    caches = []
+    for r in range(32):
+        c = int(ctx[r])
+        shape = (spec.n_layers, (c + 15) // 16, 2, spec.n_kv_heads, 16, spec.head_dim)
+        vals = torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.bfloat16)
+        caches.append(cache_from_pages(spec, synth.bf16_to_u16(vals), c))
+    decode = {}
+    for B in (1, 8, 32):
+        for threads in ((1, cores) if B == 1 else (cores,)):
+            t0 = time.perf_counter()
+            oracle_decode_rows(spec, W, caches[:B], toks[:B], threads)
+            dt = time.perf_counter() - t0
+            decode[f"B{B}_threads_{threads}"] = {"tok_s": round(B / dt, 3), "seconds": round(dt, 2)}
+    out["decode_step_llama8b_layer"] = dict(decode, workload="llama3.1-8b-shape 1 decoder layer + LM head, one "
+                                                            "decode step, contexts U[512,8192]")
+    print(json.dumps(out))
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -1016,7 +1072,8 @@ def main():
     ap.add_argument("--attention-fold", type=int, default=0, choices=[0, 1, 2],
                     help="decode attention mapping: 0 default (one CTA per split), 1 fold splits in one CTA, 2 split")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "serve", "llm42", "ceiling"])
+    ap.add_argument("--mode", default="decode",
+                    choices=["decode", "prefill", "serve", "llm42", "ceiling", "cpu-baseline"])
     ap.add_argument("--ceiling-batches", default="1,256", help="ceiling mode: token counts")
     ap.add_argument("--ceiling-sweep", action="store_true", help="ceiling mode: also time every forced GEMM plan")
     ap.add_argument("--ceiling-gemms", default="", help="ceiling mode: only these GEMMs (comma-separated names)")
@@ -1045,6 +1102,8 @@ def main():
         run_llm42(args)
     elif args.mode == "ceiling":
         run_ceiling(args)
+    elif args.mode == "cpu-baseline":
+        run_cpu_baseline(args)
     else:
         run_gpu(args)
 
