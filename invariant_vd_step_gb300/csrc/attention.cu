@@ -415,17 +415,29 @@ __global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
   float M = a.part_ml[(base + s0) * 2], L = a.part_ml[(base + s0) * 2 + 1];
   float O[PER];
   load_part<PER>(a.part_o + (base + s0) * HD + lane * PER, O);
-#pragma unroll 4
-  for (int s = s0 + 1; s <= s1; ++s) {
-    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + (base + s) * 2);
-    float P[PER];
-    load_part<PER>(a.part_o + (base + s) * HD + lane * PER, P);
-    const float mn = fmaxf(M, ml.x);
-    const float ca = ex2(__fsub_rn(M, mn)), cb = ex2(__fsub_rn(ml.x, mn));
-    L = __fadd_rn(__fmul_rn(L, ca), __fmul_rn(ml.y, cb));
+  // The partials of up to kBatch splits are loaded together (one memory
+  // round trip per batch instead of one per split), then folded one by one
+  // in ascending split order exactly as before.
+  constexpr int kBatch = 8;
+  for (int sb = s0 + 1; sb <= s1; sb += kBatch) {
+    float2 ml[kBatch];
+    float P[kBatch][PER];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) O[i] = __fadd_rn(__fmul_rn(O[i], ca), __fmul_rn(P[i], cb));
-    M = mn;
+    for (int c = 0; c < kBatch; ++c)
+      if (sb + c <= s1) {
+        ml[c] = *reinterpret_cast<const float2*>(a.part_ml + (base + sb + c) * 2);
+        load_part<PER>(a.part_o + (base + sb + c) * HD + lane * PER, P[c]);
+      }
+#pragma unroll
+    for (int c = 0; c < kBatch; ++c)
+      if (sb + c <= s1) {
+        const float mn = fmaxf(M, ml[c].x);
+        const float ca = ex2(__fsub_rn(M, mn)), cb = ex2(__fsub_rn(ml[c].x, mn));
+        L = __fadd_rn(__fmul_rn(L, ca), __fmul_rn(ml[c].y, cb));
+#pragma unroll
+        for (int i = 0; i < PER; ++i) O[i] = __fadd_rn(__fmul_rn(O[i], ca), __fmul_rn(P[c][i], cb));
+        M = mn;
+      }
   }
   __nv_bfloat16* out = a.out + (static_cast<size_t>(tok) * a.Hq + h) * HD + lane * PER;
 #pragma unroll

@@ -79,10 +79,10 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* _
   const uint4* wr = reinterpret_cast<const uint4*>(w);
   uint4* yr = reinterpret_cast<uint4*>(y + static_cast<size_t>(r) * d);
   const int d8 = d >> 3;
-  auto out8 = [&](const uint4& xv, int c, float inv) {
+  auto out8 = [&](const uint4& xv, const uint4& wv, int c, float inv) {
     float f[8], g[8];
     unpack8(xv, f);
-    unpack8(wr[c], g);
+    unpack8(wv, g);
     if (off != 0.f) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) g[i] = __fadd_rn(g[i], off);
@@ -103,10 +103,15 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* _
   };
   float ss = 0.f;
   if constexpr (CH > 0) {
-    uint4 xv[CH];
+    // the row and its gains in flight together: one memory round trip, not
+    // one per gain chunk after the sum
+    uint4 xv[CH], wv[CH];
 #pragma unroll
     for (int k = 0; k < CH; ++k)
-      if (lane + 32 * k < d8) xv[k] = xr[lane + 32 * k];
+      if (lane + 32 * k < d8) {
+        xv[k] = xr[lane + 32 * k];
+        wv[k] = wr[lane + 32 * k];
+      }
 #pragma unroll
     for (int k = 0; k < CH; ++k)
       if (lane + 32 * k < d8) ss = add8(ss, xv[k]);
@@ -114,13 +119,13 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const int* _
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(d)), eps)));
 #pragma unroll
     for (int k = 0; k < CH; ++k)
-      if (lane + 32 * k < d8) out8(xv[k], lane + 32 * k, inv);
+      if (lane + 32 * k < d8) out8(xv[k], wv[k], lane + 32 * k, inv);
   } else {
 #pragma unroll 4
     for (int c = lane; c < d8; c += 32) ss = add8(ss, xr[c]);
     ss = warp_sum_fixed(ss);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(d)), eps)));
-    for (int c = lane; c < d8; c += 32) out8(xr[c], c, inv);
+    for (int c = lane; c < d8; c += 32) out8(xr[c], wr[c], c, inv);
   }
 }
 
@@ -152,8 +157,8 @@ __global__ void postnorm_residual_kernel(const __nv_bfloat16* __restrict__ h, __
     for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(f[i], f[i]));
     return ss;
   };
-  auto gains8 = [&](const uint4* w, int c, float* g) {
-    unpack8(w[c], g);
+  auto gains8 = [&](const uint4& wv, float* g) {
+    unpack8(wv, g);
     if (off != 0.f) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) g[i] = __fadd_rn(g[i], off);
@@ -164,31 +169,33 @@ __global__ void postnorm_residual_kernel(const __nv_bfloat16* __restrict__ h, __
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(d)), eps)));
   };
   // x + bf16(h * inv * g) for one chunk, rounded to bf16
-  auto resid8 = [&](const uint4& hv, const uint4& xv, int c, float inv) {
+  auto resid8 = [&](const uint4& hv, const uint4& xv, const uint4& gv, float inv) {
     float fh[8], fx[8], g[8], o[8];
     unpack8(hv, fh);
     unpack8(xv, fx);
-    gains8(wp, c, g);
+    gains8(gv, g);
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = __fadd_rn(fx[i], bf16_round(__fmul_rn(__fmul_rn(fh[i], inv), g[i])));
     return make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
   };
-  auto norm8 = [&](const uint4& xv, int c, float inv) {
+  auto norm8 = [&](const uint4& xv, const uint4& gv, float inv) {
     float f[8], g[8];
     unpack8(xv, f);
-    gains8(wq, c, g);
+    gains8(gv, g);
     return make_uint4(pack_bf16x2(__fmul_rn(__fmul_rn(f[0], inv), g[0]), __fmul_rn(__fmul_rn(f[1], inv), g[1])),
                       pack_bf16x2(__fmul_rn(__fmul_rn(f[2], inv), g[2]), __fmul_rn(__fmul_rn(f[3], inv), g[3])),
                       pack_bf16x2(__fmul_rn(__fmul_rn(f[4], inv), g[4]), __fmul_rn(__fmul_rn(f[5], inv), g[5])),
                       pack_bf16x2(__fmul_rn(__fmul_rn(f[6], inv), g[6]), __fmul_rn(__fmul_rn(f[7], inv), g[7])));
   };
   if constexpr (CH > 0) {
-    uint4 hv[CH], xv[CH];
+    uint4 hv[CH], xv[CH], pv[CH], qv[CH];  // the row, the residual and both gains in flight together
 #pragma unroll
     for (int k = 0; k < CH; ++k)
       if (lane + 32 * k < d8) {
         hv[k] = hr[lane + 32 * k];
         xv[k] = xr[lane + 32 * k];
+        pv[k] = wp[lane + 32 * k];
+        if (w_pre) qv[k] = wq[lane + 32 * k];
       }
     float ss = 0.f;
 #pragma unroll
@@ -198,7 +205,7 @@ __global__ void postnorm_residual_kernel(const __nv_bfloat16* __restrict__ h, __
 #pragma unroll
     for (int k = 0; k < CH; ++k)
       if (lane + 32 * k < d8) {
-        xv[k] = resid8(hv[k], xv[k], lane + 32 * k, inv);
+        xv[k] = resid8(hv[k], xv[k], pv[k], inv);
         xr[lane + 32 * k] = xv[k];
       }
     if (!w_pre) return;
@@ -209,20 +216,20 @@ __global__ void postnorm_residual_kernel(const __nv_bfloat16* __restrict__ h, __
     const float inv2 = inv_of(s2);
 #pragma unroll
     for (int k = 0; k < CH; ++k)
-      if (lane + 32 * k < d8) yr[lane + 32 * k] = norm8(xv[k], lane + 32 * k, inv2);
+      if (lane + 32 * k < d8) yr[lane + 32 * k] = norm8(xv[k], qv[k], inv2);
   } else {
     float ss = 0.f;
     for (int c = lane; c < d8; c += 32) ss = add8(ss, hr[c]);
     const float inv = inv_of(ss);
     float s2 = 0.f;
     for (int c = lane; c < d8; c += 32) {
-      const uint4 xn = resid8(hr[c], xr[c], c, inv);
+      const uint4 xn = resid8(hr[c], xr[c], wp[c], inv);
       xr[c] = xn;
       s2 = add8(s2, xn);
     }
     if (!w_pre) return;
     const float inv2 = inv_of(s2);
-    for (int c = lane; c < d8; c += 32) yr[c] = norm8(xr[c], c, inv2);
+    for (int c = lane; c < d8; c += 32) yr[c] = norm8(xr[c], wq[c], inv2);
   }
 }
 
@@ -322,6 +329,7 @@ int launch_rmsnorm(const void* x, const int* row_idx, const void* w, void* y, in
            : per_lane <= 2  ? rmsnorm_kernel<2>
            : per_lane <= 4  ? rmsnorm_kernel<4>
            : per_lane <= 8  ? rmsnorm_kernel<8>
+           : per_lane <= 12 ? rmsnorm_kernel<12>
            : per_lane <= 16 ? rmsnorm_kernel<16>
                             : rmsnorm_kernel<0>;
   VD_CUDA_TRY(launch_k(k, dim3(blocks), dim3(128), 0, s, xp, row_idx, wp, yp, rows, d, eps, gain_offset));
@@ -337,11 +345,13 @@ int launch_postnorm_residual(const void* h, void* x, const void* w_post, const v
   const auto* wq = static_cast<const __nv_bfloat16*>(w_pre);
   auto* yp = static_cast<__nv_bfloat16*>(y);
   const int per_lane = (d / 8 + 31) / 32, blocks = (rows + 3) / 4;
+  // register-resident forms hold four arrays of CH chunks per lane; past 12
+  // chunks (d > 3072) they would spill, so longer rows stream
   auto k = per_lane <= 1    ? postnorm_residual_kernel<1>
            : per_lane <= 2  ? postnorm_residual_kernel<2>
            : per_lane <= 4  ? postnorm_residual_kernel<4>
            : per_lane <= 8  ? postnorm_residual_kernel<8>
-           : per_lane <= 16 ? postnorm_residual_kernel<16>
+           : per_lane <= 12 ? postnorm_residual_kernel<12>
                             : postnorm_residual_kernel<0>;
   VD_CUDA_TRY(launch_k(k, dim3(blocks), dim3(128), 0, s, hp, xp, wp, wq, yp, rows, d, eps, gain_offset));
   return VD_OK;
