@@ -111,13 +111,25 @@ __global__ void __launch_bounds__(kFinalThreads) sample_final_kernel(const float
   const int r = blockIdx.x;
   float bv = -INFINITY;
   int bi = INT_MAX;
-  for (int c = threadIdx.x; c < nchunk; c += kFinalThreads) {
-    const float v = part_v[static_cast<size_t>(r) * nchunk + c];
-    const int i = part_i[static_cast<size_t>(r) * nchunk + c];
-    if (better(v, i, bv, bi)) {
-      bv = v;
-      bi = i;
+  // Each thread's candidates are loaded kPer at a time (one memory round
+  // trip per batch); the winner is unique under `better`, so the order in
+  // which candidates are compared does not matter.
+  constexpr int kPer = 16;
+  for (int c0 = threadIdx.x; c0 < nchunk; c0 += kFinalThreads * kPer) {
+    float v[kPer];
+    int ix[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int c = c0 + u * kFinalThreads;
+      v[u] = c < nchunk ? part_v[static_cast<size_t>(r) * nchunk + c] : -INFINITY;
+      ix[u] = c < nchunk ? part_i[static_cast<size_t>(r) * nchunk + c] : INT_MAX;
     }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)
+      if (better(v[u], ix[u], bv, bi)) {
+        bv = v[u];
+        bi = ix[u];
+      }
   }
   warp_best(bv, bi);
   __shared__ float sv[kFinalThreads / 32];
