@@ -144,9 +144,9 @@ def _spread(ctx, n):
 # How far the GPU's mean distance from the float64 evaluation may exceed the
 # float32 oracle's.  One or two layers: the tensor cores' fp32 accumulation
 # truncates toward zero (its error on the 8B-shaped GEMMs is ~10x that of an
-# ascending float32 sum), which puts the GPU at 1.07-1.41x the float32
-# oracle there; at full depth the cascade saturates and the two sit at
-# 0.98-1.02x (the design doc has the measurements).
+# ascending float32 sum), which put the GPU at 1.07-1.41x the float32 oracle
+# there when measured; at full depth the cascade saturates and the two sat
+# at 0.98-1.02x.
 MARGIN_SHALLOW = 1.5
 MARGIN_DEEP = 1.25
 
