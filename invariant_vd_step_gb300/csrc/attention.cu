@@ -44,6 +44,8 @@ struct AttnCfg {
   static constexpr int PAGE_BYTES = 16 * HD * 2;     // one page of one KV head
   static constexpr int TILE_BYTES = BNK * HD * 2;
   static constexpr int MAX_STAGES = 8;
+  static constexpr int PIDS = 64;  // page ids a decode CTA stages: every page of its split
+  static constexpr int STATIC_SMEM = PIDS * 4 + 16;
   // K + V tiles of `stages` pipeline stages, their barriers, the abort flag
   static constexpr int smem(int stages) { return 1024 + stages * 2 * TILE_BYTES + MAX_STAGES * 8 + 16; }
 };
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   const int NS = a.stages;  // tiles in flight; changes when copies are issued, never the fold order
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * 2 * C::TILE_BYTES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + C::MAX_STAGES);
+  __shared__ int pid_s[C::PIDS];
 
   pdl_wait();
   pdl_trigger();
@@ -213,6 +216,19 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   if (key_lo > key_hi) return;  // no visible key of these rows in this split
   const int tile_lo = key_lo / C::BNK;
   const int ntiles = key_hi / C::BNK - tile_lo + 1;
+  // Decode-shaped split CTAs (few CTAs per SM, so each copy's issue latency
+  // shows): the physical ids of the (at most PIDS) pages this CTA streams,
+  // read by one warp in one round trip, so that the copies are issued
+  // without a dependent page-table load each.  Fold CTAs walk the whole
+  // context and prefill CTAs run several per SM: they look ids up as they go.
+  constexpr bool kStagePids = DS > 1 && !FOLD;
+  const int lp_first = (tile_lo * C::BNK) >> 4;
+  if (kStagePids && threadIdx.x < 32)
+    for (int j = threadIdx.x; j < C::PIDS; j += 32) {
+      const int lp = lp_first + j;
+      pid_s[j] = (j < ntiles * C::PAGES && lp * 16 < kv_len)
+                     ? a.page_table[static_cast<size_t>(b) * a.pt_stride + lp] : -1;
+    }
 
   if (threadIdx.x == 0) {
     for (int k = 0; k < NS; ++k) mbar_init(&full[k], 1);
@@ -230,7 +246,13 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
     for (int pg = 0; pg < C::PAGES; ++pg) {
       const int lp = lp0 + pg;
       int rk = a.pool_rows, rvw = a.pool_rows;  // outside the pool: zero fill
-      if (lp * 16 < kv_len) {
+      if constexpr (kStagePids) {
+        const int phys = pid_s[it * C::PAGES + pg];  // -1 past the context
+        if (phys >= 0) {
+          rk = a.layer_row0 + ((phys * 2) * a.Hkv + kvh) * 16;
+          rvw = rk + a.Hkv * 16;
+        }
+      } else if (lp * 16 < kv_len) {
         const int phys = a.page_table[static_cast<size_t>(b) * a.pt_stride + lp];
         rk = a.layer_row0 + ((phys * 2) * a.Hkv + kvh) * 16;
         rvw = rk + a.Hkv * 16;
@@ -463,8 +485,9 @@ int attn_stages(int n_items) {
   using C = AttnCfg<HD>;
   constexpr int kSmemPerSM = 228 * 1024, kSmemPerCTA = 227 * 1024;
   for (int ns = C::MAX_STAGES; ns > 2; --ns) {
-    if (C::smem(ns) > kSmemPerCTA) continue;
-    const long long slots = static_cast<long long>(sm_count_attn()) * (kSmemPerSM / (C::smem(ns) + 1024));
+    if (C::smem(ns) + C::STATIC_SMEM > kSmemPerCTA) continue;
+    const long long slots =
+        static_cast<long long>(sm_count_attn()) * (kSmemPerSM / (C::smem(ns) + C::STATIC_SMEM + 1024));
     if (slots >= n_items) return ns;
   }
   return 2;
@@ -476,7 +499,7 @@ int launch_attn_t(const CUtensorMap& kvmap, const AttnArgs& a0, int n_items, cud
   static bool configured = false;
   if (!configured) {
     int max_ns = C::MAX_STAGES;
-    while (C::smem(max_ns) > 227 * 1024) --max_ns;
+    while (C::smem(max_ns) + C::STATIC_SMEM > 227 * 1024) --max_ns;
     VD_CUDA_TRY(cudaFuncSetAttribute(attn_kernel<HD, NW, DS, FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::smem(max_ns)));
     configured = true;
@@ -515,6 +538,8 @@ int launch_attention(const CUtensorMap& kvmap, const AttnArgs& a, int hd, bool p
                      cudaStream_t s) {
   if (n_items <= 0) return VD_OK;
   if (prefill_class && a.fold) return fail(VD_ERR_INVALID_ARG, "split folding is for decode-class CTAs");
+  if (a.split > AttnCfg<64>::PIDS * 16)  // a split CTA stages the ids of every page it streams
+    return fail(VD_ERR_INVALID_ARG, "KV split larger than the staged page ids");
   // Decode CTAs split the head dimension of P V over 2 warps, or over 4 when
   // the launch has at most one CTA per SM (small batches); every
   // output element keeps the same instruction chain either way.
