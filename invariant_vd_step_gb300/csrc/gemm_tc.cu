@@ -187,6 +187,73 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tac
   }  // halves
 }
 
+// What the MMA issuer needs from the kernel's set-up.
+struct MmaLoop {
+  uint8_t* ring;
+  uint64_t *full, *empty, *acc_full, *acc_empty;
+  volatile int* abort_flag;
+  uint32_t tmem;
+  int ntiles, nbuf, n_ops, KS;
+  uint32_t idesc;
+  int a_bytes, a_sub, b_sub;
+};
+
+// The MMA issuer (one thread).  For each of the CTA's tiles it takes an
+// accumulator, then per stage waits for the stage's copies, issues its MMAs
+// (KPO K blocks of four K = 16 steps; HALVES: both M = 128 halves of a
+// 256-row tile per step) and releases the stage.  A stage is one straight
+// run of MMAs whose descriptors advance by 32-bit adds: with few tokens per
+// tile an MMA takes the tensor core about 45 cycles, so this thread's
+// instructions between two MMAs, not the tensor core, would otherwise set
+// the pace.  The MMAs, their operands and their order are those of the
+// K-ascending chain described at the top of this file.
+template <int KPO, bool HALVES>
+__device__ __forceinline__ void mma_issuer(const GemmArgs& args, const MmaLoop& L) {
+  const int S = args.stages, BN = args.bn;
+  const uint32_t ring_lo = sw128_desc_lo(smem_u32(L.ring));
+  const uint32_t st_step = static_cast<uint32_t>(args.stage_bytes) >> 4;  // one stage, 16-byte units
+  const uint32_t b_off = static_cast<uint32_t>(L.a_bytes) >> 4;           // a stage's B blocks
+  const uint32_t a_step = static_cast<uint32_t>(L.a_sub) >> 4, b_step = static_cast<uint32_t>(L.b_sub) >> 4;
+  int i = 0, s = 0;
+  uint32_t ph = 0, st_lo = ring_lo;
+  for (int tile = blockIdx.x; tile < L.ntiles && !*L.abort_flag; tile += gridDim.x, ++i) {
+    const int b = i % L.nbuf;
+    if (i >= L.nbuf && !mbar_wait(&L.acc_empty[b], ((i / L.nbuf) - 1) & 1, L.abort_flag, args.status)) break;
+    tc_fence_after();
+    const uint32_t tacc = L.tmem + b * kGemmBN;
+    const int split = tile % L.KS;
+    const int op_end = (split + 1) * L.n_ops / L.KS;
+    uint32_t acc = 0;  // the tile's first MMA starts from a zeroed accumulator
+    for (int op = split * L.n_ops / L.KS; op < op_end; ++op) {
+      if (!mbar_wait(&L.full[s], ph, L.abort_flag, args.status)) break;
+      tc_fence_after();
+      const uint32_t a_lo = st_lo, b_lo = st_lo + b_off;  // a K step of 16 elements: 32 bytes, 2 units
+      if constexpr (HALVES) {  // rows 128..255 of the tile: A rows 16 KB on, accumulator BN columns on
+#pragma unroll
+        for (int kk = 0; kk < kGemmBK / 16; ++kk) {
+          umma_bf16_lo(tacc, a_lo + 2 * kk, b_lo + 2 * kk, L.idesc, acc | kk);
+          umma_bf16_lo(tacc + BN, a_lo + ((kGemmBM * 128) >> 4) + 2 * kk, b_lo + 2 * kk, L.idesc, acc | kk);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < KPO; ++j)
+#pragma unroll
+          for (int kk = 0; kk < kGemmBK / 16; ++kk)
+            umma_bf16_lo(tacc, a_lo + j * a_step + 2 * kk, b_lo + j * b_step + 2 * kk, L.idesc, acc | j | kk);
+      }
+      acc = 1;
+      umma_commit(&L.empty[s]);
+      st_lo += st_step;
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+        st_lo = ring_lo;
+      }
+    }
+    umma_commit(&L.acc_full[b]);
+  }
+}
+
 // Persistent: CTA b handles tiles b, b + gridDim.x, ...; tile i = (token
 // tile i % n_tok_tiles, weight tile i / n_tok_tiles), so CTAs working on the
 // same weight tile at the same time share its reads through L2.  Two TMEM
@@ -290,44 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       const int HM = BM > kGemmBM ? kGemmBM : BM;  // rows per MMA (a 256-row tile issues two)
-      const uint32_t idesc = umma_idesc_bf16(HM, BN);
-      int i = 0, s = 0;
-      uint32_t ph = 0;
-      for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x, ++i) {
-        const int b = i % nbuf;
-        if (i >= nbuf && !mbar_wait(&acc_empty[b], ((i / nbuf) - 1) & 1, abort_flag, args.status)) break;
-        tc_fence_after();
-        const uint32_t tacc = tmem + b * kGemmBN;
-        const int op0 = op_lo(tile);
-        for (int op = op0; op < op_hi(tile); ++op) {
-          if (!mbar_wait(&full[s], ph, abort_flag, args.status)) break;
-          tc_fence_after();
-          // One descriptor per operand and stage; a K step of 16 elements is 32
-          // bytes, i.e. 2 in the descriptor's address field (16-byte units).
-          // This thread issues every MMA, so its loop is kept short.
-          const uint32_t a0 = smem_u32(ring + s * args.stage_bytes);
-          const uint64_t ad = sw128_desc(a0), bd = sw128_desc(a0 + a_bytes);
-          if (BM <= kGemmBM) {
-            for (int j = 0; j < kpo; ++j)
-#pragma unroll
-              for (int kk = 0; kk < kGemmBK / 16; ++kk)
-                umma_bf16(tacc, ad + j * (a_sub >> 4) + 2 * kk, bd + j * (b_sub >> 4) + 2 * kk, idesc,
-                          (op - op0) | j | kk);
-          } else {  // rows 128..255 of the tile: A rows 16 KB on, accumulator BN columns on
-#pragma unroll
-            for (int kk = 0; kk < kGemmBK / 16; ++kk) {
-              umma_bf16(tacc, ad + 2 * kk, bd + 2 * kk, idesc, (op - op0) | kk);
-              umma_bf16(tacc + BN, ad + ((kGemmBM * 128) >> 4) + 2 * kk, bd + 2 * kk, idesc, (op - op0) | kk);
-            }
-          }
-          umma_commit(&empty[s]);
-          if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-        umma_commit(&acc_full[b]);
-      }
+      const MmaLoop L{ring, full, empty, acc_full, acc_empty, abort_flag, tmem, ntiles, nbuf, n_ops, KS,
+                      umma_idesc_bf16(HM, BN), a_bytes, a_sub, b_sub};
+      if (BM > kGemmBM)
+        mma_issuer<1, true>(args, L);
+      else if (kpo == 4)
+        mma_issuer<4, false>(args, L);
+      else if (kpo == 2)
+        mma_issuer<2, false>(args, L);
+      else
+        mma_issuer<1, false>(args, L);
       umma_commit(mma_done);  // fires once every issued MMA has completed
     }
   } else {
