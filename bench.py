@@ -609,6 +609,24 @@ def run_ceiling(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / (3 * n)
 
+    # What one thread issuing MMAs costs (the GEMM's issuer is built around it):
+    # 896 MMAs of 128 x N x 16, 16 per stage, with no test, a test_wait or a
+    # try_wait of a completed mbarrier phase per stage (the stage's MMAs
+    # waiting for its result), or the test issued one stage ahead; SM clock
+    # cycles per MMA.
+    issue = []
+    cyc = torch.zeros(2, dtype=torch.int64, device=dev)
+    for N in (16, 32, 64, 128, 256):
+        for wait, wname in ((0, "none"), (1, "test_wait"), (2, "try_wait"), (3, "test_wait one stage ahead")):
+            vals = []
+            for _ in range(3):
+                vd.mma_issue_probe(128, N, 896, wait, cyc)
+                torch.cuda.synchronize()
+                vals.append(cyc.cpu().tolist())
+            best = min(vals, key=lambda v: v[1])
+            issue.append({"M": 128, "N": N, "per_stage_wait": wname, "mmas": 896,
+                          "cycles_per_mma_issue": round(best[0] / 896, 1),
+                          "cycles_per_mma_complete": round(best[1] / 896, 1)})
     only = set(args.ceiling_gemms.split(",")) if args.ceiling_gemms else None
     for T in [int(t) for t in args.ceiling_batches.split(",")]:
         for name, N, K, epi in gemms:
@@ -664,7 +682,7 @@ def run_ceiling(args):
             torch.cuda.empty_cache()
     print(json.dumps({"metric": "decode GEMM weight-stream ceilings (Llama-8B shape, 1 GB300)", "unit": "GB/s",
                       "peak": hbm, "peak_source": peak_kind, "launch": "one launch per graph node, replayed",
-                      "l2": "weight copies rotated, together > 400 MB", "rows": rows_out}))
+                      "l2": "weight copies rotated, together > 400 MB", "mma_issue": issue, "rows": rows_out}))
 
 
 def step_roofline_s(spec, seqs, R, hbm_gbs, tf_peak):

@@ -157,6 +157,20 @@ int vd_op_philox(uint64_t seed, uint64_t step, int32_t n, uint32_t* out, void* s
 int vd_op_tma_stream(const void* w, int64_t rows, int64_t K, const void* x, int64_t x_rows, int32_t box_rows,
                      int32_t kpo, int32_t x_box_rows, int32_t k_parts, int32_t ctas, void* stream);
 
+/* Measurement op (no counterpart in the paper; the figures the GEMM's MMA
+ * issuer is designed against): one CTA, one thread issuing n_mma bf16
+ * tcgen05 MMAs of M x N x 16 (fp32 accumulation) into one TMEM accumulator,
+ * 16 per stage, on zeroed shared-memory operands; before each stage it tests
+ * an mbarrier phase that has already completed with wait = 0 (no test),
+ * 1 (mbarrier.test_wait) or 2 (mbarrier.try_wait), each stage's MMAs issued
+ * only once the test returned true, or 3 (test_wait one stage ahead: the
+ * next stage's test is issued before this stage's MMAs).  out: dev int64 [2],
+ * SM clock cycles from the first issue to the last issue and to the
+ * completion of every MMA (-1 if the final bounded wait gave up).  M in
+ * {64, 128}; N a multiple of 16 in [16, 256]; n_mma a multiple of 16 in
+ * [16, 65536]; wait in {0, 1, 2, 3}.  Errors: VD_ERR_INVALID_ARG. */
+int vd_op_mma_issue_probe(int32_t M, int32_t N, int32_t n_mma, int32_t wait, int64_t* out, void* stream);
+
 /* Test of the failure path of every on-device wait (the bounded waits of
  * the pipelined GEMM and attention kernels; no counterpart in the paper, it
  * exercises this library's own failure detection).  Launches one CTA whose

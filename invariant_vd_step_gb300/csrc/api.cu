@@ -1452,6 +1452,16 @@ int vd_op_tma_stream(const void* w, int64_t rows, int64_t K, const void* x, int6
                            ctas, op_status(), static_cast<cudaStream_t>(stream));
 }
 
+int vd_op_mma_issue_probe(int32_t M, int32_t N, int32_t n_mma, int32_t wait, int64_t* out, void* stream) {
+  if (!out || (reinterpret_cast<uintptr_t>(out) & 7)) return fail(VD_ERR_INVALID_ARG, "out: 8-byte aligned dev int64 [2]");
+  if ((M != 64 && M != 128) || N < 16 || N > 256 || N % 16 || n_mma < 16 || n_mma > 65536 || n_mma % 16 ||
+      wait < 0 || wait > 3)
+    return fail(VD_ERR_INVALID_ARG, "M in {64, 128}; N a multiple of 16 in [16, 256]; n_mma a multiple of 16 in "
+                                    "[16, 65536]; wait in {0, 1, 2, 3}");
+  return launch_mma_issue_probe(M, N, n_mma, wait, reinterpret_cast<long long*>(out), op_status(),
+                                static_cast<cudaStream_t>(stream));
+}
+
 int vd_op_wait_probe(vd_model* m, int32_t limit_us, int32_t* out, void* stream) {
   if (check_model(m)) return fail(VD_ERR_INVALID_ARG, "null model");
   if (limit_us < 1 || limit_us > 2000000) return fail(VD_ERR_INVALID_ARG, "limit_us must be in [1, 2000000]");

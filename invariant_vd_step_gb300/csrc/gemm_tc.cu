@@ -205,7 +205,8 @@ struct MmaLoop {
 // run of MMAs whose descriptors advance by 32-bit adds: with few tokens per
 // tile an MMA takes the tensor core about 45 cycles, so this thread's
 // instructions between two MMAs, not the tensor core, would otherwise set
-// the pace.  The MMAs, their operands and their order are those of the
+// the pace (vd_op_mma_issue_probe measures the instruction and the per-stage
+// wait).  The MMAs, their operands and their order are those of the
 // K-ascending chain described at the top of this file.
 template <int KPO, bool HALVES>
 __device__ __forceinline__ void mma_issuer(const GemmArgs& args, const MmaLoop& L) {

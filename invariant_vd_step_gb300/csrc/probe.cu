@@ -1,5 +1,10 @@
 // Measurement ops: the ceilings the decode GEMMs are held against.
 //
+// mma_issue_kernel times one thread issuing a chain of tcgen05 MMAs into one
+// accumulator, 16 per stage, as the GEMM's issuer does, optionally testing an
+// mbarrier phase (already completed) before each stage: the per-instruction
+// costs the issuer is designed against.
+//
 // tma_stream_kernel streams a bf16 weight matrix [rows][K] from HBM through
 // shared memory with exactly the copies a GEMM launch of a given plan
 // issues -- 3-D TMA boxes (64, BM, kpo) into a 200 KB ring of stages, in the
@@ -107,6 +112,80 @@ __global__ void __launch_bounds__(64, 1)
   __syncthreads();
 }
 
+// One CTA: thread 32 issues n_mma MMAs (M x N x 16, 16 per stage: four K
+// blocks of four K steps) on zeroed operands -- A: four 128-row K blocks
+// (64 KB), B: one 256-row block (32 KB) -- into one TMEM accumulator; WAIT 1
+// or 2 tests a completed phase before each stage with test_wait or
+// try_wait, WAIT 3 with test_wait one stage ahead (before the previous
+// stage's MMAs).  out[0]: cycles from the first issue to the last, out[1]: to
+// the completion of every MMA.
+constexpr int kIssueA = 4 * 128 * 128, kIssueB = 256 * 128;
+constexpr int kIssueSmem = 1024 + kIssueA + kIssueB;
+
+template <int WAIT>
+__global__ void __launch_bounds__(128, 1) mma_issue_kernel(int M, int N, int n_mma, long long* out, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  __shared__ uint64_t bars[2];  // [0] every MMA done, [1] a phase completed at set-up
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  for (int i = threadIdx.x; i < (kIssueA + kIssueB) / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(smem)[i] = 0;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    mbar_arrive(&bars[1]);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (threadIdx.x < 32) {
+    tmem_alloc(&tmem_slot, 256);
+    tmem_relinquish();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeros, for the tensor core
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tacc = tmem_slot;
+  if (threadIdx.x == 32) {
+    const uint32_t idesc = umma_idesc_bf16(M, N);
+    const uint32_t a_lo = sw128_desc_lo(smem_u32(smem)), b_lo = sw128_desc_lo(smem_u32(smem) + kIssueA);
+    const long long t0 = clock64();
+    uint32_t acc = 0;
+    bool ok = true, next = mbar_test_wait(&bars[1], 0);
+    for (int st = 0; st < n_mma / 16; ++st) {
+      // As in the GEMM, the stage's MMAs are issued only once the test has
+      // returned true, so the test's latency is on the issuing path.
+      bool ready = true;
+      if constexpr (WAIT == 1) ready = mbar_test_wait(&bars[1], 0);
+      if constexpr (WAIT == 2) ready = mbar_try_wait(&bars[1], 0);
+      if constexpr (WAIT == 3) ready = next;  // tested one stage ahead
+      if (!ready) {
+        ok = false;
+        break;
+      }
+      if constexpr (WAIT == 3) next = mbar_test_wait(&bars[1], 0);  // the next stage's test, before this one's MMAs
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_lo(tacc, a_lo + j * ((128 * 128) >> 4) + 2 * kk, b_lo + 2 * kk, idesc, acc | j | kk);
+      acc = 1;
+    }
+    const long long t1 = clock64();
+    umma_commit(&bars[0]);
+    if (!mbar_wait(&bars[0], 0, &abort_flag, status)) ok = false;
+    const long long t2 = clock64();
+    out[0] = ok ? t1 - t0 : -1;
+    out[1] = ok ? t2 - t0 : -1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    tmem_dealloc(tacc, 256);
+  }
+}
+
 int stream_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -116,6 +195,20 @@ int stream_sm_count() {
 }
 
 }  // namespace
+
+int launch_mma_issue_probe(int M, int N, int n_mma, int wait, long long* out, int* status, cudaStream_t s) {
+  static bool configured[4] = {false, false, false, false};
+  auto k = wait == 0   ? mma_issue_kernel<0>
+           : wait == 1 ? mma_issue_kernel<1>
+           : wait == 2 ? mma_issue_kernel<2>
+                       : mma_issue_kernel<3>;
+  if (!configured[wait]) {
+    VD_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kIssueSmem));
+    configured[wait] = true;
+  }
+  VD_CUDA_TRY(launch_k(k, dim3(1), dim3(128), kIssueSmem, s, M, N, n_mma, out, status));
+  return VD_OK;
+}
 
 int launch_tma_stream(const CUtensorMap& wmap, const CUtensorMap& xmap, int rows, int K, int box_rows, int kpo,
                       int x_box_rows, int k_parts, int ctas, int* status, cudaStream_t s) {

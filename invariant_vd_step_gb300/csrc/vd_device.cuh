@@ -62,10 +62,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Non-blocking test of the same condition.  A phase that has already
-// completed is seen several times faster this way than through try_wait,
-// which matters to the single threads that issue MMAs and copies stage by
-// stage (measured on sm_103a: about 90 against 280 cycles).
+// Non-blocking test of the same condition (true if the phase has completed).
+// On sm_103a a test whose result the following work waits for costs the
+// issuing thread about 250 cycles, like try_wait on a completed phase, and
+// issuing it a stage early does not hide that (vd_op_mma_issue_probe).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

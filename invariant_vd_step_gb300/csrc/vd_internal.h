@@ -222,5 +222,9 @@ int launch_wait_probe(int* status, uint64_t limit_ns, int* out, cudaStream_t s);
 // arithmetic.  ctas = 0: one CTA per SM (at most one per tile).
 int launch_tma_stream(const CUtensorMap& wmap, const CUtensorMap& xmap, int rows, int K, int box_rows, int kpo,
                       int x_box_rows, int k_parts, int ctas, int* status, cudaStream_t s);
+// One thread issuing n_mma MMAs (M x N x 16), 16 per stage, with an optional
+// test (wait 1: test_wait, 2: try_wait) of a completed mbarrier phase per
+// stage; out: dev int64 [2] cycles to the last issue and to completion.
+int launch_mma_issue_probe(int M, int N, int n_mma, int wait, long long* out, int* status, cudaStream_t s);
 
 }  // namespace vd

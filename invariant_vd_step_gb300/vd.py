@@ -127,6 +127,7 @@ _SIGS = {
     "vd_op_wait_probe": (ctypes.c_int, [_VP, ctypes.c_int32, _VP, _VP]),
     "vd_op_tma_stream": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_int64, _VP, ctypes.c_int64, ctypes.c_int32,
                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _VP]),
+    "vd_op_mma_issue_probe": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _VP, _VP]),
     "vd_engine_create": (ctypes.c_int, [ctypes.POINTER(EngineConfig), ctypes.POINTER(_VP)]),
     "vd_engine_destroy": (None, [_VP]),
     "vd_engine_add_request": (ctypes.c_int, [_VP, _I32P, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64,
@@ -446,6 +447,11 @@ def tma_stream(w, box_rows, kpo, x=None, x_box_rows=0, k_parts=1, ctas=0, stream
     x_rows = x.shape[0] if x is not None else 0
     check(lib().vd_op_tma_stream(_ptr(w), rows, K, _ptr(x), x_rows, box_rows, kpo, x_box_rows, k_parts, ctas,
                                  _stream(stream)))
+
+
+def mma_issue_probe(M, N, n_mma, wait, out, stream=None):
+    """vd_op_mma_issue_probe: out (dev int64 [2]) = cycles to the last MMA issue and to completion."""
+    check(lib().vd_op_mma_issue_probe(M, N, n_mma, wait, _ptr(out), _stream(stream)))
 
 
 def rmsnorm(x, w, y, eps, stream=None):

@@ -1,6 +1,8 @@
-"""The weight-stream measurement op (vd_op_tma_stream): it runs every copy
-shape the GEMM plans use, with and without activation copies and K parts,
-leaves the device status clean, and rejects shapes the GEMM cannot take."""
+"""The measurement ops.  The weight-stream op (vd_op_tma_stream) runs every
+copy shape the GEMM plans use, with and without activation copies and K
+parts, leaves the device status clean, and rejects shapes the GEMM cannot
+take.  The MMA-issue op (vd_op_mma_issue_probe) completes every MMA it
+issues, reports plausible cycle counts, and rejects shapes it cannot take."""
 
 import pytest
 import torch
@@ -36,3 +38,26 @@ def test_stream_rejects_shapes_no_plan_has():
         with pytest.raises(vd.VDError) as e:
             vd.tma_stream(W, bm, kpo, k_parts=kp)
         assert e.value.code == vd.VD_ERR_INVALID_ARG
+
+
+def test_mma_issue_probe_runs_and_reports_cycles():
+    ready()
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    for M in (64, 128):
+        for N in (16, 64, 256):
+            for wait in (0, 1, 2, 3):
+                out.fill_(0)
+                vd.mma_issue_probe(M, N, 160, wait, out)
+                torch.cuda.synchronize()
+                issue, done = out.cpu().tolist()
+                # every MMA completed (no timeout); at least a few cycles each, far below a microsecond
+                assert 0 < issue <= done < 160 * 5000, (M, N, wait, issue, done)
+
+
+def test_mma_issue_probe_rejects_shapes_it_cannot_take():
+    ready()
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    for bad in [(32, 16, 16, 0), (128, 8, 16, 0), (128, 272, 16, 0), (128, 16, 15, 0), (128, 16, 0, 0),
+                (128, 16, 16, 4)]:
+        with pytest.raises(vd.VDError):
+            vd.mma_issue_probe(*bad, out)
