@@ -68,8 +68,11 @@ struct RowState {
 // One key tile for the 16 rows of a warp, which accumulates output dims
 // [dim0, dim0 + ND).  S and the softmax state are computed over the full
 // head either way, so every output element gets the same instruction chain
-// whether one warp owns all dims or several warps share them.
-template <int HD, int BNK, int ND>
+// whether one warp owns all dims or several warps share them.  LOWER8: rows
+// 8..15 of the warp are known to hold no row (a decode CTA of at most 8
+// rows), so their masking, softmax and rescale are skipped: their weights
+// are exactly 0 either way, and the other rows' instructions are unchanged.
+template <int HD, int BNK, int ND, bool LOWER8>
 __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)[HD / 16][4], uint32_t kbase,
                                           uint32_t vbase, int key0, const int (&pos)[2], const int (&lo)[2],
                                           float scale_log2, int lane, int dim0) {
@@ -93,6 +96,10 @@ __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int r = e >> 1;
+      if (LOWER8 && r == 1) {
+        s[j][e] = -INFINITY;
+        continue;
+      }
       const int key = key0 + j * 8 + t4 * 2 + (e & 1);
       const bool vis = key >= lo[r] && key <= pos[r];
       const float v = vis ? __fmul_rn(s[j][e], scale_log2) : -INFINITY;
@@ -104,6 +111,12 @@ __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)
   bool rv[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
+    if (LOWER8 && r == 1) {  // no row: the state stays as it is, as a fully masked row's does
+      rv[r] = false;
+      mnew[r] = st.m[r];
+      alpha[r] = 1.0f;
+      continue;
+    }
     mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
     mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
     rv[r] = mx[r] != -INFINITY;
@@ -121,6 +134,10 @@ __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int r = e >> 1;
+      if (LOWER8 && r == 1) {
+        p[e] = h[e] = l[e] = 0.f;
+        continue;
+      }
       p[e] = (s[j][e] == -INFINITY) ? 0.f : ex2(__fsub_rn(s[j][e], mnew[r]));
       h[e] = bf16_round(p[e]);
       l[e] = __fsub_rn(p[e], h[e]);
@@ -134,6 +151,7 @@ __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)
   }
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
+    if (LOWER8 && r == 1) continue;
     rs[r] = __fadd_rn(rs[r], __shfl_xor_sync(0xffffffffu, rs[r], 1));
     rs[r] = __fadd_rn(rs[r], __shfl_xor_sync(0xffffffffu, rs[r], 2));
     st.l[r] = rv[r] ? __fadd_rn(__fmul_rn(st.l[r], alpha[r]), rs[r]) : st.l[r];
@@ -143,8 +161,10 @@ __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)
   for (int n = 0; n < ND / 8; ++n) {
     st.o[n][0] = __fmul_rn(st.o[n][0], alpha[0]);
     st.o[n][1] = __fmul_rn(st.o[n][1], alpha[0]);
-    st.o[n][2] = __fmul_rn(st.o[n][2], alpha[1]);
-    st.o[n][3] = __fmul_rn(st.o[n][3], alpha[1]);
+    if (!LOWER8) {  // rows 8..15 (with LOWER8 their alpha is 1, and their sums are never stored)
+      st.o[n][2] = __fmul_rn(st.o[n][2], alpha[1]);
+      st.o[n][3] = __fmul_rn(st.o[n][3], alpha[1]);
+    }
   }
   const int np0 = dim0 / 16;
 #pragma unroll
@@ -308,6 +328,9 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
 #pragma unroll
     for (int n = 0; n < ND / 8; ++n) fo[n][0] = fo[n][1] = fo[n][2] = fo[n][3] = 0.f;
   }
+  // A decode CTA (one block of 16 rows) with at most 8 rows: its warps'
+  // rows 8..15 are empty (the same for every warp, so the branch is uniform).
+  const bool lower8 = DS > 1 && rows - r0 <= 8;
   bool ok = true;
   int it = 0, stg = 0;
   uint32_t ph = 0;  // tile it sits in stage it % NS, round it / NS
@@ -320,7 +343,10 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
     mine = __any_sync(0xffffffffu, mine);
     if (ok && mine) {
       const uint32_t kb = smem_u32(smem + stg * 2 * C::TILE_BYTES);
-      attn_tile<HD, C::BNK, ND>(st, qf, kb, kb + C::TILE_BYTES, key0, pos, lo, a.scale_log2, lane, dim0);
+      if (DS > 1 && lower8)
+        attn_tile<HD, C::BNK, ND, DS != 1>(st, qf, kb, kb + C::TILE_BYTES, key0, pos, lo, a.scale_log2, lane, dim0);
+      else
+        attn_tile<HD, C::BNK, ND, false>(st, qf, kb, kb + C::TILE_BYTES, key0, pos, lo, a.scale_log2, lane, dim0);
     }
     if (FOLD && ((key0 + C::BNK) % a.split == 0 || it == ntiles - 1)) {
       // end of a split: fold it into the merged state of every row that saw a
