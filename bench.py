@@ -728,6 +728,8 @@ def run_serve(args):
     decode.  Reports tok/s of each kind over its own steps, all computed
     tokens over the wall clock, and the wall-clock roofline fraction (sum of
     per-step roofline times / time)."""
+    if args.workload == "c4":
+        return run_serve_c4(args)
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -770,9 +772,33 @@ def run_serve(args):
         res = sessions.run_sessions(work, model, pool, eng, conc, logits, tok_dev, stream)
     wall = time.perf_counter() - t_start
     assert model.device_status() == 0
+    split = split_steps(spec, res.steps, hbm, tf_sust)
+    total_T = split["tokens_computed"]
+    gen = sum(len(t) for outs in res.outputs.values() for t in outs)
+    print(json.dumps({
+        "metric": f"serving tok/s ({args.workload}, Llama-3.1-8B shape 32 layers, 1 GB300)",
+        "value": round(total_T / wall, 1), "unit": "tok/s (tokens computed: prefill chunks + decode)",
+        "generated_tok_s": round(gen / wall, 1),
+        "n_gpus": 1, "higher_is_better": True, "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": spec.n_layers, "budget": budget, "max_batch": conc,
+                   "sessions": work.n_sessions, "turns": work.turns, "pool_pages": pages, "graphs": args.graphs},
+        "steps": len(res.steps), "wall_s": round(wall, 3),
+        "prefill": split["prefill"], "decode": split["decode"],
+        "roofline_frac": round(split["roofline_s"] / wall, 4),
+        "tokens": {"prompt_submitted": res.submitted, "computed": total_T, "generated": gen},
+        "engine": eng.stats, "graphs": model.graph_stats(), "clocks": clk.summary(),
+        "peaks": {"hbm_gbs": hbm, "bf16_tflops_sustained": tf_sust, "source": peak_kind},
+    }))
+
+
+def split_steps(spec, steps, hbm, tf_sust):
+    """Prefill and decode tok/s and roofline fractions over a run's steps.  A
+    step that carries prompt tokens counts as prefill (its tokens minus its
+    decode rows are prefill tokens); a step of decode rows only counts as
+    decode."""
     t_pre = t_dec = roof_pre = roof_dec = 0.0
     n_pre_tok = n_dec_tok = total_T = 0
-    for st in res.steps:
+    for st in steps:
         T = sum(q for _, q in st.seqs)
         total_T += T
         roof, _ = step_roofline_s(spec, st.seqs, st.rows, hbm, tf_sust)
@@ -784,22 +810,91 @@ def run_serve(args):
             t_dec += st.seconds
             roof_dec += roof
             n_dec_tok += st.rows
-    gen = sum(len(t) for outs in res.outputs.values() for t in outs)
+    return {"steps": len(steps), "tokens_computed": total_T,
+            "prefill": {"tok_s": round(n_pre_tok / max(t_pre, 1e-9), 1), "steps_s": round(t_pre, 3),
+                        "roofline_frac": round(roof_pre / max(t_pre, 1e-9), 4)},
+            "decode": {"tok_s": round(n_dec_tok / max(t_dec, 1e-9), 1), "steps_s": round(t_dec, 3),
+                       "roofline_frac": round(roof_dec / max(t_dec, 1e-9), 4)},
+            "gpu_steps_s": round(t_pre + t_dec, 3), "roofline_s": round(roof_pre + roof_dec, 4)}
+
+
+def run_serve_c4(args):
+    """C4: the Gemma-3-4B shape (34 layers: QK-norm, GeGLU, sandwich norms, 5
+    local layers of window 1024 per global one) served by the native engine:
+    32 requests, prompts U[2048, 8192], 128 decode tokens each, at batch
+    {1, 8, 32} x chunk budget {512, 4096}.  Each run reports prefill and
+    decode tok/s and roofline fractions over its own steps; every emitted
+    row's logits (a fingerprint of their bits taken on the GPU: the sum and
+    an index-weighted sum of the int32 views) and token are compared with
+    the batch-1, budget-4096 run, the invariance pairs of this workload."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from invariant_vd_step_gb300 import engine, sessions, synth, vd
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = synth.GEMMA3_4B
+    V = spec.vocab
+    n_req, dec = 32, 128
+    prompts = synth.make_prompts(n_req, 2048, 8192, V, seed=1)
+    work = sessions.SessionWorkload(V, n_req, 1, decode_lo=dec, decode_hi=dec, prompts=prompts)
+    pages = sum((len(p) + dec + 15) // 16 for p in prompts) + 64
+    weights = synth.make_weights(spec, seed=0, device=dev)
+    model = vd.Model(spec, weights, max_tokens=4096, max_seqs=n_req, max_logit_rows=n_req,
+                     max_context=work.max_context())
+    model.set_graph_mode(args.graphs)
+    pool = vd.KVPool(model, pages)
+    stream = torch.cuda.current_stream(dev)
+    logits = torch.empty((n_req, V), dtype=torch.float32, device=dev)
+    tok_dev = torch.empty(n_req, dtype=torch.int32, device=dev)
+    wvec = (torch.arange(V, device=dev, dtype=torch.int64) % 1021) + 1
+    hbm, _, peak_kind = load_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tf_sust = float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        tf_sust = 1700.0
+    runs = [(1, 4096), (1, 512), (8, 512), (8, 4096), (32, 512), (32, 4096)]  # the first is the reference
+    out, prints = [], []
+    with Clocks(local) as clk:
+        for bsz, budget in runs:
+            eng = engine.Engine(None, pages, max_batch=bsz, token_budget=budget, prefix_reuse=True, placement_seed=2)
+            fp = {}
+
+            def on_rows(sids, turns, lg, toks):
+                bits = lg.view(torch.int32).to(torch.int64)
+                f = torch.stack([bits.sum(dim=1), (bits * wvec).sum(dim=1)], 1).cpu().numpy()
+                for i, sid in enumerate(sids):
+                    fp.setdefault(sid, []).append((int(f[i, 0]), int(f[i, 1]), int(toks[i])))
+
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            res = sessions.run_sessions(work, model, pool, eng, bsz, logits, tok_dev, stream, on_rows=on_rows)
+            wall = time.perf_counter() - t0
+            assert model.device_status() == 0
+            row = {"batch": bsz, "budget": budget, "wall_s": round(wall, 3)}
+            row.update(split_steps(spec, res.steps, hbm, tf_sust))
+            out.append(row)
+            prints.append(fp)
+    ref = prints[0]
+    pairs = equal = 0
+    for fp in prints[1:]:
+        for sid, rows in ref.items():
+            for a, b in zip(rows, fp.get(sid, [])):
+                pairs += 1
+                equal += a == b
+            pairs += abs(len(rows) - len(fp.get(sid, [])))
     print(json.dumps({
-        "metric": f"serving tok/s ({args.workload}, Llama-3.1-8B shape 32 layers, 1 GB300)",
-        "value": round(total_T / wall, 1), "unit": "tok/s (tokens computed: prefill chunks + decode)",
-        "generated_tok_s": round(gen / wall, 1),
-        "n_gpus": 1, "higher_is_better": True, "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "layers": spec.n_layers, "budget": budget, "max_batch": conc,
-                   "sessions": work.n_sessions, "turns": work.turns, "pool_pages": pages, "graphs": args.graphs},
-        "steps": len(res.steps), "wall_s": round(wall, 3),
-        "prefill": {"tok_s": round(n_pre_tok / max(t_pre, 1e-9), 1), "steps_s": round(t_pre, 3),
-                    "roofline_frac": round(roof_pre / max(t_pre, 1e-9), 4)},
-        "decode": {"tok_s": round(n_dec_tok / max(t_dec, 1e-9), 1), "steps_s": round(t_dec, 3),
-                   "roofline_frac": round(roof_dec / max(t_dec, 1e-9), 4)},
-        "roofline_frac": round((roof_pre + roof_dec) / wall, 4),
-        "tokens": {"prompt_submitted": res.submitted, "computed": total_T, "generated": gen},
-        "engine": eng.stats, "graphs": model.graph_stats(), "clocks": clk.summary(),
+        "metric": "C4 serving (Gemma-3-4B shape, 34 layers, 1 GB300): tok/s and invariance pass %",
+        "n_gpus": 1, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "c4", "requests": n_req, "prompts": "U[2048, 8192]", "decode_tokens": dec,
+                   "pool_pages": pages, "graphs": args.graphs},
+        "runs": out,
+        "invariance": {"reference": "batch 1, budget 4096", "pairs": pairs, "bitwise_equal": equal,
+                       "pass_pct": round(100.0 * equal / max(pairs, 1), 3),
+                       "compared": "per emitted row: logits bit fingerprint and token"},
+        "graphs": model.graph_stats(), "clocks": clk.summary(),
         "peaks": {"hbm_gbs": hbm, "bf16_tflops_sustained": tf_sust, "source": peak_kind},
     }))
 
@@ -1097,7 +1192,7 @@ def main():
     ap.add_argument("--ceiling-gemms", default="", help="ceiling mode: only these GEMMs (comma-separated names)")
     ap.add_argument("--window", type=int, default=8, help="llm42 mode: verification window")
     ap.add_argument("--new-tokens", type=int, default=64, help="llm42 mode: tokens per request")
-    ap.add_argument("--workload", default="c3", choices=["c3", "c5"], help="serve mode workload")
+    ap.add_argument("--workload", default="c3", choices=["c3", "c4", "c5"], help="serve mode workload")
     ap.add_argument("--budget", type=int, default=2048, help="serve mode: chunked-prefill token budget")
     ap.add_argument("--sessions", type=int, default=128, help="serve c5: sessions")
     ap.add_argument("--turns", type=int, default=8, help="serve c5: turns per session")
