@@ -18,7 +18,7 @@ token per request.
             feeds the previous step's sampled tokens back, uploads the host
             descriptor and reads the sampled tokens back to the host.
 
-The line also carries: the same step at B = 1 and 64 (``decode_points``),
+The line also carries: the same step at B = 1, 8 and 64 (``decode_points``),
 an 8192-token prefill step with each GEMM's TFLOP/s (``prefill``), repeated
 K-step windows (``stability``), the 3,200-pair invariance matrix, and the
 C++ oracle timed on the host cores for a sample of one step's rows
@@ -452,9 +452,9 @@ def run_gpu(args):
                              "ms_per_step_max": round(max([step_ms] + windows), 4),
                              "note": "value is the first window; the clock record covers all windows"}
     if not args.no_points:
-        # decode at B = 1 and 64 (same workload, graph replay) and the 8192-token prefill step
+        # decode at B = 1, 8 and 64 (same workload, graph replay) and the 8192-token prefill step
         line["decode_points"] = {str(b): decode_sweep_point(spec, weights, b, K, Wm, args.graphs, dev, hbm)
-                                 for b in (1, 64)}
+                                 for b in (1, 8, 64)}
         line["prefill"] = prefill_result(dev, 8192, 4, max(5, min(K, 20)), Wm)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, weights, ctx + check_step, tables, mem, check_toks, check_logits,
