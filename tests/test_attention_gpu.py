@@ -53,6 +53,11 @@ def test_causal_contract_bitwise_across_schedules(hd):
         [(0, 299, 1)], [(1, 511, 1)], [(1, 512, 1)],              # alone, at split edges
         [(1, 1000, 30), (0, 290, 10)],
         [(0, 63, 2), (1, 63, 2)],
+        # decode-shaped CTAs of 9..16 rows (q_len 3 or 4 with a group of 4; 5..8 with a group of 2),
+        # which keep the softmax of the warp's rows 8..15, next to CTAs of at most 8 rows, which skip
+        # it, in one launch
+        [(0, 100, 3), (1, 600, 1), (2, 20, 2)],
+        [(1, 700, 4), (0, 200, 5), (2, 40, 8)],
     ]
     seen = {}
     for parts in runs:
