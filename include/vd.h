@@ -211,6 +211,18 @@ int vd_set_reduction_mode(vd_model* m, int32_t mode);
  * Head dimensions above 128 never fold.  Errors: VD_ERR_INVALID_ARG. */
 int vd_set_attention_fold(vd_model* m, int32_t mode);
 
+/* Kernel of the prefill-class attention rows (q_len * Hq/Hkv > 16), with the
+ * per-row traversal and arithmetic of 深入解析 Vosti §六 6.2 either way.
+ * kernel 0 (default): 5th-generation tensor cores (tcgen05, accumulators in
+ * tensor memory, 128 rows per CTA) for head dimensions 64 and 128, mma.sync
+ * for 256; kernel 1: mma.sync (64 rows per CTA) for every head dimension.  A
+ * tcgen05 K = 16 MMA step computes what an mma.sync m16n8k16 step computes,
+ * bit for bit, and both kernels take the same steps in the same order, so
+ * logits are bitwise identical under either choice.  Applies to the steps
+ * and attention ops issued after the call (captured step graphs are keyed
+ * on it).  Errors: VD_ERR_INVALID_ARG. */
+int vd_set_attention_prefill(vd_model* m, int32_t kernel);
+
 /* Graph replay of steps (an engineering addition; the pages' design has no
  * counterpart).  With max_graphs > 0, vd_step keeps the descriptor upload as
  * an ordinary copy on the stream and replays the step's kernel sequence as

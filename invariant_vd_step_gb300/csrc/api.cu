@@ -111,12 +111,16 @@ int make_weight_maps(WeightMaps* w, const void* base, uint64_t rows, uint64_t K,
   return VD_OK;
 }
 
-int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd) {
+// K/V pool rows as (64 head dims, hd / 64 blocks, rows).  A box is one page
+// (16 rows) of `box_blocks` 64-wide blocks: all hd / 64 for the mma.sync
+// kernels (a key's head dims side by side), 1 for the tcgen05 kernel (one
+// block of 16 keys, the MMA's canonical operand layout).
+int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd, int box_blocks) {
   auto fn = encode_fn();
   if (!fn) return fail(VD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(hd / 64), rows};
   cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(hd) * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(hd / 64), 16};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_blocks), 16};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -176,6 +180,7 @@ struct Desc {
   // (merge_tok: offset of the token list the merge kernel folds)
   int n_dec = 0, n_pre = 0, items_dec = 0, items_pre = 0;
   bool fold = false;  // decode class in fold mode
+  bool pre_tc = false;  // prefill class on the tcgen05 kernel (128 rows per CTA), else mma.sync (64)
   int merge_tok = 0, n_merge = 0;
   int grid_dec = 0, grid_pre = 0;  // attention CTAs launched (>= items; extra CTAs exit)
   int total = 0;
@@ -190,12 +195,13 @@ struct GraphKey {
   const void* tokens = nullptr;  // fused token choice (vd_step_sample) or null
   const void* feed = nullptr;    // device-side token feedback or null
   int T = 0, B = 0, R = 0, stride = 0, n_dec = 0, n_pre = 0, grid_dec = 0, grid_pre = 0, fold = 0, n_merge = 0;
+  int pre_tc = 0;
   int fast = 0;
   unsigned plan_epoch = 0;  // GEMM plan override in force
   bool operator==(const GraphKey& o) const {
     return pool_id == o.pool_id && logits == o.logits && tokens == o.tokens && feed == o.feed && T == o.T && B == o.B && R == o.R && stride == o.stride &&
            n_dec == o.n_dec && n_pre == o.n_pre && grid_dec == o.grid_dec && grid_pre == o.grid_pre &&
-           fold == o.fold && n_merge == o.n_merge && fast == o.fast &&
+           fold == o.fold && pre_tc == o.pre_tc && n_merge == o.n_merge && fast == o.fast &&
            plan_epoch == o.plan_epoch;
   }
 };
@@ -228,6 +234,7 @@ struct vd_model {
   __nv_bfloat16* hsub = nullptr;  // sandwich norms: a sub-layer's output before its norm
   float embed_scale = 0.f;        // 0: none, else bf16(sqrt(d)) as float
   int fold_mode = 0;              // 0: default (split mode), 1: fold the decode class whenever legal, 2: never
+  int prefill_kernel = 0;         // 0: tcgen05 attention for the prefill class where hd allows, 1: mma.sync
   // fast (non-invariant) path: split-K for GEMMs with too few weight tiles
   int fast = 0;
   int n_sm = 0;
@@ -272,7 +279,8 @@ struct vd_kv_pool {
   void* data = nullptr;
   bool owned = false;
   long long rows = 0;  // 16-slot rows of hd elements
-  CUtensorMap map{};
+  CUtensorMap map{};     // boxes for the mma.sync attention kernels
+  CUtensorMap map_tc{};  // boxes for the tcgen05 attention kernel
 };
 
 namespace {
@@ -473,6 +481,8 @@ int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_token
     h[d.logit_rows + j] = b->logit_rows[j];
   }
   // attention work classes: decode-shaped requests (one warp of rows) and the rest
+  d.pre_tc = m->prefill_kernel == 0 && attn_tc_supported(c.head_dim);
+  const int pre_rows = d.pre_tc ? 128 : 64;  // rows per prefill-class CTA
   int nd = 0, npre = 0, ipre = 0;
   std::vector<int>& dec = m->scratch_dec;
   dec.clear();
@@ -484,7 +494,7 @@ int build_desc(vd_model* m, vd_kv_pool* pool, const vd_batch* b, bool need_token
     } else {
       h[d.pre_seq + npre] = s;
       h[d.pre_start + npre] = ipre;
-      ipre += attn_items(ql, kv, m->G, c.n_kv_heads, 64);
+      ipre += attn_items(ql, kv, m->G, c.n_kv_heads, pre_rows);
       ++npre;
     }
   }
@@ -576,7 +586,9 @@ int run_attention(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d, const
     a.cls_seq = m->d_desc + d.pre_seq;
     a.cls_start = m->d_desc + d.pre_start;
     a.n_cls = d.n_pre;
-    if ((rc = launch_attention(pool->map, a, hd, true, d.grid_pre, s))) return rc;
+    if ((rc = d.pre_tc ? launch_attention_tc(pool->map_tc, a, hd, d.grid_pre, s)
+                        : launch_attention(pool->map, a, hd, true, d.grid_pre, s)))
+      return rc;
   }
   if (d.n_merge == 0) return VD_OK;  // every row was folded inside the attention kernel
   MergeArgs g{};
@@ -657,7 +669,9 @@ int run_attention_static(vd_model* m, vd_kv_pool* pool, int layer, const Desc& d
     a.cls_seq = m->d_desc + d.pre_seq;
     a.cls_start = m->d_desc + d.pre_start;
     a.n_cls = d.n_pre;
-    if ((rc = launch_attention(pool->map, a, hd, true, d.items_pre, s))) return rc;
+    if ((rc = d.pre_tc ? launch_attention_tc(pool->map_tc, a, hd, d.items_pre, s)
+                        : launch_attention(pool->map, a, hd, true, d.items_pre, s)))
+      return rc;
   }
   if (d.n_merge == 0) return VD_OK;
   MergeArgs g{};
@@ -853,6 +867,7 @@ int replay_step(vd_model* m, vd_kv_pool* pool, const Desc& d, float* logits_out,
   k.grid_dec = d.grid_dec;
   k.grid_pre = d.grid_pre;
   k.fold = d.fold;
+  k.pre_tc = d.pre_tc;
   k.n_merge = d.n_merge;
   k.fast = m->fast;
   k.plan_epoch = gemm_plan_epoch();
@@ -1087,7 +1102,8 @@ int vd_kv_pool_alloc(vd_model* m, int32_t num_pages, void* dev_mem, size_t bytes
     vd_destroy_kv_pool(p);
     return fail(VD_ERR_CUDA, "cudaMemset(pool) failed");
   }
-  int rc = make_map_kv(&p->map, p->data, static_cast<uint64_t>(rows), c.head_dim);
+  int rc = make_map_kv(&p->map, p->data, static_cast<uint64_t>(rows), c.head_dim, c.head_dim / 64);
+  if (!rc) rc = make_map_kv(&p->map_tc, p->data, static_cast<uint64_t>(rows), c.head_dim, 1);
   if (rc) {
     vd_destroy_kv_pool(p);
     return rc;
@@ -1185,6 +1201,13 @@ int vd_set_attention_fold(vd_model* m, int32_t mode) {
   if (check_model(m)) return VD_ERR_INVALID_ARG;
   if (mode < 0 || mode > 2) return fail(VD_ERR_INVALID_ARG, "mode must be 0 (auto), 1 (always) or 2 (never)");
   m->fold_mode = mode;
+  return VD_OK;
+}
+
+int vd_set_attention_prefill(vd_model* m, int32_t kernel) {
+  if (check_model(m)) return VD_ERR_INVALID_ARG;
+  if (kernel < 0 || kernel > 1) return fail(VD_ERR_INVALID_ARG, "kernel must be 0 (tcgen05 where supported) or 1 (mma.sync)");
+  m->prefill_kernel = kernel;
   return VD_OK;
 }
 

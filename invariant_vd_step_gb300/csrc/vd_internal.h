@@ -51,7 +51,7 @@ cudaError_t launch_k(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
 // columns (128 bytes), 128-byte swizzle, zero fill outside the matrix.
 int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 // 3-D bf16 map for the KV pool: dims (64, hd/64, rows), box (64, hd/64, 16).
-int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd);
+int make_map_kv(CUtensorMap* map, const void* base, uint64_t rows, int hd, int box_blocks);
 
 // ---------------------------------------------------------------- GEMM
 // EPI_F32_SAMPLE: fp32 logits (stored unless out is null) plus, per token and
@@ -174,6 +174,11 @@ int attn_key_tile(int hd);
 int launch_attention(const CUtensorMap& kvmap, const AttnArgs& a, int hd, bool prefill_class, int n_items,
                      cudaStream_t s);
 int launch_merge(const MergeArgs& a, int hd, cudaStream_t s);
+// Prefill-class attention on tcgen05 (128 rows per CTA), same per-row
+// arithmetic as launch_attention's kernels; kvmap_tc has one-page boxes of
+// 64 head dims.
+bool attn_tc_supported(int hd);
+int launch_attention_tc(const CUtensorMap& kvmap_tc, const AttnArgs& a, int hd, int n_items, cudaStream_t s);
 // Fixed-size device scratch of vd_op_attention_static (bytes) and its
 // device address on the current device (looked up once per device).
 constexpr size_t kAttnStaticScratchBytes = static_cast<size_t>(16) << 20;

@@ -107,6 +107,7 @@ _SIGS = {
     "vd_device_status": (ctypes.c_int, [_VP]),
     "vd_set_graph_mode": (ctypes.c_int, [_VP, ctypes.c_int32]),
     "vd_set_attention_fold": (ctypes.c_int, [_VP, ctypes.c_int32]),
+    "vd_set_attention_prefill": (ctypes.c_int, [_VP, ctypes.c_int32]),
     "vd_set_reduction_mode": (ctypes.c_int, [_VP, ctypes.c_int32]),
     "vd_graph_stats": (ctypes.c_int, [_VP, _I64P]),
     "vd_profile_enable": (ctypes.c_int, [_VP, ctypes.c_int32]),
@@ -364,6 +365,10 @@ class Model:
     def set_attention_fold(self, mode: int):
         """Decode attention mapping: 0 default (one CTA per split), 1 fold all splits in one CTA, 2 split."""
         check(lib().vd_set_attention_fold(self.h, int(mode)))
+
+    def set_attention_prefill(self, kernel: int):
+        """Prefill-class attention kernel: 0 default (tcgen05 for head dims 64 and 128), 1 mma.sync."""
+        check(lib().vd_set_attention_prefill(self.h, int(kernel)))
 
     def set_graph_mode(self, max_graphs: int):
         """Replay steps as captured CUDA graphs (0 = eager launches)."""
