@@ -467,16 +467,18 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def prefill_result(dev, T, nreq, K, Wm):
+def prefill_result(dev, T, nreq, K, Wm, attn_kernel=0):
     """One prefill step of T new tokens (nreq requests of T / nreq tokens
     from an empty cache) through the layer + LM head: prefill tok/s and each
-    GEMM's TFLOP/s against the measured bf16 tensor peak (sustained)."""
+    GEMM's TFLOP/s against the measured bf16 tensor peak (sustained).
+    attn_kernel: the prefill-class attention kernel (0 tcgen05, 1 mma.sync)."""
     import torch
     from invariant_vd_step_gb300 import synth, vd
     spec = synth.LLAMA8B_1L
     per = T // nreq
     weights = synth.make_weights(spec, seed=0, device=dev)
     model = vd.Model(spec, weights, max_tokens=T, max_seqs=nreq, max_logit_rows=nreq, max_context=per + 16)
+    model.set_attention_prefill(attn_kernel)
     npg = (per + 15) // 16
     pool = vd.KVPool(model, nreq * npg)
     toks = synth.make_tokens(T, spec.vocab, seed=1)
@@ -537,6 +539,7 @@ def prefill_result(dev, T, nreq, K, Wm):
         "value": round(Tt * K / (ms * 1e-3), 1), "unit": "tok/s", "ms_per_step": round(ms / K, 4), "steps": K,
         "warmup": Wm, "tokens_per_step": Tt, "requests": nreq,
         "workload": "llama3.1-8b-shape 1 decoder layer + LM head, prefill from an empty cache",
+        "attention_kernel": "tcgen05" if attn_kernel == 0 and spec.head_dim in (64, 128) else "mma.sync",
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": kernels[dom]["TFLOP_s"], "peak": tf_sust,
                      "unit": "TFLOP/s", "frac": kernels[dom]["tensor_frac"], "traffic": None,
                      "peak_source": peak_kind + " (sustained)"},
@@ -554,7 +557,8 @@ def run_prefill(args):
     ws, rank, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    r = prefill_result(dev, args.tokens, args.prefill_requests, args.steps, args.warmup)
+    r = prefill_result(dev, args.tokens, args.prefill_requests, args.steps, args.warmup,
+                       0 if args.prefill_attention == "tc" else 1)
     print(json.dumps({
         "metric": "prefill tok/s (Llama-8B shape, 1 GB300)", "value": r["value"], "unit": "tok/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
@@ -1178,6 +1182,8 @@ def main():
                     help="decode: keep up to N captured step graphs (0 = eager launches)")
     ap.add_argument("--cpu-sample", type=int, default=8)
     ap.add_argument("--no-points", action="store_true", help="decode: leave out the B = 1 / 64 points and the prefill step")
+    ap.add_argument("--prefill-attention", choices=["tc", "mma"], default="tc",
+                    help="prefill mode: the prefill-class attention kernel (tcgen05 or mma.sync; the same bits)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-invariance", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="decode: add the batch sweep 1..256 to the line")
