@@ -26,7 +26,7 @@
 // creation), never on the batch, q_len, page table or split placement.
 //
 // Numerics: S = Q K^T and O += P V on mma.sync m16n8k16 (bf16 in, fp32
-// accumulate), scores scaled by log2(e)/sqrt(hd), exp2 by ex2.approx,
+// accumulate), scores scaled by log2(e)/sqrt(hd), exp2 by ex2.approx.ftz,
 // P split into bf16 hi + lo terms for the P V product (fp32 for the row
 // sum), every other float operation an explicitly rounded intrinsic.
 #include <math.h>

@@ -321,10 +321,14 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, uint32_t saddr) {
 }
 
 // ------------------------------------------------------------------ numerics
-// 2^x with the hardware approximation (one instruction; no flush to zero).
+// 2^x with the hardware approximation, subnormal inputs and results flushed
+// to zero (one instruction).  Every attention kernel and the split merge use
+// this one helper, so they stay bitwise consistent with each other; a result
+// below 2^-126 is a softmax weight or rescale factor too small to move any
+// fp32 sum it enters.
 __device__ __forceinline__ float ex2(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
