@@ -25,16 +25,19 @@
 // row run here equals the same row run by the mma.sync decode or prefill
 // kernel; the attention tests check that bitwise.
 //
-// Roles (320 threads): warp 0 allocates TMEM and one lane issues the K/V
-// page copies (3-D TMA boxes of one page and 64 head dims, so that a K or V
-// tile is [hd block][32 keys][64] with the 128-byte swizzle, the canonical
-// operand layout); warp 1, one lane, issues the MMAs; warps 2..9 each hold
-// 16 rows, read from TMEM in the layout of an mma.sync C fragment (two rows
-// and eight keys per thread), and run the softmax, the O rescale and the
-// epilogue with the mma.sync kernel's per-row code.  TMEM: two 32-column score buffers, so that S of the next
-// tile is computed while this tile's softmax runs, and hd columns of O.
-// P (hi | lo, 128 bytes a row) goes through shared memory as the A operand
-// of P V; V is the MN-major B operand.  Every wait is bounded.
+// Roles (320 threads): warp 0 allocates TMEM, reads the split's page ids
+// and one lane issues the K/V page copies (3-D TMA boxes of one page and 64
+// head dims, so that the K or V of a stage, two tiles, is [hd block][64
+// keys][64] with the 128-byte swizzle, the canonical operand layout); warp 1,
+// one lane, issues the MMAs; warps 2..9 each hold 16 rows, read from TMEM in
+// the layout of an mma.sync C fragment (two rows and eight keys per thread),
+// and run the softmax, the O rescale and the epilogue with the mma.sync
+// kernel's per-row code.  S of a stage's two tiles is one chain of N = 64
+// MMAs (an MMA's N does not change an element) into 64 TMEM columns, issued
+// once the softmax has read the previous stage's scores.  P (hi and lo bf16,
+// two per 32-bit column) goes to one of two TMEM buffers and is the A operand
+// of P V, straight from TMEM; V is the MN-major B operand; O takes hd TMEM
+// columns.  Every wait is bounded.
 #include <math.h>
 
 #include "vd_device.cuh"
@@ -43,19 +46,42 @@
 namespace vd {
 namespace {
 
+// x[0] *= y, x[1] *= y (or -= y) in one instruction: each element rounded to
+// nearest exactly as mul.rn.f32 / sub.rn.f32 round it.
+__device__ __forceinline__ void mul2_rn(float& x0, float& x1, float y) {
+  uint64_t v, w;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(w) : "f"(y));
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(v) : "l"(w));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(v));
+}
+__device__ __forceinline__ void sub2_rn(float& x0, float& x1, float y) {
+  uint64_t v, w;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(w) : "f"(y));
+  asm("sub.rn.f32x2 %0, %0, %1;" : "+l"(v) : "l"(w));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(v));
+}
+
 template <int HD>
 struct TcAttnCfg {
   static constexpr int ROWS = 128;                 // rows per CTA (MMA M)
-  static constexpr int BNK = 32;                   // keys per tile, as in every attention kernel
+  static constexpr int BNK = 32;                   // keys per tile: the softmax step of every attention kernel
+  static constexpr int SK = 2 * BNK;               // keys per K/V stage (two tiles share one S MMA chain)
   static constexpr int KB = HD / 64;               // 64-wide head-dim blocks
   static constexpr int Q_BYTES = KB * ROWS * 128;  // [hd block][row][64]
-  static constexpr int TILE_BYTES = BNK * HD * 2;  // K or V: [hd block][key][64]
-  static constexpr int HALF_BYTES = BNK * 128;     // one hd block of a tile
-  static constexpr int P_BYTES = ROWS * 128;       // [row][hi 32 | lo 32]
-  static constexpr int STAGES = 3;
-  static constexpr int O_COL = 2 * BNK;            // TMEM: S buffers at 0 and BNK, O after them
-  static constexpr int TMEM_COLS = 2 * BNK + HD <= 128 ? 128 : 256;
-  static constexpr int SMEM = 1024 + Q_BYTES + STAGES * 2 * TILE_BYTES + P_BYTES + 256;
+  static constexpr int HB = SK * 128;              // one hd block of a stage's K or V: [key][64]
+  static constexpr int KV_BYTES = KB * HB;         // K or V of a stage: [hd block][key][64]
+  static constexpr int STAGES = HD == 64 ? 4 : 2;  // K/V stages in flight (two tiles each)
+  // TMEM: the scores of a stage's two tiles (SK columns), O (hd columns),
+  // then two P buffers of BNK columns (hi and lo bf16 of a row's BNK keys,
+  // two per column)
+  static constexpr int O_COL = SK;
+  static constexpr int P_COL = O_COL + HD;
+  static constexpr int TMEM_COLS = 256;
+  static_assert(P_COL + 2 * BNK <= TMEM_COLS, "TMEM columns per CTA");
+  static constexpr int PIDS = 64;  // page ids of a split (at most 32 pages of 16 keys)
+  static constexpr int SMEM = 1024 + Q_BYTES + STAGES * 2 * KV_BYTES + 256 + PIDS * 4;
   // At most 512 / TMEM_COLS CTAs may share an SM (a CTA that found too few
   // TMEM columns would wait in tcgen05.alloc); shared memory bounds it.
   static constexpr int CTAS_PER_SM = (228 * 1024) / (SMEM + 1024);
@@ -69,18 +95,18 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sq = smem;
-  uint8_t* skv = sq + C::Q_BYTES;  // stage s: K at skv + s * 2 * TILE_BYTES, V right after
-  uint8_t* sp = skv + C::STAGES * 2 * C::TILE_BYTES;
-  uint64_t* kv_full = reinterpret_cast<uint64_t*>(sp + C::P_BYTES);
+  uint8_t* skv = sq + C::Q_BYTES;  // stage s: K at skv + s * 2 * KV_BYTES, V right after
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(skv + C::STAGES * 2 * C::KV_BYTES);
   uint64_t* kv_empty = kv_full + C::STAGES;
-  uint64_t* s_full = kv_empty + C::STAGES;  // [2] S of a tile is in its buffer
-  uint64_t* s_free = s_full + 2;            // [2] the softmax threads have read it
-  uint64_t* p_full = s_free + 2;            // P written and O rescaled
+  uint64_t* s_full = kv_empty + C::STAGES;  // the scores of a stage's tiles are in TMEM
+  uint64_t* s_free = s_full + 1;            // the softmax threads have read them
+  uint64_t* p_full = s_free + 1;            // P of a tile written and O rescaled
   uint64_t* pv_done = p_full + 1;           // the tile's P V steps completed
   uint64_t* q_full = pv_done + 1;           // Q rows in shared memory
   uint64_t* mma_done = q_full + 1;          // every MMA issued has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* pid_s = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(kv_full) + 256);  // [PIDS]
 
   pdl_wait();
   pdl_trigger();
@@ -118,17 +144,26 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
   if (key_lo > key_hi) return;  // no visible key of these rows in this split
   const int tile_lo = key_lo / C::BNK;
   const int ntiles = key_hi / C::BNK - tile_lo + 1;
+  const int nstage = (ntiles + 1) >> 1;  // K/V stages: tiles 2 g and 2 g + 1 (the latter may be past the end)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The physical ids of the split's pages (-1 past its tiles or the
+  // context), read by one warp in one round trip, so that no copy waits for a
+  // page-table load.
+  const int lp_first = (tile_lo * C::BNK) >> 4;
+  if (warp == 0)
+    for (int j = lane; j < C::PIDS; j += 32) {
+      const int lp = lp_first + j;
+      pid_s[j] = (j < ntiles * (C::BNK / 16) && lp * 16 < kv_len)
+                     ? a.page_table[static_cast<size_t>(b) * a.pt_stride + lp] : -1;
+    }
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 256);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 256);
     mbar_init(p_full, 256);
     mbar_init(pv_done, 1);
     mbar_init(q_full, 256);
@@ -145,29 +180,27 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  int issued = 0;  // producer: tiles whose copies were issued
+  int issued = 0;  // producer: stages whose copies were issued
   if (warp == 0) {
     if (lane == 0) {
-      for (int g = 0; g < ntiles && !*abort_flag; ++g) {
+      for (int g = 0; g < nstage && !*abort_flag; ++g) {
         const int s = g % C::STAGES;
         if (g >= C::STAGES && !mbar_wait(&kv_empty[s], ((g / C::STAGES) - 1) & 1, abort_flag, a.status)) break;
-        uint8_t* sk = skv + s * 2 * C::TILE_BYTES;
-        uint8_t* sv = sk + C::TILE_BYTES;
-        mbar_arrive_expect_tx(&kv_full[s], 2 * C::TILE_BYTES);
-        const int lp0 = ((tile_lo + g) * C::BNK) >> 4;
+        uint8_t* sk = skv + s * 2 * C::KV_BYTES;
+        uint8_t* sv = sk + C::KV_BYTES;
+        mbar_arrive_expect_tx(&kv_full[s], 2 * C::KV_BYTES);
 #pragma unroll
-        for (int pg = 0; pg < C::BNK / 16; ++pg) {
-          const int lp = lp0 + pg;
-          int rk = a.pool_rows, rvw = a.pool_rows;  // outside the pool: zero fill
-          if (lp * 16 < kv_len) {
-            const int phys = a.page_table[static_cast<size_t>(b) * a.pt_stride + lp];
+        for (int pg = 0; pg < C::SK / 16; ++pg) {
+          const int phys = pid_s[g * (C::SK / 16) + pg];
+          int rk = a.pool_rows, rvw = a.pool_rows;  // outside the pool (past the tiles or the context): zero fill
+          if (phys >= 0) {
             rk = a.layer_row0 + ((phys * 2) * a.Hkv + kvh) * 16;
             rvw = rk + a.Hkv * 16;
           }
 #pragma unroll
           for (int c = 0; c < C::KB; ++c) {
-            tma_load_3d(sk + c * C::HALF_BYTES + pg * 2048, &kvmap, &kv_full[s], 0, c, rk);
-            tma_load_3d(sv + c * C::HALF_BYTES + pg * 2048, &kvmap, &kv_full[s], 0, c, rvw);
+            tma_load_3d(sk + c * C::HB + pg * 2048, &kvmap, &kv_full[s], 0, c, rk);
+            tma_load_3d(sv + c * C::HB + pg * 2048, &kvmap, &kv_full[s], 0, c, rvw);
           }
         }
         issued = g + 1;
@@ -175,44 +208,49 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id_s = umma_idesc_bf16(C::ROWS, C::BNK);
+      const uint32_t id_s = umma_idesc_bf16(C::ROWS, C::SK);
       const uint32_t id_pv = umma_idesc_bf16(C::ROWS, HD) | (1u << 16);  // B (V) MN-major
       const uint32_t q_lo = sw128_desc_lo(smem_u32(sq));
-      const uint32_t p_lo = sw128_desc_lo(smem_u32(sp));
-      // S of tile t into score buffer t & 1
-      auto issue_s = [&](int t) -> bool {
-        const int s = t % C::STAGES, sb = t & 1;
-        if (!mbar_wait(&kv_full[s], (t / C::STAGES) & 1, abort_flag, a.status)) return false;
-        if (t >= 2 && !mbar_wait(&s_free[sb], ((t >> 1) - 1) & 1, abort_flag, a.status)) return false;
+      // S of stage g's two tiles, one chain of hd/16 K = 16 steps per element
+      auto issue_s = [&](int g) -> bool {
+        const int s = g % C::STAGES;
+        if (!mbar_wait(&kv_full[s], (g / C::STAGES) & 1, abort_flag, a.status)) return false;
         tc_fence_after();
-        const uint32_t k_lo = sw128_desc_lo(smem_u32(skv + s * 2 * C::TILE_BYTES));
+        const uint32_t k_lo = sw128_desc_lo(smem_u32(skv + s * 2 * C::KV_BYTES));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_lo(tmem + sb * C::BNK, q_lo + (kk >> 2) * (C::ROWS * 128 >> 4) + 2 * (kk & 3),
-                       k_lo + (kk >> 2) * (C::HALF_BYTES >> 4) + 2 * (kk & 3), id_s, kk ? 1u : 0u);
-        umma_commit(&s_full[sb]);
+          umma_bf16_lo(tmem, q_lo + (kk >> 2) * (C::ROWS * 128 >> 4) + 2 * (kk & 3),
+                       k_lo + (kk >> 2) * (C::HB >> 4) + 2 * (kk & 3), id_s, kk ? 1u : 0u);
+        umma_commit(s_full);
         return true;
       };
-      // O += P V of tile t: hi then lo per 16 keys, onto the rescaled O
+      // O += P V of tile t: hi then lo per 16 keys, onto the rescaled O; P
+      // from TMEM buffer t & 1, V from the tile's half of its stage
       auto issue_pv = [&](int t) -> bool {
         if (!mbar_wait(p_full, t & 1, abort_flag, a.status)) return false;
         tc_fence_after();
-        const int s = t % C::STAGES;
-        const uint32_t v_lo = sw128_desc_lo_mn(smem_u32(skv + s * 2 * C::TILE_BYTES + C::TILE_BYTES), C::HALF_BYTES);
+        const int s = (t >> 1) % C::STAGES;
+        const uint32_t pt = tmem + C::P_COL + (t & 1) * C::BNK;  // hi: keys 2j, 2j + 1 in column j; lo BNK / 2 on
+        const uint32_t v_lo = sw128_desc_lo_mn(
+            smem_u32(skv + s * 2 * C::KV_BYTES + C::KV_BYTES + (t & 1) * C::BNK * 128), C::HB);
 #pragma unroll
         for (int ks = 0; ks < C::BNK / 16; ++ks) {
           const uint32_t vk = v_lo + ks * (16 * 128 >> 4);
-          umma_bf16_lo(tmem + C::O_COL, p_lo + 2 * ks, vk, id_pv, 1u);
-          umma_bf16_lo(tmem + C::O_COL, p_lo + 4 + 2 * ks, vk, id_pv, 1u);
+          umma_bf16_ta(tmem + C::O_COL, pt + 8 * ks, vk, id_pv, 1u);
+          umma_bf16_ta(tmem + C::O_COL, pt + C::BNK / 2 + 8 * ks, vk, id_pv, 1u);
         }
-        umma_commit(&kv_empty[s]);
         umma_commit(pv_done);
+        if ((t & 1) || t == ntiles - 1) umma_commit(&kv_empty[s]);  // the stage's last reader
         return true;
       };
       if (mbar_wait(q_full, 0, abort_flag, a.status) && issue_s(0)) {
         for (int t = 0; t < ntiles; ++t) {
-          if (t + 1 < ntiles && !issue_s(t + 1)) break;
           if (!issue_pv(t)) break;
+          // once the softmax threads have read this stage's second scores,
+          // the next stage's S goes into the score columns
+          if (!(t & 1) && (t >> 1) + 1 < nstage) {
+            if (!mbar_wait(s_free, (t >> 1) & 1, abort_flag, a.status) || !issue_s((t >> 1) + 1)) break;
+          }
         }
       }
       umma_commit(mma_done);
@@ -266,16 +304,19 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
     };
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
-      const int sb = t & 1;
-      if (!warp_wait(&s_full[sb], (t >> 1) & 1)) {
-        ok = false;
-        break;
+      if (!(t & 1)) {  // a new stage's scores
+        if (!warp_wait(s_full, (t >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
       }
-      tc_fence_after();
       float sv[16];  // s[j][e] = sv[4 j + e]
-      tmem_ld16x4(frag + sb * C::BNK, sv);
-      tc_fence_before();
-      mbar_arrive(&s_free[sb]);
+      tmem_ld16x4(frag + (t & 1) * C::BNK, sv);
+      if ((t & 1) || t == ntiles - 1) {  // the stage's scores are all read
+        tc_fence_before();
+        mbar_arrive(s_free);
+      }
       const int key0 = (tile_lo + t) * C::BNK;
       // every row of the warp sees every key of the tile: no masking (the
       // same values the masked path computes for visible keys)
@@ -284,9 +325,9 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
       float mx[2] = {-INFINITY, -INFINITY};
       if (full) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          sv[i] = __fmul_rn(sv[i], a.scale_log2);
-          mx[(i >> 1) & 1] = fmaxf(mx[(i >> 1) & 1], sv[i]);
+        for (int i = 0; i < 16; i += 2) {
+          mul2_rn(sv[i], sv[i + 1], a.scale_log2);
+          mx[(i >> 1) & 1] = fmaxf(fmaxf(mx[(i >> 1) & 1], sv[i]), sv[i + 1]);
         }
       } else {
 #pragma unroll
@@ -314,9 +355,16 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
       for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const float s0 = sv[4 * j + 2 * r], s1 = sv[4 * j + 2 * r + 1];
-          const float p0 = (full || s0 != -INFINITY) ? ex2(__fsub_rn(s0, mnew[r])) : 0.f;
-          const float p1 = (full || s1 != -INFINITY) ? ex2(__fsub_rn(s1, mnew[r])) : 0.f;
+          float s0 = sv[4 * j + 2 * r], s1 = sv[4 * j + 2 * r + 1];
+          float p0, p1;
+          if (full) {  // every score finite, m' finite
+            sub2_rn(s0, s1, mnew[r]);
+            p0 = ex2(s0);
+            p1 = ex2(s1);
+          } else {
+            p0 = s0 != -INFINITY ? ex2(__fsub_rn(s0, mnew[r])) : 0.f;
+            p1 = s1 != -INFINITY ? ex2(__fsub_rn(s1, mnew[r])) : 0.f;
+          }
           const uint32_t h = pack_bf16x2(p0, p1);
           ph[j][r] = h;
           pl[j][r] = pack_bf16x2(__fsub_rn(p0, bf16_lo(h)), __fsub_rn(p1, bf16_hi(h)));
@@ -329,36 +377,40 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
         l[r] = rv[r] ? __fadd_rn(__fmul_rn(l[r], alpha[r]), rs[r]) : l[r];
         m[r] = mnew[r];
       }
-      if (t > 0) {  // P V of the previous tile has completed: O and the P buffer are free
+      // P of this tile into TMEM buffer t & 1 (16x128b: thread (g, t4) column
+      // 4x + t4, rows g and g + 8: hi pairs of keys 8x + 2 t4 in x < 4, lo pairs
+      // after them).  The buffer's last reader, P V of tile t - 2, completed
+      // before the previous tile's wait below.
+      {
+        uint32_t pw[16];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          pw[2 * x] = ph[x][0];
+          pw[2 * x + 1] = ph[x][1];
+          pw[8 + 2 * x] = pl[x][0];
+          pw[8 + 2 * x + 1] = pl[x][1];
+        }
+        tmem_st16x128x8(frag + C::P_COL + (t & 1) * C::BNK, pw);
+      }
+      if (t > 0) {  // P V of the previous tile has completed: O is free
         if (!warp_wait(pv_done, (t - 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
+        // O * alpha; alpha = 1 leaves O's bits as they are
+        if (!__all_sync(0xffffffffu, alpha[0] == 1.0f && alpha[1] == 1.0f)) {
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        uint8_t* prow = sp + (lrow0 + gq + 8 * r) * 128 + t4 * 4;  // row & 7 == gq
+          for (int c = 0; c < HD / 32; ++c) {
+            float o[16];
+            tmem_ld16x4(frag + C::O_COL + 32 * c, o);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          *reinterpret_cast<uint32_t*>(prow + ((j ^ gq) << 4)) = ph[j][r];
-          *reinterpret_cast<uint32_t*>(prow + (((4 + j) ^ gq) << 4)) = pl[j][r];
+            for (int i = 0; i < 16; i += 2) mul2_rn(o[i], o[i + 1], alpha[(i >> 1) & 1]);
+            tmem_st16x4(frag + C::O_COL + 32 * c, o);
+          }
         }
       }
-      // O * alpha; alpha = 1 leaves O's bits as they are, and so does any
-      // alpha on the first tile (O is +0)
-      if (t > 0 && !__all_sync(0xffffffffu, alpha[0] == 1.0f && alpha[1] == 1.0f)) {
-#pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          float o[16];
-          tmem_ld16x4(frag + C::O_COL + 32 * c, o);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = __fmul_rn(o[i], alpha[(i >> 1) & 1]);
-          tmem_st16x4(frag + C::O_COL + 32 * c, o);
-        }
-        tmem_wait_st();
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full);
     }
@@ -422,6 +474,8 @@ bool attn_tc_supported(int hd) { return hd == 64 || hd == 128; }
 int launch_attention_tc(const CUtensorMap& kvmap_tc, const AttnArgs& a, int hd, int n_items, cudaStream_t s) {
   if (n_items <= 0) return VD_OK;
   if (a.fold) return fail(VD_ERR_INVALID_ARG, "split folding is for decode-class CTAs");
+  if (a.split > TcAttnCfg<128>::PIDS * 16)  // a CTA stages the ids of every page its split streams
+    return fail(VD_ERR_INVALID_ARG, "KV split larger than the staged page ids");
   if (hd == 64) return launch_attn_tc_t<64>(kvmap_tc, a, n_items, s);
   if (hd == 128) return launch_attn_tc_t<128>(kvmap_tc, a, n_items, s);
   return fail(VD_ERR_UNSUPPORTED, "the tcgen05 attention kernel takes head_dim 64 or 128");
