@@ -465,8 +465,10 @@ __global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
   load_part<PER>(a.part_o + (base + s0) * HD + lane * PER, O);
   // The partials of up to kBatch splits are loaded together (one memory
   // round trip per batch instead of one per split), then folded one by one
-  // in ascending split order exactly as before.
-  constexpr int kBatch = 8;
+  // in ascending split order exactly as before.  Four at a time keeps the
+  // registers low enough for ten CTAs per SM (eight at a time held 75
+  // registers and six CTAs: the kernel waits on memory and needs the warps).
+  constexpr int kBatch = 4;
   for (int sb = s0 + 1; sb <= s1; sb += kBatch) {
     float2 ml[kBatch];
     float P[kBatch][PER];
