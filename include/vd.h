@@ -214,8 +214,8 @@ int vd_set_attention_fold(vd_model* m, int32_t mode);
 /* Kernel of the prefill-class attention rows (q_len * Hq/Hkv > 16), with the
  * per-row traversal and arithmetic of 深入解析 Vosti §六 6.2 either way.
  * kernel 0 (default): 5th-generation tensor cores (tcgen05, accumulators in
- * tensor memory, 128 rows per CTA) for head dimensions 64 and 128, mma.sync
- * for 256; kernel 1: mma.sync (64 rows per CTA) for every head dimension.  A
+ * tensor memory, 128 rows per CTA) for head dimensions 64, 128 and 256;
+ * kernel 1: mma.sync (64 rows per CTA) for every head dimension.  A
  * tcgen05 K = 16 MMA step computes what an mma.sync m16n8k16 step computes,
  * bit for bit, and both kernels take the same steps in the same order, so
  * logits are bitwise identical under either choice.  Applies to the steps

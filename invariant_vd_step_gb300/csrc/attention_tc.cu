@@ -1,5 +1,5 @@
 // Prefill-class paged attention on 5th-generation tensor cores (tcgen05),
-// head dimensions 64 and 128.
+// head dimensions 64, 128 and 256.
 //
 // Same rows, tiles, splits and per-row arithmetic as the mma.sync kernel of
 // attention.cu (深入解析 Vosti §六 6.2: causal prefix equivalence, the
@@ -73,12 +73,18 @@ struct TcAttnCfg {
   static constexpr int HB = SK * 128;              // one hd block of a stage's K or V: [key][64]
   static constexpr int KV_BYTES = KB * HB;         // K or V of a stage: [hd block][key][64]
   static constexpr int STAGES = HD == 64 ? 4 : 2;  // K/V stages in flight (two tiles each)
+  // Softmax warps: eight hold 16 rows each; at hd 256 two warps share each 16
+  // rows (both run the same softmax; each owns 128 of O's columns)
+  static constexpr int NSW = HD == 256 ? 16 : 8;
+  static constexpr int NS = 32 * NSW;  // softmax threads
+  static constexpr int THREADS = 64 + NS;
+  static constexpr int OW = HD / (NSW / 8);  // O columns per softmax warp
   // TMEM: the scores of a stage's two tiles (SK columns), O (hd columns),
   // then two P buffers of BNK columns (hi and lo bf16 of a row's BNK keys,
   // two per column)
   static constexpr int O_COL = SK;
   static constexpr int P_COL = O_COL + HD;
-  static constexpr int TMEM_COLS = 256;
+  static constexpr int TMEM_COLS = HD == 256 ? 512 : 256;
   static_assert(P_COL + 2 * BNK <= TMEM_COLS, "TMEM columns per CTA");
   static constexpr int PIDS = 64;  // page ids of a split (at most 32 pages of 16 keys)
   static constexpr int SMEM = 1024 + Q_BYTES + STAGES * 2 * KV_BYTES + 256 + PIDS * 4;
@@ -90,7 +96,8 @@ struct TcAttnCfg {
 };
 
 template <int HD>
-__global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__ CUtensorMap kvmap, AttnArgs a) {
+__global__ void __launch_bounds__(TcAttnCfg<HD>::THREADS, HD == 256 ? 1 : 2)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap kvmap, AttnArgs a) {
   using C = TcAttnCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -163,10 +170,10 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 256);
-    mbar_init(p_full, 256);
+    mbar_init(s_free, C::NS);
+    mbar_init(p_full, C::NS);
     mbar_init(pv_done, 1);
-    mbar_init(q_full, 256);
+    mbar_init(q_full, C::NS);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -256,25 +263,28 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
       umma_commit(mma_done);
     }
   } else {
-    // ---- softmax warps 2..9: warp w holds CTA rows (TMEM lanes) 32 (w % 4) + 16 h .. + 15, h = (w - 2) / 4,
-    // as an mma.sync m16n8 C fragment: thread (g, t4) has rows g and g + 8, keys 8 j + 2 t4 + {0, 1}
-    const int st = threadIdx.x - 64;  // 0..255
-    {  // Q -> [hd block][row][64], 128-byte swizzle; zeros for rows past the block.  Two threads a row.
-      const int qr = st >> 1, half = st & 1;
-      const int row = r0 + qr;
-      const bool valid = row < rows;
-      const int tok = row / G, hq = kvh * G + row % G;
-      const uint4* qs = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(q0 + tok) * a.Hq + hq) * HD);
+    // ---- softmax warps 2 .. NSW + 1: warp w holds CTA rows (TMEM lanes) 32 (w % 4) + 16 h .. + 15,
+    // h = ((w - 2) / 4) % 2, and O's columns 128 hs .. + 127, hs = (w - 2) / 8, as an mma.sync m16n8 C
+    // fragment: thread (g, t4) has rows g and g + 8, keys 8 j + 2 t4 + {0, 1}
+    const int st = threadIdx.x - 64;  // 0 .. NS - 1
+    {  // Q -> [hd block][row][64], 128-byte swizzle; zeros for rows past the block
+      constexpr int CH = HD / 8;  // 16-byte chunks of a row
 #pragma unroll
-      for (int i = 0; i < HD / 16; ++i) {
-        const int c16 = half * (HD / 16) + i;
+      for (int i = 0; i < C::ROWS * CH / C::NS; ++i) {
+        const int idx = st + i * C::NS, qr = idx / CH, c16 = idx % CH;
+        const int row = r0 + qr;
+        const bool valid = row < rows;
+        const int tok = row / G, hq = kvh * G + row % G;
+        const uint4* qs = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(q0 + tok) * a.Hq + hq) * HD);
         const uint4 v = valid ? qs[c16] : make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(sq + (c16 >> 3) * (C::ROWS * 128) + qr * 128 + (((c16 & 7) ^ (qr & 7)) << 4)) = v;
       }
       fence_proxy_async_smem();
       mbar_arrive(q_full);
     }
-    const int lrow0 = 32 * (warp & 3) + 16 * ((warp - 2) >> 2);  // first CTA row of this warp
+    const int lrow0 = 32 * (warp & 3) + 16 * (((warp - 2) >> 2) & 1);  // first CTA row of this warp
+    const int ocol = C::O_COL + 128 * ((warp - 2) >> 3);             // first O column of this warp
+    const bool writes_p = warp - 2 < 8;                              // one warp of a pair writes P and m, l
     const uint32_t frag = tmem + (static_cast<uint32_t>(lrow0) << 16);
     const int gq = lane >> 2, t4 = lane & 3;
     int pos[2], lo[2], tok[2], hq[2];
@@ -293,7 +303,7 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
 #pragma unroll
       for (int i = 0; i < 16; ++i) z[i] = 0.f;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) tmem_st16x4(frag + C::O_COL + 32 * c, z);
+      for (int c = 0; c < C::OW / 32; ++c) tmem_st16x4(frag + ocol + 32 * c, z);
       tmem_wait_st();
     }
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
@@ -390,7 +400,7 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
           pw[8 + 2 * x] = pl[x][0];
           pw[8 + 2 * x + 1] = pl[x][1];
         }
-        tmem_st16x128x8(frag + C::P_COL + (t & 1) * C::BNK, pw);
+        if (writes_p) tmem_st16x128x8(frag + C::P_COL + (t & 1) * C::BNK, pw);
       }
       if (t > 0) {  // P V of the previous tile has completed: O is free
         if (!warp_wait(pv_done, (t - 1) & 1)) {
@@ -401,12 +411,12 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
         // O * alpha; alpha = 1 leaves O's bits as they are
         if (!__all_sync(0xffffffffu, alpha[0] == 1.0f && alpha[1] == 1.0f)) {
 #pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
+          for (int c = 0; c < C::OW / 32; ++c) {
             float o[16];
-            tmem_ld16x4(frag + C::O_COL + 32 * c, o);
+            tmem_ld16x4(frag + ocol + 32 * c, o);
 #pragma unroll
             for (int i = 0; i < 16; i += 2) mul2_rn(o[i], o[i + 1], alpha[(i >> 1) & 1]);
-            tmem_st16x4(frag + C::O_COL + 32 * c, o);
+            tmem_st16x4(frag + ocol + 32 * c, o);
           }
         }
       }
@@ -422,16 +432,16 @@ __global__ void __launch_bounds__(320, 2) attn_tc_kernel(const __grid_constant__
       for (int r = 0; r < 2; ++r) {
         if (!valid[r] || m[r] == -INFINITY) continue;
         const size_t base = (static_cast<size_t>(q0 + tok[r]) * a.Hq + hq[r]) * a.max_splits + sidx;
-        if (t4 == 0) {
+        if (t4 == 0 && writes_p) {
           a.part_ml[base * 2] = m[r];
           a.part_ml[base * 2 + 1] = l[r];
         }
-        po[r] = a.part_o + base * HD + 2 * t4;
+        po[r] = a.part_o + base * HD + (ocol - C::O_COL) + 2 * t4;
       }
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < C::OW / 32; ++c) {
         float o[16];
-        tmem_ld16x4(frag + C::O_COL + 32 * c, o);
+        tmem_ld16x4(frag + ocol + 32 * c, o);
 #pragma unroll
         for (int r = 0; r < 2; ++r)
           if (po[r]) {
@@ -463,13 +473,13 @@ int launch_attn_tc_t(const CUtensorMap& kvmap, const AttnArgs& a, int n_items, c
     VD_CUDA_TRY(cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     configured = true;
   }
-  VD_CUDA_TRY(launch_k(attn_tc_kernel<HD>, dim3(n_items), dim3(320), C::SMEM, s, kvmap, a));
+  VD_CUDA_TRY(launch_k(attn_tc_kernel<HD>, dim3(n_items), dim3(C::THREADS), C::SMEM, s, kvmap, a));
   return VD_OK;
 }
 
 }  // namespace
 
-bool attn_tc_supported(int hd) { return hd == 64 || hd == 128; }
+bool attn_tc_supported(int hd) { return hd == 64 || hd == 128 || hd == 256; }
 
 int launch_attention_tc(const CUtensorMap& kvmap_tc, const AttnArgs& a, int hd, int n_items, cudaStream_t s) {
   if (n_items <= 0) return VD_OK;
@@ -478,7 +488,8 @@ int launch_attention_tc(const CUtensorMap& kvmap_tc, const AttnArgs& a, int hd, 
     return fail(VD_ERR_INVALID_ARG, "KV split larger than the staged page ids");
   if (hd == 64) return launch_attn_tc_t<64>(kvmap_tc, a, n_items, s);
   if (hd == 128) return launch_attn_tc_t<128>(kvmap_tc, a, n_items, s);
-  return fail(VD_ERR_UNSUPPORTED, "the tcgen05 attention kernel takes head_dim 64 or 128");
+  if (hd == 256) return launch_attn_tc_t<256>(kvmap_tc, a, n_items, s);
+  return fail(VD_ERR_UNSUPPORTED, "the tcgen05 attention kernel takes head_dim 64, 128 or 256");
 }
 
 }  // namespace vd

@@ -367,7 +367,7 @@ class Model:
         check(lib().vd_set_attention_fold(self.h, int(mode)))
 
     def set_attention_prefill(self, kernel: int):
-        """Prefill-class attention kernel: 0 default (tcgen05 for head dims 64 and 128), 1 mma.sync."""
+        """Prefill-class attention kernel: 0 default (tcgen05), 1 mma.sync."""
         check(lib().vd_set_attention_prefill(self.h, int(kernel)))
 
     def set_graph_mode(self, max_graphs: int):

@@ -1,7 +1,7 @@
 """The tcgen05 prefill attention kernel against the mma.sync one and the oracle.
 
 Prefill-class rows (q_len * Hq/Hkv > 16) run on tcgen05 by default for head
-dims 64 and 128 (128 rows per CTA, accumulators in tensor memory) and on
+dims 64, 128 and 256 (128 rows per CTA, accumulators in tensor memory) and on
 mma.sync when asked (64 rows per CTA).  Both take the per-row steps of the
 unified traversal (深入解析 Vosti §六 6.2) in the same order, and a tcgen05
 K = 16 step computes what an mma.sync m16n8k16 step computes, so every row
@@ -42,7 +42,7 @@ SCHEDULES = [
 ]
 
 
-@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("hd", [64, 128, 256])
 def test_tc_equals_mma_sync_bitwise_and_matches_oracle(hd):
     ready()
     lens = [1100, 300, 77, 5]
