@@ -52,9 +52,10 @@ def test_tc_equals_mma_sync_bitwise_and_matches_oracle(hd):
         check_parity(sc, res)
 
 
-def test_tc_sliding_window():
+@pytest.mark.parametrize("hd", [128, 256])
+def test_tc_sliding_window(hd):
     ready()
-    spec = SPECS[128].with_(sliding_window=100, local_global_period=1000)
+    spec = SPECS[hd].with_(sliding_window=100, local_global_period=1000)
     lens = [700, 101, 40]
     sc = Scenario(spec, lens, num_pages=120, seed=41)
     for parts in ([(0, 0, 700)], [(0, 600, 100), (1, 0, 101), (2, 0, 40)], [(0, 150, 9)]):
