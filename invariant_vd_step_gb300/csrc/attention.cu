@@ -183,9 +183,14 @@ __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)
 
 // NW warps per CTA; groups of DS warps own the same 16 rows and split the
 // head dimension between them (DS = 2 for decode-shaped CTAs, which have one
-// row block only; DS = 1 for prefill CTAs).
-template <int HD, int NW, int DS, bool FOLD>
-__global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ CUtensorMap kvmap, AttnArgs a) {
+// row block only; DS = 1 for prefill CTAs).  PROD: one more warp issues the
+// K/V copies, and each warp releases a stage on its own as soon as it is done
+// with it, instead of all warps meeting at a barrier after every tile (a
+// launch with one CTA per SM has no other CTA to hide that barrier and the
+// copy issue behind).
+template <int HD, int NW, int DS, bool FOLD, bool PROD = false>
+__global__ void __launch_bounds__((NW + PROD) * 32)
+    attn_kernel(const __grid_constant__ CUtensorMap kvmap, AttnArgs a) {
   using C = AttnCfg<HD>;
   constexpr int RB = 16 * NW / DS;  // rows per CTA
   constexpr int ND = HD / DS;       // output dims per warp
@@ -195,6 +200,7 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * 2 * C::TILE_BYTES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + C::MAX_STAGES);
   __shared__ int pid_s[C::PIDS];
+  __shared__ uint64_t empty_s[PROD ? C::MAX_STAGES : 1];  // PROD: the NW warps are done with a stage
 
   pdl_wait();
   pdl_trigger();
@@ -252,6 +258,8 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
 
   if (threadIdx.x == 0) {
     for (int k = 0; k < NS; ++k) mbar_init(&full[k], 1);
+    if constexpr (PROD)
+      for (int k = 0; k < NS; ++k) mbar_init(&empty_s[k], NW);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -282,13 +290,28 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
     }
   };
   int issued = 0;
-  if (threadIdx.x == 0) {
+  if (!PROD && threadIdx.x == 0) {
     issued = min(NS, ntiles);
     for (int k = 0; k < issued; ++k) issue(k, k);
   }
 
   // ---- this warp's rows
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if constexpr (PROD) {
+    if (warp == NW) {  // the copy warp: a stage is refilled once every warp has released it
+      if (lane == 0) {
+        for (int g = 0; g < ntiles && !*abort_flag; ++g) {
+          const int s = g % NS;
+          if (g >= NS && !mbar_wait(&empty_s[s], ((g / NS) - 1) & 1, abort_flag, a.status)) break;
+          issue(g, s);
+          issued = g + 1;
+        }
+        // every copy lands before this warp leaves (the last use of each stage)
+        for (int k = max(0, issued - NS); k < issued; ++k) drain_wait(&full[k % NS], (k / NS) & 1);
+      }
+      return;
+    }
+  }
   const int gq = lane >> 2, t4 = lane & 3;
   const int dim0 = (warp % DS) * ND;
   int pos[2], lo[2], tok[2], hq[2];
@@ -335,7 +358,11 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
   int it = 0, stg = 0;
   uint32_t ph = 0;  // tile it sits in stage it % NS, round it / NS
   for (; it < ntiles; ++it) {
-    if (!mbar_wait(&full[stg], ph, abort_flag, a.status)) ok = false;
+    if constexpr (PROD) {  // the warp's lanes agree, then the warp leaves or goes on
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[stg], ph, abort_flag, a.status))) break;
+    } else if (!mbar_wait(&full[stg], ph, abort_flag, a.status)) {
+      ok = false;
+    }
     const int key0 = (tile_lo + it) * C::BNK;
     bool mine = false;  // any row of this warp sees a key of this tile
 #pragma unroll
@@ -380,18 +407,23 @@ __global__ void __launch_bounds__(NW * 32) attn_kernel(const __grid_constant__ C
 #pragma unroll
       for (int n = 0; n < ND / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
     }
-    if (__syncthreads_or(!ok)) break;
-    if (threadIdx.x == 0 && it + NS < ntiles) {
-      issue(it + NS, stg);
-      issued = it + NS + 1;
+    if constexpr (PROD) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_s[stg]);
+    } else {
+      if (__syncthreads_or(!ok)) break;
+      if (threadIdx.x == 0 && it + NS < ntiles) {
+        issue(it + NS, stg);
+        issued = it + NS + 1;
+      }
     }
     if (++stg == NS) {
       stg = 0;
       ph ^= 1u;
     }
   }
-  if (it < ntiles) {  // gave up: let copies in flight land before leaving
-    if (threadIdx.x == 0)
+  if (it < ntiles) {  // gave up: let copies in flight land before leaving (PROD: the copy warp does)
+    if (!PROD && threadIdx.x == 0)
       for (int k = it; k < issued; ++k) drain_wait(&full[k % NS], (k / NS) & 1);
     return;
   }
@@ -509,33 +541,35 @@ int sm_count_attn() {
 // fit on the GPU at once, so that few work items (small batches) keep as many
 // key tiles in flight per SM as a full wave of 2-stage CTAs does.
 template <int HD>
-int attn_stages(int n_items) {
+int attn_stages(int n_items, int static_smem) {
   using C = AttnCfg<HD>;
   constexpr int kSmemPerSM = 228 * 1024, kSmemPerCTA = 227 * 1024;
   for (int ns = C::MAX_STAGES; ns > 2; --ns) {
-    if (C::smem(ns) + C::STATIC_SMEM > kSmemPerCTA) continue;
+    if (C::smem(ns) + static_smem > kSmemPerCTA) continue;
     const long long slots =
-        static_cast<long long>(sm_count_attn()) * (kSmemPerSM / (C::smem(ns) + C::STATIC_SMEM + 1024));
+        static_cast<long long>(sm_count_attn()) * (kSmemPerSM / (C::smem(ns) + static_smem + 1024));
     if (slots >= n_items) return ns;
   }
   return 2;
 }
 
-template <int HD, int NW, int DS, bool FOLD>
+template <int HD, int NW, int DS, bool FOLD, bool PROD = false>
 int launch_attn_t(const CUtensorMap& kvmap, const AttnArgs& a0, int n_items, cudaStream_t s) {
   using C = AttnCfg<HD>;
+  constexpr int kStatic = C::STATIC_SMEM + (PROD ? C::MAX_STAGES * 8 : 0);  // + the release barriers
   static bool configured = false;
   if (!configured) {
     int max_ns = C::MAX_STAGES;
-    while (C::smem(max_ns) + C::STATIC_SMEM > 227 * 1024) --max_ns;
-    VD_CUDA_TRY(cudaFuncSetAttribute(attn_kernel<HD, NW, DS, FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    while (C::smem(max_ns) + kStatic > 227 * 1024) --max_ns;
+    VD_CUDA_TRY(cudaFuncSetAttribute(attn_kernel<HD, NW, DS, FOLD, PROD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::smem(max_ns)));
     configured = true;
   }
   AttnArgs a = a0;
-  a.stages = attn_stages<HD>(n_items);
+  a.stages = attn_stages<HD>(n_items, kStatic);
   VD_CUDA_TRY(
-      launch_k(attn_kernel<HD, NW, DS, FOLD>, dim3(n_items), dim3(NW * 32), C::smem(a.stages), s, kvmap, a));
+      launch_k(attn_kernel<HD, NW, DS, FOLD, PROD>, dim3(n_items), dim3((NW + PROD) * 32), C::smem(a.stages), s, kvmap,
+               a));
   return VD_OK;
 }
 
@@ -576,7 +610,7 @@ int launch_attention(const CUtensorMap& kvmap, const AttnArgs& a, int hd, bool p
   if (hd == HD_)                                                                              \
     return prefill_class ? launch_attn_t<HD_, 4, 1, false>(kvmap, a, n_items, s)               \
            : a.fold      ? launch_attn_t<HD_, 2, 2, true>(kvmap, a, n_items, s)                \
-           : wide        ? launch_attn_t<HD_, 4, 4, false>(kvmap, a, n_items, s)               \
+           : wide        ? launch_attn_t<HD_, 4, 4, false, true>(kvmap, a, n_items, s)         \
                          : launch_attn_t<HD_, 2, 2, false>(kvmap, a, n_items, s);
   VD_ATTN_LAUNCH(64)
   VD_ATTN_LAUNCH(128)
