@@ -25,14 +25,15 @@
 // row run here equals the same row run by the mma.sync decode or prefill
 // kernel; the attention tests check that bitwise.
 //
-// Roles (320 threads): warp 0 allocates TMEM, reads the split's page ids
-// and one lane issues the K/V page copies (3-D TMA boxes of one page and 64
-// head dims, so that the K or V of a stage, two tiles, is [hd block][64
-// keys][64] with the 128-byte swizzle, the canonical operand layout); warp 1,
-// one lane, issues the MMAs; warps 2..9 each hold 16 rows, read from TMEM in
-// the layout of an mma.sync C fragment (two rows and eight keys per thread),
-// and run the softmax, the O rescale and the epilogue with the mma.sync
-// kernel's per-row code.  S of a stage's two tiles is one chain of N = 64
+// Roles (320 threads; 576 at hd 256): warp 0 allocates TMEM, reads the
+// split's page ids and one lane issues the K/V page copies (3-D TMA boxes of
+// one page and 64 head dims, so that the K or V of a stage, two tiles, is [hd
+// block][64 keys][64] with the 128-byte swizzle, the canonical operand
+// layout); warp 1, one lane, issues the MMAs; the softmax warps (8, or 16 at
+// hd 256, two for each 16 rows) each hold 16 rows, read from TMEM in the
+// layout of an mma.sync C fragment (two rows and eight keys per thread), and
+// run the softmax, the O rescale and the epilogue with the mma.sync kernel's
+// per-row code.  S of a stage's two tiles is one chain of N = 64
 // MMAs (an MMA's N does not change an element) into 64 TMEM columns, issued
 // once the softmax has read the previous stage's scores.  P (hi and lo bf16,
 // two per 32-bit column) goes to one of two TMEM buffers and is the A operand
