@@ -16,7 +16,7 @@ import pytest
 
 from attn_scenario import SPECS, Scenario, check_parity
 from gpu_util import bits, ready
-from invariant_vd_step_gb300 import synth
+from invariant_vd_step_gb300 import synth, vd
 
 pytestmark = pytest.mark.gpu
 
@@ -85,3 +85,13 @@ def test_tc_rows_equal_decode_rows():
     for r, p in [(0, 0), (0, 31), (0, 32), (0, 511), (0, 512), (0, 1029), (1, 127), (1, 128), (1, 199)]:
         one = sc.run([(r, p, 1)])
         np.testing.assert_array_equal(bits(one[(r, p)]), bits(full[(r, p)]), err_msg=f"row {(r, p)}")
+
+
+def test_prefill_kernel_choice_is_validated():
+    ready()
+    sc = Scenario(SPECS[128], [40], num_pages=8, seed=49)
+    for bad in (-1, 2, 7):
+        with pytest.raises(vd.VDError):
+            sc.model.set_attention_prefill(bad)
+    sc.model.set_attention_prefill(1)
+    sc.model.set_attention_prefill(0)
