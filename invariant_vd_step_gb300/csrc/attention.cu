@@ -65,19 +65,20 @@ struct RowState {
   float o[ND / 8][4];   // mma C fragments of the ND output dims this warp owns
 };
 
-// One key tile for the 16 rows of a warp, which accumulates output dims
-// [dim0, dim0 + ND).  S and the softmax state are computed over the full
-// head either way, so every output element gets the same instruction chain
-// whether one warp owns all dims or several warps share them.  LOWER8: rows
-// 8..15 of the warp are known to hold no row (a decode CTA of at most 8
-// rows), so their masking, softmax and rescale are skipped: their weights
-// are exactly 0 either way, and the other rows' instructions are unchanged.
-template <int HD, int BNK, int ND, bool LOWER8>
-__device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)[HD / 16][4], uint32_t kbase,
-                                          uint32_t vbase, int key0, const int (&pos)[2], const int (&lo)[2],
-                                          float scale_log2, int lane, int dim0) {
-  const int t4 = lane & 3, mi = lane >> 3, r8 = lane & 7;
-  float s[BNK / 8][4];
+// The steps of one key tile for the 16 rows of a warp (rows g and g + 8 of
+// lane (g, t4)).  `attn_tile` runs them back to back, one tile at a time;
+// the scores-first decode kernel runs the same steps over a whole split in
+// three phases.  Either way every row's values pass through the same
+// operations in the same order.  LOWER8: rows 8..15 of the warp are known
+// to hold no row (a decode CTA of at most 8 rows), so their masking,
+// softmax and rescale are skipped: their weights are exactly 0 either way,
+// and the other rows' instructions are unchanged.
+
+// S = Q K^T of a 32-key tile: per 8-key block, HD/16 K = 16 steps from zero.
+template <int HD, int BNK>
+__device__ __forceinline__ void tile_scores(float (&s)[BNK / 8][4], const uint32_t (&qf)[HD / 16][4], uint32_t kbase,
+                                            int lane) {
+  const int mi = lane >> 3, r8 = lane & 7;
 #pragma unroll
   for (int j = 0; j < BNK / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
 #pragma unroll
@@ -90,7 +91,15 @@ __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)
       mma_bf16_16816(s[2 * jp + 1], qf[kk], b + 2);
     }
   }
-  float mx[2] = {-INFINITY, -INFINITY};
+}
+
+// Scores to the log2 domain, -inf outside each row's keys [lo, pos]; the
+// tile's maximum of rows g and g + 8 over the lane quad.
+template <int BNK, bool LOWER8>
+__device__ __forceinline__ void tile_mask_max(float (&s)[BNK / 8][4], float (&mx)[2], int key0, const int (&pos)[2],
+                                              const int (&lo)[2], float scale_log2, int lane) {
+  const int t4 = lane & 3;
+  mx[0] = mx[1] = -INFINITY;
 #pragma unroll
   for (int j = 0; j < BNK / 8; ++j) {
 #pragma unroll
@@ -107,27 +116,31 @@ __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)
       mx[r] = fmaxf(mx[r], v);
     }
   }
-  float mnew[2], alpha[2];
-  bool rv[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    if (LOWER8 && r == 1) {  // no row: the state stays as it is, as a fully masked row's does
-      rv[r] = false;
-      mnew[r] = st.m[r];
-      alpha[r] = 1.0f;
-      continue;
-    }
+    if (LOWER8 && r == 1) continue;  // stays -inf: the row keeps its state
     mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
     mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-    rv[r] = mx[r] != -INFINITY;
-    mnew[r] = rv[r] ? fmaxf(st.m[r], mx[r]) : st.m[r];
-    alpha[r] = rv[r] ? ex2(__fsub_rn(st.m[r], mnew[r])) : 1.0f;
   }
-  // P enters the P V product as two bf16 terms, hi = bf16(p) and
-  // lo = bf16(p - hi) (p - hi is exact in fp32), so the weights carry about
-  // 16 significant bits; the row sum uses the fp32 weights.
-  uint32_t pa[BNK / 16][4], pl[BNK / 16][4];
-  float rs[2] = {0.f, 0.f};
+}
+
+// The running maximum after a tile with row maximum mx, the factor that
+// rescales the state before it, and whether the row saw a key in it (a row
+// that saw none keeps its state bit for bit: alpha = 1, m unchanged).
+__device__ __forceinline__ void tile_running_max(float m, float mx, float& mnew, float& alpha, bool& rv) {
+  rv = mx != -INFINITY;
+  mnew = rv ? fmaxf(m, mx) : m;
+  alpha = rv ? ex2(__fsub_rn(m, mnew)) : 1.0f;
+}
+
+// P = 2^(s - m_new) as the A fragments of the P V product, and the fp32 row
+// sums over the quad.  P enters the product as two bf16 terms, hi = bf16(p)
+// and lo = bf16(p - hi) (p - hi is exact in fp32), so the weights carry
+// about 16 significant bits; the row sum uses the fp32 weights.
+template <int BNK, bool LOWER8>
+__device__ __forceinline__ void tile_probs(const float (&s)[BNK / 8][4], const float (&mnew)[2],
+                                           uint32_t (&pa)[BNK / 16][4], uint32_t (&pl)[BNK / 16][4], float (&rs)[2]) {
+  rs[0] = rs[1] = 0.f;
 #pragma unroll
   for (int j = 0; j < BNK / 8; ++j) {
     float p[4], h[4], l[4];
@@ -154,18 +167,35 @@ __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)
     if (LOWER8 && r == 1) continue;
     rs[r] = __fadd_rn(rs[r], __shfl_xor_sync(0xffffffffu, rs[r], 1));
     rs[r] = __fadd_rn(rs[r], __shfl_xor_sync(0xffffffffu, rs[r], 2));
-    st.l[r] = rv[r] ? __fadd_rn(__fmul_rn(st.l[r], alpha[r]), rs[r]) : st.l[r];
-    st.m[r] = mnew[r];
   }
+}
+
+// l <- l alpha + (the tile's row sum) for a row that saw a key of the tile.
+__device__ __forceinline__ void tile_update_l(float& l, float alpha, float rs, bool rv) {
+  l = rv ? __fadd_rn(__fmul_rn(l, alpha), rs) : l;
+}
+
+// O <- O alpha (with LOWER8 rows 8..15 have alpha 1 and are never stored).
+template <int ND, bool LOWER8>
+__device__ __forceinline__ void tile_rescale(float (&o)[ND / 8][4], const float (&alpha)[2]) {
 #pragma unroll
   for (int n = 0; n < ND / 8; ++n) {
-    st.o[n][0] = __fmul_rn(st.o[n][0], alpha[0]);
-    st.o[n][1] = __fmul_rn(st.o[n][1], alpha[0]);
-    if (!LOWER8) {  // rows 8..15 (with LOWER8 their alpha is 1, and their sums are never stored)
-      st.o[n][2] = __fmul_rn(st.o[n][2], alpha[1]);
-      st.o[n][3] = __fmul_rn(st.o[n][3], alpha[1]);
+    o[n][0] = __fmul_rn(o[n][0], alpha[0]);
+    o[n][1] = __fmul_rn(o[n][1], alpha[0]);
+    if (!LOWER8) {
+      o[n][2] = __fmul_rn(o[n][2], alpha[1]);
+      o[n][3] = __fmul_rn(o[n][3], alpha[1]);
     }
   }
+}
+
+// O += P_hi V, P_lo V over the tile's two 16-key steps, for the output dims
+// [dim0, dim0 + ND); per 8-dim block the order is hi, lo, hi, lo.  Each V
+// fragment is loaded right before its products (the tile-at-a-time order).
+template <int HD, int BNK, int ND>
+__device__ __forceinline__ void tile_pv(float (&o)[ND / 8][4], const uint32_t (&pa)[BNK / 16][4],
+                                        const uint32_t (&pl)[BNK / 16][4], uint32_t vbase, int lane, int dim0) {
+  const int mi = lane >> 3, r8 = lane & 7;
   const int np0 = dim0 / 16;
 #pragma unroll
   for (int ks = 0; ks < BNK / 16; ++ks) {
@@ -173,12 +203,69 @@ __device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)
     for (int np = 0; np < ND / 16; ++np) {
       uint32_t b[4];
       ldmatrix_x4_trans(b, vbase + kv_off<HD>(ks * 16 + (mi & 1) * 8 + r8, (np0 + np) * 2 + (mi >> 1)));
-      mma_bf16_16816(st.o[2 * np], pa[ks], b);
-      mma_bf16_16816(st.o[2 * np], pl[ks], b);
-      mma_bf16_16816(st.o[2 * np + 1], pa[ks], b + 2);
-      mma_bf16_16816(st.o[2 * np + 1], pl[ks], b + 2);
+      mma_bf16_16816(o[2 * np], pa[ks], b);
+      mma_bf16_16816(o[2 * np], pl[ks], b);
+      mma_bf16_16816(o[2 * np + 1], pa[ks], b + 2);
+      mma_bf16_16816(o[2 * np + 1], pl[ks], b + 2);
     }
   }
+}
+
+// The same products in two steps, so that a tile's V fragments can be
+// loaded while the previous tile's products run: the fragments for the
+// output dims [dim0, dim0 + ND) per 16-key step and 16-dim block ...
+template <int HD, int BNK, int ND>
+__device__ __forceinline__ void tile_v_frags(uint32_t (&vb)[BNK / 16][ND / 16][4], uint32_t vbase, int lane,
+                                             int dim0) {
+  const int mi = lane >> 3, r8 = lane & 7;
+  const int np0 = dim0 / 16;
+#pragma unroll
+  for (int ks = 0; ks < BNK / 16; ++ks)
+#pragma unroll
+    for (int np = 0; np < ND / 16; ++np)
+      ldmatrix_x4_trans(vb[ks][np], vbase + kv_off<HD>(ks * 16 + (mi & 1) * 8 + r8, (np0 + np) * 2 + (mi >> 1)));
+}
+
+// ... then the products, in tile_pv's order.
+template <int BNK, int ND>
+__device__ __forceinline__ void tile_pv_mma(float (&o)[ND / 8][4], const uint32_t (&pa)[BNK / 16][4],
+                                            const uint32_t (&pl)[BNK / 16][4],
+                                            const uint32_t (&vb)[BNK / 16][ND / 16][4]) {
+#pragma unroll
+  for (int ks = 0; ks < BNK / 16; ++ks) {
+#pragma unroll
+    for (int np = 0; np < ND / 16; ++np) {
+      mma_bf16_16816(o[2 * np], pa[ks], vb[ks][np]);
+      mma_bf16_16816(o[2 * np], pl[ks], vb[ks][np]);
+      mma_bf16_16816(o[2 * np + 1], pa[ks], vb[ks][np] + 2);
+      mma_bf16_16816(o[2 * np + 1], pl[ks], vb[ks][np] + 2);
+    }
+  }
+}
+
+// One key tile for the 16 rows of a warp, which accumulates output dims
+// [dim0, dim0 + ND).  S and the softmax state are computed over the full
+// head either way, so every output element gets the same instruction chain
+// whether one warp owns all dims or several warps share them.
+template <int HD, int BNK, int ND, bool LOWER8>
+__device__ __forceinline__ void attn_tile(RowState<ND>& st, const uint32_t (&qf)[HD / 16][4], uint32_t kbase,
+                                          uint32_t vbase, int key0, const int (&pos)[2], const int (&lo)[2],
+                                          float scale_log2, int lane, int dim0) {
+  float s[BNK / 8][4], mx[2], mnew[2], alpha[2], rs[2];
+  bool rv[2];
+  uint32_t pa[BNK / 16][4], pl[BNK / 16][4];
+  tile_scores<HD, BNK>(s, qf, kbase, lane);
+  tile_mask_max<BNK, LOWER8>(s, mx, key0, pos, lo, scale_log2, lane);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) tile_running_max(st.m[r], mx[r], mnew[r], alpha[r], rv[r]);
+  tile_probs<BNK, LOWER8>(s, mnew, pa, pl, rs);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    tile_update_l(st.l[r], alpha[r], rs[r], rv[r]);
+    st.m[r] = mnew[r];
+  }
+  tile_rescale<ND, LOWER8>(st.o, alpha);
+  tile_pv<HD, BNK, ND>(st.o, pa, pl, vbase, lane, dim0);
 }
 
 // NW warps per CTA; groups of DS warps own the same 16 rows and split the
@@ -456,6 +543,348 @@ __global__ void __launch_bounds__((NW + PROD) * 32)
   }
 }
 
+// Scores-first decode CTA, for launches of at most one CTA per SM (small
+// batches) at head dims 64 and 128.  There the tile-at-a-time kernel's time
+// is one chain of dependent steps over the split's 16 tiles, each waiting
+// for its copies.  One block of at most 16 rows, one split of at most
+// kSfTiles tiles.  Warp 4 issues the copies, one tile per lane: every K
+// tile into a slot of its own, the first V_OWN V tiles into slots of their
+// own (one barrier for all of them), the remaining V tiles into K slots as
+// the warps that scored those K tiles release them (one barrier again).
+// Warps 0..3 run three phases:
+//   1. scores: warp w takes S, the mask and the row maxima of tiles
+//      w, w + 4, ..., keeps S in registers and posts the maxima;
+//   2. weights: every warp runs the running maximum over all the tiles'
+//      maxima (keeping each tile's rescale factor), then turns its own
+//      tiles' S into P (the bf16 hi/lo A fragments, posted to shared
+//      memory) and row sums;
+//   3. P V: every warp folds the tiles in order into its quarter of the
+//      head dimension: l and O rescaled, then the P V steps.
+// Each value is computed by the same step functions as in `attn_tile`,
+// from the same inputs, so every row's partial is bit for bit the one the
+// tile-at-a-time kernels write; what changes is that only O's rescale and
+// P V remain a chain from tile to tile, and that no step waits for a copy
+// once the scores are in.
+constexpr int kSfTiles = 16;  // tiles of a 512-key split
+constexpr int kSfWarps = 4;
+
+template <int HD>
+struct SfCfg {
+  using C = AttnCfg<HD>;
+  static constexpr int P_BYTES = kSfTiles * 4 * 32 * 16;  // [tile][hi0, hi1, lo0, lo1][lane]: 16 B each
+  static constexpr int STATIC_SMEM = C::PIDS * 4 + 2 * kSfTiles * 16 * 4 + 16;
+  static constexpr int BAR_BYTES = (2 * kSfTiles + 2) * 8 + 16;
+  static constexpr int FIXED = 1024 + P_BYTES + kSfTiles * C::TILE_BYTES + BAR_BYTES + STATIC_SMEM;
+  static constexpr int V_FIT = (227 * 1024 - FIXED) / C::TILE_BYTES;
+  static constexpr int V_OWN = V_FIT < kSfTiles ? V_FIT : kSfTiles;  // V tiles with slots of their own
+  static constexpr int SMEM = 1024 + P_BYTES + (kSfTiles + V_OWN) * C::TILE_BYTES + BAR_BYTES;
+  static_assert(V_OWN >= 1 && kSfTiles - V_OWN <= 32, "one lane per reused slot");
+};
+
+template <int HD>
+struct SfShared {
+  uint8_t* kslot;  // K tile t in slot t; V tile V_OWN + j later in slot j
+  uint8_t* vslot;  // V tiles 0 .. V_OWN - 1
+  uint4* pbuf;
+  uint64_t* kfull;   // [kSfTiles] K tile t landed
+  uint64_t* kempty;  // [kSfTiles] K tile t scored (its slot is free)
+  uint64_t* vfull;   // [2] the V tiles in slots of their own / in K slots landed
+  volatile int* abort_flag;
+  float (*tmax)[16];  // [tile][row] row maxima of the tile's scores
+  float (*rsum)[16];  // [tile][row] row sums of the tile's weights
+  __device__ uint32_t vaddr(int t) const {
+    return smem_u32(t < SfCfg<HD>::V_OWN ? vslot + t * AttnCfg<HD>::TILE_BYTES
+                                         : kslot + (t - SfCfg<HD>::V_OWN) * AttnCfg<HD>::TILE_BYTES);
+  }
+};
+
+// FULL: the split has all kSfTiles tiles (every split but a context's last
+// and, under a window, its first), so that every loop has a fixed trip count
+// and each round is straight-line code.
+template <int HD, bool LOWER8, bool FULL>
+__device__ __forceinline__ void sf_rows(const AttnArgs& a, const SfShared<HD>& sh, int ntiles, int tile_lo,
+                                        const uint32_t (&qf)[HD / 16][4], const int (&pos)[2], const int (&lo)[2],
+                                        const bool (&valid)[2], size_t base0, size_t base1, int warp, int lane) {
+  using C = AttnCfg<HD>;
+  constexpr int ND = HD / kSfWarps, KS = C::BNK / 16, NP = ND / 16;
+  constexpr int V_OWN = SfCfg<HD>::V_OWN;
+  constexpr int ROUNDS = kSfTiles / kSfWarps;
+  const int nt = FULL ? kSfTiles : ntiles;
+  const int gq = lane >> 2, t4 = lane & 3;
+  const int dim0 = warp * ND;
+  bool ok = true;
+  auto wait = [&](uint64_t* bar) {
+    ok = ok && __all_sync(0xffffffffu, mbar_wait(bar, 0, sh.abort_flag, a.status));
+  };
+
+  // ---- 1. scores of this warp's tiles.  Every tile of the CTA's key range
+  // holds a key that some row sees (the rows' ranges [lo, pos] belong to
+  // consecutive positions, so they overlap, and the CTA's range lies in
+  // their union): no tile is skipped, as none is in the tile-at-a-time
+  // kernels.  Tiles past the range post -inf maxima, which leave every
+  // row's state as it is.
+  float s[ROUNDS][C::BNK / 8][4];
+#pragma unroll
+  for (int i = 0; i < ROUNDS; ++i) {
+    const int t = warp + kSfWarps * i;
+    float mx[2] = {-INFINITY, -INFINITY};
+    if (t < nt) {
+      wait(&sh.kfull[t]);
+      if (ok) {
+        tile_scores<HD, C::BNK>(s[i], qf, smem_u32(sh.kslot + t * C::TILE_BYTES), lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.kempty[t]);
+        tile_mask_max<C::BNK, LOWER8>(s[i], mx, (tile_lo + t) * C::BNK, pos, lo, a.scale_log2, lane);
+      }
+    }
+    if (t4 == 0) {
+      sh.tmax[t][gq] = mx[0];
+      sh.tmax[t][gq + 8] = mx[1];
+    }
+  }
+  bar_sync_named(1, kSfWarps * 32);
+
+  // ---- 2. the running maximum over all tiles, with each tile's rescale factor
+  float m[2] = {-INFINITY, -INFINITY};
+  float alpha[kSfTiles][2], mown[ROUNDS][2];
+#pragma unroll
+  for (int t = 0; t < kSfTiles; ++t) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float mn;
+      bool rv;
+      tile_running_max(m[r], sh.tmax[t][gq + 8 * r], mn, alpha[t][r], rv);
+      m[r] = mn;
+      if (t % kSfWarps == warp) mown[t / kSfWarps][r] = mn;
+    }
+  }
+  // P of this warp's tile of round i (bf16 hi/lo fragments) and its row sums
+  auto post_p = [&](int i) {
+    const int t = warp + kSfWarps * i;
+    if (t >= nt) return;
+    uint32_t pa[KS][4], pl[KS][4];
+    float rs[2];
+    tile_probs<C::BNK, LOWER8>(s[i], mown[i], pa, pl, rs);
+    uint4* dst = sh.pbuf + t * 4 * 32 + lane;
+    dst[0] = make_uint4(pa[0][0], pa[0][1], pa[0][2], pa[0][3]);
+    dst[32] = make_uint4(pa[1][0], pa[1][1], pa[1][2], pa[1][3]);
+    dst[64] = make_uint4(pl[0][0], pl[0][1], pl[0][2], pl[0][3]);
+    dst[96] = make_uint4(pl[1][0], pl[1][1], pl[1][2], pl[1][3]);
+    if (t4 == 0) {
+      sh.rsum[t][gq] = rs[0];
+      sh.rsum[t][gq + 8] = rs[1];
+    }
+  };
+
+  // ---- 3. rounds of 4 tiles: every warp's P of the round posted, then
+  // P V of the round's tiles in order (each tile's fragments loaded while
+  // the previous tile's products run), then this warp's P of the next round
+  float l[2] = {0.f, 0.f};
+  float o[ND / 8][4];
+#pragma unroll
+  for (int n = 0; n < ND / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  uint32_t fa[2][KS][4], fl[2][KS][4], vb[2][KS][NP][4];
+  auto load = [&](int t, int buf) {
+    const uint4* src = sh.pbuf + t * 4 * 32 + lane;
+    const uint4 h0 = src[0], h1 = src[32], l0 = src[64], l1 = src[96];
+    fa[buf][0][0] = h0.x; fa[buf][0][1] = h0.y; fa[buf][0][2] = h0.z; fa[buf][0][3] = h0.w;
+    fa[buf][1][0] = h1.x; fa[buf][1][1] = h1.y; fa[buf][1][2] = h1.z; fa[buf][1][3] = h1.w;
+    fl[buf][0][0] = l0.x; fl[buf][0][1] = l0.y; fl[buf][0][2] = l0.z; fl[buf][0][3] = l0.w;
+    fl[buf][1][0] = l1.x; fl[buf][1][1] = l1.y; fl[buf][1][2] = l1.z; fl[buf][1][3] = l1.w;
+    tile_v_frags<HD, C::BNK, ND>(vb[buf], sh.vaddr(t), lane, dim0);
+  };
+  if (ok) post_p(0);
+#pragma unroll
+  for (int i = 0; i < ROUNDS; ++i) {
+    bar_sync_named(1, kSfWarps * 32);
+    const int t0 = kSfWarps * i;
+    if (t0 < nt) {
+      if (t0 == 0) wait(&sh.vfull[0]);
+      if (t0 == V_OWN) wait(&sh.vfull[1]);
+      load(t0, 0);
+#pragma unroll
+      for (int j = 0; j < kSfWarps; ++j) {
+        const int t = t0 + j, u = t + 1;
+        if (t >= nt) break;
+        if (j + 1 < kSfWarps && u < nt) {
+          if (u == V_OWN) wait(&sh.vfull[1]);
+          load(u, (j + 1) & 1);
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int row = gq + 8 * r;
+          tile_update_l(l[r], alpha[t][r], sh.rsum[t][row], sh.tmax[t][row] != -INFINITY);
+        }
+        tile_rescale<ND, LOWER8>(o, alpha[t]);
+        tile_pv_mma<C::BNK, ND>(o, fa[j & 1], fl[j & 1], vb[j & 1]);
+      }
+    }
+    if (i + 1 < ROUNDS && ok) post_p(i + 1);
+  }
+  if (!ok) return;  // a wait gave up: the data of some tiles may not have landed
+
+  // ---- split partial of every row that saw a key here
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (!valid[r] || m[r] == -INFINITY) continue;
+    const size_t base = r ? base1 : base0;
+    if (t4 == 0 && dim0 == 0) {
+      a.part_ml[base * 2] = m[r];
+      a.part_ml[base * 2 + 1] = l[r];
+    }
+    float* po = a.part_o + base * HD + dim0;
+#pragma unroll
+    for (int n = 0; n < ND / 8; ++n)
+      *reinterpret_cast<float2*>(po + n * 8 + t4 * 2) = make_float2(o[n][2 * r], o[n][2 * r + 1]);
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__((kSfWarps + 1) * 32, 1)
+    attn_sf_kernel(const __grid_constant__ CUtensorMap kvmap, AttnArgs a) {
+  using C = AttnCfg<HD>;
+  using SC = SfCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  __shared__ int pid_s[C::PIDS];
+  __shared__ float tmax[kSfTiles][16], rsum[kSfTiles][16];
+  SfShared<HD> sh;
+  sh.pbuf = reinterpret_cast<uint4*>(smem);
+  sh.kslot = smem + SC::P_BYTES;
+  sh.vslot = sh.kslot + kSfTiles * C::TILE_BYTES;
+  sh.kfull = reinterpret_cast<uint64_t*>(sh.vslot + SC::V_OWN * C::TILE_BYTES);
+  sh.kempty = sh.kfull + kSfTiles;
+  sh.vfull = sh.kempty + kSfTiles;
+  sh.abort_flag = reinterpret_cast<volatile int*>(sh.vfull + 2);
+  sh.tmax = tmax;
+  sh.rsum = rsum;
+
+  pdl_wait();
+  pdl_trigger();
+  {
+    __shared__ int skip;  // once any bounded wait has given up, later CTAs skip their work
+    if (threadIdx.x == 0) skip = a.status ? *reinterpret_cast<volatile int*>(a.status) : 0;
+    __syncthreads();
+    if (skip) return;
+  }
+  // ---- work item -> (request, KV head, split); one block of 16 rows
+  const int item = blockIdx.x;
+  if (item >= a.cls_start[a.n_cls]) return;
+  int lo_i = 0, hi_i = a.n_cls - 1;
+  while (lo_i < hi_i) {
+    const int mid = (lo_i + hi_i + 1) >> 1;
+    if (a.cls_start[mid] <= item) lo_i = mid; else hi_i = mid - 1;
+  }
+  const int b = a.cls_seq[lo_i];
+  int local = item - a.cls_start[lo_i];
+  const int q0 = a.cu_q[b], qlen = a.cu_q[b + 1] - q0, cached = a.cached_len[b];
+  const int kv_len = cached + qlen;
+  const int G = a.Hq / a.Hkv;
+  const int nsplit = (kv_len - 1) / a.split + 1;
+  const int sidx = local % nsplit;
+  local /= nsplit;
+  const int kvh = local % a.Hkv;
+  const int r0 = (local / a.Hkv) * 16;
+  const int rows = qlen * G;
+  const int r_end = min(rows, r0 + 16);
+  const int p_min = cached + r0 / G, p_max = cached + (r_end - 1) / G;
+  const int lo_min = a.window > 0 ? max(0, p_min - a.window + 1) : 0;
+  const int key_lo = max(sidx * a.split, lo_min);
+  const int key_hi = min((sidx + 1) * a.split - 1, p_max);
+  if (key_lo > key_hi) return;
+  const int tile_lo = key_lo / C::BNK;
+  const int ntiles = key_hi / C::BNK - tile_lo + 1;  // <= kSfTiles (checked at launch)
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == kSfWarps) {  // the copy warp reads the page ids it needs
+    const int lp_first = (tile_lo * C::BNK) >> 4;
+    for (int j = lane; j < C::PIDS; j += 32) {
+      const int lp = lp_first + j;
+      pid_s[j] = (j < ntiles * C::PAGES && lp * 16 < kv_len)
+                     ? a.page_table[static_cast<size_t>(b) * a.pt_stride + lp] : -1;
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kSfTiles; ++k) {
+      mbar_init(&sh.kfull[k], 1);
+      mbar_init(&sh.kempty[k], 1);
+    }
+    mbar_init(&sh.vfull[0], 1);
+    mbar_init(&sh.vfull[1], 1);
+    *sh.abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kSfWarps) {
+    // One tile per lane: K tile `lane`, V tile `lane - 16` into its own slot,
+    // then V tile V_OWN + `lane` into the slot of K tile `lane` once scored.
+    auto copy_tile = [&](int t, bool is_v, uint8_t* dst, uint64_t* bar) {
+#pragma unroll
+      for (int pg = 0; pg < C::PAGES; ++pg) {
+        const int phys = pid_s[t * C::PAGES + pg];  // -1 past the context: zero fill
+        const int row = phys >= 0 ? a.layer_row0 + ((phys * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh) * 16 : a.pool_rows;
+        tma_load_3d(dst + pg * C::PAGE_BYTES, &kvmap, bar, 0, 0, row);
+      }
+    };
+    const int nv0 = min(ntiles, SC::V_OWN), nv1 = ntiles - nv0;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&sh.vfull[0], nv0 * C::TILE_BYTES);
+      if (nv1 > 0) mbar_arrive_expect_tx(&sh.vfull[1], nv1 * C::TILE_BYTES);
+    }
+    __syncwarp();
+    if (lane < ntiles) {
+      mbar_arrive_expect_tx(&sh.kfull[lane], C::TILE_BYTES);
+      copy_tile(lane, false, sh.kslot + lane * C::TILE_BYTES, &sh.kfull[lane]);
+    }
+    if (lane >= 16 && lane - 16 < nv0) copy_tile(lane - 16, true, sh.vslot + (lane - 16) * C::TILE_BYTES, &sh.vfull[0]);
+    if (lane < nv1 && mbar_wait(&sh.kempty[lane], 0, sh.abort_flag, a.status))
+      copy_tile(SC::V_OWN + lane, true, sh.kslot + lane * C::TILE_BYTES, &sh.vfull[1]);
+    __syncwarp();
+    if (lane == 0) {  // every copy lands before the CTA leaves, also when a wait gave up
+      for (int t = 0; t < ntiles; ++t) drain_wait(&sh.kfull[t], 0);
+      drain_wait(&sh.vfull[0], 0);
+      if (nv1 > 0) drain_wait(&sh.vfull[1], 0);
+    }
+    return;
+  }
+
+  // ---- the block's rows (every compute warp holds all 16 and a quarter of the head)
+  const int gq = lane >> 2, t4 = lane & 3;
+  int pos[2], lo[2], tok[2], hq[2];
+  bool valid[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int row = r0 + gq + 8 * r;
+    valid[r] = row < rows;
+    tok[r] = row / G;
+    hq[r] = kvh * G + row % G;
+    pos[r] = valid[r] ? cached + tok[r] : -1;
+    lo[r] = valid[r] ? (a.window > 0 ? max(0, pos[r] - a.window + 1) : 0) : 1;
+  }
+  uint32_t qf[HD / 16][4];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const __nv_bfloat16* qr = a.q + (static_cast<size_t>(q0 + tok[r]) * a.Hq + hq[r]) * HD;
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      qf[kk][r] = valid[r] ? *reinterpret_cast<const uint32_t*>(qr + kk * 16 + t4 * 2) : 0u;
+      qf[kk][2 + r] = valid[r] ? *reinterpret_cast<const uint32_t*>(qr + kk * 16 + 8 + t4 * 2) : 0u;
+    }
+  }
+  const size_t base0 = (static_cast<size_t>(q0 + tok[0]) * a.Hq + hq[0]) * a.max_splits + sidx;
+  const size_t base1 = (static_cast<size_t>(q0 + tok[1]) * a.Hq + hq[1]) * a.max_splits + sidx;
+  const bool lower8 = rows - r0 <= 8, full = ntiles == kSfTiles;
+  if (lower8 && full)
+    sf_rows<HD, true, true>(a, sh, ntiles, tile_lo, qf, pos, lo, valid, base0, base1, warp, lane);
+  else if (lower8)
+    sf_rows<HD, true, false>(a, sh, ntiles, tile_lo, qf, pos, lo, valid, base0, base1, warp, lane);
+  else if (full)
+    sf_rows<HD, false, true>(a, sh, ntiles, tile_lo, qf, pos, lo, valid, base0, base1, warp, lane);
+  else
+    sf_rows<HD, false, false>(a, sh, ntiles, tile_lo, qf, pos, lo, valid, base0, base1, warp, lane);
+}
+
 // Left-to-right fold of a row's split partials, then o / l -> bf16.  The
 // loop is unrolled so that the loads of later splits are in flight while
 // earlier ones are folded; the fold itself stays strictly left to right.
@@ -573,6 +1002,29 @@ int launch_attn_t(const CUtensorMap& kvmap, const AttnArgs& a0, int n_items, cud
   return VD_OK;
 }
 
+template <int HD>
+int launch_attn_sf(const CUtensorMap& kvmap, const AttnArgs& a, int n_items, cudaStream_t s) {
+  using SC = SfCfg<HD>;
+  static_assert(kSfTiles * AttnCfg<HD>::PAGES <= AttnCfg<HD>::PIDS, "page ids of a split");
+  static_assert(SC::SMEM + SC::STATIC_SMEM <= 227 * 1024, "shared memory");
+  static bool configured = false;
+  if (!configured) {
+    VD_CUDA_TRY(cudaFuncSetAttribute(attn_sf_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SC::SMEM));
+    configured = true;
+  }
+  VD_CUDA_TRY(launch_k(attn_sf_kernel<HD>, dim3(n_items), dim3((kSfWarps + 1) * 32), SC::SMEM, s, kvmap, a));
+  return VD_OK;
+}
+
+// One CTA per SM: the scores-first CTA where a split's K tiles fit in shared
+// memory at once (head dims 64 and 128), else the copy-warp CTA.
+template <int HD>
+int launch_attn_wide(const CUtensorMap& kvmap, const AttnArgs& a, int n_items, bool sf, cudaStream_t s) {
+  if constexpr (HD <= 128)
+    if (sf) return launch_attn_sf<HD>(kvmap, a, n_items, s);
+  return launch_attn_t<HD, 4, 4, false, true>(kvmap, a, n_items, s);
+}
+
 }  // namespace
 
 // Scratch for vd_op_attention_static: the split partials (o, then m/l) of
@@ -602,15 +1054,17 @@ int launch_attention(const CUtensorMap& kvmap, const AttnArgs& a, int hd, bool p
   if (prefill_class && a.fold) return fail(VD_ERR_INVALID_ARG, "split folding is for decode-class CTAs");
   if (a.split > AttnCfg<64>::PIDS * 16)  // a split CTA stages the ids of every page it streams
     return fail(VD_ERR_INVALID_ARG, "KV split larger than the staged page ids");
-  // Decode CTAs split the head dimension of P V over 2 warps, or over 4 when
-  // the launch has at most one CTA per SM (small batches); every
-  // output element keeps the same instruction chain either way.
+  // Decode CTAs split the head dimension of P V over 2 warps; a launch of at
+  // most one CTA per SM (small batches) runs the scores-first CTA, whose 4
+  // warps share the split's scores and a quarter of P V each.  Every output
+  // element keeps the same instruction chain either way.
   const bool wide = !prefill_class && !a.fold && n_items <= sm_count_attn();
+  const bool sf = wide && a.split <= kSfTiles * AttnCfg<64>::BNK;
 #define VD_ATTN_LAUNCH(HD_)                                                                     \
   if (hd == HD_)                                                                              \
     return prefill_class ? launch_attn_t<HD_, 4, 1, false>(kvmap, a, n_items, s)               \
            : a.fold      ? launch_attn_t<HD_, 2, 2, true>(kvmap, a, n_items, s)                \
-           : wide        ? launch_attn_t<HD_, 4, 4, false, true>(kvmap, a, n_items, s)         \
+           : wide        ? launch_attn_wide<HD_>(kvmap, a, n_items, sf, s)                     \
                          : launch_attn_t<HD_, 2, 2, false>(kvmap, a, n_items, s);
   VD_ATTN_LAUNCH(64)
   VD_ATTN_LAUNCH(128)
