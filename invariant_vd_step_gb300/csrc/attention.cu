@@ -909,7 +909,7 @@ __device__ __forceinline__ void load_part(const float* p, float* o) {
   }
 }
 
-template <int HD>
+template <int HD, int kBatch>
 __global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
   constexpr int PER = HD / 32;
   pdl_wait();
@@ -926,10 +926,11 @@ __global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
   load_part<PER>(a.part_o + (base + s0) * HD + lane * PER, O);
   // The partials of up to kBatch splits are loaded together (one memory
   // round trip per batch instead of one per split), then folded one by one
-  // in ascending split order exactly as before.  Four at a time keeps the
-  // registers low enough for ten CTAs per SM (eight at a time held 75
-  // registers and six CTAs: the kernel waits on memory and needs the warps).
-  constexpr int kBatch = 4;
+  // in ascending split order exactly as before.  Launches of many rows take
+  // four at a time, which keeps the registers low enough for ten CTAs per SM
+  // (eight at a time held 75 registers and six CTAs: the kernel waits on
+  // memory and needs the warps); launches of at most one CTA per SM take all
+  // the splits of a context in one round trip.
   for (int sb = s0 + 1; sb <= s1; sb += kBatch) {
     float2 ml[kBatch];
     float P[kBatch][PER];
@@ -955,6 +956,8 @@ __global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
   for (int i = 0; i < PER; i += 2)
     *reinterpret_cast<uint32_t*>(out + i) = pack_bf16x2(__fdiv_rn(O[i], L), __fdiv_rn(O[i + 1], L));
 }
+
+constexpr int kMergeWide = 16;  // splits of an 8192-key context
 
 int sm_count_attn() {
   static int n = 0;
@@ -1077,7 +1080,11 @@ int launch_merge(const MergeArgs& a, int hd, cudaStream_t s) {
   const int warps = a.T * a.Hq;
   if (warps <= 0) return VD_OK;
   const int blocks = (warps + 3) / 4;
-  auto k = hd == 64 ? merge_kernel<64> : hd == 128 ? merge_kernel<128> : hd == 256 ? merge_kernel<256> : nullptr;
+  const bool few = blocks <= sm_count_attn();
+  auto k = hd == 64    ? (few ? merge_kernel<64, kMergeWide> : merge_kernel<64, 4>)
+           : hd == 128 ? (few ? merge_kernel<128, kMergeWide> : merge_kernel<128, 4>)
+           : hd == 256 ? (few ? merge_kernel<256, kMergeWide> : merge_kernel<256, 4>)
+                       : nullptr;
   if (!k) return fail(VD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
   VD_CUDA_TRY(launch_k(k, dim3(blocks), dim3(128), 0, s, a));
   return VD_OK;
