@@ -1338,7 +1338,8 @@ int vd_op_gemm(const void* A, const void* W, void* C, int32_t T, int32_t N, int3
   if (epilogue < 0 || epilogue > VD_EPI_GEGLU) return fail(VD_ERR_INVALID_ARG, "unknown epilogue");
   if (K % kGemmBK || (glu ? N % 64 : N % kGemmBM)) return fail(VD_ERR_UNSUPPORTED, "N or K not a multiple of the tile");
   if (epilogue == VD_EPI_RESIDUAL && !residual) return fail(VD_ERR_INVALID_ARG, "residual required");
-  if (!aligned16(A) || !aligned16(W) || !aligned16(C)) return fail(VD_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  if (!aligned16(A) || !aligned16(W) || !aligned16(C) || (residual && !aligned16(residual)))
+    return fail(VD_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
   WeightMaps wm;
   std::array<CUtensorMap, kNumBn> xm;
   int rc;

@@ -57,6 +57,14 @@ constexpr int kSmemBytes = 1024 + kRingBytes + kXchgFloats * 4 + 256;
 static_assert((2 * kMaxStages + 5) * 8 + 8 <= 256, "barrier block");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
+// bf16(a + b) of eight bf16 pairs (a, b exact in fp32; one rounding).
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+  return pack_bf16x2(__fadd_rn(bf16_lo(a), bf16_lo(b)), __fadd_rn(bf16_hi(a), bf16_hi(b)));
+}
+__device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b) {
+  return make_uint4(add_bf16x2(a.x, b.x), add_bf16x2(a.y, b.y), add_bf16x2(a.z, b.z), add_bf16x2(a.w, b.w));
+}
+
 __device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
 __device__ __forceinline__ float gelu_tanh_f(float g) {
   const float g3 = __fmul_rn(__fmul_rn(g, g), g);
@@ -146,29 +154,44 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tac
           args.part_i[pi] = bi;
         }
         __syncwarp();
-      } else if (EPI == EPI_BF16) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * BM + row;
+      } else if (EPI == EPI_BF16 || EPI == EPI_RESIDUAL) {
+        // The warp's block (rpw feature rows x 32 tokens) is turned around in
+        // shared memory so that each output row (one token's rpw features)
+        // is written, and its residual read, as 16-byte vectors: a few wide
+        // accesses instead of one 2-byte access per (feature, token).  The
+        // staged value is bf16(acc) for EPI_BF16 and bf16_round(acc) for
+        // EPI_RESIDUAL (exact in bf16), so each element's arithmetic is as
+        // before: bf16(acc), or bf16(bf16_round(acc) + residual).
+        __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(xchg) + lg * 32 * 32;  // [token][rpw]
         if (live) {
   #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nt) out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(v[j]);
+          for (int j = 0; j < 32; ++j) xs[j * rpw + lane] = __float2bfloat16_rn(v[j]);
         }
-      } else if (EPI == EPI_RESIDUAL) {
-        const size_t col = static_cast<size_t>(tile_n) * BM + row;
-        const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(args.residual) + col;
+        __syncwarp();
+        const int lpr = rpw >> 3, tpp = 32 / lpr;  // lanes per output row, rows per pass
+        const int f8 = (lane % lpr) * 8;
+        const size_t col = static_cast<size_t>(tile_n) * BM + h * HM + lg * rpw + f8;
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + col;
-        if (live) {
-          // The residual may alias the output: load the whole chunk first so
-          // the loads are not serialised behind the stores.
-          float r[32];
+        uint4 val[4], rr[4];
   #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            r[j] = (j < nt) ? __bfloat162float(res[static_cast<size_t>(t0 + j) * args.ldo]) : 0.f;
-  #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nt)
-              out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fadd_rn(bf16_round(v[j]), r[j]));
+        for (int k = 0; k < 4; ++k) {  // tpp >= 8: at most four passes cover 32 tokens
+          const int j = k * tpp + lane / lpr;
+          if (j < nt) {
+            val[k] = *reinterpret_cast<const uint4*>(xs + j * rpw + f8);
+            if (EPI == EPI_RESIDUAL)  // the residual may alias the output: every load before any store
+              rr[k] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.residual) + col +
+                                                      static_cast<size_t>(t0 + j) * args.ldo);
+          }
         }
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = k * tpp + lane / lpr;
+          if (j < nt) {
+            if (EPI == EPI_RESIDUAL) val[k] = add_bf16x8(val[k], rr[k]);
+            *reinterpret_cast<uint4*>(out + static_cast<size_t>(t0 + j) * args.ldo) = val[k];
+          }
+        }
+        __syncwarp();  // the block's shared memory is rewritten by the next chunk
       } else {  // GLU: tile row 2f holds gate, 2f+1 up of feature f (the weight box interleaves them)
         const bool gate_lane = live && (lane & 1) == 0;
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * (BM >> 1) + h * (HM >> 1) +

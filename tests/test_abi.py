@@ -48,6 +48,7 @@ def test_ops_validate_arguments(L):
     assert L.vd_op_gemm(None, None, None, 1, 128, 64, 0, None, None) == 1
     assert L.vd_op_gemm(16, 16, 16, 1, 100, 64, 0, None, None) == 2      # N not a tile multiple
     assert L.vd_op_gemm(16, 16, 16, 1, 128, 64, 1, None, None) == 1      # residual missing
+    assert L.vd_op_gemm(16, 16, 16, 1, 128, 64, 1, 18, None) == 1        # residual not 16-byte aligned
     assert L.vd_op_gemm(16, 16, 16, 1, 128, 64, 9, None, None) == 1      # unknown epilogue
     assert L.vd_op_rmsnorm(16, 16, 16, 4, 12, 1e-5, None) == 1           # d % 8
     assert L.vd_op_philox(1, 2, -1, None, None) == 1

@@ -83,6 +83,34 @@ def test_residual_epilogue_vs_oracle_and_in_place():
     np.testing.assert_array_equal(bits(X), bits(_run(A, W, N, vd.EPI_RESIDUAL, R)))
 
 
+@pytest.mark.parametrize("plan", [(0, 0, 0), (64, 16, 4), (64, 32, 4), (128, 64, 2), (128, 128, 2), (256, 64, 1)])
+def test_bf16_and_residual_epilogues_round_the_f32_accumulator(plan):
+    # The bf16 epilogues take the same fp32 accumulator as the f32 one: C = bf16(acc) and
+    # C = bf16(bf16(acc) + R), each element rounded once to nearest even.  Pinned bit for bit
+    # against the f32 epilogue's output rounded here, for token counts inside one 32-token chunk,
+    # across several and with ragged tails, at 64-, 128- and 256-row tiles.
+    ready()
+    N, K = 512, 256
+    W = synth.make_normal_bf16((N, K), seed=61, std=0.05).cuda()
+    vd.set_gemm_plan(*plan)
+    try:
+        for T in (1, 3, 8, 31, 33, 64, 100, 257):
+            A = synth.make_normal_bf16((T, K), seed=60 + T).cuda()
+            R = synth.make_normal_bf16((T, N), seed=62 + T).cuda()
+            acc = _run(A, W, N, vd.EPI_F32).cpu()
+            want_bf16 = acc.to(torch.bfloat16)
+            want_res = (want_bf16.float() + R.cpu().float()).to(torch.bfloat16)
+            np.testing.assert_array_equal(bits(_run(A, W, N, vd.EPI_BF16)), bits(want_bf16), err_msg=f"bf16 T={T}")
+            np.testing.assert_array_equal(bits(_run(A, W, N, vd.EPI_RESIDUAL, R)), bits(want_res),
+                                          err_msg=f"residual T={T}")
+            X = R.clone()
+            vd.gemm(A, W, X, vd.EPI_RESIDUAL, X)  # in place
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(bits(X), bits(want_res), err_msg=f"in place T={T}")
+    finally:
+        vd.set_gemm_plan(0, 0, 0)
+
+
 @pytest.mark.parametrize("epi", [vd.EPI_SWIGLU, vd.EPI_GEGLU])
 def test_glu_epilogue_vs_oracle(epi):
     ready()
