@@ -759,8 +759,12 @@ __global__ void __launch_bounds__((kSfWarps + 1) * 32, 1)
   sh.tmax = tmax;
   sh.rsum = rsum;
 
-  pdl_wait();
-  pdl_trigger();
+  // Up to the wait for the previous kernel this CTA reads only the status
+  // word and the step's description (sequence classes, lengths, page table),
+  // which are written before the step's first kernel, so that their round
+  // trips hide behind that wait; the Q rows and K/V pages the previous
+  // kernels write are read after it.  (A failure of the kernel right before
+  // this one is then seen by the next kernel instead.)
   {
     __shared__ int skip;  // once any bounded wait has given up, later CTAs skip their work
     if (threadIdx.x == 0) skip = a.status ? *reinterpret_cast<volatile int*>(a.status) : 0;
@@ -815,6 +819,8 @@ __global__ void __launch_bounds__((kSfWarps + 1) * 32, 1)
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == kSfWarps) {
     // One tile per lane: K tile `lane`, V tile `lane - 16` into its own slot,

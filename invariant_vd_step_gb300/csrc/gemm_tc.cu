@@ -333,13 +333,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, 2 * kGemmBN);
     tmem_relinquish();
   }
-  // The prologue above touches no global memory; everything below may read
-  // what the previous kernel of the stream writes.
-  pdl_wait();
   // Once any bounded wait has given up, later CTAs skip their work instead
-  // of each waiting out the limit (the status word reports the failure).
+  // of each waiting out the limit (the status word reports the failure).  The
+  // word is read before the wait for the previous kernel, so that its latency
+  // hides behind that wait; a failure of the kernel right before this one is
+  // then seen by the next kernel instead (every result after a failure is
+  // discarded either way).
   __shared__ int skip;  // one read for the whole CTA keeps the exit uniform
-  if (threadIdx.x == 0) skip = args.status ? *reinterpret_cast<volatile int*>(args.status) : 0;
+  const int status_seen = (threadIdx.x == 0 && args.status) ? *reinterpret_cast<volatile int*>(args.status) : 0;
+  // The prologue above touches no global memory but the status word; everything
+  // below may read what the previous kernel of the stream writes.
+  pdl_wait();
+  if (threadIdx.x == 0) skip = status_seen;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
