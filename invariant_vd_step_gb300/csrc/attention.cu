@@ -289,9 +289,12 @@ __global__ void __launch_bounds__((NW + PROD) * 32)
   __shared__ int pid_s[C::PIDS];
   __shared__ uint64_t empty_s[PROD ? C::MAX_STAGES : 1];  // PROD: the NW warps are done with a stage
 
-  pdl_wait();
-  pdl_trigger();
-  // Once any bounded wait has given up, later CTAs skip their work.
+  // Up to the wait for the previous kernel this CTA reads only the status
+  // word and the step's description (sequence classes, lengths, page table),
+  // written before the step's first kernel, so that those round trips hide
+  // behind the wait; Q and the K/V pages are read after it.  Once any
+  // bounded wait has given up, later CTAs skip their work (a failure of the
+  // kernel right before this one is seen by the next kernel).
   {
     __shared__ int skip;  // one read for the whole CTA keeps the exit uniform
     if (threadIdx.x == 0) skip = a.status ? *reinterpret_cast<volatile int*>(a.status) : 0;
@@ -351,6 +354,8 @@ __global__ void __launch_bounds__((NW + PROD) * 32)
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
 
   auto issue = [&](int it, int stg) {
     uint8_t* sk = smem + stg * 2 * C::TILE_BYTES;
@@ -918,12 +923,16 @@ __device__ __forceinline__ void load_part(const float* p, float* o) {
 template <int HD, int kBatch>
 __global__ void __launch_bounds__(128) merge_kernel(MergeArgs a) {
   constexpr int PER = HD / 32;
+  // The row's token and position come from the step's description (written
+  // before the step's first kernel): read before the wait for the attention
+  // kernel, whose partials are read after it.
+  const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const bool row = w < a.T * a.Hq;
+  const int tok = !row ? 0 : a.tokens ? a.tokens[w / a.Hq] : w / a.Hq, h = w % a.Hq;
+  const int p = row ? a.positions[tok] : 0;
   pdl_wait();
   pdl_trigger();
-  const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (w >= a.T * a.Hq) return;
-  const int tok = a.tokens ? a.tokens[w / a.Hq] : w / a.Hq, h = w % a.Hq;
-  const int p = a.positions[tok];
+  if (!row) return;
   const int lo = a.window > 0 ? max(0, p - a.window + 1) : 0;
   const int s0 = lo / a.split, s1 = p / a.split;
   const size_t base = (static_cast<size_t>(tok) * a.Hq + h) * a.max_splits;

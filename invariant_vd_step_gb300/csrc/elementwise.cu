@@ -238,17 +238,34 @@ __global__ void postnorm_residual_kernel(const __nv_bfloat16* __restrict__ h, __
 // slot, v heads -> pool V slot of the token's (page, position % 16).
 constexpr int kRopeWarps = 8;
 __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_kernel(RopeArgs a) {
-  pdl_wait();
-  pdl_trigger();
   const int t = blockIdx.x;
   const int head = blockIdx.y * kRopeWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int nh = a.Hq + 2 * a.Hkv;
-  if (head >= nh) return;
   const int hd = a.hd, half = hd >> 1;
-  const __nv_bfloat16* src = a.qkv + (static_cast<size_t>(t) * nh + head) * hd;
-  const int p = a.positions[t];
-  const size_t page = static_cast<size_t>(a.slot_page[t]);
+  // The token's position and page slot (the step's description, written
+  // before the step's first kernel) and its rotation factors (constant
+  // tables) are read before the wait for the QKV GEMM, whose output is read
+  // after it.
+  const bool live = head < nh;
+  const int p = live ? a.positions[t] : 0;
+  const size_t page = live ? static_cast<size_t>(a.slot_page[t]) : 0;
   const int slot = p & 15;
+  const int np = (half + 31) / 32;
+  float cs[4] = {0.f, 0.f, 0.f, 0.f}, sn[4] = {0.f, 0.f, 0.f, 0.f};
+  if (live && head < a.Hq + a.Hkv) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = lane + 32 * k;
+      if (k < np && i < half) {
+        cs[k] = a.cos_t[static_cast<size_t>(p) * half + i];
+        sn[k] = a.sin_t[static_cast<size_t>(p) * half + i];
+      }
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (!live) return;
+  const __nv_bfloat16* src = a.qkv + (static_cast<size_t>(t) * nh + head) * hd;
   if (head >= a.Hq + a.Hkv) {  // v: plain copy
     const int g = head - a.Hq - a.Hkv;
     __nv_bfloat16* dst = a.pool + a.layer_elem0 + ((page * 2 + 1) * a.Hkv + g) * 16 * hd + slot * hd;
@@ -257,7 +274,6 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_kernel(RopeArgs a) {
   }
   const bool is_q = head < a.Hq;
   float x1[4], x2[4];
-  const int np = (half + 31) / 32;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int i = lane + 32 * k;
@@ -295,13 +311,11 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_kernel(RopeArgs a) {
     const int g = head - a.Hq;
     dst = a.pool + a.layer_elem0 + ((page * 2 + 0) * a.Hkv + g) * 16 * hd + slot * hd;
   }
-  const float* ct = a.cos_t + static_cast<size_t>(p) * half;
-  const float* st = a.sin_t + static_cast<size_t>(p) * half;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int i = lane + 32 * k;
     if (k < np && i < half) {
-      const float c = ct[i], s = st[i];
+      const float c = cs[k], s = sn[k];
       dst[i] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(x1[k], c), __fmul_rn(x2[k], s)));
       dst[i + half] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(x2[k], c), __fmul_rn(x1[k], s)));
     }
