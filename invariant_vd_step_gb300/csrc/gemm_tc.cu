@@ -193,18 +193,33 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t tac
         }
         __syncwarp();  // the block's shared memory is rewritten by the next chunk
       } else {  // GLU: tile row 2f holds gate, 2f+1 up of feature f (the weight box interleaves them)
+        // z = bf16(act(bf16(gate)) * bf16(up)) per (feature, token), staged
+        // transposed in shared memory and written as 16-byte rows, as above.
         const bool gate_lane = live && (lane & 1) == 0;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * (BM >> 1) + h * (HM >> 1) +
-                             lg * (rpw >> 1) + (lane >> 1);
+        const int fpw = rpw >> 1;  // features per warp: 16 (128-row halves) or 8 (64-row tiles)
+        __nv_bfloat16* zs = reinterpret_cast<__nv_bfloat16*>(xchg) + lg * 32 * 16;  // [token][fpw]
   #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float u = __shfl_xor_sync(0xffffffffu, bf16_round(v[j]), 1);  // the neighbour's up value
           if (gate_lane && j < nt) {
             const float g = bf16_round(v[j]);
             const float a = (EPI == EPI_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
-            out[static_cast<size_t>(t0 + j) * args.ldo] = __float2bfloat16_rn(__fmul_rn(a, u));
+            zs[j * fpw + (lane >> 1)] = __float2bfloat16_rn(__fmul_rn(a, u));
           }
         }
+        __syncwarp();
+        const int lpr = fpw >> 3, tpp = 32 / lpr;  // lanes per output row, rows per pass
+        const int f8 = (lane % lpr) * 8;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + tile_n * (BM >> 1) + h * (HM >> 1) +
+                             lg * fpw + f8;
+  #pragma unroll
+        for (int k = 0; k < 2; ++k) {  // tpp >= 16: two passes cover 32 tokens
+          const int j = k * tpp + lane / lpr;
+          if (j < nt)
+            *reinterpret_cast<uint4*>(out + static_cast<size_t>(t0 + j) * args.ldo) =
+                *reinterpret_cast<const uint4*>(zs + j * fpw + f8);
+        }
+        __syncwarp();  // the block's shared memory is rewritten by the next chunk
       }
     }
   }  // halves
