@@ -5,9 +5,13 @@
 // (request, KV head) and one KV split.  Decode-shaped requests (q_len *
 // Hq/Hkv <= 16, one block of 16 rows) run with two warps that share the rows
 // and split the head dimension of the P V product; longer chunks run four
-// warps of 16 rows each, sharing every K/V tile.  The per-element instruction
-// sequence is the same in both instantiations (the same `attn_tile` body),
-// so a row's result does not depend on which of them ran it.
+// warps of 16 rows each, sharing every K/V tile.  A decode launch of at most
+// one CTA per SM (small batches) runs the scores-first CTA instead (head
+// dims 64 and 128; see attn_sf_kernel), whose warps score the split's tiles
+// first and then fold P V in rounds.  Each value goes through the same step
+// functions in the same order per row in every variant (the `tile_*` steps
+// that `attn_tile` strings together), so a row's result does not depend on
+// which of them ran it.
 //
 // Traversal (深入解析 Vosti §六 6.2, causal prefix equivalence and the
 // sliding-window traversal; "Deterministic and bit-exact inference",
