@@ -560,15 +560,18 @@ __global__ void __launch_bounds__((NW + PROD) * 32)
 // tile into a slot of its own, the first V_OWN V tiles into slots of their
 // own (one barrier for all of them), the remaining V tiles into K slots as
 // the warps that scored those K tiles release them (one barrier again).
-// Warps 0..3 run three phases:
+// Warps 0..3:
 //   1. scores: warp w takes S, the mask and the row maxima of tiles
-//      w, w + 4, ..., keeps S in registers and posts the maxima;
-//   2. weights: every warp runs the running maximum over all the tiles'
-//      maxima (keeping each tile's rescale factor), then turns its own
-//      tiles' S into P (the bf16 hi/lo A fragments, posted to shared
-//      memory) and row sums;
-//   3. P V: every warp folds the tiles in order into its quarter of the
-//      head dimension: l and O rescaled, then the P V steps.
+//      w, w + 4, ... as they land, keeps S in registers and posts the
+//      maxima;
+//   2. every warp runs the running maximum over all the tiles' maxima,
+//      keeping each tile's rescale factor;
+//   3. rounds of four tiles: each warp turns S of its tile of the round
+//      into P (the bf16 hi/lo A fragments, posted to shared memory) and row
+//      sums; after a named barrier every warp folds the round's tiles in
+//      order into its quarter of the head dimension (l and O rescaled,
+//      then the P V steps), with each tile's fragments loaded while the
+//      previous tile's products run.
 // Each value is computed by the same step functions as in `attn_tile`,
 // from the same inputs, so every row's partial is bit for bit the one the
 // tile-at-a-time kernels write; what changes is that only O's rescale and
