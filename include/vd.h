@@ -295,7 +295,11 @@ int vd_copy_kv(vd_model* m, vd_kv_pool* pool, int32_t layer, const int32_t* page
 
 /* Reads (synchronising the device) the on-device status word: VD_OK,
  * VD_ERR_TIMEOUT if a bounded wait in a kernel gave up, or VD_ERR_OUT_OF_RANGE
- * if a token fed on the device was outside the vocabulary; clears it. */
+ * if a token fed on the device was outside the vocabulary; clears it.  While
+ * it is set, the GEMM and attention kernels skip their work.  They read it
+ * before waiting for the kernel ahead of them, so the kernel right after a
+ * failing one may still run; every result of a step that set the word is to
+ * be discarded either way. */
 int vd_device_status(vd_model* m);
 
 /* Per-kernel timing with CUDA events on the launching stream. */
